@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN slot-pool layer on one GB300 (replicas on N GPUs).
+
+Headline: batched decode at m = 256 active slots of a 256-slot pool, on a
+Qwen3.5-35B-A3B-shaped GDN layer (16 q/k heads, 32 v heads, d_k = d_v = 128,
+conv width 4, bf16 io, fp32 state ~ N(0, 0.1)), new random inputs every step:
+slot-steps/s.  One step is one decode launch over the 256 slots (conv + SiLU,
+L2 norms, gates, delta-rule update of every head's state in place, gated
+RMSNorm).  The 537 MB of state read and written per step is far larger than
+L2, so no flush is needed between steps.
+
+Also reported on the same line: the decode m-sweep {1,4,8,16,64,256}, the
+varlen prefill of 8 sequences {1,17,300,4095,1024,2048,513,8000} (tok/s), the
+end-to-end number through the public API with host buffers, the roofline of
+the decode kernel, the fp64 CPU oracle as a baseline, and the SM clocks seen.
+
+--impl reference times the fp64 CPU oracle on the host cores for the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HQK, HV, D, W = 16, 32, 128, 4
+C = 2 * HQK * D + HV * D
+NUM_SLOTS = 256
+M_HEAD = 256
+SWEEP = [1, 4, 8, 16, 64, 256]
+PREFILL_LENGTHS = [1, 17, 300, 4095, 1024, 2048, 513, 8000]
+WORKLOAD_DECODE, WORKLOAD_PREFILL = 2, 3
+METRIC = "GDN decode slot-steps/s @m=256"
+UNIT = "slot-steps/s"
+HEAD_WORKLOAD = ("decode m=256: Qwen3.5-35B-A3B-shaped GDN layer (Hqk 16, Hv 32, d 128, conv 4), "
+                 "bf16 io, fp32 state, 256-slot pool, new random inputs each step")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------- algorithmic bytes ----
+
+def decode_bytes_per_slot_step(io=2):
+    """HBM bytes one slot-step must move: S read + write (fp32), conv buffer read (W-1 rows) and one new
+    row written, q/k/v/z/a/b read, out written (io dtype)."""
+    s = HV * D * D * 4 * 2
+    conv = (W - 1) * C * io + C * io
+    inputs = C * io + HV * D * io + 2 * HV * io
+    out = HV * D * io
+    return s + conv + inputs + out
+
+
+def decode_param_bytes():
+    return C * W * 4 + 2 * HV * 4 + D * 4
+
+
+def prefill_bytes(lengths, io=2):
+    """Per token: q, k, v, z, a, b in and out; per sequence: S read + write and the conv buffer read + write."""
+    T = sum(lengths)
+    per_tok = C * io + HV * D * io + 2 * HV * io + HV * D * io
+    per_seq = HV * D * D * 4 * 2 + 2 * (W - 1) * C * io
+    return T * per_tok + len(lengths) * per_seq + decode_param_bytes()
+
+
+# -------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- ranks ----
+
+def dist_init():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU arm ----
+
+def make_decode_pool(torch, binding, synth, out_dtype="bf16"):
+    pool = binding.Pool(HQK, HV, D, D, NUM_SLOTS, 1, W, "bf16", out_dtype)
+    p = synth.layer_params(WORKLOAD_DECODE, 0, HQK, HV, D, D, W)
+    pool.layer_params(0, *(torch.from_numpy(p[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")))
+    for _ in range(NUM_SLOTS):
+        pool.alloc()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(20260)
+    for s in range(NUM_SLOTS):
+        Sv, _ = pool.state_views(0, s)
+        Sv.copy_(torch.randn(Sv.shape, generator=g, device="cuda") * math.sqrt(0.1))
+    torch.cuda.synchronize()
+    return pool
+
+
+def device_inputs(torch, m, n_sets, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    sets = []
+    for _ in range(n_sets):
+        sets.append({
+            "q": torch.randn((m, HQK * D), generator=g, device="cuda").to(torch.bfloat16),
+            "k": torch.randn((m, HQK * D), generator=g, device="cuda").to(torch.bfloat16),
+            "v": torch.randn((m, HV * D), generator=g, device="cuda").to(torch.bfloat16),
+            "z": torch.randn((m, HV * D), generator=g, device="cuda").to(torch.bfloat16),
+            "a": torch.randn((m, HV), generator=g, device="cuda").to(torch.bfloat16),
+            "b": torch.randn((m, HV), generator=g, device="cuda").to(torch.bfloat16),
+        })
+    return sets
+
+
+def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
+    """Device time of `steps` decode launches at m slots (events on the launching stream)."""
+    ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
+    ptrs = pool.slot_ptrs(0, ids)
+    n_sets = min(steps + warmup, 200)
+    sets = device_inputs(torch, m, n_sets, seed)
+    out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        s = sets[i % n_sets]
+        pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        s = sets[(warmup + i) % n_sets]
+        ev[i][0].record(stream)
+        pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    assert pool.device_status() == 0
+    return t0.elapsed_time(t1) / steps, statistics.mean(per), statistics.median(per)
+
+
+def time_decode_e2e(torch, pool, synth, m, steps, warmup):
+    """Public-API end to end: pinned host inputs copied in, decode, output copied back, every step."""
+    ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
+    ptrs = pool.slot_ptrs(0, ids)
+    n_sets = min(steps + warmup, 8)
+    host_sets = [{k: v.cpu().pin_memory() for k, v in s.items()} for s in device_inputs(torch, m, n_sets, 7)]
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host_sets[0].items()}
+    out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
+    d2h = out.numel() * out.element_size()
+
+    def step(i):
+        hs = host_sets[i % n_sets]
+        for k in dev:
+            dev[k].copy_(hs[k], non_blocking=True)
+        pool.decode_step(0, ptrs, m, dev["q"], dev["k"], dev["v"], dev["a"], dev["b"], dev["z"], out, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return m / (ms * 1e-3), h2d, d2h
+
+
+def time_prefill(torch, binding, synth, steps, warmup):
+    lengths = PREFILL_LENGTHS
+    T = sum(lengths)
+    pool = binding.Pool(HQK, HV, D, D, 2 * len(lengths), 1, W, "bf16", "bf16", max_prefill_tokens=T)
+    p = synth.layer_params(WORKLOAD_PREFILL, 0, HQK, HV, D, D, W)
+    pool.layer_params(0, *(torch.from_numpy(p[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")))
+    slots = [pool.alloc() for _ in lengths]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(33)
+    inp = {n: torch.randn((T, w), generator=g, device="cuda").to(torch.bfloat16)
+           for n, w in (("q", HQK * D), ("k", HQK * D), ("v", HV * D), ("z", HV * D), ("a", HV), ("b", HV))}
+    cu = torch.tensor([0] + list(__import__("itertools").accumulate(lengths)), dtype=torch.int32, device="cuda")
+    ids = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, HV * D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pool.prefill_varlen(0, cu, ids, len(lengths), T, inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"],
+                            out, stream)
+
+    for _ in range(warmup):
+        for s in slots:
+            pool.recycle(s, stream)
+            pool.alloc()
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        for s in slots:  # every timed prefill starts from zeroed slots (zeroing is outside the events)
+            pool.recycle(s, stream)
+            pool.alloc()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert pool.device_status() == 0
+    pool.close()
+    return statistics.median(times), T
+
+
+def cpu_baseline_decode(seconds=10.0, m_sample=16):
+    """fp64 oracle decode steps over a sample of slots, on all host cores, for about `seconds`."""
+    import numpy as np
+
+    import oracle
+    from gated_deltanet_linear_rule_gb300 import synth
+
+    o = oracle.load()
+    p = synth.layer_params(WORKLOAD_DECODE, 0, HQK, HV, D, D, W)
+    shape = {"hqk": HQK, "hv": HV, "dk": D, "dv": D, "conv_w": W, "l2_eps": 1e-6, "norm_eps": 1e-6}
+    slots = synth.distinct_slots(WORKLOAD_DECODE, M_HEAD, NUM_SLOTS)[:m_sample]
+    S = np.stack([synth.initial_state(WORKLOAD_DECODE, 0, int(s), HV, D, D) for s in slots]).astype(np.float64)
+    conv = np.zeros((m_sample, W - 1, C))
+    done, t0 = 0, time.perf_counter()
+    step = 0
+    while True:
+        inp = synth.batch_inputs(WORKLOAD_DECODE, 0, list(range(m_sample)), 1, HQK, HV, D, D, "bf16", tag="decode",
+                                 sub=step)
+        ts = time.perf_counter()
+        r = o.layer(shape, np.arange(m_sample + 1), inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"],
+                    p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], S, conv)
+        done += m_sample
+        S, conv = r["S"], r["convbuf"]
+        step += 1
+        if time.perf_counter() - t0 >= seconds or step >= 200:
+            break
+        del ts
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+            "sample": f"{step} decode steps of {m_sample} of the 256 slots (all 32 heads), {el:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    from gated_deltanet_linear_rule_gb300 import binding, synth
+
+    rank, world, local = dist_init()
+    torch.cuda.set_device(local)
+    hbm, bf16, peak_kind = peaks()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        uuid = None
+
+    pool = make_decode_pool(torch, binding, synth)
+    barrier(world)
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall0 = time.perf_counter()
+    step_ms, kern_mean, kern_med = time_decode(torch, pool, synth, M_HEAD, args.steps, args.warmup)
+    wall = time.perf_counter() - wall0
+    ck = clocks.stop()
+    step_ms = reduce_max(step_ms, world)
+    value = world * M_HEAD / (step_ms * 1e-3)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": HEAD_WORKLOAD, "m": M_HEAD, "pool_slots": NUM_SLOTS, "io": "bf16",
+                   "state": "fp32 N(0,0.1)", "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: inputs larger than L2 ({M_HEAD * HV * D * D * 4 / 1e6:.0f} MB of state per step)"},
+        "gpu_launches": args.steps,
+    }
+    algo = M_HEAD * decode_bytes_per_slot_step() + decode_param_bytes()
+    ach = algo / (kern_mean * 1e-3) / 1e9
+    result["roofline"] = {"kernel": "decode_kernel<128,bf16,bf16>", "bound": "hbm", "achieved": ach, "peak": hbm,
+                          "unit": "GB/s", "frac": ach / hbm, "peak_kind": peak_kind,
+                          "frac_of_8TBs": ach / 8000.0, "traffic": None,
+                          "bytes_per_launch": algo, "launch_ms": kern_mean}
+    if ck:
+        result["clocks"] = {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
+                            "samples": ck["samples"]}
+    if rank == 0 and not args.no_sweep:
+        sweep = []
+        for m in SWEEP:
+            sm, km, _ = time_decode(torch, pool, synth, m, max(10, args.steps), 3, seed=100 + m)
+            b = m * decode_bytes_per_slot_step() + decode_param_bytes()
+            sweep.append({"m": m, "slot_steps_per_s": m / (sm * 1e-3), "us_per_step": sm * 1e3,
+                          "gbs": b / (km * 1e-3) / 1e9, "frac": b / (km * 1e-3) / 1e9 / hbm})
+        result["decode_sweep"] = sweep
+    if rank == 0:
+        e2e, h2d, d2h = time_decode_e2e(torch, pool, synth, M_HEAD, args.steps, args.warmup)
+        result["e2e"] = {"value": e2e * world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    pool.close()
+    if rank == 0 and not args.no_prefill:
+        pms, T = time_prefill(torch, binding, synth, max(3, min(args.steps, 10)), 2)
+        pb = prefill_bytes(PREFILL_LENGTHS)
+        result["prefill"] = {"workload": "8 sequences {1,17,300,4095,1024,2048,513,8000}, bf16 io, zero state",
+                             "tokens": T, "ms": pms, "tok_per_s": T / (pms * 1e-3),
+                             "gbs": pb / (pms * 1e-3) / 1e9, "frac_hbm": pb / (pms * 1e-3) / 1e9 / hbm,
+                             "bytes": pb}
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds)
+    result["wall_s_timed_region"] = wall
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, on the host cores: same metric, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from gated_deltanet_linear_rule_gb300 import synth
+
+    o = oracle.load()
+    p = synth.layer_params(WORKLOAD_DECODE, 0, HQK, HV, D, D, W)
+    shape = {"hqk": HQK, "hv": HV, "dk": D, "dv": D, "conv_w": W, "l2_eps": 1e-6, "norm_eps": 1e-6}
+    m_sample = 8
+    slots = synth.distinct_slots(WORKLOAD_DECODE, M_HEAD, NUM_SLOTS)[:m_sample]
+    S = np.stack([synth.initial_state(WORKLOAD_DECODE, 0, int(s), HV, D, D) for s in slots]).astype(np.float64)
+    conv = np.zeros((m_sample, W - 1, C))
+    times = []
+    for step in range(args.warmup + args.steps):
+        inp = synth.batch_inputs(WORKLOAD_DECODE, 0, list(range(m_sample)), 1, HQK, HV, D, D, "bf16",
+                                 tag="decode", sub=step)
+        t0 = time.perf_counter()
+        r = o.layer(shape, np.arange(m_sample + 1), inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"],
+                    p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], S, conv)
+        el = time.perf_counter() - t0
+        S, conv = r["S"], r["convbuf"]
+        if step >= args.warmup:
+            times.append(el)
+    ms = 1e3 * sum(times) / len(times)
+    value = m_sample / (ms * 1e-3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEAD_WORKLOAD, "m": M_HEAD, "pool_slots": NUM_SLOTS, "io": "bf16",
+                   "parallelism": "host cores (OpenMP over slot x head)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"each step: {m_sample} of the 256 slots, all 32 heads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

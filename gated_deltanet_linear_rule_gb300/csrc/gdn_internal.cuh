@@ -1,0 +1,264 @@
+// gdn_internal.cuh -- types and device helpers shared by the libgdn translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// ----------------------------------------------------------------- pool ----
+
+struct LayerParams {
+    const float* conv_w = nullptr;
+    const float* A_log = nullptr;
+    const float* dt_bias = nullptr;
+    const float* norm_w = nullptr;
+    bool set() const { return conv_w && A_log && dt_bias && norm_w; }
+};
+
+// Prefill workspace: per-token intermediates of the varlen prefill.
+struct PrefillWorkspace {
+    float* qh = nullptr;     // [T][Hqk*dk] normalised q, scaled by dk^-1/2
+    float* kh = nullptr;     // [T][Hqk*dk] normalised k
+    float* vc = nullptr;     // [T][Hv*dv]  conv + SiLU v
+    float* g = nullptr;      // [T][Hv]     log decay
+    float* beta = nullptr;   // [T][Hv]
+    float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm
+    float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat
+    int* valid = nullptr;    // [1] 1 when the call's cu_seqlens / slot ids passed validation
+    void* base = nullptr;
+    size_t bytes = 0;
+};
+
+struct Pool {
+    gdn_shape shape{};
+    int num_slots = 0, num_layers = 0;
+    int C = 0, r = 0, io_size = 0;
+    size_t state_bytes = 0, conv_bytes = 0, slot_bytes = 0, total_bytes = 0;
+    char* base = nullptr;
+    unsigned char* live_dev = nullptr;   // [num_slots] 1 = allocated (read by device-side checks)
+    unsigned int* status_dev = nullptr;  // device status word (GDN_DEV_* bits)
+    std::vector<int> free_list;          // free slot ids, popped from the back (lowest id first)
+    std::vector<unsigned char> live;     // host mirror of live_dev
+    std::vector<LayerParams> params;
+    PrefillWorkspace ws;
+    int device = 0, num_sms = 0;
+};
+
+// Facts every kernel needs to check a slot pointer before touching memory.
+struct SlotCheck {
+    uint64_t base, total_bytes, slot_bytes;
+    int num_layers, layer;
+};
+
+__device__ __forceinline__ bool slot_ptr_ok(uint64_t p, const SlotCheck& c)
+{
+    if (p < c.base) return false;
+    uint64_t off = p - c.base;
+    if (off >= c.total_bytes || off % c.slot_bytes) return false;
+    return (int)((off / c.slot_bytes) % (uint64_t)c.num_layers) == c.layer;
+}
+
+// ----------------------------------------------------------- io dtypes ----
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ------------------------------------------------------------- scalars ----
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+// softplus(x) = log(1 + e^x); above 20 the correction log1p(e^-x) is below 2.1e-9 and dropped.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// g = -exp(A_log) * softplus(a + dt_bias): the log of the per-token decay alpha.
+__device__ __forceinline__ float log_decay(float A_log, float a, float dt_bias)
+{
+    return -expf(A_log) * softplus_f(a + dt_bias);
+}
+
+// ----------------------------------------------------------- mbarriers ----
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Gives up after kWaitLimitNs,
+// or as soon as *abort is set by another thread; returns false in both cases.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared (the TMA engine), completing on an mbarrier.
+// dst, src 16-B aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, float4 v)
+{
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------- shared layer arithmetic ----
+// The decode kernel and the recurrent prefill kernels use these same routines,
+// with the same reduction orders, so a prefill over L tokens reproduces L decode
+// steps bit for bit.
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// sum_i x[i] * y[i] over n values by one warp (lane-strided partial sums, then a butterfly)
+__device__ __forceinline__ float warp_dot(const float* x, const float* y, int n, int lane)
+{
+    float s = 0.0f;
+    for (int i = lane; i < n; i += 32) s = fmaf(x[i], y[i], s);
+    return warp_sum(s);
+}
+
+// q and k scales: q_hat = q * rsqrt(|q|^2 + eps) * D^-1/2, k_hat = k * rsqrt(|k|^2 + eps)
+__device__ __forceinline__ float q_scale(float ssq, float eps, int D) { return rsqrtf(ssq + eps) * rsqrtf((float)D); }
+__device__ __forceinline__ float k_scale(float ssk, float eps) { return rsqrtf(ssk + eps); }
+
+// gated RMSNorm factor 1 / sqrt(mean(o^2) + eps)
+__device__ __forceinline__ float rms_scale(float sso, float eps, int D) { return rsqrtf(sso / (float)D + eps); }
+
+// One row i of one head's state S (d_k columns spread over LPR lanes, 16 per lane) for one token:
+//   u_i = alpha (S_i . k);  delta_i = beta (v_i - u_i);  S_i <- alpha S_i + delta_i k;
+//   o_i = S_i(new) . q = alpha (S_i . q) + delta_i (k . q)
+// kq is k . q over the whole head.  All LPR lanes of the row get the same o.
+template <int LPR>
+__device__ __forceinline__ float row_update(float (&s)[16], const float (&kr)[16], const float (&qr)[16], float alpha,
+                                            float beta, float v, float kq)
+{
+    float k0 = 0.f, k1 = 0.f, k2 = 0.f, k3 = 0.f, q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        k0 = fmaf(s[j], kr[j], k0);
+        k1 = fmaf(s[j + 1], kr[j + 1], k1);
+        k2 = fmaf(s[j + 2], kr[j + 2], k2);
+        k3 = fmaf(s[j + 3], kr[j + 3], k3);
+        q0 = fmaf(s[j], qr[j], q0);
+        q1 = fmaf(s[j + 1], qr[j + 1], q1);
+        q2 = fmaf(s[j + 2], qr[j + 2], q2);
+        q3 = fmaf(s[j + 3], qr[j + 3], q3);
+    }
+    float dk = (k0 + k1) + (k2 + k3);
+    float dq = (q0 + q1) + (q2 + q3);
+#pragma unroll
+    for (int off = LPR / 2; off >= 1; off >>= 1) {
+        dk += __shfl_xor_sync(0xffffffffu, dk, off);
+        dq += __shfl_xor_sync(0xffffffffu, dq, off);
+    }
+    const float u = alpha * dk;
+    const float delta = beta * (v - u);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s[j] = fmaf(delta, kr[j], alpha * s[j]);
+    return fmaf(delta, kq, alpha * dq);
+}
+
+// Column j (0..15) of lane cl in a row spread over LPR lanes: float4 groups interleaved
+// across the row's lanes, so a quarter-warp touches 128 contiguous bytes.
+template <int LPR>
+__device__ __forceinline__ int row_col(int j, int cl) { return (j >> 2) * 4 * LPR + 4 * cl + (j & 3); }
+
+// --------------------------------------------------------- launchers ----
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, int m, const void* q, const void* k,
+                          const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st);
+
+cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
+                           int total_tokens, const void* q, const void* k, const void* v, const void* a,
+                           const void* b, const void* z, void* out, cudaStream_t st);
+
+size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens);
+void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens);
+
+inline SlotCheck slot_check(const Pool& P, int layer)
+{
+    return SlotCheck{reinterpret_cast<uint64_t>(P.base), (uint64_t)P.total_bytes, (uint64_t)P.slot_bytes,
+                     P.num_layers, layer};
+}
+
+}  // namespace gdn

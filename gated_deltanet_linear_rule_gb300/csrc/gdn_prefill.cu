@@ -1,0 +1,359 @@
+// gdn_prefill.cu -- varlen prefill of one GDN layer into the slot pool.
+//
+// The prefill branch of the System Design page's "GDN Kernel Dispatch Detail": conv1d,
+// L2norm, the gated delta rule over the prompt starting from the sequence's state, then
+// "Update temporal_state" (the final S and conv buffer land in the slot, where the
+// decode kernel reads them) and the gated RMSNorm.
+//
+// Kernels (all on the caller's stream, no host synchronisation):
+//   1. validate   one CTA: cu_seqlens 0-based, non-decreasing, ending at total_tokens;
+//                 slot ids allocated and distinct.  The verdict gates every later kernel.
+//   2. prep       one CTA per token: conv + SiLU over all C channels (the left context
+//                 before a sequence's first token comes from its slot's conv buffer),
+//                 L2 scales of q and k, k.q per q/k head, gates per v-head.
+//   3. conv_tail  one CTA per sequence: the slot's conv buffer becomes the last W-1 raw
+//                 inputs (after prep has read the old buffer).
+//   4. recurrent  one CTA per (sequence, v-head, row tile of S): the tile of S stays in
+//                 registers across the whole sequence, token after token.
+//   5. epilogue   gated RMSNorm per (token, v-head).
+// Kernels 2, 4 and 5 use the decode kernel's arithmetic in the same order, so a prefill
+// of L tokens equals L decode steps bit for bit.
+#include <algorithm>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+namespace {
+
+struct PrefillArgs {
+    const int* cu;
+    const int* ids;
+    int n, T;
+    const void *q, *k, *v, *a, *b, *z;
+    void* out;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    char* base;
+    uint64_t slot_bytes;
+    uint32_t state_bytes;
+    int num_layers, layer, num_slots;
+    const unsigned char* live;
+    unsigned int* status;
+    int hqk, hv, r, D, W, C;
+    float l2_eps, norm_eps;
+    PrefillWorkspace ws;
+    float* kq;  // [T][Hqk] k.q before the L2 scales (workspace)
+};
+
+__global__ void validate_kernel(PrefillArgs A)
+{
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    if (threadIdx.x == 0 && (A.cu[0] != 0 || A.cu[A.n] != A.T)) atomicOr(&bad, 1);
+    for (int s = threadIdx.x; s < A.n; s += blockDim.x) {
+        if (A.cu[s + 1] < A.cu[s]) atomicOr(&bad, 1);
+        const int id = A.ids[s];
+        bool ok = id >= 0 && id < A.num_slots && A.live[id];
+        for (int j = 0; ok && j < s; ++j) ok = A.ids[j] != id;
+        if (!ok) atomicOr(&bad, 2);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        *A.ws.valid = bad == 0;
+        if (bad & 1) atomicOr(A.status, GDN_DEV_BAD_SEQLENS);
+        if (bad & 2) atomicOr(A.status, GDN_DEV_BAD_SLOT_ID);
+    }
+}
+
+// sequence owning packed token t: the largest s with cu[s] <= t
+__device__ __forceinline__ int seq_of(const int* cu, int n, int t)
+{
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <typename TIn>
+__device__ __forceinline__ TIn channel_input(const PrefillArgs& A, int t, int c)
+{
+    const int Dq = A.hqk * A.D;
+    if (c < Dq) return static_cast<const TIn*>(A.q)[(size_t)t * Dq + c];
+    if (c < 2 * Dq) return static_cast<const TIn*>(A.k)[(size_t)t * Dq + (c - Dq)];
+    return static_cast<const TIn*>(A.v)[(size_t)t * (A.hv * A.D) + (c - 2 * Dq)];
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(256) prep_kernel(PrefillArgs A)
+{
+    extern __shared__ float y[];  // [C] conv + SiLU of this token, then [3*Hqk] scales and dots
+    if (!*A.ws.valid) return;
+    const int t = blockIdx.x;
+    const int s = seq_of(A.cu, A.n, t);
+    const int pos = t - A.cu[s];
+    const TIn* cbuf =
+        reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes + A.state_bytes);
+    const int W = A.W, C = A.C, D = A.D;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        const float* w = A.conv_w + (size_t)c * W;
+        float acc = 0.0f;
+        for (int j = 0; j < W; ++j) {
+            const int pp = pos - (W - 1) + j;
+            const TIn x = pp >= 0 ? channel_input<TIn>(A, t - (W - 1) + j, c) : cbuf[(size_t)(W - 1 + pp) * C + c];
+            acc = fmaf(w[j], to_f(x), acc);
+        }
+        y[c] = silu_f(acc);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int Dq = A.hqk * D;
+    float* scale = y + C;            // [2*Hqk] q scales, then k scales
+    float* dots = scale + 2 * A.hqk;  // [Hqk] q.k before scaling
+    for (int hh = warp; hh < 3 * A.hqk; hh += nwarps) {
+        if (hh < 2 * A.hqk) {  // q heads then k heads: contiguous channel blocks
+            const float ss = warp_dot(y + hh * D, y + hh * D, D, lane);
+            if (lane == 0) scale[hh] = hh < A.hqk ? q_scale(ss, A.l2_eps, D) : k_scale(ss, A.l2_eps);
+        } else {
+            const int hk = hh - 2 * A.hqk;
+            const float d = warp_dot(y + hk * D, y + Dq + hk * D, D, lane);
+            if (lane == 0) dots[hk] = d;
+        }
+    }
+    for (int h = threadIdx.x; h < A.hv; h += blockDim.x) {
+        const TIn* ain = static_cast<const TIn*>(A.a);
+        const TIn* bin = static_cast<const TIn*>(A.b);
+        A.ws.g[(size_t)t * A.hv + h] = log_decay(A.A_log[h], to_f(ain[(size_t)t * A.hv + h]), A.dt_bias[h]);
+        A.ws.beta[(size_t)t * A.hv + h] = sigmoid_f(to_f(bin[(size_t)t * A.hv + h]));
+    }
+    __syncthreads();
+    for (int hk = threadIdx.x; hk < A.hqk; hk += blockDim.x)
+        A.kq[(size_t)t * A.hqk + hk] = dots[hk] * scale[hk] * scale[A.hqk + hk];
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        if (c < Dq) A.ws.qh[(size_t)t * Dq + c] = y[c] * scale[c / D];
+        else if (c < 2 * Dq) A.ws.kh[(size_t)t * Dq + (c - Dq)] = y[c] * scale[c / D];
+        else A.ws.vc[(size_t)t * (A.hv * D) + (c - 2 * Dq)] = y[c];
+    }
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(256) conv_tail_kernel(PrefillArgs A)
+{
+    if (!*A.ws.valid) return;
+    const int s = blockIdx.x;
+    const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
+    if (L == 0) return;
+    TIn* cbuf = reinterpret_cast<TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes +
+                                       A.state_bytes);
+    const int W = A.W, C = A.C;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        TIn old[8];
+        for (int j = 0; j < W - 1; ++j) old[j] = cbuf[(size_t)j * C + c];
+        for (int i = 0; i < W - 1; ++i) {
+            const int pp = L - (W - 1) + i;
+            cbuf[(size_t)i * C + c] = pp >= 0 ? channel_input<TIn>(A, t0 + pp, c) : old[W - 1 + pp];
+        }
+    }
+}
+
+// S row tile of one (sequence, v-head): 8 warps x RPW rows, LPR lanes per row.
+template <int D>
+__global__ void __launch_bounds__(256) recurrent_kernel(PrefillArgs A)
+{
+    constexpr int LPR = D / 16, RPW = 32 / LPR, ROWS = 8 * RPW < D ? 8 * RPW : D;
+    if (!*A.ws.valid) return;
+    const int s = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
+    const int t0 = A.cu[s], t1 = A.cu[s + 1];
+    if (t0 == t1) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rsub = lane / LPR, cl = lane % LPR;
+    const int lr = warp * RPW + rsub;
+    const int i = tile * ROWS + lr;
+    const bool rv = lr < ROWS;
+    const int hk = h / A.r, Dq = A.hqk * D, Dv = A.hv * D;
+    float* S = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
+               (size_t)h * D * D;
+
+    float sv[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        float4 x = rv ? *reinterpret_cast<const float4*>(S + (size_t)i * D + row_col<LPR>(j, cl))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        sv[j] = x.x;
+        sv[j + 1] = x.y;
+        sv[j + 2] = x.z;
+        sv[j + 3] = x.w;
+    }
+    // software pipeline: the next token's operands are loaded while this token is processed
+    float kr[16], qr[16], nk[16], nq[16];
+    float v_i, g, be, kq, nv = 0.f, ng = 0.f, nb = 0.f, nkq = 0.f;
+    auto load = [&](int t, float (&kk)[16], float (&qq)[16], float& vv, float& gg, float& bb, float& dot) {
+        const float* kp = A.ws.kh + (size_t)t * Dq + hk * D;
+        const float* qp = A.ws.qh + (size_t)t * Dq + hk * D;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(kp + row_col<LPR>(j, cl));
+            const float4 b4 = *reinterpret_cast<const float4*>(qp + row_col<LPR>(j, cl));
+            kk[j] = a4.x; kk[j + 1] = a4.y; kk[j + 2] = a4.z; kk[j + 3] = a4.w;
+            qq[j] = b4.x; qq[j + 1] = b4.y; qq[j + 2] = b4.z; qq[j + 3] = b4.w;
+        }
+        vv = rv ? A.ws.vc[(size_t)t * Dv + (size_t)h * D + i] : 0.f;
+        gg = A.ws.g[(size_t)t * A.hv + h];
+        bb = A.ws.beta[(size_t)t * A.hv + h];
+        dot = A.kq[(size_t)t * A.hqk + hk];
+    };
+    load(t0, kr, qr, v_i, g, be, kq);
+    for (int t = t0; t < t1; ++t) {
+        if (t + 1 < t1) load(t + 1, nk, nq, nv, ng, nb, nkq);
+        const float o = row_update<LPR>(sv, kr, qr, expf(g), be, v_i, kq);
+        if (rv && cl == 0) A.ws.o[(size_t)t * Dv + (size_t)h * D + i] = o;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            kr[j] = nk[j];
+            qr[j] = nq[j];
+        }
+        v_i = nv;
+        g = ng;
+        be = nb;
+        kq = nkq;
+    }
+    if (rv) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(S + (size_t)i * D + row_col<LPR>(j, cl)) =
+                make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+    }
+}
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(256) epilogue_kernel(PrefillArgs A)
+{
+    if (!*A.ws.valid) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = blockIdx.x * 8 + warp;  // (token, v-head)
+    if (pair >= A.T * A.hv) return;
+    const int t = pair / A.hv, h = pair % A.hv, D = A.D;
+    const size_t base = (size_t)t * A.hv * D + (size_t)h * D;
+    const float* o = A.ws.o + base;
+    const float rs = rms_scale(warp_dot(o, o, D, lane), A.norm_eps, D);
+    const TIn* zin = static_cast<const TIn*>(A.z);
+    TOut* out = static_cast<TOut*>(A.out);
+    for (int i = lane; i < D; i += 32)
+        out[base + i] = from_f<TOut>(o[i] * rs * A.norm_w[i] * silu_f(to_f(zin[base + i])));
+}
+
+template <typename TIn, typename TOut>
+cudaError_t run(const PrefillArgs& A, cudaStream_t st)
+{
+    validate_kernel<<<1, 256, 0, st>>>(A);
+    if (A.T > 0) {
+        const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);
+        if (smem > 48 * 1024) {
+            cudaError_t e =
+                cudaFuncSetAttribute(prep_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
+    }
+    conv_tail_kernel<TIn><<<A.n, 256, 0, st>>>(A);
+    if (A.T > 0) {
+        const int rows = std::min(A.D, 8 * (32 / (A.D / 16)));
+        dim3 grid(A.n, A.hv, A.D / rows);
+        switch (A.D) {
+            case 16: recurrent_kernel<16><<<grid, 256, 0, st>>>(A); break;
+            case 32: recurrent_kernel<32><<<grid, 256, 0, st>>>(A); break;
+            case 64: recurrent_kernel<64><<<grid, 256, 0, st>>>(A); break;
+            case 128: recurrent_kernel<128><<<grid, 256, 0, st>>>(A); break;
+            default: return cudaErrorInvalidValue;
+        }
+        const int pairs = A.T * A.hv;
+        epilogue_kernel<TIn, TOut><<<(pairs + 7) / 8, 256, 0, st>>>(A);
+    }
+    return cudaGetLastError();
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const gdn_shape& s, int T)
+{
+    const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
+    size_t b = 0;
+    b += align256((size_t)T * Dq * 4) * 2;            // qh, kh
+    b += align256((size_t)T * Dv * 4) * 2;            // vc, o
+    b += align256((size_t)T * s.hv * 4) * 2;          // g, beta
+    b += align256((size_t)T * s.hqk * 4);             // k.q
+    b += 256;                                         // valid flag
+    return b;
+}
+
+void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T)
+{
+    const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
+    char* p = static_cast<char*>(ws.base);
+    auto take = [&](size_t bytes) {
+        char* r = p;
+        p += align256(bytes);
+        return r;
+    };
+    ws.qh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
+    ws.kh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
+    ws.vc = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
+    ws.o = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
+    ws.g = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
+    ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
+    ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
+    ws.valid = reinterpret_cast<int*>(take(256));
+}
+
+cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
+                           int total_tokens, const void* q, const void* k, const void* v, const void* a,
+                           const void* b, const void* z, void* out, cudaStream_t st)
+{
+    const LayerParams& L = P.params[(size_t)layer];
+    PrefillArgs A;
+    A.cu = cu_seqlens;
+    A.ids = slot_ids;
+    A.n = n_seqs;
+    A.T = total_tokens;
+    A.q = q;
+    A.k = k;
+    A.v = v;
+    A.a = a;
+    A.b = b;
+    A.z = z;
+    A.out = out;
+    A.conv_w = L.conv_w;
+    A.A_log = L.A_log;
+    A.dt_bias = L.dt_bias;
+    A.norm_w = L.norm_w;
+    A.base = P.base;
+    A.slot_bytes = P.slot_bytes;
+    A.state_bytes = (uint32_t)P.state_bytes;
+    A.num_layers = P.num_layers;
+    A.layer = layer;
+    A.num_slots = P.num_slots;
+    A.live = P.live_dev;
+    A.status = P.status_dev;
+    A.hqk = P.shape.hqk;
+    A.hv = P.shape.hv;
+    A.r = P.r;
+    A.D = P.shape.dk;
+    A.W = P.shape.conv_w;
+    A.C = P.C;
+    A.l2_eps = P.shape.l2_eps;
+    A.norm_eps = P.shape.norm_eps;
+    A.ws = P.ws;
+    A.kq = P.ws.kq;
+    const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
+    if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st);
+    if (in_bf16) return run<__nv_bfloat16, float>(A, st);
+    if (out_bf16) return run<float, __nv_bfloat16>(A, st);
+    return run<float, float>(A, st);
+}
+
+}  // namespace gdn

@@ -1,0 +1,186 @@
+/*
+ * gdn.h -- C ABI of libgdn, a GB300 (sm_103a) library that runs the Gated
+ * Delta Rule (GDN) linear-attention layer of Qwen3.5-style hybrid models over
+ * many sequences at once, each sequence owning a fixed-size slot of a state pool.
+ *
+ * Where the calls come from:
+ *   - The slot pool is the fixed-size recurrent-state / conv-buffer pool that
+ *     the qLLM README ("What this is": StateManager) wires in next to the KV
+ *     block manager, and that the System Design page lists as the GDN state
+ *     cache manager (mamba_cache.py, "Architecture").
+ *   - The call set follows the seven-method engine trait of issue #5279
+ *     ("serve: Qwen3.5 on CUDA never batches ...", phase plan P0: setup+prefill,
+ *     decode step, add slot, recycle slot, cleanup, reset) and its phase P5
+ *     (the GDN conv1d and delta rule gain a slot dimension: one launch over m
+ *     slots through a device array of u64 per-layer state pointers).
+ *   - The arithmetic is the GatedDeltaNet layer of the System Design page
+ *     ("Runtime Data Flow" and "GDN Kernel Dispatch Detail"): depthwise causal
+ *     conv1d + SiLU over the q/k/v channels, L2 normalisation of q and k, gates
+ *     g = -exp(A_log) softplus(a + dt_bias), alpha = exp(g), beta = sigmoid(b),
+ *     the state update S <- alpha S; u = S k; S <- S + beta (v - u) k^T, the
+ *     read-out o = S q d_k^-1/2, and the gated RMSNorm rmsnorm(o) * silu(z).
+ *
+ * Conventions for every call:
+ *   - Return value: GDN_OK (0) or a negative gdn_status code.  Calls validate
+ *     their host-side arguments before enqueuing any GPU work; a call that
+ *     returns an error has enqueued nothing.
+ *   - Pointers named *_dev are device pointers; everything else is host memory.
+ *   - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ *     default stream).  GPU work is enqueued on it; the hot calls
+ *     (gdn_slot_ptrs, gdn_decode_step, gdn_prefill_varlen) neither allocate nor
+ *     synchronise the host.
+ *   - Ownership: the pool owns its state memory and its prefill workspace.
+ *     Activation buffers, parameter arrays and streams belong to the caller
+ *     and are only borrowed for the duration of the call (parameter arrays:
+ *     for as long as they are registered with gdn_layer_params).
+ *   - Layouts are row-major and contiguous; a token's heads are contiguous:
+ *       q, k    [rows][Hqk * dk]     v, z, out  [rows][Hv * dv]     a, b [rows][Hv]
+ *     in the pool's io dtype (out in its out dtype).  v-head h reads q/k head
+ *     h / (Hv / Hqk).
+ *   - Device-side faults in the arguments (a slot pointer outside the layer's
+ *     slots, a freed or repeated slot id, a non-monotone cu_seqlens) are not
+ *     turned into memory faults: the affected work is skipped and a bit is set
+ *     in the pool's device status word, read by gdn_last_device_status.
+ *   - Work on one slot is ordered by the stream; calls on different streams
+ *     that touch the same slot must be ordered by the caller.
+ *   - Not thread-safe: one host thread per pool at a time.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,       /* NULL or out-of-range host argument */
+    GDN_ERR_POOL_FULL = -2,         /* no free slot */
+    GDN_ERR_BAD_SLOT = -3,          /* slot id out of range, or not in the state the call needs */
+    GDN_ERR_CUDA = -4,              /* a CUDA runtime call failed (allocation, launch, copy) */
+    GDN_ERR_TIMEOUT = -5,           /* a kernel's bounded wait ran out (device status bit) */
+    GDN_ERR_UNSUPPORTED_SHAPE = -6, /* the shape is valid but not built into this library */
+    GDN_ERR_NO_PARAMS = -7,         /* the layer's parameters were never registered */
+    GDN_ERR_DEVICE = -8             /* the device status word reports skipped work */
+} gdn_status;
+
+/* Bits of the device status word (see gdn_last_device_status). */
+#define GDN_DEV_BAD_SLOT_PTR 0x1u  /* a slot pointer was not a slot of the call's layer: item skipped */
+#define GDN_DEV_BAD_SLOT_ID 0x2u   /* gdn_slot_ptrs / prefill got a freed, repeated or out-of-range id */
+#define GDN_DEV_BAD_SEQLENS 0x4u   /* prefill cu_seqlens not 0-based, non-decreasing, ending at total */
+#define GDN_DEV_TIMEOUT 0x8u       /* a pipeline wait gave up (the kernel returned early) */
+
+typedef struct {
+    int hqk;        /* q/k heads */
+    int hv;         /* v heads; a multiple of hqk (GQA ratio r = hv / hqk) */
+    int dk, dv;     /* head dims; this build supports dk == dv in {16, 32, 64, 128} */
+    int conv_w;     /* causal conv taps W, 1..8 */
+    int chunk;      /* prefill chunk length (0 = 64); a performance parameter only */
+    int io_dtype;   /* q, k, v, z, a, b and the conv buffer: 0 = fp32, 1 = bf16 */
+    int out_dtype;  /* out: 0 = fp32, 1 = bf16 */
+    float l2_eps;   /* q, k L2 norm: x * rsqrt(sum x^2 + l2_eps) */
+    float norm_eps; /* gated RMSNorm: o * rsqrt(mean o^2 + norm_eps) */
+    int max_prefill_tokens; /* capacity of the pool's prefill workspace, in tokens (0 = no prefill) */
+} gdn_shape;
+
+typedef struct gdn_pool gdn_pool;
+
+/* Sizes and addresses of a pool (host-side facts, no GPU work). */
+typedef struct {
+    uint64_t base;        /* device address of slot 0, layer 0 */
+    uint64_t total_bytes; /* bytes of state memory */
+    uint64_t slot_bytes;  /* bytes of one (slot, layer): state then conv buffer, 256-B aligned */
+    uint64_t state_bytes; /* Hv * dv * dk * 4: fp32 S, head-major, rows indexed by dv */
+    uint64_t conv_bytes;  /* (W - 1) * C * io size, C = 2 Hqk dk + Hv dv, channels [q | k | v] */
+    int num_slots, num_layers, free_slots;
+    uint64_t workspace_bytes; /* prefill workspace owned by the pool */
+} gdn_pool_info;
+
+/* Create a pool of num_slots slots for num_layers GDN layers on the current
+ * CUDA device.  (slot, layer) lives at base + (slot * num_layers + layer) *
+ * slot_bytes and holds [S: Hv x dv x dk fp32 | conv buffer: (W-1) x C io].
+ * All slots start zeroed and free.  Allocates the state memory and the
+ * prefill workspace (cudaMalloc); *out receives the pool.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA (allocation failed). */
+int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_pool** out);
+
+/* Free the pool and everything it owns ("cleanup").  Waits for the device. */
+int gdn_pool_destroy(gdn_pool* pool);
+
+/* Mark every slot free and enqueue zeroing of all state memory on `stream` ("reset"). */
+int gdn_pool_reset(gdn_pool* pool, void* stream);
+
+/* Take a free slot ("add slot").  The slot is zero (S and conv buffer of every
+ * layer) once work already enqueued by recycle/reset on their streams has run.
+ * Errors: INVALID_ARG, POOL_FULL. */
+int gdn_slot_alloc(gdn_pool* pool, int* slot_id);
+
+/* Return a slot to the free list ("recycle slot") after enqueuing, on
+ * `stream`, the zeroing of its S and conv buffer in every layer, so that a
+ * later owner starts from a clean state (the slot-reuse contamination checks
+ * of the qLLM README, "Results").  Errors: INVALID_ARG, BAD_SLOT (free or out of range). */
+int gdn_slot_recycle(gdn_pool* pool, int slot_id, void* stream);
+
+/* Device address of (slot, layer) (host computation, no GPU work). */
+int gdn_slot_addr(gdn_pool* pool, int layer, int slot_id, uint64_t* addr);
+
+/* Enqueue on `stream` the gather out_dev[i] = address of (slot_ids_dev[i], layer),
+ * for i < m: the device u64 slot-pointer array of issue #5279 phase P5.  An id
+ * that is out of range or not allocated gives 0 and sets GDN_DEV_BAD_SLOT_ID.
+ * Errors: INVALID_ARG. */
+int gdn_slot_ptrs(gdn_pool* pool, int layer, const int* slot_ids_dev, int m, uint64_t* out_dev, void* stream);
+
+/* Register the parameters of one layer (device fp32 arrays, borrowed until
+ * replaced or the pool is destroyed): conv_w [C][W] (tap W-1 multiplies the
+ * current token), A_log [Hv], dt_bias [Hv], norm_w [dv] (shared by all heads).
+ * Errors: INVALID_ARG. */
+int gdn_layer_params(gdn_pool* pool, int layer, const float* conv_w, const float* A_log, const float* dt_bias,
+                     const float* norm_w);
+
+/* One decode step of `layer` for m sequences ("decode step"): row i of
+ * q_dev..z_dev is the current token of the sequence whose (slot, layer) state
+ * is at slot_ptrs_dev[i].  For each row: conv + SiLU against the slot's conv
+ * buffer (which then shifts by one token), L2 norms, gates, the delta-rule
+ * update of every v-head's S in place, the gated RMSNorm; out_dev[i] receives
+ * the result.  The slot pointers must be distinct.  Each row's result depends
+ * only on that row's inputs and state, never on m or the other rows.
+ * Errors: INVALID_ARG, NO_PARAMS, CUDA (launch). */
+int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, int m, const void* q_dev,
+                    const void* k_dev, const void* v_dev, const void* a_dev, const void* b_dev, const void* z_dev,
+                    void* out_dev, void* stream);
+
+/* Varlen prefill of `layer` ("setup+prefill"): n_seqs sequences packed along
+ * the token axis, sequence s owning rows [cu_seqlens_dev[s], cu_seqlens_dev[s+1])
+ * and slot slot_ids_dev[s].  Each sequence continues from its slot's current S
+ * and conv buffer (zero after alloc/recycle), so a prompt may be split across
+ * calls, and leaves its final S and conv buffer in the slot where
+ * gdn_decode_step reads them (the System Design page, "GDN Kernel Dispatch
+ * Detail": prefill, then "Update temporal_state").  total_tokens must equal
+ * cu_seqlens_dev[n_seqs] and not exceed the pool's max_prefill_tokens; slot
+ * ids must be allocated and distinct.  Uses the pool's workspace: calls on one
+ * pool must not overlap on the GPU.
+ * Errors: INVALID_ARG, NO_PARAMS, UNSUPPORTED_SHAPE (too many tokens), CUDA. */
+int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
+                       int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
+                       const void* b_dev, const void* z_dev, void* out_dev, void* stream);
+
+/* Synchronise `stream`, then read and clear the pool's device status word.
+ * Returns the GDN_DEV_* bits (>= 0), or CUDA / INVALID_ARG. */
+int gdn_last_device_status(gdn_pool* pool, void* stream);
+
+/* Host-side facts about the pool. */
+int gdn_pool_get_info(gdn_pool* pool, gdn_pool_info* info);
+
+/* Static text for a gdn_status code. */
+const char* gdn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,113 @@
+"""Slot pool behaviour on the GPU: allocation, recycling (zeroing), exhaustion, contamination."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_linear_rule_gb300 import binding, synth
+from gdn_harness import Layer, host
+
+pytestmark = pytest.mark.gpu
+
+
+def test_alloc_recycle_exhaustion():
+    L = Layer(3, 2, 2, 16, io="f32", num_slots=3)
+    p = L.pool
+    ids = [p.alloc() for _ in range(3)]
+    assert ids == [0, 1, 2]
+    with pytest.raises(binding.GdnError) as e:
+        p.alloc()
+    assert e.value.code == -2
+    p.recycle(1)
+    with pytest.raises(binding.GdnError) as e:
+        p.recycle(1)  # already free
+    assert e.value.code == -3
+    with pytest.raises(binding.GdnError) as e:
+        p.recycle(7)
+    assert e.value.code == -3
+    assert p.info().free_slots == 1
+    assert p.alloc() == 1
+    p.reset()
+    assert p.info().free_slots == 3 and p.alloc() == 0
+    L.close()
+
+
+def test_recycle_zeroes_every_layer_of_the_slot():
+    L = Layer(3, 2, 4, 32, io="bf16", num_slots=4, num_layers=3, layer_ids=(0, 1, 2), max_prefill_tokens=64)
+    a, b = L.pool.alloc(), L.pool.alloc()
+    for layer in range(3):
+        for s in (a, b):
+            Sv, Cv = L.pool.state_views(layer, s)
+            Sv.normal_()
+            Cv.normal_()
+    L.pool.recycle(a)
+    torch.cuda.synchronize()
+    for layer in range(3):
+        Sa, Ca = L.get_state(layer, a)
+        Sb, Cb = L.get_state(layer, b)
+        assert not Sa.any() and not Ca.any(), f"layer {layer} of the recycled slot is not zero"
+        assert Sb.any() and Cb.any(), "recycling one slot touched another"
+    L.close()
+
+
+def test_pool_sizes_match_the_layout():
+    L = Layer(2, 16, 32, 128, io="bf16", num_slots=4, num_layers=2, layer_ids=(0, 1))
+    inf = L.pool.info()
+    assert inf.state_bytes == 32 * 128 * 128 * 4
+    assert inf.conv_bytes == 3 * (2 * 16 * 128 + 32 * 128) * 2
+    assert inf.slot_bytes % 256 == 0 and inf.slot_bytes >= inf.state_bytes + inf.conv_bytes
+    assert L.pool.slot_addr(1, 2) - L.pool.slot_addr(0, 0) == (2 * 2 + 1) * inf.slot_bytes
+    L.close()
+
+
+def test_contamination_reused_slots_equal_isolated_runs():
+    """Mixed batch with slot reuse (a small version of the 512-slot continuous-batching workload): each
+    iteration finishes some sequences (recycle), admits new prefills into the freed slots and decodes every
+    active slot.  Every admitted sequence's outputs equal an isolated run of the same sequence in a fresh
+    pool, bit for bit."""
+    hqk, hv, d = 2, 4, 64
+    plen = 40
+    L = Layer(4, hqk, hv, d, io="bf16", num_slots=6, max_prefill_tokens=2 * plen)
+    rng = synth.rng(4)
+    active = {}  # slot -> (sequence id, decode steps done)
+    record = {}  # sequence id -> list of output rows (prefill block, then decode rows)
+    next_id = 0
+    for it in range(6):
+        if len(active) >= 4:
+            for s in rng.choice(sorted(active), size=2, replace=False):
+                del active[int(s)]
+                L.pool.recycle(int(s))
+        new = []
+        while len(active) + len(new) < 6 and len(new) < 2:
+            new.append((L.pool.alloc(), next_id))
+            next_id += 1
+        if new:
+            parts = [synth.token_inputs(4, 0, sid, plen, hqk, hv, d, d, "bf16") for _, sid in new]
+            inp = {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
+            cu = np.arange(len(new) + 1) * plen
+            out = host(L.gpu_prefill(0, [s for s, _ in new], inp, cu))
+            for j, (s, sid) in enumerate(new):
+                active[s] = (sid, 0)
+                record[sid] = [out[j * plen:(j + 1) * plen]]
+        slots = sorted(active)
+        dinp = [synth.token_inputs(4, 0, active[s][0], 1, hqk, hv, d, d, "bf16", tag="decode", sub=active[s][1])
+                for s in slots]
+        inp = {k: np.concatenate([p[k] for p in dinp]) for k in dinp[0]}
+        out = host(L.gpu_decode(0, slots, inp))
+        for j, s in enumerate(slots):
+            sid, n = active[s]
+            record[sid].append(out[j:j + 1])
+            active[s] = (sid, n + 1)
+    assert L.pool.device_status() == 0
+    L.close()
+    # isolated runs: a fresh pool per sequence, same kernels at n = 1 / m = 1
+    for sid, rows in record.items():
+        I = Layer(4, hqk, hv, d, io="bf16", num_slots=1, max_prefill_tokens=plen)
+        s = I.pool.alloc()
+        inp = synth.token_inputs(4, 0, sid, plen, hqk, hv, d, d, "bf16")
+        got = [host(I.gpu_prefill(0, [s], inp, [0, plen]))]
+        for step in range(len(rows) - 1):
+            dinp = synth.token_inputs(4, 0, sid, 1, hqk, hv, d, d, "bf16", tag="decode", sub=step)
+            got.append(host(I.gpu_decode(0, [s], dinp)))
+        for a, b in zip(got, rows):
+            assert np.array_equal(a, b), f"sequence {sid} differs from its isolated run"
+        I.close()

@@ -1,0 +1,127 @@
+"""GPU parity of the varlen prefill against the fp64 oracle, and its hand-off to decode."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_linear_rule_gb300 import synth
+from gdn_harness import DECODE_TOL, PREFILL_TOL, Layer, check_out, host, relerr
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill_then_decode(L, lengths, decode_steps, tol_p, sample_heads=None, S_init=None):
+    n = len(lengths)
+    slots = [L.pool.alloc() for _ in range(n)]
+    inp, cu = synth.varlen_inputs(L.workload, 0, lengths, L.hqk, L.hv, L.d, L.d, L.io)
+    S0 = np.zeros((n, L.hv, L.d, L.d)) if S_init is None else S_init
+    if S_init is not None:
+        for s, Si in zip(slots, S_init):
+            L.set_state(0, s, Si)
+    conv0 = np.zeros((n, L.W - 1, L.C))
+    out = host(L.gpu_prefill(0, slots, inp, cu))
+    mask = None
+    if sample_heads is not None:
+        mask = np.zeros(L.hv, dtype=np.int32)
+        mask[sample_heads] = 1
+    ref = L.oracle_run(0, cu, inp, S0, conv0, head_mask=mask)
+    cols = np.concatenate([np.arange(h * L.d, (h + 1) * L.d) for h in (sample_heads or range(L.hv))])
+    check_out(out[:, cols], ref["out"][:, cols], L.out, tol_p, "prefill out")
+    heads = list(sample_heads or range(L.hv))
+    for j, s in enumerate(slots):
+        Sg, Cg = L.get_state(0, s)
+        if lengths[j] > 0:
+            r = relerr(Sg[heads], ref["S"][j][heads])
+            assert r <= tol_p, f"prefill final S seq {j} (len {lengths[j]}): {r:.3e}"
+        assert np.array_equal(Cg, ref["convbuf"][j]), f"conv buffer seq {j}"
+    S, conv = ref["S"], ref["convbuf"]
+    for step in range(decode_steps):
+        dinp = L.decode_inputs(list(range(n)), step)
+        o = host(L.gpu_decode(0, slots, dinp))
+        r = L.oracle_run(0, np.arange(n + 1), dinp, S, conv, head_mask=mask)
+        S, conv = r["S"], r["convbuf"]
+        check_out(o[:, cols], r["out"][:, cols], L.out, tol_p, f"decode after prefill step {step}")
+    assert L.pool.device_status() == 0
+    return slots
+
+
+def test_prefill_tiny_fp32():
+    """2 sequences of 32 tokens, 2 q/k and 2 v heads, d = 16, chunk 8, then 8 decode steps (fp32)."""
+    L = Layer(1, 2, 2, 16, io="f32", num_slots=4, chunk=8, max_prefill_tokens=64)
+    _prefill_then_decode(L, [32, 32], 8, 2e-5)
+    L.close()
+
+
+def test_prefill_ragged_small_fp32():
+    """Ragged and empty sequences, lengths shorter than the conv window, GQA ratio 2, d = 32."""
+    L = Layer(4, 2, 4, 32, io="f32", num_slots=8, max_prefill_tokens=512)
+    _prefill_then_decode(L, [1, 0, 2, 3, 17, 70, 130], 3, 2e-5)
+    L.close()
+
+
+def test_prefill_from_nonzero_state_and_split_calls():
+    """Prefill continues from the slot's state: one call over L tokens equals two calls over the halves."""
+    L = Layer(5, 2, 4, 64, io="bf16", out="f32", num_slots=4, max_prefill_tokens=256)
+    a, b = L.pool.alloc(), L.pool.alloc()
+    inp, cu = synth.varlen_inputs(5, 0, [90], 2, 4, 64, 64, "bf16")
+    S0 = synth.initial_state(5, 0, 0, 4, 64, 64)
+    L.set_state(0, a, S0)
+    L.set_state(0, b, S0)
+    whole = host(L.gpu_prefill(0, [a], inp, cu))
+    first = {k: v[:37] for k, v in inp.items()}
+    second = {k: v[37:] for k, v in inp.items()}
+    o1 = host(L.gpu_prefill(0, [b], first, [0, 37]))
+    o2 = host(L.gpu_prefill(0, [b], second, [0, 53]))
+    assert relerr(np.concatenate([o1, o2]), whole) <= PREFILL_TOL
+    Sa, Ca = L.get_state(0, a)
+    Sb, Cb = L.get_state(0, b)
+    assert relerr(Sb, Sa) <= PREFILL_TOL and np.array_equal(Ca, Cb)
+    ref = L.oracle_run(0, cu, inp, S0[None].astype(np.float64), np.zeros((1, 3, L.C)))
+    check_out(whole, ref["out"], "f32", PREFILL_TOL, "prefill from a random state")
+    L.close()
+
+
+def test_prefill_cfg3_ragged_8_sequences():
+    """Lengths {1,17,300,4095,1024,2048,513,8000} (15 998 tokens), 16/32 heads, d = 128, chunk 64, bf16 io,
+    zero initial state; final states handed to 16 decode steps.  The oracle computes 4 sampled v-heads
+    (covering both v-heads of one q/k head and the last head)."""
+    lengths = [1, 17, 300, 4095, 1024, 2048, 513, 8000]
+    L = Layer(3, 16, 32, 128, io="bf16", out="bf16", num_slots=16, max_prefill_tokens=sum(lengths))
+    _prefill_then_decode(L, lengths, 16, PREFILL_TOL, sample_heads=[0, 1, 17, 31])
+    L.close()
+
+
+def test_prefill_batch_equals_sequences_alone_bitwise():
+    """A sequence prefilled inside a varlen batch equals the same sequence prefilled alone, bit for bit."""
+    lengths = [5, 300, 64, 129]
+    L = Layer(6, 4, 8, 128, io="bf16", num_slots=8, max_prefill_tokens=sum(lengths))
+    inp, cu = synth.varlen_inputs(6, 0, lengths, 4, 8, 128, 128, "bf16")
+    slots = [L.pool.alloc() for _ in lengths]
+    out_b = L.gpu_prefill(0, slots, inp, cu).clone()
+    states = [L.get_state(0, s) for s in slots]
+    for j, s in enumerate(slots):
+        L.pool.recycle(s)
+        assert L.pool.alloc() == s
+        part = {k: v[cu[j]:cu[j + 1]] for k, v in inp.items()}
+        o = L.gpu_prefill(0, [s], part, [0, lengths[j]])
+        assert torch.equal(o, out_b[cu[j]:cu[j + 1]]), f"sequence {j} output differs"
+        Sg, Cg = L.get_state(0, s)
+        assert np.array_equal(Sg, states[j][0]) and np.array_equal(Cg, states[j][1])
+    L.close()
+
+
+def test_prefill_rejects_bad_metadata_on_device():
+    """Non-monotone cu_seqlens or a repeated / freed slot id: nothing is written, a status bit is set."""
+    L = Layer(3, 2, 2, 16, io="f32", num_slots=4, max_prefill_tokens=64)
+    a, b = L.pool.alloc(), L.pool.alloc()
+    inp, _ = synth.varlen_inputs(3, 0, [6, 4], 2, 2, 16, 16, "f32")
+    d = L.to_dev(inp)
+    res = torch.full((10, 32), 3.0, device="cuda")
+    for cu, ids, bit in (([0, 7, 6], [a, b], 0x4), ([0, 6, 10], [a, a], 0x2), ([0, 6, 10], [a, 3], 0x2)):
+        L.pool.prefill_varlen(0, torch.tensor(cu, dtype=torch.int32, device="cuda"),
+                              torch.tensor(ids, dtype=torch.int32, device="cuda"), 2, 10,
+                              d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], res)
+        assert L.pool.device_status() & bit
+        assert torch.all(res == 3.0)
+        Sa, Ca = L.get_state(0, a)
+        assert not Sa.any() and not Ca.any()
+    L.close()
