@@ -79,6 +79,45 @@ def prefill_bytes(lengths, io=2):
     return T * per_tok + len(lengths) * per_seq + decode_param_bytes()
 
 
+# ------------------------------------------------------- profiled traffic ----
+
+DECODE_SOURCES = ["gated_deltanet_linear_rule_gb300/csrc/gdn_decode.cu",
+                  "gated_deltanet_linear_rule_gb300/csrc/gdn_internal.cuh"]
+
+
+def sources_sha256(paths):
+    import hashlib
+
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, sources, units: float):
+    """DRAM bytes per launch from a committed ncu summary (profiles/*.md) of this kernel, scaled from the
+    captured launch's units to `units`; None when no summary matches the current source hash."""
+    want = sources_sha256(sources)
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        meta = {}
+        for line in open(os.path.join(pdir, name)):
+            if line.startswith("    ") and ":" in line:
+                k, v = line.strip().split(":", 1)
+                meta[k.strip()] = v.strip()
+        if meta.get("kernel") == kernel and meta.get("source_sha256") == want:
+            try:
+                return float(meta["dram_bytes_per_launch"]) * units / float(meta["units_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
 # -------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -97,7 +136,7 @@ class ClockSampler:
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
             os.close(fd)
-            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
             if self.uuid:
                 cmd += ["-i", self.uuid]
             self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
@@ -173,27 +212,19 @@ def make_decode_pool(torch, binding, synth, out_dtype="bf16"):
         pool.alloc()
     g = torch.Generator(device="cuda")
     g.manual_seed(20260)
-    for s in range(NUM_SLOTS):
-        Sv, _ = pool.state_views(0, s)
-        Sv.copy_(torch.randn(Sv.shape, generator=g, device="cuda") * math.sqrt(0.1))
+    block = pool.state_block(0)
+    block.copy_(torch.randn(block.shape, generator=g, device="cuda") * math.sqrt(0.1))
     torch.cuda.synchronize()
     return pool
 
 
 def device_inputs(torch, m, n_sets, seed):
+    """n_sets distinct input sets of m rows, N(0, 1) rounded to bf16 (one draw per tensor kind)."""
     g = torch.Generator(device="cuda")
     g.manual_seed(seed)
-    sets = []
-    for _ in range(n_sets):
-        sets.append({
-            "q": torch.randn((m, HQK * D), generator=g, device="cuda").to(torch.bfloat16),
-            "k": torch.randn((m, HQK * D), generator=g, device="cuda").to(torch.bfloat16),
-            "v": torch.randn((m, HV * D), generator=g, device="cuda").to(torch.bfloat16),
-            "z": torch.randn((m, HV * D), generator=g, device="cuda").to(torch.bfloat16),
-            "a": torch.randn((m, HV), generator=g, device="cuda").to(torch.bfloat16),
-            "b": torch.randn((m, HV), generator=g, device="cuda").to(torch.bfloat16),
-        })
-    return sets
+    widths = {"q": HQK * D, "k": HQK * D, "v": HV * D, "z": HV * D, "a": HV, "b": HV}
+    full = {n: torch.randn((n_sets, m, w), generator=g, device="cuda").to(torch.bfloat16) for n, w in widths.items()}
+    return [{n: full[n][i] for n in widths} for i in range(n_sets)]
 
 
 def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
@@ -211,6 +242,7 @@ def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push(f"decode_timed_m{m}")
     t0.record(stream)
     for i in range(steps):
         s = sets[(warmup + i) % n_sets]
@@ -219,6 +251,7 @@ def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     per = [a.elapsed_time(b) for a, b in ev]
     assert pool.device_status() == 0
     return t0.elapsed_time(t1) / steps, statistics.mean(per), statistics.median(per)
@@ -249,11 +282,13 @@ def time_decode_e2e(torch, pool, synth, m, steps, warmup):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("e2e_timed")
     t0.record(stream)
     for i in range(steps):
         step(warmup + i)
     t1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     ms = t0.elapsed_time(t1) / steps
     return m / (ms * 1e-3), h2d, d2h
 
@@ -291,10 +326,12 @@ def time_prefill(torch, binding, synth, steps, warmup):
             pool.alloc()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("prefill_timed")
         a.record(stream)
         call()
         b.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         times.append(a.elapsed_time(b))
     assert pool.device_status() == 0
     pool.close()
@@ -325,7 +362,7 @@ def cpu_baseline_decode(seconds=10.0, m_sample=16):
         done += m_sample
         S, conv = r["S"], r["convbuf"]
         step += 1
-        if time.perf_counter() - t0 >= seconds or step >= 200:
+        if time.perf_counter() - t0 >= seconds:
             break
         del ts
     el = time.perf_counter() - t0
@@ -374,7 +411,8 @@ def run_ours(args):
     ach = algo / (kern_mean * 1e-3) / 1e9
     result["roofline"] = {"kernel": "decode_kernel<128,bf16,bf16>", "bound": "hbm", "achieved": ach, "peak": hbm,
                           "unit": "GB/s", "frac": ach / hbm, "peak_kind": peak_kind,
-                          "frac_of_8TBs": ach / 8000.0, "traffic": None,
+                          "frac_of_8TBs": ach / 8000.0,
+                          "traffic": profiled_traffic("decode_kernel<128,bf16,bf16>", DECODE_SOURCES, M_HEAD),
                           "bytes_per_launch": algo, "launch_ms": kern_mean}
     if ck:
         result["clocks"] = {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
@@ -382,13 +420,13 @@ def run_ours(args):
     if rank == 0 and not args.no_sweep:
         sweep = []
         for m in SWEEP:
-            sm, km, _ = time_decode(torch, pool, synth, m, max(10, args.steps), 3, seed=100 + m)
+            sm, km, _ = time_decode(torch, pool, synth, m, max(10, min(args.steps, 500)), 3, seed=100 + m)
             b = m * decode_bytes_per_slot_step() + decode_param_bytes()
             sweep.append({"m": m, "slot_steps_per_s": m / (sm * 1e-3), "us_per_step": sm * 1e3,
                           "gbs": b / (km * 1e-3) / 1e9, "frac": b / (km * 1e-3) / 1e9 / hbm})
         result["decode_sweep"] = sweep
     if rank == 0:
-        e2e, h2d, d2h = time_decode_e2e(torch, pool, synth, M_HEAD, args.steps, args.warmup)
+        e2e, h2d, d2h = time_decode_e2e(torch, pool, synth, M_HEAD, min(args.steps, 2000), args.warmup)
         result["e2e"] = {"value": e2e * world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     pool.close()
     if rank == 0 and not args.no_prefill:
@@ -455,7 +493,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")

@@ -208,6 +208,15 @@ class Pool:
             conv = torch.as_tensor(_DevView(base + inf.state_bytes, (W1, self.C), "<f4"), device="cuda")
         return S, conv
 
+    def state_block(self, layer: int):
+        """Strided fp32 view [num_slots][Hv][dv][dk] over the S of every slot of one layer."""
+        inf = self.info()
+        base = self.slot_addr(layer, 0)
+        slot_stride = inf.slot_bytes * self.num_layers
+        view = _DevView(base, (self.num_slots, self.hv, self.dv, self.dk), "<f4")
+        view.__cuda_array_interface__["strides"] = (slot_stride, self.dv * self.dk * 4, self.dk * 4, 4)
+        return torch.as_tensor(view, device="cuda")
+
     # -- layer -------------------------------------------------------------
     def layer_params(self, layer: int, conv_w, A_log, dt_bias, norm_w):
         ts = [t.contiguous().to(device="cuda", dtype=torch.float32) for t in (conv_w, A_log, dt_bias, norm_w)]
