@@ -29,6 +29,7 @@ EXPORTS = [
     "gdn_pool_create", "gdn_pool_destroy", "gdn_pool_reset", "gdn_slot_alloc", "gdn_slot_recycle",
     "gdn_slot_addr", "gdn_slot_ptrs", "gdn_layer_params", "gdn_decode_step", "gdn_prefill_varlen",
     "gdn_last_device_status", "gdn_pool_get_info", "gdn_status_string", "gdn_version",
+    "gdn_prefill_varlen_noalloc",
 ]
 
 
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_varlen.argtypes = [vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gdn_last_device_status.argtypes = [vp, vp]
         L.gdn_pool_get_info.argtypes = [vp, ctypes.POINTER(GdnPoolInfo)]
+        L.gdn_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(GdnShape), vp, vp, vp, vp, vp, i, vp, vp, i, i,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gdn_status_string.argtypes = [i]
         L.gdn_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -235,6 +238,24 @@ class Pool:
 
     def device_status(self, stream=None) -> int:
         return _check(lib().gdn_last_device_status(self._h, _stream(stream)), "gdn_last_device_status")
+
+
+def slot_bytes(hqk: int, hv: int, dk: int, dv: int, conv_w: int = 4, io_dtype: str = "bf16") -> int:
+    """Bytes of one slot (fp32 S then the conv buffer, rounded up to 256), as a pool lays it out."""
+    io = 2 if io_dtype == "bf16" else 4
+    raw = hv * dv * dk * 4 + (conv_w - 1) * (2 * hqk * dk + hv * dv) * io
+    return (raw + 255) // 256 * 256
+
+
+def prefill_varlen_noalloc(shape: GdnShape, conv_w, A_log, dt_bias, norm_w, states, num_slots: int, cu_seqlens,
+                           slot_ids, n_seqs: int, total_tokens: int, q, k, v, a, b, z, out, status=None,
+                           stream=None):
+    """gdn_prefill_varlen_noalloc: the prefill kernels on caller-owned slots, with the library's static
+    scratch instead of a pool workspace (no device allocation inside the call)."""
+    _check(lib().gdn_prefill_varlen_noalloc(ctypes.byref(shape), _p(conv_w), _p(A_log), _p(dt_bias), _p(norm_w),
+                                            _p(states), int(num_slots), _p(cu_seqlens), _p(slot_ids), int(n_seqs),
+                                            int(total_tokens), _p(q), _p(k), _p(v), _p(a), _p(b), _p(z), _p(out),
+                                            _p(status), _stream(stream)), "gdn_prefill_varlen_noalloc")
 
 
 def version() -> int:

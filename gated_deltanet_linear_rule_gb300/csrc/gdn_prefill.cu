@@ -357,3 +357,137 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
 }
 
 }  // namespace gdn
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free varlen prefill.
+//
+// For callers that cannot call cudaMalloc (for example code running where the device heap
+// belongs to someone else, or inside a region that must not allocate), this entry point
+// runs the same prefill kernels as gdn_prefill_varlen, but takes the scratch it needs
+// from one fixed static device array instead of a pool's workspace, and takes the state
+// slots from memory the caller already owns.  It allocates nothing.
+namespace gdn {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB, held by every GPU that loads libgdn
+
+// Host code must not use this name as a device address: the address comes from
+// cudaGetSymbolAddress, once per device (see static_scratch_address).
+static __device__ __align__(256) unsigned char g_prefill_scratch[kStaticScratchBytes];
+
+__global__ void fill_ones_kernel(unsigned char* p, int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 1;
+}
+
+std::mutex g_scratch_mu;
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_prefill_scratch on the current device, looked up on the first call per device.
+cudaError_t static_scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace gdn
+
+extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, const float* A_log,
+                                          const float* dt_bias, const float* norm_w, void* states_dev, int num_slots,
+                                          const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
+                                          int total_tokens, const void* q, const void* k, const void* v,
+                                          const void* a, const void* b, const void* z, void* out,
+                                          unsigned int* status_dev, void* stream)
+{
+    using namespace gdn;
+    if (!shape || !conv_w || !A_log || !dt_bias || !norm_w || !states_dev || num_slots <= 0) return GDN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(states_dev) % 256 != 0) return GDN_ERR_INVALID_ARG;
+    if (n_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+    if (n_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens_dev || !slot_ids_dev) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
+    const gdn_shape& s = *shape;
+    if (s.hqk <= 0 || s.hv <= 0 || s.hv % s.hqk != 0 || s.conv_w < 1 || s.conv_w > 8) return GDN_ERR_INVALID_ARG;
+    if (s.io_dtype < 0 || s.io_dtype > 1 || s.out_dtype < 0 || s.out_dtype > 1) return GDN_ERR_INVALID_ARG;
+    if (!(s.l2_eps >= 0.0f) || !(s.norm_eps >= 0.0f)) return GDN_ERR_INVALID_ARG;
+    if (s.dk != s.dv || (s.dk != 16 && s.dk != 32 && s.dk != 64 && s.dk != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
+
+    // everything the call needs must fit in the static scratch: workspace, live flags, status word
+    const size_t ws_bytes = prefill_workspace_bytes(s, total_tokens);
+    const size_t live_bytes = align256((size_t)num_slots);
+    if (ws_bytes + live_bytes + 256 > kStaticScratchBytes) return GDN_ERR_UNSUPPORTED_SHAPE;
+
+    void* scratch = nullptr;
+    if (static_scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
+    PrefillWorkspace ws;
+    ws.base = scratch;
+    ws.bytes = ws_bytes;
+    prefill_workspace_carve(ws, s, total_tokens);
+    unsigned char* live = static_cast<unsigned char*>(scratch) + ws_bytes;
+    unsigned int* status = status_dev ? status_dev : reinterpret_cast<unsigned int*>(live + live_bytes);
+
+    const int C = 2 * s.hqk * s.dk + s.hv * s.dv;
+    const int io_size = s.io_dtype == 1 ? 2 : 4;
+    const size_t state_bytes = (size_t)s.hv * s.dv * s.dk * sizeof(float);
+    const size_t slot_bytes = (state_bytes + (size_t)(s.conv_w - 1) * C * io_size + 255) / 256 * 256;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    fill_ones_kernel<<<(num_slots + 255) / 256, 256, 0, st>>>(live, num_slots);
+
+    PrefillArgs A;
+    A.cu = cu_seqlens_dev;
+    A.ids = slot_ids_dev;
+    A.n = n_seqs;
+    A.T = total_tokens;
+    A.q = q;
+    A.k = k;
+    A.v = v;
+    A.a = a;
+    A.b = b;
+    A.z = z;
+    A.out = out;
+    A.conv_w = conv_w;
+    A.A_log = A_log;
+    A.dt_bias = dt_bias;
+    A.norm_w = norm_w;
+    A.base = static_cast<char*>(states_dev);
+    A.slot_bytes = slot_bytes;
+    A.state_bytes = (uint32_t)state_bytes;
+    A.num_layers = 1;
+    A.layer = 0;
+    A.num_slots = num_slots;
+    A.live = live;
+    A.status = status;
+    A.hqk = s.hqk;
+    A.hv = s.hv;
+    A.r = s.hv / s.hqk;
+    A.D = s.dk;
+    A.W = s.conv_w;
+    A.C = C;
+    A.l2_eps = s.l2_eps;
+    A.norm_eps = s.norm_eps;
+    A.ws = ws;
+    A.kq = ws.kq;
+    cudaError_t e;
+    const bool in_bf16 = s.io_dtype == 1, out_bf16 = s.out_dtype == 1;
+    if (in_bf16 && out_bf16) e = run<__nv_bfloat16, __nv_bfloat16>(A, st);
+    else if (in_bf16) e = run<__nv_bfloat16, float>(A, st);
+    else if (out_bf16) e = run<float, __nv_bfloat16>(A, st);
+    else e = run<float, float>(A, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+

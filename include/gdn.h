@@ -166,6 +166,35 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);
 
+/* Allocation-free varlen prefill.  The pages have no counterpart of this call; it
+ * exists for callers that cannot call cudaMalloc -- code that runs where device memory
+ * is owned and budgeted by someone else, or in a phase that must not allocate -- and so
+ * cannot create a pool or its workspace.  It runs the same kernels as
+ * gdn_prefill_varlen and allocates nothing: its scratch is one static device array of
+ * 32 MiB inside libgdn (held by every GPU that loads the library until the process
+ * exits), and the state slots are memory the caller owns.
+ *   shape         as for gdn_pool_create (max_prefill_tokens is ignored).
+ *   conv_w, A_log, dt_bias, norm_w   the layer's device parameters (as gdn_layer_params).
+ *   states_dev    num_slots slots laid out like one layer of a pool: slot i at
+ *                 states_dev + i * slot_bytes, slot_bytes = the 256-rounded sum of
+ *                 Hv*dv*dk*4 (fp32 S) and (W-1)*C*io_size (conv buffer); 256-B aligned.
+ *   cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, q..z, out   as for gdn_prefill_varlen
+ *                 (every slot id below num_slots counts as allocated).
+ *   status_dev    a device word receiving GDN_DEV_* bits (OR-ed in), or NULL to drop them.
+ * The scratch is shared by every call and keeps the last call's contents; every value the
+ * kernels read from it is written earlier in the same call, so nothing needs clearing, but
+ * calls that overlap on the GPU (on different streams, or from different host threads)
+ * race on it.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Errors: INVALID_ARG; UNSUPPORTED_SHAPE when the shape is not built or the call needs more
+ * than the 32 MiB of scratch (about 49.5 KB per token at Hqk 16, Hv 32, d 128: split longer
+ * prompts into several calls, which continue from the slots' state); CUDA. */
+int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, const float* A_log, const float* dt_bias,
+                               const float* norm_w, void* states_dev, int num_slots, const int* cu_seqlens_dev,
+                               const int* slot_ids_dev, int n_seqs, int total_tokens, const void* q_dev,
+                               const void* k_dev, const void* v_dev, const void* a_dev, const void* b_dev,
+                               const void* z_dev, void* out_dev, unsigned int* status_dev, void* stream);
+
 /* Synchronise `stream`, then read and clear the pool's device status word.
  * Returns the GDN_DEV_* bits (>= 0), or CUDA / INVALID_ARG. */
 int gdn_last_device_status(gdn_pool* pool, void* stream);
