@@ -58,7 +58,7 @@ size_t decode_smem_bytes(int D, int r)
 }
 
 template <int D, typename TIn, typename TOut>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs A)
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
 {
     constexpr int LPR = D / 16;    // lanes per S row (16 columns per lane)
     constexpr int RPW = 32 / LPR;  // rows per warp per stage
