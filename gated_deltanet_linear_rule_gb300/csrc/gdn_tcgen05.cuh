@@ -1,0 +1,169 @@
+// gdn_tcgen05.cuh -- 5th-generation tensor-core (tcgen05 / TMEM) helpers, written from the PTX ISA.
+//
+// Operand tiles are bf16, K-major, in the 128-byte swizzle layout: a tile holds R rows
+// (the M or N index) of 64 K-elements (128 B per row); rows are grouped by 8 into 1024-B
+// atoms, and inside an atom the 16-B chunk c of row r sits at chunk position c ^ (r % 8).
+// A K extent of 128 is two such tiles side by side in memory (k 0..63, then 64..127).
+// Tile bases are 1024-B aligned.  Accumulators are fp32 in tensor memory: for M = 128
+// (cta_group::1) row i of D is TMEM lane i and column j is TMEM column j.
+#pragma once
+
+#include <stdint.h>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace tc {
+
+// byte offset of element (r, k), k < 64, inside a swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int k)
+{
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ r) & 7) << 4) + (k & 7) * 2);
+}
+
+// byte offset of the 16-B chunk holding elements (r, 8c .. 8c+7)
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int c)
+{
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((c ^ r) & 7) << 4));
+}
+
+// Shared-memory matrix descriptor of a swizzled K-major tile starting at shared address saddr
+// (saddr may be advanced by 32 B steps inside an atom to select K = 16 slices).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address, 16-B units
+    d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset: 8-row groups 1024 B apart
+    d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 slice; issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// K = 16 * ksteps GEMM slice loop over operands of K extent 64 * ktiles (each K tile is
+// R rows * 128 B; a_rows / b_rows give the tile pitch of A and B in rows).
+__device__ __forceinline__ void mma_bf16_k(uint32_t d_tmem, uint32_t a_saddr, int a_rows, uint32_t b_saddr,
+                                           int b_rows, int kdim, uint32_t idesc, uint32_t accumulate)
+{
+    for (int k16 = 0; k16 < kdim / 16; ++k16) {
+        const int kt = k16 >> 2, kin = (k16 & 3) * 32;
+        const uint64_t a = sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
+        const uint64_t b = sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
+        mma_bf16(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
+    }
+}
+
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// One full warp: allocate ncols (power of two >= 32) TMEM columns; the base address lands in *dst.
+__device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// generic-proxy shared-memory writes -> visible to the tensor cores (async proxy)
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4) .. +31).
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+// TMEM address of (lane quarter of this warp, column col) relative to the allocation base
+__device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, int col)
+{
+    return base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)col;
+}
+
+// pack two floats into a bf16x2 word (round to nearest even), low half = first
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// store 8 bf16 values (row r, elements 8c .. 8c+7) of a swizzled tile as one 16-B chunk
+__device__ __forceinline__ void st_chunk(unsigned char* tile, int r, int c, const float* v8)
+{
+    uint4 w;
+    w.x = pack_bf16(v8[0], v8[1]);
+    w.y = pack_bf16(v8[2], v8[3]);
+    w.z = pack_bf16(v8[4], v8[5]);
+    w.w = pack_bf16(v8[6], v8[7]);
+    *reinterpret_cast<uint4*>(tile + sw128_chunk(r, c)) = w;
+}
+
+// store one bf16 element (r, k) of a swizzled tile
+__device__ __forceinline__ void st_elem(unsigned char* tile, int r, int k, float v)
+{
+    *reinterpret_cast<__nv_bfloat16*>(tile + sw128(r, k)) = __float2bfloat16_rn(v);
+}
+
+}  // namespace tc
+}  // namespace gdn
