@@ -31,6 +31,7 @@ struct PrefillWorkspace {
     float* beta = nullptr;   // [T][Hv]
     float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm
     float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat
+    int* order = nullptr;    // [T + 64] sequences ranked by length, longest first
     int* valid = nullptr;    // [1] 1 when the call's cu_seqlens / slot ids passed validation
     void* base = nullptr;
     size_t bytes = 0;
@@ -49,6 +50,26 @@ struct Pool {
     std::vector<LayerParams> params;
     PrefillWorkspace ws;
     int device = 0, num_sms = 0;
+};
+
+// Everything the prefill kernels of one call need (device pointers and sizes).
+struct PrefillArgs {
+    const int* cu;
+    const int* ids;
+    int n, T;
+    const void *q, *k, *v, *a, *b, *z;
+    void* out;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    char* base;
+    uint64_t slot_bytes;
+    uint32_t state_bytes;
+    int num_layers, layer, num_slots;
+    const unsigned char* live;
+    unsigned int* status;
+    int hqk, hv, r, D, W, C;
+    float l2_eps, norm_eps;
+    PrefillWorkspace ws;
+    float* kq;  // [T][Hqk] k_hat . q_hat (workspace)
 };
 
 // Facts every kernel needs to check a slot pointer before touching memory.
@@ -253,6 +274,12 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
                            const void* b, const void* z, void* out, cudaStream_t st);
 
 size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens);
+// sequences a call may carry for a workspace of max_tokens tokens
+inline int prefill_max_seqs(int max_tokens) { return max_tokens + 64; }
+
+// chunked tensor-core prefill of the delta rule + gated RMSNorm (d_k = d_v = 128); io dtypes
+template <typename TIn, typename TOut>
+cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st);
 void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens);
 
 inline SlotCheck slot_check(const Pool& P, int layer)

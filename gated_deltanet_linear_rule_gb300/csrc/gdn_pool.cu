@@ -257,6 +257,7 @@ int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const 
     if (total_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
     if (!P->params[(size_t)layer].set()) return GDN_ERR_NO_PARAMS;
     if (total_tokens > P->shape.max_prefill_tokens) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (n_seqs > gdn::prefill_max_seqs(P->shape.max_prefill_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
     cudaError_t e = gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, q, k, v, a,
                                         b, z, out, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

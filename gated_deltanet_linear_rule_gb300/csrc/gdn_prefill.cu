@@ -26,25 +26,6 @@ namespace gdn {
 
 namespace {
 
-struct PrefillArgs {
-    const int* cu;
-    const int* ids;
-    int n, T;
-    const void *q, *k, *v, *a, *b, *z;
-    void* out;
-    const float *conv_w, *A_log, *dt_bias, *norm_w;
-    char* base;
-    uint64_t slot_bytes;
-    uint32_t state_bytes;
-    int num_layers, layer, num_slots;
-    const unsigned char* live;
-    unsigned int* status;
-    int hqk, hv, r, D, W, C;
-    float l2_eps, norm_eps;
-    PrefillWorkspace ws;
-    float* kq;  // [T][Hqk] k.q before the L2 scales (workspace)
-};
-
 __global__ void validate_kernel(PrefillArgs A)
 {
     __shared__ int bad;
@@ -57,6 +38,14 @@ __global__ void validate_kernel(PrefillArgs A)
         bool ok = id >= 0 && id < A.num_slots && A.live[id];
         for (int j = 0; ok && j < s; ++j) ok = A.ids[j] != id;
         if (!ok) atomicOr(&bad, 2);
+        // rank by length, longest first (ties by index): long sequences start in the first wave
+        const int len = A.cu[s + 1] - A.cu[s];
+        int rank = 0;
+        for (int j = 0; j < A.n; ++j) {
+            const int lj = A.cu[j + 1] - A.cu[j];
+            rank += (lj > len) || (lj == len && j < s);
+        }
+        A.ws.order[rank] = s;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -259,6 +248,11 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
         prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
     }
     conv_tail_kernel<TIn><<<A.n, 256, 0, st>>>(A);
+    if (A.T > 0 && A.D == 128) {
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_chunk<TIn, TOut>(A, st);
+    }
     if (A.T > 0) {
         const int rows = std::min(A.D, 8 * (32 / (A.D / 16)));
         dim3 grid(A.n, A.hv, A.D / rows);
@@ -266,7 +260,6 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
             case 16: recurrent_kernel<16><<<grid, 256, 0, st>>>(A); break;
             case 32: recurrent_kernel<32><<<grid, 256, 0, st>>>(A); break;
             case 64: recurrent_kernel<64><<<grid, 256, 0, st>>>(A); break;
-            case 128: recurrent_kernel<128><<<grid, 256, 0, st>>>(A); break;
             default: return cudaErrorInvalidValue;
         }
         const int pairs = A.T * A.hv;
@@ -287,6 +280,7 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T)
     b += align256((size_t)T * Dv * 4) * 2;            // vc, o
     b += align256((size_t)T * s.hv * 4) * 2;          // g, beta
     b += align256((size_t)T * s.hqk * 4);             // k.q
+    b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
     b += 256;                                         // valid flag
     return b;
 }
@@ -307,6 +301,7 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T)
     ws.g = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
+    ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
     ws.valid = reinterpret_cast<int*>(take(256));
 }
 
@@ -426,6 +421,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     if (!(s.l2_eps >= 0.0f) || !(s.norm_eps >= 0.0f)) return GDN_ERR_INVALID_ARG;
     if (s.dk != s.dv || (s.dk != 16 && s.dk != 32 && s.dk != 64 && s.dk != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
 
+    if (n_seqs > prefill_max_seqs(total_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
     // everything the call needs must fit in the static scratch: workspace, live flags, status word
     const size_t ws_bytes = prefill_workspace_bytes(s, total_tokens);
     const size_t live_bytes = align256((size_t)num_slots);
