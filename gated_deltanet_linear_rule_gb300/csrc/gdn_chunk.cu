@@ -354,14 +354,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                     ss = fmaf(o, o, ss);
                 }
             }
-            if (i < n) {
-                const float rs = rms_scale(ss, A.norm_eps, D);
-                const size_t obase = (size_t)(tc0 + i) * Dv + (size_t)h * D;
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float a_[32], b_[32];
-                    tc::ld32(tc::taddr(tm, warp, TM_D4 + c0), a_);
-                    tc::ld32(tc::taddr(tm, warp, TM_PU + c0), b_);
-                    tc::wait_ld();
+            // tcgen05.ld is warp-collective: every lane loads, only rows of real tokens are stored
+            const float rs = rms_scale(ss, A.norm_eps, D);
+            const size_t obase = (size_t)(tc0 + (i < n ? i : 0)) * Dv + (size_t)h * D;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float a_[32], b_[32];
+                tc::ld32(tc::taddr(tm, warp, TM_D4 + c0), a_);
+                tc::ld32(tc::taddr(tm, warp, TM_PU + c0), b_);
+                tc::wait_ld();
+                if (i < n) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int dv = c0 + e;
