@@ -23,7 +23,7 @@
 //     MMA5  [P; P]  x W, U     -> P W, P U                                        2 x 128 x 128 x 64
 //     MMA4  [W; Q'] x S0^T     -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)      128 x 128 x 128
 //     MMA6  S += Delta~^T x K  (S pre-scaled by e^{G_last} in TMEM)              128 x 128 x 64
-// with bf16 operands and fp32 accumulation; the state S itself stays fp32 in TMEM for the
+// with fp16 operands and fp32 accumulation; the state S itself stays fp32 in TMEM for the
 // whole sequence.  The triangular inverse, the decay factors, Delta, and the gated RMSNorm
 // of each output row run on the CUDA cores (one thread per TMEM lane = one token or one
 // d_v row).  One CTA (4 warps, 1 per SM) owns one (sequence, v-head); CTAs are ordered so
@@ -37,15 +37,18 @@ namespace gdn {
 namespace {
 
 constexpr int D = 128, CH = 64, NT = 128;
+// MMA operand type: fp16 (11-bit significand) -- bf16 operands (8-bit) put the chunked
+// result at ~5e-3 of the recurrent definition; fp16 runs at the same tensor-core rate.
+using Op = __half;
 
-// shared memory (offsets from a 1024-aligned base); every operand tile is swizzled K-major bf16
+// shared memory (offsets from a 1024-aligned base); every operand tile is swizzled K-major fp16
 constexpr uint32_t OFF_A1 = 0;         // [K; Q] (MMA1 A), then [W; Q'] (MMA4 A): 2 K-tiles x 128 rows
 constexpr uint32_t OFF_KT = 32768;     // K^T: 128 dk rows x 64 tokens (MMA3 B rows 0-127, MMA6 B)
 constexpr uint32_t OFF_VT = 49152;     // V^T: 128 dv rows x 64 tokens (MMA3 B rows 128-255)
 constexpr uint32_t OFF_AP = 65536;     // [P; P] (MMA5 A), then Delta~^T (MMA6 A): 128 rows x 64
 constexpr uint32_t OFF_AT = 81920;     // [T2; T1] (MMA3 A): 128 rows x 64
 constexpr uint32_t OFF_BWU = 98304;    // [W^T; U^T] (MMA5 B): 256 rows x 64
-constexpr uint32_t OFF_B4 = 131072;    // S0 in bf16 (MMA4 B): 2 K-tiles x 128 rows
+constexpr uint32_t OFF_B4 = 131072;    // S0 in fp16 (MMA4 B): 2 K-tiles x 128 rows
 constexpr uint32_t OFF_FA = 163840;    // fp32 A, 64 x 64
 constexpr uint32_t OFF_FT = 180224;    // fp32 T, 64 x 64
 constexpr uint32_t OFF_SMALL = 196608; // per-chunk scalars, barrier, TMEM slot
@@ -141,10 +144,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
             const int r = idx >> 4, c16 = idx & 15, i = r & 63;
             float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (i < n) load8((r < 64 ? A.ws.kh : A.ws.qh) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8, v);
-            tc::st_chunk(sm + OFF_A1 + (c16 >> 3) * 16384, r, c16 & 7, v);
+            tc::st_chunk<Op>(sm + OFF_A1 + (c16 >> 3) * 16384, r, c16 & 7, v);
             if (r < 64) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) tc::st_elem(sm + OFF_KT, c16 * 8 + e, i, v[e]);
+                for (int e = 0; e < 8; ++e) tc::st_elem<Op>(sm + OFF_KT, c16 * 8 + e, i, v[e]);
             }
         }
         for (int idx = tid; idx < 64 * 16; idx += NT) {
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
             float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (i < n) load8(A.ws.vc + (size_t)(tc0 + i) * Dv + h * D + c16 * 8, v);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tc::st_elem(sm + OFF_VT, c16 * 8 + e, i, v[e]);
+            for (int e = 0; e < 8; ++e) tc::st_elem<Op>(sm + OFF_VT, c16 * 8 + e, i, v[e]);
         }
         if (tid < 64) {
             const bool in = tid < n;
@@ -176,12 +179,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 
         // (b) MMA1: [K; Q] x K^T -> K K^T (rows 0-63), Q K^T (rows 64-127), 64 columns
         if (tid == 0)
-            tc::mma_bf16_k(tm + TM_D1, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_A1), 128, D,
-                           tc::idesc_bf16(128, 64), 0);
+            tc::mma_k(tm + TM_D1, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_A1), 128, D,
+                           tc::idesc_f16(128, 64), 0);
         mma_done();
         if (!ok) break;
 
-        // (c) A (fp32, rows 0-63) and P (bf16 tile, rows 64-127 -> both halves of [P; P])
+        // (c) A (fp32, rows 0-63) and P (fp16 tile, rows 64-127 -> both halves of [P; P])
         {
             const int i = tid & 63;
             const float Gi = sG[i];
@@ -206,8 +209,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        tc::st_chunk(sm + OFF_AP, i, c0 / 8 + q, p + 8 * q);
-                        tc::st_chunk(sm + OFF_AP, 64 + i, c0 / 8 + q, p + 8 * q);
+                        tc::st_chunk<Op>(sm + OFF_AP, i, c0 / 8 + q, p + 8 * q);
+                        tc::st_chunk<Op>(sm + OFF_AP, 64 + i, c0 / 8 + q, p + 8 * q);
                     }
                 }
             }
@@ -232,8 +235,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
             const float bj = sB[j], bej = sB[j] * sEG[j];
             for (int i = 0; i < 64; ++i) {
                 const float t = FT[i * 64 + j];
-                tc::st_elem(sm + OFF_AT, i, j, t * bj);
-                tc::st_elem(sm + OFF_AT, 64 + i, j, t * bej);
+                tc::st_elem<Op>(sm + OFF_AT, i, j, t * bj);
+                tc::st_elem<Op>(sm + OFF_AT, 64 + i, j, t * bej);
             }
         }
         tc::fence_proxy_async();
@@ -241,8 +244,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 
         // (e) MMA3: [T2; T1] x [K^T; V^T] -> U (rows 0-63, cols 256-383), W (rows 64-127, cols 128-255)
         if (tid == 0)
-            tc::mma_bf16_k(tm + TM_D3, smem_addr(sm + OFF_AT), 128, smem_addr(sm + OFF_KT), 256, CH,
-                           tc::idesc_bf16(128, 256), 0);
+            tc::mma_k(tm + TM_D3, smem_addr(sm + OFF_AT), 128, smem_addr(sm + OFF_KT), 256, CH,
+                           tc::idesc_f16(128, 256), 0);
         mma_done();
         if (!ok) break;
 
@@ -255,12 +258,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                 tc::wait_ld();
                 if (tid >= 64) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) tc::st_chunk(sm + OFF_A1 + (c0 >> 6) * 16384, i, (c0 & 63) / 8 + q, v + 8 * q);
+                    for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_A1 + (c0 >> 6) * 16384, i, (c0 & 63) / 8 + q, v + 8 * q);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) tc::st_elem(sm + OFF_BWU, c0 + e, i, v[e]);
+                    for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_BWU, c0 + e, i, v[e]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) tc::st_elem(sm + OFF_BWU, 128 + c0 + e, i, v[e]);
+                    for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_BWU, 128 + c0 + e, i, v[e]);
                 }
             }
         }
@@ -269,10 +272,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 
         // (g) MMA5: [P; P] x W^T -> P W (cols 128-255); [P; P] x U^T -> P U (cols 384-511)
         if (tid == 0) {
-            tc::mma_bf16_k(tm + TM_PW, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU), 256, CH,
-                           tc::idesc_bf16(128, 128), 0);
-            tc::mma_bf16_k(tm + TM_PU, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU) + 128 * 128, 256, CH,
-                           tc::idesc_bf16(128, 128), 0);
+            tc::mma_k(tm + TM_PW, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU), 256, CH,
+                           tc::idesc_f16(128, 128), 0);
+            tc::mma_k(tm + TM_PU, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU) + 128 * 128, 256, CH,
+                           tc::idesc_f16(128, 128), 0);
         }
         mma_done();
         if (!ok) break;
@@ -298,11 +301,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = eg * qv[e] - v[e];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tc::st_chunk(sm + OFF_A1 + (c0 >> 6) * 16384, 64 + i, (c0 & 63) / 8 + q, v + 8 * q);
+                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_A1 + (c0 >> 6) * 16384, 64 + i, (c0 & 63) / 8 + q, v + 8 * q);
             }
         }
 
-        // (i) S0 (bf16) for MMA4; S <- e^{G_last} S in TMEM for MMA6
+        // (i) S0 (fp16) for MMA4; S <- e^{G_last} S in TMEM for MMA6
         {
             const float egl = sMisc[0];
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                 tc::ld32(tc::taddr(tm, warp, TM_S + c0), v);
                 tc::wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tc::st_chunk(sm + OFF_B4 + (c0 >> 6) * 16384, tid, (c0 & 63) / 8 + q, v + 8 * q);
+                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_B4 + (c0 >> 6) * 16384, tid, (c0 & 63) / 8 + q, v + 8 * q);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= egl;
                 tc::st32(tc::taddr(tm, warp, TM_S + c0), v);
@@ -322,8 +325,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 
         // (j) MMA4: [W; Q'] x S0^T -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)
         if (tid == 0)
-            tc::mma_bf16_k(tm + TM_D4, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_B4), 128, D,
-                           tc::idesc_bf16(128, 128), 0);
+            tc::mma_k(tm + TM_D4, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_B4), 128, D,
+                           tc::idesc_f16(128, 128), 0);
         mma_done();
         if (!ok) break;
 
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                 tc::ld32(tc::taddr(tm, warp, TM_U + c0), u);
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) tc::st_elem(sm + OFF_AP, c0 + e, i, gm * (u[e] - ws_[e]));
+                for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_AP, c0 + e, i, gm * (u[e] - ws_[e]));
             }
         } else {
             const int i = tid - 64;
@@ -377,8 +380,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
 
         // (l) MMA6: S += Delta~^T x K (accumulate onto the pre-scaled state)
         if (tid == 0)
-            tc::mma_bf16_k(tm + TM_S, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_KT), 128, CH,
-                           tc::idesc_bf16(128, 128), 1);
+            tc::mma_k(tm + TM_S, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_KT), 128, CH,
+                           tc::idesc_f16(128, 128), 1);
         mma_done();
     }
 

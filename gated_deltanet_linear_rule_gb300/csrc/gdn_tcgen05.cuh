@@ -1,6 +1,7 @@
 // gdn_tcgen05.cuh -- 5th-generation tensor-core (tcgen05 / TMEM) helpers, written from the PTX ISA.
 //
-// Operand tiles are bf16, K-major, in the 128-byte swizzle layout: a tile holds R rows
+// Operand tiles are 16-bit (fp16 or bf16; one MMA uses one type for both), K-major, in the
+// 128-byte swizzle layout: a tile holds R rows
 // (the M or N index) of 64 K-elements (128 B per row); rows are grouped by 8 into 1024-B
 // atoms, and inside an atom the 16-B chunk c of row r sits at chunk position c ^ (r % 8).
 // A K extent of 128 is two such tiles side by side in memory (k 0..63, then 64..127).
@@ -8,6 +9,7 @@
 // (cta_group::1) row i of D is TMEM lane i and column j is TMEM column j.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "gdn_internal.cuh"
@@ -39,14 +41,18 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+// Instruction descriptor: kind::f16, fp32 accumulator, A and B both K-major and both of the
+// 16-bit type given (format code 0 = fp16, 1 = bf16).
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_format)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) { return idesc_kind_f16(M, N, 1u); }
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) { return idesc_kind_f16(M, N, 0u); }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 slice; issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
     asm volatile(
@@ -58,14 +64,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
 
 // K = 16 * ksteps GEMM slice loop over operands of K extent 64 * ktiles (each K tile is
 // R rows * 128 B; a_rows / b_rows give the tile pitch of A and B in rows).
-__device__ __forceinline__ void mma_bf16_k(uint32_t d_tmem, uint32_t a_saddr, int a_rows, uint32_t b_saddr,
+__device__ __forceinline__ void mma_k(uint32_t d_tmem, uint32_t a_saddr, int a_rows, uint32_t b_saddr,
                                            int b_rows, int kdim, uint32_t idesc, uint32_t accumulate)
 {
     for (int k16 = 0; k16 < kdim / 16; ++k16) {
         const int kt = k16 >> 2, kin = (k16 & 3) * 32;
         const uint64_t a = sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
         const uint64_t b = sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
-        mma_bf16(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
+        mma(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
     }
 }
 
@@ -141,28 +147,40 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, int col)
     return base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)col;
 }
 
-// pack two floats into a bf16x2 word (round to nearest even), low half = first
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+// pack two floats into a 16-bit pair (round to nearest even), low half = first
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi)
 {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&p);
 }
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi)
+{
+    __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
 
-// store 8 bf16 values (row r, elements 8c .. 8c+7) of a swizzled tile as one 16-B chunk
+template <typename T> __device__ __forceinline__ T to16(float v);
+template <> __device__ __forceinline__ __nv_bfloat16 to16<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ __half to16<__half>(float v) { return __float2half_rn(v); }
+
+// store 8 values (row r, elements 8c .. 8c+7) of a swizzled tile as one 16-B chunk
+template <typename T>
 __device__ __forceinline__ void st_chunk(unsigned char* tile, int r, int c, const float* v8)
 {
     uint4 w;
-    w.x = pack_bf16(v8[0], v8[1]);
-    w.y = pack_bf16(v8[2], v8[3]);
-    w.z = pack_bf16(v8[4], v8[5]);
-    w.w = pack_bf16(v8[6], v8[7]);
+    w.x = pack2<T>(v8[0], v8[1]);
+    w.y = pack2<T>(v8[2], v8[3]);
+    w.z = pack2<T>(v8[4], v8[5]);
+    w.w = pack2<T>(v8[6], v8[7]);
     *reinterpret_cast<uint4*>(tile + sw128_chunk(r, c)) = w;
 }
 
-// store one bf16 element (r, k) of a swizzled tile
+// store one element (r, k) of a swizzled tile
+template <typename T>
 __device__ __forceinline__ void st_elem(unsigned char* tile, int r, int k, float v)
 {
-    *reinterpret_cast<__nv_bfloat16*>(tile + sw128(r, k)) = __float2bfloat16_rn(v);
+    *reinterpret_cast<T*>(tile + sw128(r, k)) = to16<T>(v);
 }
 
 }  // namespace tc

@@ -1,6 +1,6 @@
 // umma_probe.cu -- test-only GEMM through the library's tcgen05 helpers (gdn_tcgen05.cuh).
 //
-// D[128 x N] = A[128 x K] * B[N x K]^T with bf16 inputs (row-major, K contiguous) and an fp32
+// D[128 x N] = A[128 x K] * B[N x K]^T with bf16 or fp16 inputs (row-major, K contiguous) and an fp32
 // result, computed by one CTA: operands staged into swizzled K-major shared-memory tiles,
 // K/16 tcgen05.mma issues, commit to an mbarrier, tcgen05.ld of the accumulator.  The GPU test
 // compares the result with a plain fp32 matmul: it checks the descriptor and instruction
@@ -13,8 +13,8 @@
 
 using namespace gdn;
 
-__global__ void __launch_bounds__(128) umma_probe_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D,
-                                                         int N, int K, uint32_t ncols, unsigned int* status)
+__global__ void __launch_bounds__(128) umma_probe_kernel(const uint16_t* A, const uint16_t* B, float* D, int N,
+                                                         int K, uint32_t ncols, uint32_t idesc, unsigned int* status)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(const __nv_bfloat16* A,
     tc::fence_after_sync();
     const uint32_t base = *tmem_slot;
     if (tid == 0) {
-        tc::mma_bf16_k(base, smem_addr(a_tiles), 128, smem_addr(b_tiles), N, K, tc::idesc_bf16(128, N), 0);
+        tc::mma_k(base, smem_addr(a_tiles), 128, smem_addr(b_tiles), N, K, idesc, 0);
         tc::commit(bar);
     }
     if (!mbar_wait_bounded(bar, 0, nullptr)) {
@@ -67,7 +67,9 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(const __nv_bfloat16* A,
     if (warp == 0) tc::dealloc(base, ncols);
 }
 
-extern "C" int umma_probe_gemm(const void* A, const void* B, void* D, int N, int K, unsigned int* status, void* stream)
+// half_inputs: 0 = bf16 operands, 1 = fp16 operands
+extern "C" int umma_probe_gemm(const void* A, const void* B, void* D, int N, int K, int half_inputs,
+                               unsigned int* status, void* stream)
 {
     if ((N != 64 && N != 128 && N != 256) || (K != 64 && K != 128)) return -1;
     const uint32_t ncols = N < 32 ? 32 : (uint32_t)N;
@@ -77,7 +79,7 @@ extern "C" int umma_probe_gemm(const void* A, const void* B, void* D, int N, int
     cudaError_t e = cudaFuncSetAttribute(umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return -4;
     umma_probe_kernel<<<1, 128, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), static_cast<float*>(D), N, K,
-        ncols, status);
+        static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(B), static_cast<float*>(D), N, K, ncols,
+        half_inputs ? tc::idesc_f16(128, N) : tc::idesc_bf16(128, N), status);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

@@ -23,20 +23,22 @@ def probe():
            "-I", build.CSRC, src, "-o", lib]
     subprocess.run(cmd, check=True, capture_output=True)
     L = ctypes.CDLL(lib)
-    L.umma_probe_gemm.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                                           ctypes.c_void_p]
+    L.umma_probe_gemm.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                           ctypes.c_void_p, ctypes.c_void_p]
     return L
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 128), (256, 64), (256, 128)])
-def test_umma_gemm_matches_fp32_matmul(probe, N, K):
+def test_umma_gemm_matches_fp32_matmul(probe, N, K, dtype):
     g = torch.Generator(device="cuda").manual_seed(N * 1000 + K)
-    A = torch.randn((128, K), device="cuda", generator=g).to(torch.bfloat16)
-    B = torch.randn((N, K), device="cuda", generator=g).to(torch.bfloat16)
+    A = torch.randn((128, K), device="cuda", generator=g).to(dtype)
+    B = torch.randn((N, K), device="cuda", generator=g).to(dtype)
     D = torch.full((128, N), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    assert probe.umma_probe_gemm(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, status.data_ptr(), s) == 0
+    half = 1 if dtype == torch.float16 else 0
+    assert probe.umma_probe_gemm(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, half, status.data_ptr(), s) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "the MMA completion wait timed out"
     ref = A.float() @ B.float().T
