@@ -41,15 +41,34 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor: kind::f16, fp32 accumulator, A and B both K-major and both of the
-// 16-bit type given (format code 0 = fp16, 1 = bf16).
-__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_format)
+// MN-major operand tiles (the MMA reads the operand transposed) use the same swizzled rows,
+// but a row is one K index holding 64 consecutive M (or N) elements: element (mn, k) sits at
+// (mn / 64) * lbo + sw128(k, mn % 64).  8-row groups along K are 1024 B apart; the two 64-wide
+// halves of a 128-wide M or N extent are lbo bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo)
 {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64-wide M/N block
+    d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor: kind::f16, fp32 accumulator, A and B of the 16-bit type given
+// (format code 0 = fp16, 1 = bf16); a_mn / b_mn mark MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_format, uint32_t a_mn = 0,
+                                                      uint32_t b_mn = 0)
+{
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn << 15) | (b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) { return idesc_kind_f16(M, N, 1u); }
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) { return idesc_kind_f16(M, N, 0u); }
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, uint32_t a_mn = 0, uint32_t b_mn = 0)
+{
+    return idesc_kind_f16(M, N, 0u, a_mn, b_mn);
+}
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 slice; issued by one thread.
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -71,6 +90,23 @@ __device__ __forceinline__ void mma_k(uint32_t d_tmem, uint32_t a_saddr, int a_r
         const int kt = k16 >> 2, kin = (k16 & 3) * 32;
         const uint64_t a = sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
         const uint64_t b = sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
+        mma(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
+    }
+}
+
+// Same loop where either operand may be MN-major: for a K-major operand the tile pitch in rows
+// is given (as above); for an MN-major operand (mn != 0) the K slices advance by 16 rows
+// (2048 B) and lbo is the distance between its 64-wide M/N halves.
+__device__ __forceinline__ void mma_k_mixed(uint32_t d_tmem, uint32_t a_saddr, int a_rows, uint32_t a_mn,
+                                            uint32_t a_lbo, uint32_t b_saddr, int b_rows, uint32_t b_mn,
+                                            uint32_t b_lbo, int kdim, uint32_t idesc, uint32_t accumulate)
+{
+    for (int k16 = 0; k16 < kdim / 16; ++k16) {
+        const int kt = k16 >> 2, kin = (k16 & 3) * 32;
+        const uint64_t a = a_mn ? sdesc_mn(a_saddr + (uint32_t)(k16 * 2048), a_lbo)
+                                : sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
+        const uint64_t b = b_mn ? sdesc_mn(b_saddr + (uint32_t)(k16 * 2048), b_lbo)
+                                : sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
         mma(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
     }
 }
