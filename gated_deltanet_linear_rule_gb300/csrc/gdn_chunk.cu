@@ -13,21 +13,31 @@
 //     T      = (I + A)^-1                              (unit lower triangular)
 //     W      = T diag(beta e^G) K,     U = T diag(beta) V
 //     P_ij   = e^{G_i - G_j} (q_i . k_j)               (i >= j)
-//     Q'     = diag(e^G) Q - P W,      O0 = P U        (independent of S0)
+//     Q'     = diag(e^G) Q - P W,      O0 = P U
 //     Delta  = U - W S0^T,             O  = Q' S0^T + O0
 //     S_end  = e^{G_last} S0 + Delta^T diag(e^{G_last - G_j}) K
-// Only the last three lines depend on the incoming state.  Every product runs on the
-// tensor cores as a 128-row MMA:
-//     MMA1  [K; Q]  x K^T      -> K K^T (rows 0-63) and Q K^T (rows 64-127)      128 x 64  x 128
-//     MMA3  [T2; T1] x [K|V]   -> U = T2 V (rows 0-63), W = T1 K (rows 64-127)     128 x 256 x 64
-//     MMA5  [P; P]  x W, U     -> P W, P U                                        2 x 128 x 128 x 64
-//     MMA4  [W; Q'] x S0^T     -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)      128 x 128 x 128
-//     MMA6  S += Delta~^T x K  (S pre-scaled by e^{G_last} in TMEM)              128 x 128 x 64
-// with fp16 operands and fp32 accumulation; the state S itself stays fp32 in TMEM for the
-// whole sequence.  The triangular inverse, the decay factors, Delta, and the gated RMSNorm
-// of each output row run on the CUDA cores (one thread per TMEM lane = one token or one
-// d_v row).  One CTA (4 warps, 1 per SM) owns one (sequence, v-head); CTAs are ordered so
-// that the longest sequences start first.
+// Everything above the line "Delta = ..." is independent of the incoming state, so it runs
+// in a fully parallel pre-pass, one CTA per (chunk, v-head) over all chunks of all
+// sequences at once; only the last two lines form the serial chain, run by one CTA per
+// (sequence, v-head) that keeps S in fp32 tensor memory across its chunks.
+//
+// Pre-pass (chunk_prep_kernel, 2 CTAs per SM):
+//     MMA1  [K; Q]  x K^T          -> K K^T (rows 0-63), Q K^T (rows 64-127)     128 x 64  x 128
+//     blocked triangular inverse of I + A on the CUDA cores (16-wide diagonal blocks, then
+//     16 -> 32 -> 64 by  T_21 = -T_22 A_21 T_11)
+//     MMA3  [T2; T1] x K,  [T2; T1] x V  -> W (rows 64-127), U (rows 0-63)       2 x 128 x 128 x 64
+//     MMA5  [P; P] x W,  [P; P] x U      -> P W, P U                             2 x 128 x 128 x 64
+//   and writes per (chunk, v-head) a record: the [W; Q'] operand image, U and P U images, the
+//   decay factors; per (chunk, q/k head) the K image.
+// State pass (chunk_state_kernel, double-buffered bulk copies of the records):
+//     MMA4  [W; Q'] x S0^T   -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)         128 x 128 x 128
+//     Delta, O = Q' S0^T + P U with the gated RMSNorm fused, output written
+//     MMA6  S += Delta~^T x K   (S pre-scaled by e^{G_last} in TMEM)              128 x 128 x 64
+// Operands are fp16 (11-bit significand; bf16's 8 bits put the chunked result at ~5e-3 of
+// the recurrent definition) with fp32 accumulation.  Transposed operands (K, V, W, U as
+// the N side; Delta~ as the M side) are read MN-major straight from row-wise tiles.
+// Every tcgen05.ld / st is executed by whole warps (they are warp-collective); per-token
+// conditions only guard stores.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -37,31 +47,33 @@ namespace gdn {
 namespace {
 
 constexpr int D = 128, CH = 64, NT = 128;
-// MMA operand type: fp16 (11-bit significand) -- bf16 operands (8-bit) put the chunked
-// result at ~5e-3 of the recurrent definition; fp16 runs at the same tensor-core rate.
 using Op = __half;
 
-// shared memory (offsets from a 1024-aligned base); every operand tile is swizzled K-major fp16
-constexpr uint32_t OFF_A1 = 0;         // [K; Q] (MMA1 A), then [W; Q'] (MMA4 A): 2 K-tiles x 128 rows
-constexpr uint32_t OFF_KT = 32768;     // K^T: 128 dk rows x 64 tokens (MMA3 B rows 0-127, MMA6 B)
-constexpr uint32_t OFF_VT = 49152;     // V^T: 128 dv rows x 64 tokens (MMA3 B rows 128-255)
-constexpr uint32_t OFF_AP = 65536;     // [P; P] (MMA5 A), then Delta~^T (MMA6 A): 128 rows x 64
-constexpr uint32_t OFF_AT = 81920;     // [T2; T1] (MMA3 A): 128 rows x 64
-constexpr uint32_t OFF_BWU = 98304;    // [W^T; U^T] (MMA5 B): 256 rows x 64
-constexpr uint32_t OFF_B4 = 131072;    // S0 in fp16 (MMA4 B): 2 K-tiles x 128 rows
-constexpr uint32_t OFF_FA = 163840;    // fp32 A, 64 x 64
-constexpr uint32_t OFF_FT = 180224;    // fp32 T, 64 x 64
-constexpr uint32_t OFF_SMALL = 196608; // per-chunk scalars, barrier, TMEM slot
-constexpr size_t SMEM_BYTES = OFF_SMALL + 2048 + 1024;
+// record of one (chunk, v-head), written by the pre-pass, read by the state pass
+constexpr uint32_t REC_A4 = 0;       // [W; Q'] K-major image: 2 K-tiles x 128 rows
+constexpr uint32_t REC_U = 32768;    // U image [token][dv]: two 64-wide halves 8 KiB apart
+constexpr uint32_t REC_O0 = 49152;   // P U image, same layout
+constexpr uint32_t REC_SC = 65536;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
+constexpr uint32_t REC_BYTES = 66048;
+constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token][dk], halves 8 KiB apart
 
-// TMEM columns (512 allocated): S lives in [0, 128) for the whole sequence
-constexpr uint32_t TM_S = 0;
-constexpr uint32_t TM_D1 = 128;   // MMA1
-constexpr uint32_t TM_D3 = 128;   // MMA3, 256 columns: W at rows 64-127 cols 128-255, U at rows 0-63 cols 256-383
-constexpr uint32_t TM_U = 256;
-constexpr uint32_t TM_PW = 128;   // MMA5 first half
-constexpr uint32_t TM_PU = 384;   // MMA5 second half
-constexpr uint32_t TM_D4 = 128;   // MMA4
+// pre-pass shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1), then [W; Q'] (record)
+constexpr uint32_t P_AP = 32768;      // [P; P]
+constexpr uint32_t P_AT = 49152;      // inverse scratch, then [T2; T1], then the P U image
+constexpr uint32_t P_R4 = 65536;      // A (fp32, stride 65), then the V image, then the U image
+constexpr uint32_t P_R5 = 82944;      // T (fp32, stride 65), then the W image
+constexpr uint32_t P_SMALL = 99584;
+constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
+constexpr int FS = 65;                // fp32 matrix row stride (conflict-free row reads)
+
+// state-pass shared memory
+constexpr uint32_t S_BUF = 83968;     // one prefetch buffer: record (A4 | U | O0) | K image | scalars
+constexpr uint32_t B_A4 = 0, B_U = 32768, B_O0 = 49152, B_K = 65536, B_SC = 81920;
+constexpr uint32_t S_S0 = 2 * S_BUF;  // S0 in fp16, K-major: 2 K-tiles x 128 rows
+constexpr uint32_t S_A6 = S_S0 + 32768;  // Delta~ image [token][dv], halves 8 KiB apart
+constexpr uint32_t S_SMALL = S_A6 + 16384;
+constexpr size_t S_SMEM = S_SMALL + 256 + 1024;
 
 __device__ __forceinline__ void sync_all()
 {
@@ -78,42 +90,68 @@ __device__ __forceinline__ void load8(const float* p, float* v)
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
+// 8 fp16 values of a 16-B chunk -> float
+__device__ __forceinline__ void unpack8(uint4 w, float* v)
+{
+    const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(h[q]);
+        v[2 * q] = f.x;
+        v[2 * q + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p)
+{
+    return p + ((1024 - (smem_addr(p) & 1023)) & 1023);
+}
+
+// ===================================================================== pre-pass ====
+
+__global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-    float* sGraw = reinterpret_cast<float*>(sm + OFF_SMALL);  // [64] g of the chunk
-    float* sG = sGraw + 64;    // [64] inclusive prefix sums G_i
-    float* sB = sG + 64;       // [64] beta (0 past the chunk's end)
-    float* sEG = sB + 64;      // [64] e^{G_i}
-    float* sGam = sEG + 64;    // [64] e^{G_last - G_i} (0 past the end)
-    float* sMisc = sGam + 64;  // [8] e^{G_last}
+    unsigned char* sm = align1024(smem_raw);
+    float* sGraw = reinterpret_cast<float*>(sm + P_SMALL);
+    float* sG = sGraw + 64;
+    float* sB = sG + 64;
+    float* sEG = sB + 64;
+    float* sGam = sEG + 64;
+    float* sMisc = sGam + 64;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sMisc + 8);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+    float* FA = reinterpret_cast<float*>(sm + P_R4);
+    float* FT = reinterpret_cast<float*>(sm + P_R5);
+    float* X = reinterpret_cast<float*>(sm + P_AT);
 
     if (!*A.ws.valid) return;
+    const int gc = blockIdx.x / A.hv, h = blockIdx.x % A.hv;
+    if (gc >= A.ws.chunk_start[A.n]) return;
+    int lo = 0, hi = A.n;  // the sequence of chunk gc: largest s with chunk_start[s] <= gc
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (A.ws.chunk_start[mid] <= gc) lo = mid;
+        else hi = mid;
+    }
+    const int s = lo, c = gc - A.ws.chunk_start[s];
+    const int tc0 = A.cu[s] + c * CH;
+    const int n = min(CH, A.cu[s + 1] - tc0);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int s = A.ws.order[blockIdx.x / A.hv], h = blockIdx.x % A.hv;
-    const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
-    if (L <= 0) return;
     const int hk = h / A.r, Dq = A.hqk * D, Dv = A.hv * D;
-    float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
-                (size_t)h * D * D;
-    const TIn* zin = static_cast<const TIn*>(A.z);
-    TOut* out = static_cast<TOut*>(A.out);
+    const bool write_k = (h % A.r) == 0;
+    unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
+    unsigned char* kimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * KIMG_BYTES;
 
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tc::alloc(tmem_slot, 512);
+    if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
     const uint32_t tm = *tmem_slot;
     uint32_t phase = 0;
     bool ok = true;
-
-    // issue + wait helper: thread 0 issues, everyone waits for the commit
     auto mma_done = [&]() {
         if (tid == 0) tc::commit(bar);
         const bool got = mbar_wait_bounded(bar, phase, nullptr);
@@ -123,82 +161,53 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
         tc::fence_after_sync();
     };
 
-    // the sequence's incoming state into TMEM: thread = d_v row
-    for (int c0 = 0; c0 < D; c0 += 32) {
-        float v[32];
-        const float* row = Sg + (size_t)tid * D + c0;
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) load8(row + e, v + e);
-        tc::st32(tc::taddr(tm, warp, TM_S + c0), v);
+    // (a) [K; Q] tile; the K image of the record; gates
+    for (int idx = tid; idx < 128 * 16; idx += NT) {
+        const int r = idx >> 4, c16 = idx & 15, i = r & 63;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (i < n) load8((r < 64 ? A.ws.kh : A.ws.qh) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8, v);
+        tc::st_chunk<Op>(sm + P_A1 + (c16 >> 3) * 16384, r, c16 & 7, v);
+        if (r < 64 && write_k) tc::st_chunk<Op>(kimg + (c16 >> 3) * 8192, i, c16 & 7, v);
     }
-    tc::wait_st();
+    if (tid < 64) {
+        const bool in = tid < n;
+        sGraw[tid] = in ? A.ws.g[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
+        sB[tid] = in ? A.ws.beta[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
+    }
+    tc::fence_proxy_async();
     sync_all();
+    if (tid < 64) {
+        float acc = 0.f;
+        for (int t = 0; t <= tid; ++t) acc += sGraw[t];
+        sG[tid] = acc;
+        sEG[tid] = expf(acc);
+    }
+    __syncthreads();
+    if (tid < 64) {
+        const float gl = sG[n - 1];
+        sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
+        if (tid == 0) sMisc[0] = expf(gl);
+    }
 
-    const int nchunks = (L + CH - 1) / CH;
-    for (int c = 0; c < nchunks && ok; ++c) {
-        const int tc0 = t0 + c * CH;
-        const int n = min(CH, L - c * CH);
-
-        // (a) operand tiles of the chunk: [K; Q], K^T, V^T; gates
-        for (int idx = tid; idx < 128 * 16; idx += NT) {
-            const int r = idx >> 4, c16 = idx & 15, i = r & 63;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (i < n) load8((r < 64 ? A.ws.kh : A.ws.qh) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8, v);
-            tc::st_chunk<Op>(sm + OFF_A1 + (c16 >> 3) * 16384, r, c16 & 7, v);
-            if (r < 64) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) tc::st_elem<Op>(sm + OFF_KT, c16 * 8 + e, i, v[e]);
-            }
-        }
-        for (int idx = tid; idx < 64 * 16; idx += NT) {
-            const int i = idx >> 4, c16 = idx & 15;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (i < n) load8(A.ws.vc + (size_t)(tc0 + i) * Dv + h * D + c16 * 8, v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) tc::st_elem<Op>(sm + OFF_VT, c16 * 8 + e, i, v[e]);
-        }
-        if (tid < 64) {
-            const bool in = tid < n;
-            sGraw[tid] = in ? A.ws.g[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
-            sB[tid] = in ? A.ws.beta[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
-        }
-        tc::fence_proxy_async();
-        sync_all();
-        if (tid < 64) {
-            float acc = 0.f;
-            for (int t = 0; t <= tid; ++t) acc += sGraw[t];
-            sG[tid] = acc;
-            sEG[tid] = expf(acc);
-        }
-        __syncthreads();
-        if (tid < 64) {
-            const float gl = sG[n - 1];
-            sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
-            if (tid == 0) sMisc[0] = expf(gl);
-        }
-
-        // (b) MMA1: [K; Q] x K^T -> K K^T (rows 0-63), Q K^T (rows 64-127), 64 columns
-        if (tid == 0)
-            tc::mma_k(tm + TM_D1, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_A1), 128, D,
-                           tc::idesc_f16(128, 64), 0);
-        mma_done();
-        if (!ok) break;
-
-        // (c) A (fp32, rows 0-63) and P (fp16 tile, rows 64-127 -> both halves of [P; P])
+    // (b) MMA1: [K; Q] x K^T
+    if (tid == 0)
+        tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
+    mma_done();
+    if (ok) {
+        // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127
         {
             const int i = tid & 63;
             const float Gi = sG[i];
-            float* FA = reinterpret_cast<float*>(sm + OFF_FA);
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 float v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D1 + c0), v);
+                tc::ld32(tc::taddr(tm, warp, c0), v);
                 tc::wait_ld();
                 if (tid < 64) {
                     const float bi = sB[i];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int j = c0 + e;
-                        FA[i * 64 + j] = (j < i && i < n) ? bi * expf(Gi - sG[j]) * v[e] : 0.f;
+                        FA[i * FS + j] = (j < i && i < n) ? bi * expf(Gi - sG[j]) * v[e] : 0.f;
                     }
                 } else {
                     float p[32];
@@ -209,87 +218,143 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        tc::st_chunk<Op>(sm + OFF_AP, i, c0 / 8 + q, p + 8 * q);
-                        tc::st_chunk<Op>(sm + OFF_AP, 64 + i, c0 / 8 + q, p + 8 * q);
+                        tc::st_chunk<Op>(sm + P_AP, i, c0 / 8 + q, p + 8 * q);
+                        tc::st_chunk<Op>(sm + P_AP, 64 + i, c0 / 8 + q, p + 8 * q);
                     }
                 }
             }
         }
-        sync_all();
+        __syncthreads();
 
-        // (d) T = (I + A)^-1 by forward substitution, one column per thread; then [T2; T1]
+        // (d) T = (I + A)^-1, blocked.  16-wide diagonal blocks by forward substitution
+        //     (one column per thread; zero above the diagonal and in the upper blocks) ...
         if (tid < 64) {
-            const int j = tid;
-            const float* FA = reinterpret_cast<const float*>(sm + OFF_FA);
-            float* FT = reinterpret_cast<float*>(sm + OFF_FT);
-            for (int i = 0; i < 64; ++i) {
-                float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
-                int k = j;
-                for (; k + 1 < i; k += 2) {
-                    acc0 -= FA[i * 64 + k] * FT[k * 64 + j];
-                    acc1 -= FA[i * 64 + k + 1] * FT[(k + 1) * 64 + j];
+            const int b = tid >> 4, j = tid & 15, o = 16 * b;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float acc = (i == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int k = 0; k < i; ++k) acc -= FA[(o + i) * FS + o + k] * x[k];
+                x[i] = acc;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) FT[(o + i) * FS + o + j] = x[i];
+        }
+        for (int idx = tid; idx < 64 * 64; idx += NT) {
+            const int i = idx >> 6, j = idx & 63;
+            if ((j >> 4) > (i >> 4)) FT[i * FS + j] = 0.f;
+        }
+        __syncthreads();
+        //     ... then 16 -> 32: T_10 = -T_11 (A_10 T_00) for the block pairs (0,1), (2,3) ...
+        for (int idx = tid; idx < 512; idx += NT) {
+            const int p = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+            const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
+            float acc = 0.f;
+            for (int k = j; k < 16; ++k) acc += FA[(ro + i) * FS + co + k] * FT[(co + k) * FS + co + j];
+            X[(p * 16 + i) * 17 + j] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 512; idx += NT) {
+            const int p = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+            const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
+            float acc = 0.f;
+            for (int k = 0; k <= i; ++k) acc += FT[(ro + i) * FS + ro + k] * X[(p * 16 + k) * 17 + j];
+            FT[(ro + i) * FS + co + j] = -acc;
+        }
+        __syncthreads();
+        //     ... then 32 -> 64: T_BA = -T_BB (A_BA T_AA)
+        for (int idx = tid; idx < 1024; idx += NT) {
+            const int i = idx >> 5, j = idx & 31;
+            float acc = 0.f;
+            for (int k = j; k < 32; ++k) acc += FA[(32 + i) * FS + k] * FT[k * FS + j];
+            X[i * 33 + j] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 1024; idx += NT) {
+            const int i = idx >> 5, j = idx & 31;
+            float acc = 0.f;
+            for (int k = 0; k <= i; ++k) acc += FT[(32 + i) * FS + 32 + k] * X[k * 33 + j];
+            FT[(32 + i) * FS + j] = -acc;
+        }
+        __syncthreads();
+        //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one row per thread
+        {
+            const int i = tid & 63;
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = c8 * 8 + e;
+                    v[e] = FT[i * FS + j] * (tid < 64 ? sB[j] : sB[j] * sEG[j]);
                 }
-                if (k < i) acc0 -= FA[i * 64 + k] * FT[k * 64 + j];
-                FT[i * 64 + j] = (i < j) ? 0.f : acc0 + acc1;
+                tc::st_chunk<Op>(sm + P_AT, tid, c8, v);
             }
-            const float bj = sB[j], bej = sB[j] * sEG[j];
-            for (int i = 0; i < 64; ++i) {
-                const float t = FT[i * 64 + j];
-                tc::st_elem<Op>(sm + OFF_AT, i, j, t * bj);
-                tc::st_elem<Op>(sm + OFF_AT, 64 + i, j, t * bej);
-            }
+        }
+        __syncthreads();  // A (fp32) is dead from here: its space takes the V image
+        // (d') V image [token][dv] for MMA3's second product
+        for (int idx = tid; idx < 64 * 16; idx += NT) {
+            const int i = idx >> 4, c16 = idx & 15;
+            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (i < n) load8(A.ws.vc + (size_t)(tc0 + i) * Dv + h * D + c16 * 8, v);
+            tc::st_chunk<Op>(sm + P_R4 + (c16 >> 3) * 8192, i, c16 & 7, v);
         }
         tc::fence_proxy_async();
         sync_all();
 
-        // (e) MMA3: [T2; T1] x [K^T; V^T] -> U (rows 0-63, cols 256-383), W (rows 64-127, cols 128-255)
-        if (tid == 0)
-            tc::mma_k(tm + TM_D3, smem_addr(sm + OFF_AT), 128, smem_addr(sm + OFF_KT), 256, CH,
-                           tc::idesc_f16(128, 256), 0);
+        // (e) MMA3: [T2; T1] x K (K read MN-major from the [K; Q] tile) and [T2; T1] x V
+        if (tid == 0) {
+            tc::mma_k_mixed(tm, smem_addr(sm + P_AT), 128, 0, 0, smem_addr(sm + P_A1), 0, 1, 16384, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 0);
+            tc::mma_k_mixed(tm + 128, smem_addr(sm + P_AT), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 0);
+        }
         mma_done();
-        if (!ok) break;
-
-        // (f) W -> [W; .] rows 0-63 and W^T (rows 0-127 of [W^T; U^T]); U -> U^T (rows 128-255)
+    }
+    if (ok) {
+        // (f) W (rows 64-127 of the first product) -> [W; .] rows 0-63 and the W image;
+        //     U (rows 0-63 of the second product) -> the U image (over the dead V image)
         {
             const int i = tid & 63;
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float v[32];
-                tc::ld32(tc::taddr(tm, warp, (tid < 64 ? TM_U : TM_D3) + c0), v);
+                tc::ld32(tc::taddr(tm, warp, (tid < 64 ? 128 : 0) + c0), v);
                 tc::wait_ld();
-                if (tid >= 64) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_A1 + (c0 >> 6) * 16384, i, (c0 & 63) / 8 + q, v + 8 * q);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_BWU, c0 + e, i, v[e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_BWU, 128 + c0 + e, i, v[e]);
+                for (int q = 0; q < 4; ++q) {
+                    const int ch = (c0 & 63) / 8 + q;
+                    if (tid >= 64) {
+                        tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, i, ch, v + 8 * q);
+                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
+                    } else {
+                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
+                    }
                 }
             }
         }
         tc::fence_proxy_async();
         sync_all();
 
-        // (g) MMA5: [P; P] x W^T -> P W (cols 128-255); [P; P] x U^T -> P U (cols 384-511)
+        // (g) MMA5: [P; P] x W and [P; P] x U (both MN-major images)
         if (tid == 0) {
-            tc::mma_k(tm + TM_PW, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU), 256, CH,
-                           tc::idesc_f16(128, 128), 0);
-            tc::mma_k(tm + TM_PU, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_BWU) + 128 * 128, 256, CH,
-                           tc::idesc_f16(128, 128), 0);
+            tc::mma_k_mixed(tm, smem_addr(sm + P_AP), 128, 0, 0, smem_addr(sm + P_R5), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 0);
+            tc::mma_k_mixed(tm + 128, smem_addr(sm + P_AP), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 0);
         }
         mma_done();
-        if (!ok) break;
-
-        // (h) Q' = e^G Q - P W -> rows 64-127 of [W; Q'] (Q from the fp32 workspace)
+    }
+    if (ok) {
+        // (h) rows 64-127: Q' = e^G Q - P W -> [W; Q'] rows 64-127;  P U -> the P U image
         if (tid >= 64) {
             const int i = tid - 64;
             const float eg = sEG[i];
-            const float* qrow = A.ws.qh + (size_t)(tc0 + i) * Dq + hk * D;
+            const float* qrow = A.ws.qh + (size_t)(tc0 + (i < n ? i : 0)) * Dq + hk * D;
             for (int c0 = 0; c0 < D; c0 += 32) {
-                float v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_PW + c0), v);
+                float pw[32], pu[32], qv[32];
+                tc::ld32(tc::taddr(tm, warp, c0), pw);
+                tc::ld32(tc::taddr(tm, warp, 128 + c0), pu);
                 tc::wait_ld();
-                float qv[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     if (i < n) load8(qrow + c0 + e, qv + e);
@@ -299,78 +364,183 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
                     }
                 }
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = eg * qv[e] - v[e];
+                for (int e = 0; e < 32; ++e) qv[e] = eg * qv[e] - pw[e];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_A1 + (c0 >> 6) * 16384, 64 + i, (c0 & 63) / 8 + q, v + 8 * q);
+                for (int q = 0; q < 4; ++q) {
+                    const int ch = (c0 & 63) / 8 + q;
+                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv + 8 * q);
+                    tc::st_chunk<Op>(sm + P_AT + (c0 >> 6) * 8192, i, ch, pu + 8 * q);
+                }
             }
         }
+        __syncthreads();
+        // (i) the record: [W; Q'] image, U image, P U image, decay factors
+        const uint4* src_a = reinterpret_cast<const uint4*>(sm + P_A1);
+        const uint4* src_u = reinterpret_cast<const uint4*>(sm + P_R4);
+        const uint4* src_o = reinterpret_cast<const uint4*>(sm + P_AT);
+        uint4* dst = reinterpret_cast<uint4*>(rec);
+        for (int q = tid; q < 2048; q += NT) dst[REC_A4 / 16 + q] = src_a[q];
+        for (int q = tid; q < 1024; q += NT) {
+            dst[REC_U / 16 + q] = src_u[q];
+            dst[REC_O0 / 16 + q] = src_o[q];
+        }
+        float* sc = reinterpret_cast<float*>(rec + REC_SC);
+        if (tid < 64) sc[tid] = sGam[tid];
+        if (tid == 0) sc[64] = sMisc[0];
+    }
+    sync_all();
+    if (warp == 0) tc::dealloc(tm, 256);
+}
 
-        // (i) S0 (fp16) for MMA4; S <- e^{G_last} S in TMEM for MMA6
+// ================================================================== state pass ====
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_SMALL);  // [2] record buffers
+    uint64_t* bar = full + 2;                                    // MMA completion
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+
+    if (!*A.ws.valid) return;
+    const int s = A.ws.order[blockIdx.x / A.hv], h = blockIdx.x % A.hv;
+    const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
+    if (L <= 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int hk = h / A.r, Dv = A.hv * D;
+    const int nch = (L + CH - 1) / CH, gc0 = A.ws.chunk_start[s];
+    float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
+                (size_t)h * D * D;
+    const TIn* zin = static_cast<const TIn*>(A.z);
+    TOut* out = static_cast<TOut*>(A.out);
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::alloc(tmem_slot, 256);
+    sync_all();
+    const uint32_t tm = *tmem_slot;
+    uint32_t phase = 0;
+    bool ok = true;
+    auto mma_done = [&]() {
+        if (tid == 0) tc::commit(bar);
+        const bool got = mbar_wait_bounded(bar, phase, nullptr);
+        phase ^= 1u;
+        if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        ok = __syncthreads_and(got) != 0;
+        tc::fence_after_sync();
+    };
+    int issued = 0;  // records prefetched so far (thread 0)
+    auto prefetch = [&](int c) {
+        unsigned char* dst = sm + (c & 1) * S_BUF;
+        const unsigned char* rec = A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES;
+        const unsigned char* kimg = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * KIMG_BYTES;
+        mbar_arrive_expect_tx(&full[c & 1], 65536 + 16384 + 512);
+        bulk_g2s(dst + B_A4, rec, 65536, &full[c & 1]);
+        bulk_g2s(dst + B_K, kimg, 16384, &full[c & 1]);
+        bulk_g2s(dst + B_SC, rec + REC_SC, 512, &full[c & 1]);
+        issued = c + 1;
+    };
+    if (tid == 0) {
+        prefetch(0);
+        if (nch > 1) prefetch(1);
+    }
+
+    // incoming state into TMEM columns [0, 128): thread = d_v row
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        const float* row = Sg + (size_t)tid * D + c0;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) load8(row + e, v + e);
+        tc::st32(tc::taddr(tm, warp, c0), v);
+    }
+    tc::wait_st();
+    sync_all();
+
+    for (int c = 0; c < nch && ok; ++c) {
+        unsigned char* buf = sm + (c & 1) * S_BUF;
+        const int tc0 = t0 + c * CH, n = min(CH, L - c * CH);
+        const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
+        if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        ok = __syncthreads_and(got) != 0;
+        if (!ok) break;
+        const float* sc = reinterpret_cast<const float*>(buf + B_SC);
+
+        // S0 (fp16, K-major rows = d_v) for MMA4; S <- e^{G_last} S for MMA6
         {
-            const float egl = sMisc[0];
+            const float egl = sc[64];
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_S + c0), v);
+                tc::ld32(tc::taddr(tm, warp, c0), v);
                 tc::wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + OFF_B4 + (c0 >> 6) * 16384, tid, (c0 & 63) / 8 + q, v + 8 * q);
+                for (int q = 0; q < 4; ++q)
+                    tc::st_chunk<Op>(sm + S_S0 + (c0 >> 6) * 16384, tid, (c0 & 63) / 8 + q, v + 8 * q);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= egl;
-                tc::st32(tc::taddr(tm, warp, TM_S + c0), v);
+                tc::st32(tc::taddr(tm, warp, c0), v);
             }
             tc::wait_st();
         }
         tc::fence_proxy_async();
         sync_all();
 
-        // (j) MMA4: [W; Q'] x S0^T -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)
+        // MMA4: [W; Q'] x S0^T -> columns [128, 256)
         if (tid == 0)
-            tc::mma_k(tm + TM_D4, smem_addr(sm + OFF_A1), 128, smem_addr(sm + OFF_B4), 128, D,
-                           tc::idesc_f16(128, 128), 0);
+            tc::mma_k(tm + 128, smem_addr(buf + B_A4), 128, smem_addr(sm + S_S0), 128, D, tc::idesc_f16(128, 128), 0);
         mma_done();
         if (!ok) break;
 
-        // (k) rows 0-63: Delta = U - W S0^T -> Delta~^T = (gamma_j Delta_j)^T;  rows 64-127: O = Q' S0^T + P U,
-        //     gated RMSNorm, output
         if (tid < 64) {
+            // Delta~_i = gamma_i (U_i - (W S0^T)_i) -> row i of the Delta~ image
             const int i = tid;
-            const float gm = sGam[i];
+            const float gm = sc[i];
             for (int c0 = 0; c0 < D; c0 += 32) {
-                float ws_[32], u[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D4 + c0), ws_);
-                tc::ld32(tc::taddr(tm, warp, TM_U + c0), u);
+                float ws_[32];
+                tc::ld32(tc::taddr(tm, warp, 128 + c0), ws_);
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) tc::st_elem<Op>(sm + OFF_AP, c0 + e, i, gm * (u[e] - ws_[e]));
-            }
-        } else {
-            const int i = tid - 64;
-            float ss = 0.f;
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float a_[32], b_[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D4 + c0), a_);
-                tc::ld32(tc::taddr(tm, warp, TM_PU + c0), b_);
-                tc::wait_ld();
+                for (int q = 0; q < 4; ++q) {
+                    const int ch = (c0 & 63) / 8 + q;
+                    float u[8];
+                    unpack8(*reinterpret_cast<const uint4*>(buf + B_U + (c0 >> 6) * 8192 + tc::sw128_chunk(i, ch)), u);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float o = a_[e] + b_[e];
-                    ss = fmaf(o, o, ss);
+                    for (int e = 0; e < 8; ++e) u[e] = gm * (u[e] - ws_[8 * q + e]);
+                    tc::st_chunk<Op>(sm + S_A6 + (c0 >> 6) * 8192, i, ch, u);
                 }
             }
-            // tcgen05.ld is warp-collective: every lane loads, only rows of real tokens are stored
-            const float rs = rms_scale(ss, A.norm_eps, D);
-            const size_t obase = (size_t)(tc0 + (i < n ? i : 0)) * Dv + (size_t)h * D;
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float a_[32], b_[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D4 + c0), a_);
-                tc::ld32(tc::taddr(tm, warp, TM_PU + c0), b_);
-                tc::wait_ld();
-                if (i < n) {
+        } else {
+            // O_i = (Q' S0^T)_i + (P U)_i, gated RMSNorm, output
+            const int i = tid - 64;
+            float ss = 0.f;
+            for (int pass = 0; pass < 2; ++pass) {
+                const float rs = rms_scale(ss, A.norm_eps, D);
+                const size_t obase = (size_t)(tc0 + (i < n ? i : 0)) * Dv + (size_t)h * D;
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float o[32];
+                    tc::ld32(tc::taddr(tm, warp, 128 + c0), o);
+                    tc::wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int dv = c0 + e;
-                        const float y = (a_[e] + b_[e]) * rs * A.norm_w[dv] * silu_f(to_f(zin[obase + dv]));
-                        out[obase + dv] = from_f<TOut>(y);
+                    for (int q = 0; q < 4; ++q) {
+                        const int ch = (c0 & 63) / 8 + q;
+                        float p[8];
+                        unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + (c0 >> 6) * 8192 + tc::sw128_chunk(i, ch)), p);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[8 * q + e] += p[e];
+                    }
+                    if (pass == 0) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
+                    } else if (i < n) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int dv = c0 + e;
+                            out[obase + dv] = from_f<TOut>(o[e] * rs * A.norm_w[dv] * silu_f(to_f(zin[obase + dv])));
+                        }
                     }
                 }
             }
@@ -378,37 +548,49 @@ __global__ void __launch_bounds__(NT, 1) chunk_kernel(PrefillArgs A)
         tc::fence_proxy_async();
         sync_all();
 
-        // (l) MMA6: S += Delta~^T x K (accumulate onto the pre-scaled state)
+        // MMA6: S += Delta~^T x K (both read MN-major from row-wise images)
         if (tid == 0)
-            tc::mma_k(tm + TM_S, smem_addr(sm + OFF_AP), 128, smem_addr(sm + OFF_KT), 128, CH,
-                           tc::idesc_f16(128, 128), 1);
+            tc::mma_k_mixed(tm, smem_addr(sm + S_A6), 0, 1, 8192, smem_addr(buf + B_K), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 128, 1, 1), 1);
         mma_done();
+        // this buffer is free again: fetch the record two chunks ahead into it
+        if (ok && tid == 0 && c + 2 < nch) prefetch(c + 2);
     }
 
-    // the final state back to the slot
     if (ok) {
         for (int c0 = 0; c0 < D; c0 += 32) {
             float v[32];
-            tc::ld32(tc::taddr(tm, warp, TM_S + c0), v);
+            tc::ld32(tc::taddr(tm, warp, c0), v);
             tc::wait_ld();
             float* row = Sg + (size_t)tid * D + c0;
 #pragma unroll
             for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(row + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
     }
+    // every prefetched copy must land before the CTA's shared memory goes away
+    if (tid == 0) {
+        for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
+            mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
+    }
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 512);
+    if (warp == 0) tc::dealloc(tm, 256);
 }
 
 }  // namespace
 
+size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (size_t)hqk * KIMG_BYTES; }
+
 template <typename TIn, typename TOut>
 cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st)
 {
-    auto kern = chunk_kernel<TIn, TOut>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<A.n * A.hv, NT, SMEM_BYTES, st>>>(A);
+    auto state = chunk_state_kernel<TIn, TOut>;
+    e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+    if (e != cudaSuccess) return e;
+    const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
+    chunk_prep_kernel<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A);
+    state<<<A.n * A.hv, NT, S_SMEM, st>>>(A);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,10 @@ struct PrefillWorkspace {
     float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm
     float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat
     int* order = nullptr;    // [T + 64] sequences ranked by length, longest first
+    int* chunk_start = nullptr;    // [n + 1] first chunk record of each sequence (chunked path)
+    unsigned char* rec = nullptr;  // [chunk_cap][Hv] per-(chunk, v-head) records of the chunked path
+    unsigned char* kimg = nullptr; // [chunk_cap][Hqk] per-(chunk, q/k head) K images
+    int chunk_cap = 0;             // chunk records the workspace holds
     int* valid = nullptr;    // [1] 1 when the call's cu_seqlens / slot ids passed validation
     void* base = nullptr;
     size_t bytes = 0;
@@ -273,14 +277,25 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
                            const void* b, const void* z, void* out, cudaStream_t st);
 
-size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens);
+// workspace of a prefill call of up to max_tokens tokens and chunk_cap chunk records
+size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens, int chunk_cap);
 // sequences a call may carry for a workspace of max_tokens tokens
 inline int prefill_max_seqs(int max_tokens) { return max_tokens + 64; }
+// chunk records a pool reserves for calls of up to max_tokens tokens (chunked path, d = 128):
+// a call needs ceil(T / 64) + n_seqs of them at most
+inline bool prefill_chunked(const gdn_shape& s) { return s.dk == 128 && s.dv == 128; }
+inline int prefill_pool_chunk_cap(const gdn_shape& s, int max_tokens)
+{
+    return prefill_chunked(s) ? 2 * ((max_tokens + 63) / 64) + 64 : 0;
+}
+inline int prefill_call_chunks(int total_tokens, int n_seqs) { return (total_tokens + 63) / 64 + n_seqs; }
+// bytes of one chunk record set (all v-heads and q/k heads of one chunk)
+size_t chunk_record_bytes(int hv, int hqk);
 
 // chunked tensor-core prefill of the delta rule + gated RMSNorm (d_k = d_v = 128); io dtypes
 template <typename TIn, typename TOut>
 cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st);
-void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens);
+void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens, int chunk_cap);
 
 inline SlotCheck slot_check(const Pool& P, int layer)
 {

@@ -126,9 +126,10 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     if (rc == GDN_OK && cudaMalloc(&P->live_dev, (size_t)num_slots) != cudaSuccess) rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && cudaMalloc(&P->status_dev, sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && P->shape.max_prefill_tokens > 0) {
-        P->ws.bytes = gdn::prefill_workspace_bytes(P->shape, P->shape.max_prefill_tokens);
+        const int cap = gdn::prefill_pool_chunk_cap(P->shape, P->shape.max_prefill_tokens);
+        P->ws.bytes = gdn::prefill_workspace_bytes(P->shape, P->shape.max_prefill_tokens, cap);
         if (cudaMalloc(&P->ws.base, P->ws.bytes) != cudaSuccess) rc = GDN_ERR_CUDA;
-        else gdn::prefill_workspace_carve(P->ws, P->shape, P->shape.max_prefill_tokens);
+        else gdn::prefill_workspace_carve(P->ws, P->shape, P->shape.max_prefill_tokens, cap);
     }
     if (rc == GDN_OK) {
         if (enqueue_zero(P->base, P->total_bytes, 0, P->num_sms) != cudaSuccess) rc = GDN_ERR_CUDA;
@@ -258,6 +259,8 @@ int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const 
     if (!P->params[(size_t)layer].set()) return GDN_ERR_NO_PARAMS;
     if (total_tokens > P->shape.max_prefill_tokens) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs > gdn::prefill_max_seqs(P->shape.max_prefill_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (gdn::prefill_chunked(P->shape) && gdn::prefill_call_chunks(total_tokens, n_seqs) > P->ws.chunk_cap)
+        return GDN_ERR_UNSUPPORTED_SHAPE;
     cudaError_t e = gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, q, k, v, a,
                                         b, z, out, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -46,6 +46,11 @@ __global__ void validate_kernel(PrefillArgs A)
             rank += (lj > len) || (lj == len && j < s);
         }
         A.ws.order[rank] = s;
+        // first chunk record of the sequence: chunks of 64 tokens of the sequences before it
+        int cs = 0;
+        for (int j = 0; j < s; ++j) cs += (A.cu[j + 1] - A.cu[j] + 63) / 64;
+        A.ws.chunk_start[s] = cs;
+        if (s == A.n - 1) A.ws.chunk_start[A.n] = cs + (len + 63) / 64;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -272,7 +277,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
-size_t prefill_workspace_bytes(const gdn_shape& s, int T)
+size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
 {
     const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
     size_t b = 0;
@@ -281,11 +286,13 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T)
     b += align256((size_t)T * s.hv * 4) * 2;          // g, beta
     b += align256((size_t)T * s.hqk * 4);             // k.q
     b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
+    b += align256((size_t)(prefill_max_seqs(T) + 1) * 4);  // chunk starts
+    b += (size_t)chunk_cap * chunk_record_bytes(s.hv, s.hqk);  // chunk records (multiple of 256)
     b += 256;                                         // valid flag
     return b;
 }
 
-void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T)
+void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, int chunk_cap)
 {
     const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
     char* p = static_cast<char*>(ws.base);
@@ -302,6 +309,10 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T)
     ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
+    ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
+    ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 66048));
+    ws.kimg = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hqk * 16384));
+    ws.chunk_cap = chunk_cap;
     ws.valid = reinterpret_cast<int*>(take(256));
 }
 
@@ -364,7 +375,7 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
 namespace gdn {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB, held by every GPU that loads libgdn
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB, held by every GPU that loads libgdn
 
 // Host code must not use this name as a device address: the address comes from
 // cudaGetSymbolAddress, once per device (see static_scratch_address).
@@ -423,7 +434,8 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
 
     if (n_seqs > prefill_max_seqs(total_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
     // everything the call needs must fit in the static scratch: workspace, live flags, status word
-    const size_t ws_bytes = prefill_workspace_bytes(s, total_tokens);
+    const int chunk_cap = prefill_chunked(s) ? prefill_call_chunks(total_tokens, n_seqs) : 0;
+    const size_t ws_bytes = prefill_workspace_bytes(s, total_tokens, chunk_cap);
     const size_t live_bytes = align256((size_t)num_slots);
     if (ws_bytes + live_bytes + 256 > kStaticScratchBytes) return GDN_ERR_UNSUPPORTED_SHAPE;
 
@@ -432,7 +444,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     PrefillWorkspace ws;
     ws.base = scratch;
     ws.bytes = ws_bytes;
-    prefill_workspace_carve(ws, s, total_tokens);
+    prefill_workspace_carve(ws, s, total_tokens, chunk_cap);
     unsigned char* live = static_cast<unsigned char*>(scratch) + ws_bytes;
     unsigned int* status = status_dev ? status_dev : reinterpret_cast<unsigned int*>(live + live_bytes);
 
