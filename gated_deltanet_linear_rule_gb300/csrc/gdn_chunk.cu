@@ -46,7 +46,7 @@
 namespace gdn {
 namespace {
 
-constexpr int D = 128, CH = 64, NT = 128;
+constexpr int D = 128, CH = 64, NT = 256;
 using Op = __half;
 
 // record of one (chunk, v-head), written by the pre-pass, read by the state pass
@@ -73,7 +73,7 @@ constexpr uint32_t B_A4 = 0, B_U = 32768, B_O0 = 49152, B_K = 65536, B_SC = 8192
 constexpr uint32_t S_S0 = 2 * S_BUF;  // S0 in fp16, K-major: 2 K-tiles x 128 rows
 constexpr uint32_t S_A6 = S_S0 + 32768;  // Delta~ image [token][dv], halves 8 KiB apart
 constexpr uint32_t S_SMALL = S_A6 + 16384;
-constexpr size_t S_SMEM = S_SMALL + 256 + 1024;
+constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, norm weight, sums) + slack
 
 __device__ __forceinline__ void sync_all()
 {
@@ -102,12 +102,30 @@ __device__ __forceinline__ void unpack8(uint4 w, float* v)
     }
 }
 
+// 8 consecutive outputs as one 16-B (bf16) or two 16-B (fp32) stores
+template <typename T> __device__ __forceinline__ void store8(T* p, const float* y);
+template <> __device__ __forceinline__ void store8<float>(float* p, const float* y)
+{
+    reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+}
+template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const float* y)
+{
+    uint4 w;
+    w.x = tc::pack2<__nv_bfloat16>(y[0], y[1]);
+    w.y = tc::pack2<__nv_bfloat16>(y[2], y[3]);
+    w.z = tc::pack2<__nv_bfloat16>(y[4], y[5]);
+    w.w = tc::pack2<__nv_bfloat16>(y[6], y[7]);
+    *reinterpret_cast<uint4*>(p) = w;
+}
+
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 {
     return p + ((1024 - (smem_addr(p) & 1023)) & 1023);
 }
 
 // ===================================================================== pre-pass ====
+// 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 {
@@ -137,11 +155,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     const int s = lo, c = gc - A.ws.chunk_start[s];
     const int tc0 = A.cu[s] + c * CH;
     const int n = min(CH, A.cu[s + 1] - tc0);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, hf = warp >> 2;
     const int hk = h / A.r, Dq = A.hqk * D, Dv = A.hv * D;
     const bool write_k = (h % A.r) == 0;
     unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
     unsigned char* kimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * KIMG_BYTES;
+    const __half* kh16 = A.ws.kh16;
+    const __half* qh16 = A.ws.qh16;
+    const __half* vc16 = A.ws.vc16;
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -161,13 +183,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         tc::fence_after_sync();
     };
 
-    // (a) [K; Q] tile; the K image of the record; gates
+    // (a) [K; Q] tile (fp16 rows copied chunk by chunk into the swizzled layout), K image, gates
     for (int idx = tid; idx < 128 * 16; idx += NT) {
         const int r = idx >> 4, c16 = idx & 15, i = r & 63;
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (i < n) load8((r < 64 ? A.ws.kh : A.ws.qh) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8, v);
-        tc::st_chunk<Op>(sm + P_A1 + (c16 >> 3) * 16384, r, c16 & 7, v);
-        if (r < 64 && write_k) tc::st_chunk<Op>(kimg + (c16 >> 3) * 8192, i, c16 & 7, v);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (i < n) v = *reinterpret_cast<const uint4*>((r < 64 ? kh16 : qh16) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8);
+        *reinterpret_cast<uint4*>(sm + P_A1 + (c16 >> 3) * 16384 + tc::sw128_chunk(r, c16 & 7)) = v;
+        if (r < 64 && write_k) *reinterpret_cast<uint4*>(kimg + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = v;
     }
     if (tid < 64) {
         const bool in = tid < n;
@@ -194,33 +216,31 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
     mma_done();
     if (ok) {
-        // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127
+        // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127; columns 32*hf ..
         {
-            const int i = tid & 63;
+            const int row = qd * 32 + lane, i = row & 63, c0 = 32 * hf;
             const float Gi = sG[i];
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float v[32];
-                tc::ld32(tc::taddr(tm, warp, c0), v);
-                tc::wait_ld();
-                if (tid < 64) {
-                    const float bi = sB[i];
+            float v[32];
+            tc::ld32(tc::taddr(tm, warp, c0), v);
+            tc::wait_ld();
+            if (row < 64) {
+                const float bi = sB[i];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = c0 + e;
-                        FA[i * FS + j] = (j < i && i < n) ? bi * expf(Gi - sG[j]) * v[e] : 0.f;
-                    }
-                } else {
-                    float p[32];
+                for (int e = 0; e < 32; ++e) {
+                    const int j = c0 + e;
+                    FA[i * FS + j] = (j < i && i < n) ? bi * expf(Gi - sG[j]) * v[e] : 0.f;
+                }
+            } else {
+                float p[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = c0 + e;
-                        p[e] = (j <= i && i < n) ? expf(Gi - sG[j]) * v[e] : 0.f;
-                    }
+                for (int e = 0; e < 32; ++e) {
+                    const int j = c0 + e;
+                    p[e] = (j <= i && i < n) ? expf(Gi - sG[j]) * v[e] : 0.f;
+                }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        tc::st_chunk<Op>(sm + P_AP, i, c0 / 8 + q, p + 8 * q);
-                        tc::st_chunk<Op>(sm + P_AP, 64 + i, c0 / 8 + q, p + 8 * q);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    tc::st_chunk<Op>(sm + P_AP, i, c0 / 8 + q, p + 8 * q);
+                    tc::st_chunk<Op>(sm + P_AP, 64 + i, c0 / 8 + q, p + 8 * q);
                 }
             }
         }
@@ -278,26 +298,24 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             FT[(32 + i) * FS + j] = -acc;
         }
         __syncthreads();
-        //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one row per thread
-        {
-            const int i = tid & 63;
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float v[8];
+        //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one 8-column chunk per item
+        for (int idx = tid; idx < 128 * 8; idx += NT) {
+            const int r = idx >> 3, c8 = idx & 7, i = r & 63;
+            float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = c8 * 8 + e;
-                    v[e] = FT[i * FS + j] * (tid < 64 ? sB[j] : sB[j] * sEG[j]);
-                }
-                tc::st_chunk<Op>(sm + P_AT, tid, c8, v);
+            for (int e = 0; e < 8; ++e) {
+                const int j = c8 * 8 + e;
+                v[e] = FT[i * FS + j] * (r < 64 ? sB[j] : sB[j] * sEG[j]);
             }
+            tc::st_chunk<Op>(sm + P_AT, r, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
         // (d') V image [token][dv] for MMA3's second product
         for (int idx = tid; idx < 64 * 16; idx += NT) {
             const int i = idx >> 4, c16 = idx & 15;
-            float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (i < n) load8(A.ws.vc + (size_t)(tc0 + i) * Dv + h * D + c16 * 8, v);
-            tc::st_chunk<Op>(sm + P_R4 + (c16 >> 3) * 8192, i, c16 & 7, v);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (i < n) v = *reinterpret_cast<const uint4*>(vc16 + (size_t)(tc0 + i) * Dv + h * D + c16 * 8);
+            *reinterpret_cast<uint4*>(sm + P_R4 + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = v;
         }
         tc::fence_proxy_async();
         sync_all();
@@ -315,15 +333,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         // (f) W (rows 64-127 of the first product) -> [W; .] rows 0-63 and the W image;
         //     U (rows 0-63 of the second product) -> the U image (over the dead V image)
         {
-            const int i = tid & 63;
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            const int row = qd * 32 + lane, i = row & 63;
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float v[32];
-                tc::ld32(tc::taddr(tm, warp, (tid < 64 ? 128 : 0) + c0), v);
+                tc::ld32(tc::taddr(tm, warp, (row < 64 ? 128 : 0) + c0), v);
                 tc::wait_ld();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
-                    if (tid >= 64) {
+                    if (row >= 64) {
                         tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, i, ch, v + 8 * q);
                         tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                     } else {
@@ -345,30 +363,26 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         mma_done();
     }
     if (ok) {
-        // (h) rows 64-127: Q' = e^G Q - P W -> [W; Q'] rows 64-127;  P U -> the P U image
-        if (tid >= 64) {
-            const int i = tid - 64;
+        // (h) rows 64-127: Q' = e^G Q - P W -> [W; Q'] rows 64-127 (Q read from the same row of
+        //     the [K; Q] tile by the thread that overwrites it);  P U -> the P U image
+        const int row = qd * 32 + lane;
+        if (row >= 64) {
+            const int i = row - 64;
             const float eg = sEG[i];
-            const float* qrow = A.ws.qh + (size_t)(tc0 + (i < n ? i : 0)) * Dq + hk * D;
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float pw[32], pu[32], qv[32];
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
+                float pw[32], pu[32];
                 tc::ld32(tc::taddr(tm, warp, c0), pw);
                 tc::ld32(tc::taddr(tm, warp, 128 + c0), pu);
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    if (i < n) load8(qrow + c0 + e, qv + e);
-                    else {
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) qv[e + x] = 0.f;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) qv[e] = eg * qv[e] - pw[e];
-#pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
-                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv + 8 * q);
+                    unsigned char* qa = sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch);
+                    float qv[8];
+                    unpack8(*reinterpret_cast<const uint4*>(qa), qv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - pw[8 * q + e];
+                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv);
                     tc::st_chunk<Op>(sm + P_AT + (c0 >> 6) * 8192, i, ch, pu + 8 * q);
                 }
             }
@@ -393,6 +407,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 }
 
 // ================================================================== state pass ====
+// 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
+
+template <typename TIn> struct ZRow {
+    static constexpr int kWords = 64 * sizeof(TIn) / 16;  // 16-B words of 64 inputs
+};
 
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
@@ -402,12 +421,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_SMALL);  // [2] record buffers
     uint64_t* bar = full + 2;                                    // MMA completion
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+    float* s_normw = reinterpret_cast<float*>(sm + S_SMALL + 64);  // [128]
+    float* s_ss = s_normw + 128;                                   // [2][64] partial sums of O^2
 
     if (!*A.ws.valid) return;
     const int s = A.ws.order[blockIdx.x / A.hv], h = blockIdx.x % A.hv;
     const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
     if (L <= 0) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, hf = warp >> 2, row = qd * 32 + lane;
     const int hk = h / A.r, Dv = A.hv * D;
     const int nch = (L + CH - 1) / CH, gc0 = A.ws.chunk_start[s];
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
@@ -421,6 +443,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mbar_init(bar, 1);
         fence_mbar_init();
     }
+    if (tid < 128) s_normw[tid] = A.norm_w[tid];
     if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
     const uint32_t tm = *tmem_slot;
@@ -450,12 +473,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         if (nch > 1) prefetch(1);
     }
 
-    // incoming state into TMEM columns [0, 128): thread = d_v row
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    // incoming state into TMEM columns [0, 128): lane = d_v row, this warp's column half
+    for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
         float v[32];
-        const float* row = Sg + (size_t)tid * D + c0;
+        const float* srow = Sg + (size_t)row * D + c0;
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) load8(row + e, v + e);
+        for (int e = 0; e < 32; e += 8) load8(srow + e, v + e);
         tc::st32(tc::taddr(tm, warp, c0), v);
     }
     tc::wait_st();
@@ -464,6 +487,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     for (int c = 0; c < nch && ok; ++c) {
         unsigned char* buf = sm + (c & 1) * S_BUF;
         const int tc0 = t0 + c * CH, n = min(CH, L - c * CH);
+        // the gate z of this thread's output row (rows 64-127 = tokens) is fetched early
+        constexpr int ZW = ZRow<TIn>::kWords;
+        uint4 zr[ZW];
+        const int orow = row - 64;
+        const size_t obase = (size_t)(tc0 + (orow >= 0 && orow < n ? orow : 0)) * Dv + (size_t)h * D + 64 * hf;
+        if (row >= 64) {
+            const uint4* zp = reinterpret_cast<const uint4*>(zin + obase);
+#pragma unroll
+            for (int q = 0; q < ZW; ++q) zr[q] = zp[q];
+        }
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         ok = __syncthreads_and(got) != 0;
@@ -473,13 +506,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         // S0 (fp16, K-major rows = d_v) for MMA4; S <- e^{G_last} S for MMA6
         {
             const float egl = sc[64];
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float v[32];
                 tc::ld32(tc::taddr(tm, warp, c0), v);
                 tc::wait_ld();
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    tc::st_chunk<Op>(sm + S_S0 + (c0 >> 6) * 16384, tid, (c0 & 63) / 8 + q, v + 8 * q);
+                    tc::st_chunk<Op>(sm + S_S0 + (c0 >> 6) * 16384, row, (c0 & 63) / 8 + q, v + 8 * q);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= egl;
                 tc::st32(tc::taddr(tm, warp, c0), v);
@@ -495,11 +528,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mma_done();
         if (!ok) break;
 
-        if (tid < 64) {
+        if (row < 64) {
             // Delta~_i = gamma_i (U_i - (W S0^T)_i) -> row i of the Delta~ image
-            const int i = tid;
+            const int i = row;
             const float gm = sc[i];
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float ws_[32];
                 tc::ld32(tc::taddr(tm, warp, 128 + c0), ws_);
                 tc::wait_ld();
@@ -514,34 +547,43 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 }
             }
         } else {
-            // O_i = (Q' S0^T)_i + (P U)_i, gated RMSNorm, output
-            const int i = tid - 64;
+            // O_i = (Q' S0^T)_i + (P U)_i over this warp's 64 columns; the other half's sum of
+            // squares comes through shared memory
+            const int i = orow;
+            float o[64];
             float ss = 0.f;
-            for (int pass = 0; pass < 2; ++pass) {
-                const float rs = rms_scale(ss, A.norm_eps, D);
-                const size_t obase = (size_t)(tc0 + (i < n ? i : 0)) * Dv + (size_t)h * D;
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float o[32];
-                    tc::ld32(tc::taddr(tm, warp, 128 + c0), o);
-                    tc::wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int ch = (c0 & 63) / 8 + q;
-                        float p[8];
-                        unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + (c0 >> 6) * 8192 + tc::sw128_chunk(i, ch)), p);
+            for (int p2 = 0; p2 < 2; ++p2) {
+                const int c0 = 64 * hf + 32 * p2;
+                float t[32];
+                tc::ld32(tc::taddr(tm, warp, 128 + c0), t);
+                tc::wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) o[8 * q + e] += p[e];
+                for (int q = 0; q < 4; ++q) {
+                    float pu[8];
+                    unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + hf * 8192 + tc::sw128_chunk(i, 4 * p2 + q)), pu);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float x = t[8 * q + e] + pu[e];
+                        o[32 * p2 + 8 * q + e] = x;
+                        ss = fmaf(x, x, ss);
                     }
-                    if (pass == 0) {
+                }
+            }
+            s_ss[hf * 64 + i] = ss;
+            named_bar_sync(2, 128);  // the four output warps
+            const float rs = rms_scale(s_ss[i] + s_ss[64 + i], A.norm_eps, D);
+            if (i < n) {
+                const TIn* zv = reinterpret_cast<const TIn*>(zr);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
-                    } else if (i < n) {
+                for (int e8 = 0; e8 < 64; e8 += 8) {
+                    float y[8];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int dv = c0 + e;
-                            out[obase + dv] = from_f<TOut>(o[e] * rs * A.norm_w[dv] * silu_f(to_f(zin[obase + dv])));
-                        }
+                    for (int e = 0; e < 8; ++e) {
+                        const int dv = 64 * hf + e8 + e;
+                        y[e] = o[e8 + e] * rs * s_normw[dv] * silu_f(to_f(zv[e8 + e]));
                     }
+                    store8<TOut>(out + obase + e8, y);
                 }
             }
         }
@@ -558,13 +600,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
 
     if (ok) {
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
             float v[32];
             tc::ld32(tc::taddr(tm, warp, c0), v);
             tc::wait_ld();
-            float* row = Sg + (size_t)tid * D + c0;
+            float* srow = Sg + (size_t)row * D + c0;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(row + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(srow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
     }
     // every prefetched copy must land before the CTA's shared memory goes away

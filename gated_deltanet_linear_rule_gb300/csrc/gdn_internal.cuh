@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,11 +23,16 @@ struct LayerParams {
     bool set() const { return conv_w && A_log && dt_bias && norm_w; }
 };
 
-// Prefill workspace: per-token intermediates of the varlen prefill.
+// Prefill workspace: per-token intermediates of the varlen prefill.  The recurrent path
+// (d < 128) keeps q, k, v in fp32; the chunked tensor-core path (d = 128) in fp16, the
+// precision its MMA operands have anyway.
 struct PrefillWorkspace {
-    float* qh = nullptr;     // [T][Hqk*dk] normalised q, scaled by dk^-1/2
-    float* kh = nullptr;     // [T][Hqk*dk] normalised k
-    float* vc = nullptr;     // [T][Hv*dv]  conv + SiLU v
+    float* qh = nullptr;     // [T][Hqk*dk] normalised q, scaled by dk^-1/2   (recurrent path)
+    float* kh = nullptr;     // [T][Hqk*dk] normalised k                      (recurrent path)
+    float* vc = nullptr;     // [T][Hv*dv]  conv + SiLU v                     (recurrent path)
+    __half* qh16 = nullptr;  // the same three in fp16                        (chunked path)
+    __half* kh16 = nullptr;
+    __half* vc16 = nullptr;
     float* g = nullptr;      // [T][Hv]     log decay
     float* beta = nullptr;   // [T][Hv]
     float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm

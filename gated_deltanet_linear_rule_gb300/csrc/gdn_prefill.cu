@@ -124,6 +124,14 @@ __global__ void __launch_bounds__(256) prep_kernel(PrefillArgs A)
         A.ws.beta[(size_t)t * A.hv + h] = sigmoid_f(to_f(bin[(size_t)t * A.hv + h]));
     }
     __syncthreads();
+    if (A.D == 128) {  // chunked path: fp16 rows
+        for (int c = threadIdx.x; c < C; c += blockDim.x) {
+            if (c < Dq) A.ws.qh16[(size_t)t * Dq + c] = __float2half_rn(y[c] * scale[c / D]);
+            else if (c < 2 * Dq) A.ws.kh16[(size_t)t * Dq + (c - Dq)] = __float2half_rn(y[c] * scale[c / D]);
+            else A.ws.vc16[(size_t)t * (A.hv * D) + (c - 2 * Dq)] = __float2half_rn(y[c]);
+        }
+        return;
+    }
     for (int hk = threadIdx.x; hk < A.hqk; hk += blockDim.x)
         A.kq[(size_t)t * A.hqk + hk] = dots[hk] * scale[hk] * scale[A.hqk + hk];
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
@@ -281,10 +289,15 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
 {
     const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
     size_t b = 0;
-    b += align256((size_t)T * Dq * 4) * 2;            // qh, kh
-    b += align256((size_t)T * Dv * 4) * 2;            // vc, o
+    if (prefill_chunked(s)) {
+        b += align256((size_t)T * Dq * 2) * 2;        // qh16, kh16
+        b += align256((size_t)T * Dv * 2);            // vc16
+    } else {
+        b += align256((size_t)T * Dq * 4) * 2;        // qh, kh
+        b += align256((size_t)T * Dv * 4) * 2;        // vc, o
+        b += align256((size_t)T * s.hqk * 4);         // k.q
+    }
     b += align256((size_t)T * s.hv * 4) * 2;          // g, beta
-    b += align256((size_t)T * s.hqk * 4);             // k.q
     b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
     b += align256((size_t)(prefill_max_seqs(T) + 1) * 4);  // chunk starts
     b += (size_t)chunk_cap * chunk_record_bytes(s.hv, s.hqk);  // chunk records (multiple of 256)
@@ -301,13 +314,19 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
         p += align256(bytes);
         return r;
     };
-    ws.qh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
-    ws.kh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
-    ws.vc = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
-    ws.o = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
+    if (prefill_chunked(s)) {
+        ws.qh16 = reinterpret_cast<__half*>(take((size_t)T * Dq * 2));
+        ws.kh16 = reinterpret_cast<__half*>(take((size_t)T * Dq * 2));
+        ws.vc16 = reinterpret_cast<__half*>(take((size_t)T * Dv * 2));
+    } else {
+        ws.qh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
+        ws.kh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
+        ws.vc = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
+        ws.o = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
+        ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
+    }
     ws.g = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
-    ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
     ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
     ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 66048));
