@@ -121,6 +121,12 @@ __device__ __forceinline__ float log_decay(float A_log, float a, float dt_bias)
     return -expf(A_log) * softplus_f(a + dt_bias);
 }
 
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
 // ----------------------------------------------------------- mbarriers ----
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait

@@ -141,6 +141,136 @@ __global__ void __launch_bounds__(256) prep_kernel(PrefillArgs A)
     }
 }
 
+// 8 io values of one row -> float (16-B or 32-B load)
+template <typename T> __device__ __forceinline__ void load8_io(const T* p, float* v);
+template <> __device__ __forceinline__ void load8_io<float>(const float* p, float* v)
+{
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8_io<__nv_bfloat16>(const __nv_bfloat16* p, float* v)
+{
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        v[2 * q] = f.x;
+        v[2 * q + 1] = f.y;
+    }
+}
+
+// Prep for the chunked path (d = 128, conv width W <= 4): a thread owns 8 consecutive channels
+// over a block of 32 tokens, keeps the conv window and weights in registers, and normalises
+// q / k heads (128 channels = 16 threads) with half-warp shuffles.  fp16 rows out; gates from
+// the CTAs of the first channel block.
+constexpr int kPrepTokens = 32;
+
+template <typename TIn, int W>
+__global__ void __launch_bounds__(256) prep_chunked_kernel(PrefillArgs A)
+{
+    if (!*A.ws.valid) return;
+    const int D = 128, Dq = A.hqk * D, Dv = A.hv * D, C = A.C;
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
+    const int c8 = g * 8;
+    const int tb0 = blockIdx.y * kPrepTokens, tb1 = min(A.T, tb0 + kPrepTokens);
+    const bool active = c8 < C;
+
+    // gates of this token block
+    if (blockIdx.x == 0) {
+        const TIn* ain = static_cast<const TIn*>(A.a);
+        const TIn* bin = static_cast<const TIn*>(A.b);
+        for (int idx = threadIdx.x; idx < (tb1 - tb0) * A.hv; idx += blockDim.x) {
+            const int t = tb0 + idx / A.hv, h = idx % A.hv;
+            A.ws.g[(size_t)t * A.hv + h] = log_decay(A.A_log[h], to_f(ain[(size_t)t * A.hv + h]), A.dt_bias[h]);
+            A.ws.beta[(size_t)t * A.hv + h] = sigmoid_f(to_f(bin[(size_t)t * A.hv + h]));
+        }
+    }
+    if (tb0 >= tb1) return;
+
+    // channel kind and source row of these 8 channels
+    const TIn* src;
+    int width, col;
+    __half* dst;
+    int kind;  // 0 = q, 1 = k, 2 = v
+    if (c8 < Dq) { src = static_cast<const TIn*>(A.q); width = Dq; col = c8; dst = A.ws.qh16; kind = 0; }
+    else if (c8 < 2 * Dq) { src = static_cast<const TIn*>(A.k); width = Dq; col = c8 - Dq; dst = A.ws.kh16; kind = 1; }
+    else { src = static_cast<const TIn*>(A.v); width = Dv; col = c8 - 2 * Dq; dst = A.ws.vc16; kind = 2; }
+    if (!active) { src = static_cast<const TIn*>(A.q); width = Dq; col = 0; dst = nullptr; kind = 2; }
+
+    float w[8][W];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int j = 0; j < W; ++j) w[e][j] = active ? A.conv_w[(size_t)(c8 + e) * W + j] : 0.f;
+
+    // the sequence of the first token, and the W-1 inputs before it
+    int s = 0;
+    {
+        int lo = 0, hi = A.n;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (A.cu[mid] <= tb0) lo = mid;
+            else hi = mid;
+        }
+        s = lo;
+    }
+    float win[W > 1 ? W - 1 : 1][8];  // win[0] = oldest
+    auto load_window = [&](int t) {   // inputs before token t of sequence s
+        const int pos = t - A.cu[s];
+        const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
+                                                                    A.slot_bytes + A.state_bytes);
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) {
+            const int pp = pos - (W - 1) + j;  // position of window entry j
+            if (pp >= 0) load8_io<TIn>(src + (size_t)(t - (W - 1) + j) * width + col, win[j]);
+            else load8_io<TIn>(cbuf + (size_t)(W - 1 + pp) * C + c8, win[j]);
+        }
+    };
+    while (s + 1 < A.n && A.cu[s + 1] <= tb0) ++s;
+    if (active) load_window(tb0);
+
+    for (int t = tb0; t < tb1; ++t) {
+        if (t >= A.cu[s + 1]) {  // a new sequence starts here (skip empty ones)
+            while (s + 1 < A.n && A.cu[s + 1] <= t) ++s;
+            if (active) load_window(t);
+        }
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (active) load8_io<TIn>(src + (size_t)t * width + col, x);
+        float y[8];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) acc = fmaf(w[e][j], win[j][e], acc);
+            acc = fmaf(w[e][W - 1], x[e], acc);
+            y[e] = silu_f(acc);
+            ss = fmaf(y[e], y[e], ss);
+        }
+#pragma unroll
+        for (int j = 0; j + 1 < W - 1; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+        if (W > 1) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) win[W - 2][e] = x[e];
+        }
+        // q / k heads: sum of squares over the 16 threads of the head
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float sc = kind == 0 ? rsqrtf(ss + A.l2_eps) * rsqrtf((float)D) : kind == 1 ? rsqrtf(ss + A.l2_eps) : 1.f;
+        if (active) {
+            uint4 o;
+            o.x = pack_half2(y[0] * sc, y[1] * sc);
+            o.y = pack_half2(y[2] * sc, y[3] * sc);
+            o.z = pack_half2(y[4] * sc, y[5] * sc);
+            o.w = pack_half2(y[6] * sc, y[7] * sc);
+            *reinterpret_cast<uint4*>(dst + (size_t)t * width + col) = o;
+        }
+    }
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(256) conv_tail_kernel(PrefillArgs A)
 {
@@ -151,7 +281,7 @@ __global__ void __launch_bounds__(256) conv_tail_kernel(PrefillArgs A)
     TIn* cbuf = reinterpret_cast<TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes +
                                        A.state_bytes);
     const int W = A.W, C = A.C;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < C; c += gridDim.y * blockDim.x) {
         TIn old[8];
         for (int j = 0; j < W - 1; ++j) old[j] = cbuf[(size_t)j * C + c];
         for (int i = 0; i < W - 1; ++i) {
@@ -258,9 +388,19 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
                 cudaFuncSetAttribute(prep_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
         }
-        prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
+        if (A.D == 128 && A.W <= 4 && A.C % 8 == 0) {
+            dim3 grid((A.C / 8 + 255) / 256, (A.T + kPrepTokens - 1) / kPrepTokens);
+            switch (A.W) {
+                case 1: prep_chunked_kernel<TIn, 1><<<grid, 256, 0, st>>>(A); break;
+                case 2: prep_chunked_kernel<TIn, 2><<<grid, 256, 0, st>>>(A); break;
+                case 3: prep_chunked_kernel<TIn, 3><<<grid, 256, 0, st>>>(A); break;
+                default: prep_chunked_kernel<TIn, 4><<<grid, 256, 0, st>>>(A); break;
+            }
+        } else {
+            prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
+        }
     }
-    conv_tail_kernel<TIn><<<A.n, 256, 0, st>>>(A);
+    conv_tail_kernel<TIn><<<dim3(A.n, (A.C + 255) / 256), 256, 0, st>>>(A);
     if (A.T > 0 && A.D == 128) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
