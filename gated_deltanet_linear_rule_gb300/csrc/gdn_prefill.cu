@@ -160,6 +160,25 @@ template <> __device__ __forceinline__ void load8_io<__nv_bfloat16>(const __nv_b
     }
 }
 
+// 8 io values through the read-only data path (the inputs are not written by this kernel)
+template <typename T> __device__ __forceinline__ void load8_ro(const T* p, float* v);
+template <> __device__ __forceinline__ void load8_ro<float>(const float* p, float* v)
+{
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8_ro<__nv_bfloat16>(const __nv_bfloat16* p, float* v)
+{
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        v[2 * q] = f.x;
+        v[2 * q + 1] = f.y;
+    }
+}
+
 // Prep for the chunked path (d = 128, conv width W <= 4): a thread owns 8 consecutive channels
 // over a block of 32 tokens, keeps the conv window and weights in registers, and normalises
 // q / k heads (128 channels = 16 threads) with half-warp shuffles.  fp16 rows out; gates from
@@ -230,13 +249,19 @@ __global__ void __launch_bounds__(256) prep_chunked_kernel(PrefillArgs A)
     while (s + 1 < A.n && A.cu[s + 1] <= tb0) ++s;
     if (active) load_window(tb0);
 
+    // inputs are read through the read-only path one token ahead of their use, so the next
+    // load is in flight while this token is computed and stored
+    float xn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (active) load8_ro<TIn>(src + (size_t)tb0 * width + col, xn);
     for (int t = tb0; t < tb1; ++t) {
         if (t >= A.cu[s + 1]) {  // a new sequence starts here (skip empty ones)
             while (s + 1 < A.n && A.cu[s + 1] <= t) ++s;
             if (active) load_window(t);
         }
-        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (active) load8_io<TIn>(src + (size_t)t * width + col, x);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = xn[e];
+        if (active && t + 1 < tb1) load8_ro<TIn>(src + (size_t)(t + 1) * width + col, xn);
         float y[8];
         float ss = 0.f;
 #pragma unroll
