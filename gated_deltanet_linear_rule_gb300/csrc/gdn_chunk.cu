@@ -506,17 +506,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         // S0 (fp16, K-major rows = d_v) for MMA4; S <- e^{G_last} S for MMA6
         {
             const float egl = sc[64];
-            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-                float v[32];
-                tc::ld32(tc::taddr(tm, warp, c0), v);
-                tc::wait_ld();
+            float v0[32], v1[32];
+            tc::ld32(tc::taddr(tm, warp, 64 * hf), v0);
+            tc::ld32(tc::taddr(tm, warp, 64 * hf + 32), v1);
+            tc::wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tc::st_chunk<Op>(sm + S_S0 + (c0 >> 6) * 16384, row, (c0 & 63) / 8 + q, v + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] *= egl;
-                tc::st32(tc::taddr(tm, warp, c0), v);
+            for (int q = 0; q < 4; ++q) {
+                tc::st_chunk<Op>(sm + S_S0 + hf * 16384, row, q, v0 + 8 * q);
+                tc::st_chunk<Op>(sm + S_S0 + hf * 16384, row, 4 + q, v1 + 8 * q);
             }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                v0[e] *= egl;
+                v1[e] *= egl;
+            }
+            tc::st32(tc::taddr(tm, warp, 64 * hf), v0);
+            tc::st32(tc::taddr(tm, warp, 64 * hf + 32), v1);
             tc::wait_st();
         }
         tc::fence_proxy_async();
@@ -546,55 +551,61 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                     tc::st_chunk<Op>(sm + S_A6 + (c0 >> 6) * 8192, i, ch, u);
                 }
             }
-        } else {
-            // O_i = (Q' S0^T)_i + (P U)_i over this warp's 64 columns; the other half's sum of
-            // squares comes through shared memory
+        }
+        // rows 64-127: O_i = (Q' S0^T)_i + (P U)_i over this warp's 64 columns, kept in registers
+        // while MMA6 runs; the other half's sum of squares comes through shared memory
+        float o[64];
+        if (row >= 64) {
             const int i = orow;
-            float o[64];
             float ss = 0.f;
+            float t0v[32], t1v[32];
+            tc::ld32(tc::taddr(tm, warp, 128 + 64 * hf), t0v);
+            tc::ld32(tc::taddr(tm, warp, 128 + 64 * hf + 32), t1v);
+            tc::wait_ld();
 #pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                const int c0 = 64 * hf + 32 * p2;
-                float t[32];
-                tc::ld32(tc::taddr(tm, warp, 128 + c0), t);
-                tc::wait_ld();
+            for (int q = 0; q < 8; ++q) {
+                float pu[8];
+                unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + hf * 8192 + tc::sw128_chunk(i, q)), pu);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float pu[8];
-                    unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + hf * 8192 + tc::sw128_chunk(i, 4 * p2 + q)), pu);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float x = t[8 * q + e] + pu[e];
-                        o[32 * p2 + 8 * q + e] = x;
-                        ss = fmaf(x, x, ss);
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    const float x = (q < 4 ? t0v[8 * q + e] : t1v[8 * (q - 4) + e]) + pu[e];
+                    o[8 * q + e] = x;
+                    ss = fmaf(x, x, ss);
                 }
             }
             s_ss[hf * 64 + i] = ss;
-            named_bar_sync(2, 128);  // the four output warps
-            const float rs = rms_scale(s_ss[i] + s_ss[64 + i], A.norm_eps, D);
-            if (i < n) {
-                const TIn* zv = reinterpret_cast<const TIn*>(zr);
-#pragma unroll
-                for (int e8 = 0; e8 < 64; e8 += 8) {
-                    float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int dv = 64 * hf + e8 + e;
-                        y[e] = o[e8 + e] * rs * s_normw[dv] * silu_f(to_f(zv[e8 + e]));
-                    }
-                    store8<TOut>(out + obase + e8, y);
-                }
-            }
         }
         tc::fence_proxy_async();
         sync_all();
 
-        // MMA6: S += Delta~^T x K (both read MN-major from row-wise images)
-        if (tid == 0)
+        // MMA6: S += Delta~^T x K (both read MN-major from row-wise images); the output rows'
+        // gated RMSNorm runs while it does
+        if (tid == 0) {
             tc::mma_k_mixed(tm, smem_addr(sm + S_A6), 0, 1, 8192, smem_addr(buf + B_K), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 1, 1), 1);
-        mma_done();
+            tc::commit(bar);
+        }
+        if (row >= 64 && orow < n) {
+            const float rs = rms_scale(s_ss[orow] + s_ss[64 + orow], A.norm_eps, D);
+            const TIn* zv = reinterpret_cast<const TIn*>(zr);
+#pragma unroll
+            for (int e8 = 0; e8 < 64; e8 += 8) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int dv = 64 * hf + e8 + e;
+                    y[e] = o[e8 + e] * rs * s_normw[dv] * silu_f(to_f(zv[e8 + e]));
+                }
+                store8<TOut>(out + obase + e8, y);
+            }
+        }
+        {
+            const bool got6 = mbar_wait_bounded(bar, phase, nullptr);
+            phase ^= 1u;
+            if (!got6 && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = __syncthreads_and(got6) != 0;
+            tc::fence_after_sync();
+        }
         // this buffer is free again: fetch the record two chunks ahead into it
         if (ok && tid == 0 && c + 2 < nch) prefetch(c + 2);
     }
