@@ -183,30 +183,51 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         tc::fence_after_sync();
     };
 
-    // (a) [K; Q] tile (fp16 rows copied chunk by chunk into the swizzled layout), K image, gates
-    for (int idx = tid; idx < 128 * 16; idx += NT) {
-        const int r = idx >> 4, c16 = idx & 15, i = r & 63;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (i < n) v = *reinterpret_cast<const uint4*>((r < 64 ? kh16 : qh16) + (size_t)(tc0 + i) * Dq + hk * D + c16 * 8);
-        *reinterpret_cast<uint4*>(sm + P_A1 + (c16 >> 3) * 16384 + tc::sw128_chunk(r, c16 & 7)) = v;
-        if (r < 64 && write_k) *reinterpret_cast<uint4*>(kimg + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = v;
+    // (a) [K; Q] tile (fp16 rows copied chunk by chunk into the swizzled layout), K image, gates.
+    //     All loads are issued before any store; the V rows are fetched now and parked in
+    //     registers until the inverse has freed their shared-memory space.
+    {
+        uint4 kq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int idx = tid + q * NT, r = idx >> 4, c16 = idx & 15, i = r & 63;
+            kq[q] = i < n ? __ldg(reinterpret_cast<const uint4*>((r < 64 ? kh16 : qh16) + (size_t)(tc0 + i) * Dq +
+                                                                   hk * D + c16 * 8))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int idx = tid + q * NT, r = idx >> 4, c16 = idx & 15, i = r & 63;
+            *reinterpret_cast<uint4*>(sm + P_A1 + (c16 >> 3) * 16384 + tc::sw128_chunk(r, c16 & 7)) = kq[q];
+            if (r < 64 && write_k) *reinterpret_cast<uint4*>(kimg + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = kq[q];
+        }
     }
+    uint4 vpark[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int idx = tid + q * NT, i = idx >> 4, c16 = idx & 15;
+        vpark[q] = i < n ? __ldg(reinterpret_cast<const uint4*>(vc16 + (size_t)(tc0 + i) * Dv + h * D + c16 * 8))
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // decay prefix G_i = g_0 + ... + g_i: a shuffle scan per warp, then warp 1 adds warp 0's total
     if (tid < 64) {
         const bool in = tid < n;
-        sGraw[tid] = in ? A.ws.g[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
+        float x = in ? A.ws.g[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
         sB[tid] = in ? A.ws.beta[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        sG[tid] = x;
     }
     tc::fence_proxy_async();
     sync_all();
-    if (tid < 64) {
-        float acc = 0.f;
-        for (int t = 0; t <= tid; ++t) acc += sGraw[t];
-        sG[tid] = acc;
-        sEG[tid] = expf(acc);
-    }
+    if (tid >= 32 && tid < 64) sG[tid] += sG[31];
     __syncthreads();
     if (tid < 64) {
         const float gl = sG[n - 1];
+        sEG[tid] = expf(sG[tid]);
         sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
         if (tid == 0) sMisc[0] = expf(gl);
     }
@@ -310,12 +331,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             tc::st_chunk<Op>(sm + P_AT, r, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
-        // (d') V image [token][dv] for MMA3's second product
-        for (int idx = tid; idx < 64 * 16; idx += NT) {
-            const int i = idx >> 4, c16 = idx & 15;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (i < n) v = *reinterpret_cast<const uint4*>(vc16 + (size_t)(tc0 + i) * Dv + h * D + c16 * 8);
-            *reinterpret_cast<uint4*>(sm + P_R4 + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = v;
+        // (d') V image [token][dv] for MMA3's second product, from the rows parked in registers
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c16 = idx & 15;
+            *reinterpret_cast<uint4*>(sm + P_R4 + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = vpark[q];
         }
         tc::fence_proxy_async();
         sync_all();
