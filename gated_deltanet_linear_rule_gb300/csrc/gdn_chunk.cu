@@ -282,9 +282,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 #pragma unroll
             for (int i = 0; i < 16; ++i) FT[(o + i) * FS + o + j] = x[i];
         }
-        for (int idx = tid; idx < 64 * 64; idx += NT) {
-            const int i = idx >> 6, j = idx & 63;
-            if ((j >> 4) > (i >> 4)) FT[i * FS + j] = 0.f;
+        for (int idx = tid; idx < 6 * 256; idx += NT) {  // the six 16x16 blocks above the diagonal
+            const int blk = idx >> 8, e = idx & 255;
+            const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+            const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+            FT[(16 * bi + (e >> 4)) * FS + 16 * bj + (e & 15)] = 0.f;
         }
         __syncthreads();
         //     ... then 16 -> 32: T_10 = -T_11 (A_10 T_00) for the block pairs (0,1), (2,3) ...
