@@ -114,3 +114,21 @@ def distinct_slots(workload: int, m: int, num_slots: int, sub: int = 0) -> np.nd
 def rng(workload: int, tag: str = "schedule", sub: int = 0) -> np.random.Generator:
     """A generator for schedule decisions (admit/finish choices) of a workload."""
     return _gen(workload, 0, 0, tag, sub)
+
+
+def device_token_inputs(workload: int, layer: int, ident: int, L: int, hqk: int, hv: int, dk: int, dv: int,
+                        io_dtype: str, tag: str = "prefill", sub: int = 0, device: str = "cuda"):
+    """Large inputs drawn on the device with torch's seeded counter-based (Philox) CUDA generator, keyed
+    like token_inputs: q, k [L][Hqk*dk]; v, z [L][Hv*dv]; a, b [L][Hv] ~ N(0, 1) in the io dtype.
+    For workloads too large to draw on the host; the same tensors (copied to the host) feed the oracle."""
+    import torch
+
+    seed = ((int(workload) & 0xFF) << 56) | ((int(layer) & 0xFF) << 48) | ((_TAGS[tag] & 0xFF) << 40) | \
+           ((int(ident) & 0xFFFFF) << 20) | (int(sub) & 0xFFFFF)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if io_dtype == "bf16" else torch.float32
+    out = {}
+    for name, width in (("q", hqk * dk), ("k", hqk * dk), ("v", hv * dv), ("z", hv * dv), ("a", hv), ("b", hv)):
+        out[name] = torch.randn((L, width), generator=g, device=device, dtype=torch.float32).to(dt)
+    return out

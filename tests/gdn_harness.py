@@ -93,7 +93,7 @@ class Layer:
     # -- inputs ------------------------------------------------------------
     def to_dev(self, inp):
         dt = self.pool.torch_io
-        return {k: dev(v, dt) for k, v in inp.items()}
+        return {k: (v.contiguous() if isinstance(v, torch.Tensor) else dev(v, dt)) for k, v in inp.items()}
 
     def decode_inputs(self, idents, step, layer=0):
         return synth.batch_inputs(self.workload, layer, idents, 1, self.hqk, self.hv, self.d, self.d, self.io,
@@ -125,6 +125,33 @@ class Layer:
         return self.oracle.layer(self.oshape, np.asarray(cu, dtype=np.int64), inp["q"], inp["k"], inp["v"], inp["a"],
                                  inp["b"], inp["z"], p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], S, conv,
                                  head_mask=head_mask, threads=threads)
+
+
+def oracle_heads(L: "Layer", layer, cu, inp, S0, conv0, heads, threads=0):
+    """The oracle for selected v-heads only, each on a head-sliced problem (1 q/k head, 1 v head):
+    heads are independent apart from the q/k head they read, so the slice is the same computation.
+    inp: host arrays (or device tensors) as for Layer.oracle_run; S0 [n][Hv][d][d]; conv0 [n][W-1][C].
+    Returns {h: (out [T][d], S [n][d][d])}."""
+    d, r, W = L.d, L.hv // L.hqk, L.W
+    Cq = L.hqk * d
+    p = L.params[layer]
+    shape = dict(L.oshape, hqk=1, hv=1)
+    res = {}
+    for h in heads:
+        hk = h // r
+        qs, ks, vs = slice(hk * d, (hk + 1) * d), slice(hk * d, (hk + 1) * d), slice(h * d, (h + 1) * d)
+        ch = np.concatenate([np.arange(hk * d, (hk + 1) * d), Cq + np.arange(hk * d, (hk + 1) * d),
+                             2 * Cq + np.arange(h * d, (h + 1) * d)])
+        sub = {"q": inp["q"][:, qs], "k": inp["k"][:, ks], "v": inp["v"][:, vs], "z": inp["z"][:, vs],
+               "a": inp["a"][:, h:h + 1], "b": inp["b"][:, h:h + 1]}
+        # device tensors are sliced on the device and only the head's columns come to the host
+        sub = {k: (host(v) if isinstance(v, torch.Tensor) else np.asarray(v)) for k, v in sub.items()}
+        o = L.oracle.layer(shape, np.asarray(cu, dtype=np.int64), sub["q"], sub["k"], sub["v"], sub["a"], sub["b"],
+                           sub["z"], p["conv_w"][ch], p["A_log"][h:h + 1], p["dt_bias"][h:h + 1], p["norm_w"],
+                           np.ascontiguousarray(S0[:, h:h + 1]), np.ascontiguousarray(conv0[:, :, ch]),
+                           threads=threads)
+        res[h] = (o["out"], o["S"][:, 0])
+    return res
 
 
 def random_states(workload, layer, slots, hv, d, var=0.1):
