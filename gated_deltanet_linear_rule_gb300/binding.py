@@ -29,7 +29,7 @@ EXPORTS = [
     "gdn_pool_create", "gdn_pool_destroy", "gdn_pool_reset", "gdn_slot_alloc", "gdn_slot_recycle",
     "gdn_slot_addr", "gdn_slot_ptrs", "gdn_layer_params", "gdn_decode_step", "gdn_prefill_varlen",
     "gdn_last_device_status", "gdn_pool_get_info", "gdn_status_string", "gdn_version",
-    "gdn_prefill_varlen_noalloc",
+    "gdn_prefill_varlen_noalloc", "gdn_slot_snapshot", "gdn_slot_restore",
 ]
 
 
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_pool_get_info.argtypes = [vp, ctypes.POINTER(GdnPoolInfo)]
         L.gdn_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(GdnShape), vp, vp, vp, vp, vp, i, vp, vp, i, i,
                                                  vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_slot_snapshot.argtypes = [vp, i, vp, vp]
+        L.gdn_slot_restore.argtypes = [vp, i, vp, vp]
         L.gdn_status_string.argtypes = [i]
         L.gdn_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -188,6 +190,23 @@ class Pool:
         a = ctypes.c_uint64()
         _check(lib().gdn_slot_addr(self._h, int(layer), int(slot), ctypes.byref(a)), "gdn_slot_addr")
         return a.value
+
+    def snapshot_bytes(self) -> int:
+        inf = self.info()
+        return int(inf.slot_bytes) * self.num_layers
+
+    def snapshot(self, slot: int, dst: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Copy every layer of a slot into dst (a uint8 tensor on the device or in pinned host memory)."""
+        if dst is None:
+            dst = torch.empty(self.snapshot_bytes(), dtype=torch.uint8, device="cuda")
+        assert dst.numel() * dst.element_size() >= self.snapshot_bytes()
+        _check(lib().gdn_slot_snapshot(self._h, int(slot), _p(dst), _stream(stream)), "gdn_slot_snapshot")
+        return dst
+
+    def restore(self, slot: int, src: torch.Tensor, stream=None):
+        """Overwrite every layer of an allocated slot with a snapshot."""
+        assert src.numel() * src.element_size() >= self.snapshot_bytes()
+        _check(lib().gdn_slot_restore(self._h, int(slot), _p(src), _stream(stream)), "gdn_slot_restore")
 
     def slot_ptrs(self, layer: int, slot_ids: torch.Tensor, out: torch.Tensor | None = None, stream=None):
         """Device u64 slot-pointer array (returned as an int64 tensor) for the given int32 device ids."""

@@ -215,6 +215,26 @@ int gdn_slot_addr(gdn_pool* P, int layer, int slot_id, uint64_t* addr)
     return GDN_OK;
 }
 
+int gdn_slot_snapshot(gdn_pool* P, int slot_id, void* dst, void* stream)
+{
+    if (!P || !dst) return GDN_ERR_INVALID_ARG;
+    if (slot_id < 0 || slot_id >= P->num_slots || !P->live[(size_t)slot_id]) return GDN_ERR_BAD_SLOT;
+    const size_t bytes = P->slot_bytes * P->num_layers;
+    const char* src = P->base + (size_t)slot_id * bytes;
+    cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_slot_restore(gdn_pool* P, int slot_id, const void* src, void* stream)
+{
+    if (!P || !src) return GDN_ERR_INVALID_ARG;
+    if (slot_id < 0 || slot_id >= P->num_slots || !P->live[(size_t)slot_id]) return GDN_ERR_BAD_SLOT;
+    const size_t bytes = P->slot_bytes * P->num_layers;
+    char* dst = P->base + (size_t)slot_id * bytes;
+    cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_slot_ptrs(gdn_pool* P, int layer, const int* slot_ids_dev, int m, uint64_t* out_dev, void* stream)
 {
     if (!P || layer < 0 || layer >= P->num_layers || m < 0) return GDN_ERR_INVALID_ARG;

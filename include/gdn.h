@@ -126,6 +126,19 @@ int gdn_slot_recycle(gdn_pool* pool, int slot_id, void* stream);
 /* Device address of (slot, layer) (host computation, no GPU work). */
 int gdn_slot_addr(gdn_pool* pool, int layer, int slot_id, uint64_t* addr);
 
+/* Snapshot / restore of one slot, for per-slot prefix reuse and checkpoints (issue #5279,
+ * "What done needs" item 6 and phase P7: per-slot prefix reuse with longest-prefix
+ * admission; the qLLM README, "What's still open": prefix caching is off because a
+ * recurrent state cannot be rebuilt from a cached KV prefix -- a snapshot of the state is
+ * what can be reused).  A snapshot is num_layers * slot_bytes bytes (gdn_pool_get_info):
+ * every layer's S and conv buffer in the pool's own layout.
+ * gdn_slot_snapshot copies the slot's layers to dst; gdn_slot_restore overwrites an
+ * allocated slot's layers with src.  dst / src may be device or host memory (pinned host
+ * memory keeps the copy asynchronous); the copy is enqueued on `stream`.
+ * Errors: INVALID_ARG, BAD_SLOT (free or out of range), CUDA. */
+int gdn_slot_snapshot(gdn_pool* pool, int slot_id, void* dst, void* stream);
+int gdn_slot_restore(gdn_pool* pool, int slot_id, const void* src, void* stream);
+
 /* Enqueue on `stream` the gather out_dev[i] = address of (slot_ids_dev[i], layer),
  * for i < m: the device u64 slot-pointer array of issue #5279 phase P5.  An id
  * that is out of range or not allocated gives 0 and sets GDN_DEV_BAD_SLOT_ID.
@@ -145,7 +158,10 @@ int gdn_layer_params(gdn_pool* pool, int layer, const float* conv_w, const float
  * buffer (which then shifts by one token), L2 norms, gates, the delta-rule
  * update of every v-head's S in place, the gated RMSNorm; out_dev[i] receives
  * the result.  The slot pointers must be distinct.  Each row's result depends
- * only on that row's inputs and state, never on m or the other rows.
+ * only on that row's inputs and state, never on m or the other rows.  The call only
+ * enqueues one kernel, so a sequence of decode steps can be captured into a CUDA graph
+ * keyed by the slot-pointer array (issue #5279 phase P8); the first call for a given
+ * shape and dtypes also sets the kernel's attributes, so make one call before capturing.
  * Errors: INVALID_ARG, NO_PARAMS, CUDA (launch). */
 int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, int m, const void* q_dev,
                     const void* k_dev, const void* v_dev, const void* a_dev, const void* b_dev, const void* z_dev,
