@@ -67,6 +67,12 @@ def decode_bytes_per_slot_step(io=2):
     return s + conv + inputs + out
 
 
+# algorithmic flops per prefill token of the chunked form (64-token chunks, triangular halves):
+# K K^T 8 064 + Q K^T 8 320 + solve C^2/3 + W, U, intra-chunk O 3 x 8 320 + 3 state products 3 x 2 d^2,
+# times Hv (the figure of the survey's measurement plan)
+PREFILL_FLOPS_PER_TOKEN = 4.51e6
+
+
 def decode_param_bytes():
     return C * W * 4 + 2 * HV * 4 + D * 4
 
@@ -257,6 +263,109 @@ def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
     return t0.elapsed_time(t1) / steps, statistics.mean(per), statistics.median(per)
 
 
+def time_decode_graph(torch, pool, synth, m, steps, seed=11):
+    """Device time per decode step when `steps` steps are replayed from one CUDA graph (no per-call
+    host overhead): the kernel-level number for small m, where launches dominate eager timing."""
+    ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
+    ptrs = pool.slot_ptrs(0, ids)
+    sets = device_inputs(torch, m, steps, seed)
+    out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
+    cap = torch.cuda.Stream()
+    s0 = sets[0]
+    pool.decode_step(0, ptrs, m, s0["q"], s0["k"], s0["v"], s0["a"], s0["b"], s0["z"], out)  # attributes set
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for s in sets:
+                pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, cap)
+    graph.replay()  # warm-up
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert pool.device_status() == 0
+    return a.elapsed_time(b) / steps
+
+
+def time_decode_layers(torch, binding, synth, layers=30, m=M_HEAD, reps=20):
+    """One token step of a `layers`-deep stack of GDN layers at m slots (30 x 256 slots, 16 GB of state):
+    one decode launch per layer, replayed from a CUDA graph."""
+    pool = binding.Pool(HQK, HV, D, D, NUM_SLOTS, layers, W, "bf16", "bf16")
+    for layer in range(layers):
+        p = synth.layer_params(5, layer, HQK, HV, D, D, W)
+        pool.layer_params(layer, *(torch.from_numpy(p[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")))
+    for _ in range(NUM_SLOTS):
+        pool.alloc()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    for layer in range(layers):
+        blk = pool.state_block(layer)
+        blk.copy_(torch.randn(blk.shape, generator=g, device="cuda") * math.sqrt(0.1))
+    ids = torch.arange(m, dtype=torch.int32, device="cuda")
+    ptrs = [pool.slot_ptrs(layer, ids) for layer in range(layers)]
+    x = device_inputs(torch, m, 1, 9)[0]
+    out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
+    for layer in range(layers):
+        pool.decode_step(layer, ptrs[layer], m, x["q"], x["k"], x["v"], x["a"], x["b"], x["z"], out)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for layer in range(layers):
+                pool.decode_step(layer, ptrs[layer], m, x["q"], x["k"], x["v"], x["a"], x["b"], x["z"], out, cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert pool.device_status() == 0
+    pool.close()
+    ms = a.elapsed_time(b) / reps
+    return ms
+
+
+def time_prefill_long(torch, binding, synth, T=80000, reps=3):
+    """One 80 000-token prefill (1 250 chunks of 64) into a zeroed slot."""
+    pool = binding.Pool(HQK, HV, D, D, 2, 1, W, "bf16", "bf16", max_prefill_tokens=T)
+    p = synth.layer_params(5, 0, HQK, HV, D, D, W)
+    pool.layer_params(0, *(torch.from_numpy(p[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")))
+    slot = pool.alloc()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(80)
+    inp = {n: torch.randn((T, w), generator=g, device="cuda").to(torch.bfloat16)
+           for n, w in (("q", HQK * D), ("k", HQK * D), ("v", HV * D), ("z", HV * D), ("a", HV), ("b", HV))}
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    ids = torch.tensor([slot], dtype=torch.int32, device="cuda")
+    out = torch.empty((T, HV * D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = []
+    for r in range(reps + 1):
+        pool.recycle(slot, stream)
+        pool.alloc()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pool.prefill_varlen(0, cu, ids, 1, T, inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"], out, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if r > 0:
+            times.append(a.elapsed_time(b))
+    assert pool.device_status() == 0
+    pool.close()
+    return statistics.median(times)
+
+
 def time_decode_e2e(torch, pool, synth, m, steps, warmup):
     """Public-API end to end: pinned host inputs copied in, decode, output copied back, every step."""
     ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
@@ -421,9 +530,12 @@ def run_ours(args):
         sweep = []
         for m in SWEEP:
             sm, km, _ = time_decode(torch, pool, synth, m, max(10, min(args.steps, 500)), 3, seed=100 + m)
+            gm = time_decode_graph(torch, pool, synth, m, 100, seed=200 + m)
             b = m * decode_bytes_per_slot_step() + decode_param_bytes()
             sweep.append({"m": m, "slot_steps_per_s": m / (sm * 1e-3), "us_per_step": sm * 1e3,
-                          "gbs": b / (km * 1e-3) / 1e9, "frac": b / (km * 1e-3) / 1e9 / hbm})
+                          "gbs": b / (km * 1e-3) / 1e9, "frac": b / (km * 1e-3) / 1e9 / hbm,
+                          "graph_us_per_step": gm * 1e3, "graph_slot_steps_per_s": m / (gm * 1e-3),
+                          "graph_frac": b / (gm * 1e-3) / 1e9 / hbm})
         result["decode_sweep"] = sweep
     if rank == 0:
         e2e, h2d, d2h = time_decode_e2e(torch, pool, synth, M_HEAD, min(args.steps, 2000), args.warmup)
@@ -432,10 +544,22 @@ def run_ours(args):
     if rank == 0 and not args.no_prefill:
         pms, T = time_prefill(torch, binding, synth, max(3, min(args.steps, 10)), 2)
         pb = prefill_bytes(PREFILL_LENGTHS)
+        flops = PREFILL_FLOPS_PER_TOKEN * T
         result["prefill"] = {"workload": "8 sequences {1,17,300,4095,1024,2048,513,8000}, bf16 io, zero state",
                              "tokens": T, "ms": pms, "tok_per_s": T / (pms * 1e-3),
                              "gbs": pb / (pms * 1e-3) / 1e9, "frac_hbm": pb / (pms * 1e-3) / 1e9 / hbm,
-                             "bytes": pb}
+                             "bytes": pb, "tflops": flops / (pms * 1e-3) / 1e12,
+                             "frac_tensor": flops / (pms * 1e-3) / 1e12 / bf16,
+                             "bound": "hbm (137 flop/B < ridge 279)"}
+        lms = time_prefill_long(torch, binding, synth)
+        result["prefill_80k"] = {"workload": "one 80 000-token prefill, bf16 io, zero state", "ms": lms,
+                                 "tok_per_s": 80000 / (lms * 1e-3),
+                                 "frac_hbm": prefill_bytes([80000]) / (lms * 1e-3) / 1e9 / hbm}
+        l30 = time_decode_layers(torch, binding, synth)
+        result["decode_30_layers"] = {"workload": "one token step of 30 stacked GDN layers at m = 256 "
+                                                  "(30 x 256 slots, 16.1 GB of state), CUDA-graph replay",
+                                      "ms_per_token_step": l30, "tokens_per_s": M_HEAD / (l30 * 1e-3),
+                                      "slot_steps_per_s": 30 * M_HEAD / (l30 * 1e-3)}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds)
     result["wall_s_timed_region"] = wall
