@@ -187,7 +187,7 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
  * is owned and budgeted by someone else, or in a phase that must not allocate -- and so
  * cannot create a pool or its workspace.  It runs the same kernels as
  * gdn_prefill_varlen and allocates nothing: its scratch is one static device array of
- * 32 MiB inside libgdn (held by every GPU that loads the library until the process
+ * 64 MiB inside libgdn (held by every GPU that loads the library until the process
  * exits), and the state slots are memory the caller owns.
  *   shape         as for gdn_pool_create (max_prefill_tokens is ignored).
  *   conv_w, A_log, dt_bias, norm_w   the layer's device parameters (as gdn_layer_params).
@@ -203,8 +203,9 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
  * race on it.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Errors: INVALID_ARG; UNSUPPORTED_SHAPE when the shape is not built or the call needs more
- * than the 32 MiB of scratch (about 49.5 KB per token at Hqk 16, Hv 32, d 128: split longer
- * prompts into several calls, which continue from the slots' state); CUDA. */
+ * than the 64 MiB of scratch (at Hqk 16, Hv 32, d 128 about 54 KB per token plus 2.4 MB per
+ * sequence, i.e. up to ~1 170 tokens of one sequence per call: split longer prompts into
+ * several calls, which continue from the slots' state); CUDA. */
 int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, const float* A_log, const float* dt_bias,
                                const float* norm_w, void* states_dev, int num_slots, const int* cu_seqlens_dev,
                                const int* slot_ids_dev, int n_seqs, int total_tokens, const void* q_dev,
