@@ -46,6 +46,7 @@ struct DecodeArgs {
     int hqk, hv, r, W, C;
     uint32_t state_bytes;
     float l2_eps, norm_eps;
+    int stall_producer;  // test hook: the producer fills no stage, so the consumers' waits run out
 };
 
 size_t decode_smem_bytes(int D, int r)
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
         if (lane == 0) {
             int slot = 0;
             uint32_t phase = 0, issued = 0, last_parity = 0;
-            for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
+            for (int item = blockIdx.x; item < items && !*abort_flag && !A.stall_producer; item += gridDim.x) {
                 const int row = item / A.hqk, hk = item % A.hqk;
                 const uint64_t p = A.slot_ptrs[row];
                 if (!slot_ptr_ok(p, A.chk)) continue;
@@ -343,6 +344,7 @@ cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, i
     A.state_bytes = (uint32_t)P.state_bytes;
     A.l2_eps = P.shape.l2_eps;
     A.norm_eps = P.shape.norm_eps;
+    A.stall_producer = P.debug_flags & 1;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return launch_d<__nv_bfloat16, __nv_bfloat16>(P, A, st);
     if (in_bf16) return launch_d<__nv_bfloat16, float>(P, A, st);

@@ -60,6 +60,7 @@ struct Pool {
     std::vector<LayerParams> params;
     PrefillWorkspace ws;
     int device = 0, num_sms = 0;
+    int debug_flags = 0;  // GDN_DEBUG_FLAGS at creation; bit 0: decode producer fills no stage (timeout test)
 };
 
 // Everything the prefill kernels of one call need (device pointers and sizes).

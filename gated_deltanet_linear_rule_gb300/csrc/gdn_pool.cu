@@ -6,6 +6,7 @@
 // calls follow the engine trait of issue #5279 (phase P0: add slot, recycle slot,
 // cleanup, reset) and phase P5's device array of u64 per-layer state pointers.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -149,6 +150,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     P->free_list.resize((size_t)num_slots);
     for (int i = 0; i < num_slots; ++i) P->free_list[(size_t)i] = num_slots - 1 - i;
     P->params.resize((size_t)num_layers);
+    if (const char* dbg = std::getenv("GDN_DEBUG_FLAGS")) P->debug_flags = std::atoi(dbg);
     *out = P;
     return GDN_OK;
 }

@@ -44,6 +44,10 @@
  *   - Work on one slot is ordered by the stream; calls on different streams
  *     that touch the same slot must be ordered by the caller.
  *   - Not thread-safe: one host thread per pool at a time.
+ *   - Test hook: if the environment variable GDN_DEBUG_FLAGS holds 1 when a pool is
+ *     created, that pool's decode kernel fills none of its pipeline stages, so every
+ *     consumer wait runs out after its 1 s limit: the launch returns with
+ *     GDN_DEV_TIMEOUT set and the outputs unwritten, and the CUDA context stays usable.
  */
 #ifndef GDN_H
 #define GDN_H
