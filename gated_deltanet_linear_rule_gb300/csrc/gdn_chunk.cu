@@ -28,7 +28,7 @@
 //     MMA3  [T2; T1] x K,  [T2; T1] x V  -> W (rows 64-127), U (rows 0-63)       2 x 128 x 128 x 64
 //     MMA5  [P; P] x W,  [P; P] x U      -> P W, P U                             2 x 128 x 128 x 64
 //   and writes per (chunk, v-head) a record: the [W; Q'] operand image, U and P U images, the
-//   decay factors; per (chunk, q/k head) the K image.
+//   decay factors and the output gates silu(z) * w_n; per (chunk, q/k head) the K image.
 // State pass (chunk_state_kernel, double-buffered bulk copies of the records):
 //     MMA4  [W; Q'] x S0^T   -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)         128 x 128 x 128
 //     Delta, O = Q' S0^T + P U with the gated RMSNorm fused, output written
@@ -54,7 +54,8 @@ constexpr uint32_t REC_A4 = 0;       // [W; Q'] K-major image: 2 K-tiles x 128 r
 constexpr uint32_t REC_U = 32768;    // U image [token][dv]: two 64-wide halves 8 KiB apart
 constexpr uint32_t REC_O0 = 49152;   // P U image, same layout
 constexpr uint32_t REC_SC = 65536;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
-constexpr uint32_t REC_BYTES = 66048;
+constexpr uint32_t REC_GZ = 66048;   // output gates silu(z) * w_n, fp16 [token][dv] row-major (16 KiB)
+constexpr uint32_t REC_BYTES = 82432;
 constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token][dk], halves 8 KiB apart
 
 // pre-pass shared memory (offsets from a 1024-aligned base)
@@ -127,6 +128,7 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
 // ===================================================================== pre-pass ====
 // 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
+template <typename TIn>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -423,6 +425,24 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         float* sc = reinterpret_cast<float*>(rec + REC_SC);
         if (tid < 64) sc[tid] = sGam[tid];
         if (tid == 0) sc[64] = sMisc[0];
+        // the output gates silu(z) * w_n of the chunk's rows, so the state pass only multiplies
+        const TIn* zin = static_cast<const TIn*>(A.z);
+        uint4* gzo = reinterpret_cast<uint4*>(rec + REC_GZ);
+        for (int q = tid; q < 64 * 16; q += NT) {
+            const int i = q >> 4, c8 = (q & 15) * 8;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (i < n) {
+                const TIn* zr = zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8;
+                float z8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) z8[e] = to_f(zr[e]);
+                w.x = pack_half2(silu_f(z8[0]) * A.norm_w[c8], silu_f(z8[1]) * A.norm_w[c8 + 1]);
+                w.y = pack_half2(silu_f(z8[2]) * A.norm_w[c8 + 2], silu_f(z8[3]) * A.norm_w[c8 + 3]);
+                w.z = pack_half2(silu_f(z8[4]) * A.norm_w[c8 + 4], silu_f(z8[5]) * A.norm_w[c8 + 5]);
+                w.w = pack_half2(silu_f(z8[6]) * A.norm_w[c8 + 6], silu_f(z8[7]) * A.norm_w[c8 + 7]);
+            }
+            gzo[q] = w;
+        }
     }
     sync_all();
     if (warp == 0) tc::dealloc(tm, 256);
@@ -509,20 +529,20 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     for (int c = 0; c < nch && ok; ++c) {
         unsigned char* buf = sm + (c & 1) * S_BUF;
         const int tc0 = t0 + c * CH, n = min(CH, L - c * CH);
-        // the gate z of this thread's output row (rows 64-127 = tokens) is fetched early
-        constexpr int ZW = ZRow<TIn>::kWords;
-        uint4 zr[ZW];
+        // the output gates silu(z) * w_n of this thread's row half (rows 64-127 = tokens), computed
+        // by the pre-pass, are fetched early
+        uint4 gz[8];
         const int orow = row - 64;
         const size_t obase = (size_t)(tc0 + (orow >= 0 && orow < n ? orow : 0)) * Dv + (size_t)h * D + 64 * hf;
         if (row >= 64) {
-            const uint4* zp = reinterpret_cast<const uint4*>(zin + obase);
+            const uint4* gp = reinterpret_cast<const uint4*>(A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES +
+                                                             REC_GZ + (size_t)orow * 256 + hf * 128);
 #pragma unroll
-            for (int q = 0; q < ZW; ++q) zr[q] = zp[q];
+            for (int q = 0; q < 8; ++q) gz[q] = __ldg(gp + q);
         }
+        // every thread waits for the record itself; the verdict becomes uniform at the next barrier
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-        ok = __syncthreads_and(got) != 0;
-        if (!ok) break;
         const float* sc = reinterpret_cast<const float*>(buf + B_SC);
 
         // S0 (fp16, K-major rows = d_v) for MMA4; S <- e^{G_last} S for MMA6
@@ -547,7 +567,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             tc::wait_st();
         }
         tc::fence_proxy_async();
-        sync_all();
+        tc::fence_before_sync();
+        ok = __syncthreads_and(got) != 0;
+        tc::fence_after_sync();
+        if (!ok) break;
 
         // MMA4: [W; Q'] x S0^T -> columns [128, 256)
         if (tid == 0)
@@ -609,14 +632,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         }
         if (row >= 64 && orow < n) {
             const float rs = rms_scale(s_ss[orow] + s_ss[64 + orow], A.norm_eps, D);
-            const TIn* zv = reinterpret_cast<const TIn*>(zr);
 #pragma unroll
             for (int e8 = 0; e8 < 64; e8 += 8) {
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int dv = 64 * hf + e8 + e;
-                    y[e] = o[e8 + e] * rs * s_normw[dv] * silu_f(to_f(zv[e8 + e]));
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 gg = __half22float2(reinterpret_cast<const __half2*>(&gz[e8 / 8])[e / 2]);
+                    y[e] = o[e8 + e] * rs * gg.x;
+                    y[e + 1] = o[e8 + e + 1] * rs * gg.y;
                 }
                 store8<TOut>(out + obase + e8, y);
             }
@@ -658,13 +681,14 @@ size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (si
 template <typename TIn, typename TOut>
 cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    auto prep = chunk_prep_kernel<TIn>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
     auto state = chunk_state_kernel<TIn, TOut>;
     e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
     if (e != cudaSuccess) return e;
     const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
-    chunk_prep_kernel<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A);
+    prep<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A);
     state<<<A.n * A.hv, NT, S_SMEM, st>>>(A);
     return cudaGetLastError();
 }

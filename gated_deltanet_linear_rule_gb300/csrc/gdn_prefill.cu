@@ -494,7 +494,7 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
     ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
     ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
-    ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 66048));
+    ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 82432));
     ws.kimg = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hqk * 16384));
     ws.chunk_cap = chunk_cap;
     ws.valid = reinterpret_cast<int*>(take(256));
