@@ -204,6 +204,20 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             if (r < 64 && write_k) *reinterpret_cast<uint4*>(kimg + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = kq[q];
         }
     }
+    // z of the chunk (the output gates are formed while MMA1 runs)
+    constexpr int ZW = 8 * (int)sizeof(TIn) / 16 > 0 ? 8 * (int)sizeof(TIn) / 16 : 1;  // 16-B words per 8 values
+    uint4 zpark[4][ZW];
+    {
+        const TIn* zin = static_cast<const TIn*>(A.z);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
+#pragma unroll
+            for (int w = 0; w < ZW; ++w)
+                zpark[q][w] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + w)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     uint4 vpark[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -234,9 +248,26 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         if (tid == 0) sMisc[0] = expf(gl);
     }
 
-    // (b) MMA1: [K; Q] x K^T
+    // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n go straight to the record
     if (tid == 0)
         tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
+    {
+        uint4* gzo = reinterpret_cast<uint4*>(rec + REC_GZ);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
+            const TIn* zv = reinterpret_cast<const TIn*>(zpark[q]);
+            float g8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g8[e] = i < n ? silu_f(to_f(zv[e])) * A.norm_w[c8 + e] : 0.f;
+            uint4 w;
+            w.x = pack_half2(g8[0], g8[1]);
+            w.y = pack_half2(g8[2], g8[3]);
+            w.z = pack_half2(g8[4], g8[5]);
+            w.w = pack_half2(g8[6], g8[7]);
+            gzo[idx] = w;
+        }
+    }
     mma_done();
     if (ok) {
         // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127; columns 32*hf ..
@@ -251,14 +282,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int j = c0 + e;
-                    FA[i * FS + j] = (j < i && i < n) ? bi * expf(Gi - sG[j]) * v[e] : 0.f;
+                    FA[i * FS + j] = (j < i && i < n) ? bi * __expf(Gi - sG[j]) * v[e] : 0.f;
                 }
             } else {
                 float p[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int j = c0 + e;
-                    p[e] = (j <= i && i < n) ? expf(Gi - sG[j]) * v[e] : 0.f;
+                    p[e] = (j <= i && i < n) ? __expf(Gi - sG[j]) * v[e] : 0.f;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -291,36 +322,54 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             FT[(16 * bi + (e >> 4)) * FS + 16 * bj + (e & 15)] = 0.f;
         }
         __syncthreads();
-        //     ... then 16 -> 32: T_10 = -T_11 (A_10 T_00) for the block pairs (0,1), (2,3) ...
-        for (int idx = tid; idx < 512; idx += NT) {
-            const int p = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-            const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
-            float acc = 0.f;
-            for (int k = j; k < 16; ++k) acc += FA[(ro + i) * FS + co + k] * FT[(co + k) * FS + co + j];
-            X[(p * 16 + i) * 17 + j] = acc;
+        //     ... then 16 -> 32: T_10 = -T_11 (A_10 T_00) for the block pairs (0,1), (2,3), both
+        //     pairs' element (i, j) by one thread with two accumulators ...
+        {
+            const int i = (tid >> 4) & 15, j = tid & 15;
+            float a0 = 0.f, a1 = 0.f;
+            for (int k = j; k < 16; ++k) {
+                a0 += FA[(16 + i) * FS + k] * FT[k * FS + j];
+                a1 += FA[(48 + i) * FS + 32 + k] * FT[(32 + k) * FS + 32 + j];
+            }
+            X[i * 17 + j] = a0;
+            X[(16 + i) * 17 + j] = a1;
         }
         __syncthreads();
-        for (int idx = tid; idx < 512; idx += NT) {
-            const int p = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
-            const int ro = 16 * (2 * p + 1), co = 16 * (2 * p);
-            float acc = 0.f;
-            for (int k = 0; k <= i; ++k) acc += FT[(ro + i) * FS + ro + k] * X[(p * 16 + k) * 17 + j];
-            FT[(ro + i) * FS + co + j] = -acc;
+        {
+            const int i = (tid >> 4) & 15, j = tid & 15;
+            float a0 = 0.f, a1 = 0.f;
+            for (int k = 0; k <= i; ++k) {
+                a0 += FT[(16 + i) * FS + 16 + k] * X[k * 17 + j];
+                a1 += FT[(48 + i) * FS + 48 + k] * X[(16 + k) * 17 + j];
+            }
+            FT[(16 + i) * FS + j] = -a0;
+            FT[(48 + i) * FS + 32 + j] = -a1;
         }
         __syncthreads();
-        //     ... then 32 -> 64: T_BA = -T_BB (A_BA T_AA)
-        for (int idx = tid; idx < 1024; idx += NT) {
-            const int i = idx >> 5, j = idx & 31;
-            float acc = 0.f;
-            for (int k = j; k < 32; ++k) acc += FA[(32 + i) * FS + k] * FT[k * FS + j];
-            X[i * 33 + j] = acc;
+        //     ... then 32 -> 64: T_BA = -T_BB (A_BA T_AA), rows i0 + 8q (q < 4) of column j per thread
+        {
+            const int i0 = tid >> 5, j = tid & 31;
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = j; k < 32; ++k) {
+                const float t = FT[k * FS + j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[q] += FA[(32 + i0 + 8 * q) * FS + k] * t;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) X[(i0 + 8 * q) * 33 + j] = a[q];
         }
         __syncthreads();
-        for (int idx = tid; idx < 1024; idx += NT) {
-            const int i = idx >> 5, j = idx & 31;
-            float acc = 0.f;
-            for (int k = 0; k <= i; ++k) acc += FT[(32 + i) * FS + 32 + k] * X[k * 33 + j];
-            FT[(32 + i) * FS + j] = -acc;
+        {
+            const int i0 = tid >> 5, j = tid & 31;
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k <= i0 + 24; ++k) {
+                const float x = X[k * 33 + j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (k <= i0 + 8 * q) a[q] += FT[(32 + i0 + 8 * q) * FS + 32 + k] * x;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) FT[(32 + i0 + 8 * q) * FS + j] = -a[q];
         }
         __syncthreads();
         //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one 8-column chunk per item
@@ -354,8 +403,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         mma_done();
     }
     if (ok) {
-        // (f) W (rows 64-127 of the first product) -> [W; .] rows 0-63 and the W image;
-        //     U (rows 0-63 of the second product) -> the U image (over the dead V image)
+        // (f) W (rows 64-127 of the first product) -> the record's [W; Q'] rows 0-63 and the
+        //     MN-major W image; U (rows 0-63 of the second product) -> the U image (over the dead
+        //     V image) and the record's U image
         {
             const int row = qd * 32 + lane, i = row & 63;
             for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
@@ -366,10 +416,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
                     if (row >= 64) {
-                        tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, i, ch, v + 8 * q);
+                        tc::st_chunk<Op>(rec + REC_A4 + (c0 >> 6) * 16384, i, ch, v + 8 * q);
                         tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                     } else {
                         tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
+                        tc::st_chunk<Op>(rec + REC_U + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                     }
                 }
             }
@@ -387,8 +438,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         mma_done();
     }
     if (ok) {
-        // (h) rows 64-127: Q' = e^G Q - P W -> [W; Q'] rows 64-127 (Q read from the same row of
-        //     the [K; Q] tile by the thread that overwrites it);  P U -> the P U image
+        // (h) rows 64-127: Q' = e^G Q - P W -> the record's [W; Q'] rows 64-127 (Q read from the
+        //     [K; Q] tile);  P U -> the record's P U image.  Every record part is written to global
+        //     memory as it is produced.
         const int row = qd * 32 + lane;
         if (row >= 64) {
             const int i = row - 64;
@@ -406,43 +458,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
                     unpack8(*reinterpret_cast<const uint4*>(qa), qv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - pw[8 * q + e];
-                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv);
-                    tc::st_chunk<Op>(sm + P_AT + (c0 >> 6) * 8192, i, ch, pu + 8 * q);
+                    tc::st_chunk<Op>(rec + REC_A4 + (c0 >> 6) * 16384, 64 + i, ch, qv);
+                    tc::st_chunk<Op>(rec + REC_O0 + (c0 >> 6) * 8192, i, ch, pu + 8 * q);
                 }
             }
-        }
-        __syncthreads();
-        // (i) the record: [W; Q'] image, U image, P U image, decay factors
-        const uint4* src_a = reinterpret_cast<const uint4*>(sm + P_A1);
-        const uint4* src_u = reinterpret_cast<const uint4*>(sm + P_R4);
-        const uint4* src_o = reinterpret_cast<const uint4*>(sm + P_AT);
-        uint4* dst = reinterpret_cast<uint4*>(rec);
-        for (int q = tid; q < 2048; q += NT) dst[REC_A4 / 16 + q] = src_a[q];
-        for (int q = tid; q < 1024; q += NT) {
-            dst[REC_U / 16 + q] = src_u[q];
-            dst[REC_O0 / 16 + q] = src_o[q];
         }
         float* sc = reinterpret_cast<float*>(rec + REC_SC);
         if (tid < 64) sc[tid] = sGam[tid];
         if (tid == 0) sc[64] = sMisc[0];
-        // the output gates silu(z) * w_n of the chunk's rows, so the state pass only multiplies
-        const TIn* zin = static_cast<const TIn*>(A.z);
-        uint4* gzo = reinterpret_cast<uint4*>(rec + REC_GZ);
-        for (int q = tid; q < 64 * 16; q += NT) {
-            const int i = q >> 4, c8 = (q & 15) * 8;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (i < n) {
-                const TIn* zr = zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8;
-                float z8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) z8[e] = to_f(zr[e]);
-                w.x = pack_half2(silu_f(z8[0]) * A.norm_w[c8], silu_f(z8[1]) * A.norm_w[c8 + 1]);
-                w.y = pack_half2(silu_f(z8[2]) * A.norm_w[c8 + 2], silu_f(z8[3]) * A.norm_w[c8 + 3]);
-                w.z = pack_half2(silu_f(z8[4]) * A.norm_w[c8 + 4], silu_f(z8[5]) * A.norm_w[c8 + 5]);
-                w.w = pack_half2(silu_f(z8[6]) * A.norm_w[c8 + 6], silu_f(z8[7]) * A.norm_w[c8 + 7]);
-            }
-            gzo[q] = w;
-        }
     }
     sync_all();
     if (warp == 0) tc::dealloc(tm, 256);
@@ -476,7 +499,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     const int nch = (L + CH - 1) / CH, gc0 = A.ws.chunk_start[s];
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
-    const TIn* zin = static_cast<const TIn*>(A.z);
     TOut* out = static_cast<TOut*>(A.out);
 
     if (tid == 0) {
