@@ -64,6 +64,7 @@ constexpr uint32_t P_AP = 32768;      // [P; P]
 constexpr uint32_t P_AT = 49152;      // inverse scratch, then [T2; T1], then the P U image
 constexpr uint32_t P_R4 = 65536;      // A (fp32, stride 65), then the V image, then the U image
 constexpr uint32_t P_R5 = 82944;      // T (fp32, stride 65), then the W image
+constexpr uint32_t P_RAW = P_AP;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
 constexpr uint32_t P_SMALL = 99584;
 constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
 constexpr int FS = 65;                // fp32 matrix row stride (conflict-free row reads)
@@ -125,10 +126,107 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p)
     return p + ((1024 - (smem_addr(p) & 1023)) & 1023);
 }
 
+// 8 raw input values of one row (one 16-B word in bf16, two in fp32), read through the
+// read-only path
+template <typename TIn> struct Raw8 {
+    uint4 w[sizeof(TIn) / 2];
+};
+template <typename TIn> __device__ __forceinline__ void ld_raw8(Raw8<TIn>& r, const TIn* p)
+{
+#pragma unroll
+    for (int w = 0; w < (int)(sizeof(TIn) / 2); ++w) r.w[w] = __ldg(reinterpret_cast<const uint4*>(p) + w);
+}
+template <typename TIn> __device__ __forceinline__ void zero_raw8(Raw8<TIn>& r)
+{
+#pragma unroll
+    for (int w = 0; w < (int)(sizeof(TIn) / 2); ++w) r.w[w] = make_uint4(0u, 0u, 0u, 0u);
+}
+template <typename TIn> __device__ __forceinline__ float raw_at(const Raw8<TIn>& r, int e)
+{
+    return to_f(reinterpret_cast<const TIn*>(r.w)[e]);
+}
+
+// 16-B asynchronous global -> shared copy; src_bytes = 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// 8 bf16 values of a 16-B word -> float
+__device__ __forceinline__ void unpack8_bf16(uint4 w, float* v)
+{
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        v[2 * q] = f.x;
+        v[2 * q + 1] = f.y;
+    }
+}
+
+// One tensor (q, k or v) of a chunk, as a thread of the pre-pass sees it: 8 channels
+// (column col of the input rows of width `width`, channel ch of the conv's C channels) over
+// the output rows r0 .. r0 + 3.  The causal conv of width W <= WM is evaluated as a
+// WM-tap conv whose leading WM - W taps are zero, over the input rows r0 - WM + 1 .. r0 + 3.
+template <typename TIn, int WM>
+struct ConvRows {
+    static constexpr int NR = WM + 3;
+    Raw8<TIn> x[NR];
+
+    // rows before the sequence's first token come from the slot's conv buffer (its row W-1+p
+    // holds position p < 0); rows before that, and rows at or past the chunk's end, are zero
+    __device__ __forceinline__ void load(const TIn* src, int width, int col, const TIn* cbuf, int C, int ch, int W,
+                                         int tc0, int p0, int r0, int n)
+    {
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+            const int r = r0 - (WM - 1) + j, p = p0 + r;
+            if (r < n && p >= 0) ld_raw8(x[j], src + (size_t)(tc0 + r) * width + col);
+            else if (r < n && p >= -(W - 1)) ld_raw8(x[j], cbuf + (size_t)(W - 1 + p) * C + ch);
+            else zero_raw8(x[j]);
+        }
+    }
+
+    // conv taps of the 8 channels, right-aligned in WM slots
+    __device__ __forceinline__ static void taps(float (&w)[8][WM], const float* conv_w, int ch, int W)
+    {
+        if (W == WM) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int j4 = 0; j4 < WM; j4 += 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(conv_w + (size_t)(ch + e) * WM + j4));
+                    w[e][j4] = t.x; w[e][j4 + 1] = t.y; w[e][j4 + 2] = t.z; w[e][j4 + 3] = t.w;
+                }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int j = 0; j < WM; ++j)
+                    w[e][j] = j >= WM - W ? __ldg(conv_w + (size_t)(ch + e) * W + (j - (WM - W))) : 0.f;
+        }
+    }
+
+    // SiLU(conv) of output row r0 + o
+    __device__ __forceinline__ void row(const float (&w)[8][WM], int o, float (&y)[8]) const
+    {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < WM; ++j) acc = fmaf(w[e][j], raw_at(x[o + j], e), acc);
+            y[e] = silu_f(acc);
+        }
+    }
+};
+
 // ===================================================================== pre-pass ====
 // 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
-template <typename TIn>
+template <typename TIn, int WM>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -163,9 +261,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     const bool write_k = (h % A.r) == 0;
     unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
     unsigned char* kimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * KIMG_BYTES;
-    const __half* kh16 = A.ws.kh16;
-    const __half* qh16 = A.ws.qh16;
-    const __half* vc16 = A.ws.vc16;
+    const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
+                                                                A.slot_bytes + A.state_bytes);
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -185,27 +282,27 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         tc::fence_after_sync();
     };
 
-    // (a) [K; Q] tile (fp16 rows copied chunk by chunk into the swizzled layout), K image, gates.
-    //     All loads are issued before any store; the V rows are fetched now and parked in
-    //     registers until the inverse has freed their shared-memory space.
-    {
-        uint4 kq[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int idx = tid + q * NT, r = idx >> 4, c16 = idx & 15, i = r & 63;
-            kq[q] = i < n ? __ldg(reinterpret_cast<const uint4*>((r < 64 ? kh16 : qh16) + (size_t)(tc0 + i) * Dq +
-                                                                   hk * D + c16 * 8))
-                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int idx = tid + q * NT, r = idx >> 4, c16 = idx & 15, i = r & 63;
-            *reinterpret_cast<uint4*>(sm + P_A1 + (c16 >> 3) * 16384 + tc::sw128_chunk(r, c16 & 7)) = kq[q];
-            if (r < 64 && write_k) *reinterpret_cast<uint4*>(kimg + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = kq[q];
-        }
+    // (a) conv1d + SiLU of the chunk's q, k and v rows from the raw inputs (the W-1 rows
+    //     before a sequence's first token from its slot's conv buffer), L2 norms of q and k
+    //     (q also scaled by dk^-1/2), fp16 rounding; the gates of the chunk's tokens.
+    //     Thread (rb, cg) = (tid / 16, tid % 16) owns rows 4 rb .. 4 rb + 3 and channels
+    //     8 cg .. 8 cg + 7 of each tensor; a row's 16 threads are one half-warp, which sums
+    //     the row's squares by shuffles.  q, k go to the [K; Q] tile (k also to the K image);
+    //     v is parked in registers until the inverse has freed its shared-memory space.
+    //     bf16 rows are staged in shared memory by asynchronous copies; fp32 rows pass
+    //     through registers, one tensor at a time.
+    const int rb = tid >> 4, cg = tid & 15, r0 = 4 * rb, p0 = c * CH;
+    const TIn* qin = static_cast<const TIn*>(A.q);
+    const TIn* kin = static_cast<const TIn*>(A.k);
+    const TIn* vin = static_cast<const TIn*>(A.v);
+    const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg, chv = 2 * Dq + h * D + 8 * cg;
+    float ga = 0.f, gb = 0.f;  // raw gate inputs a, b of token tid (tid < n)
+    if (tid < n) {
+        ga = to_f(static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h]);
+        gb = to_f(static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h]);
     }
     // z of the chunk (the output gates are formed while MMA1 runs)
-    constexpr int ZW = 8 * (int)sizeof(TIn) / 16 > 0 ? 8 * (int)sizeof(TIn) / 16 : 1;  // 16-B words per 8 values
+    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
     uint4 zpark[4][ZW];
     {
         const TIn* zin = static_cast<const TIn*>(A.z);
@@ -213,23 +310,124 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
 #pragma unroll
-            for (int w = 0; w < ZW; ++w)
-                zpark[q][w] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + w)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+            for (int wd = 0; wd < ZW; ++wd)
+                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
+                                     : make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    uint4 vpark[4];
+    float w[8][WM];
+    // q or k row r0 + o from its conv output y: normalise, round, store
+    auto qk_row = [&](int o, float (&y)[8], bool is_q) {
+        const int i = r0 + o;
+        float ss = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int idx = tid + q * NT, i = idx >> 4, c16 = idx & 15;
-        vpark[q] = i < n ? __ldg(reinterpret_cast<const uint4*>(vc16 + (size_t)(tc0 + i) * Dv + h * D + c16 * 8))
-                         : make_uint4(0u, 0u, 0u, 0u);
+        for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float sc = i < n ? (is_q ? rsqrtf(ss + A.l2_eps) * rsqrtf((float)D) : rsqrtf(ss + A.l2_eps)) : 0.f;
+        uint4 pk;
+        pk.x = pack_half2(y[0] * sc, y[1] * sc);
+        pk.y = pack_half2(y[2] * sc, y[3] * sc);
+        pk.z = pack_half2(y[4] * sc, y[5] * sc);
+        pk.w = pack_half2(y[6] * sc, y[7] * sc);
+        const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
+        *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
+        if (!is_q && write_k) *reinterpret_cast<uint4*>(kimg + (cg >> 3) * 8192 + tc::sw128_chunk(i, cg & 7)) = pk;
+    };
+    auto v_row = [&](int o, const float (&y)[8]) {
+        const bool in = r0 + o < n;
+        uint4 pk;
+        pk.x = in ? pack_half2(y[0], y[1]) : 0u;
+        pk.y = in ? pack_half2(y[2], y[3]) : 0u;
+        pk.z = in ? pack_half2(y[4], y[5]) : 0u;
+        pk.w = in ? pack_half2(y[6], y[7]) : 0u;
+        return pk;
+    };
+    uint4 vpark[4];  // v rows r0 .. r0 + 3, channels 8 cg .. 8 cg + 7, fp16
+    if constexpr (sizeof(TIn) == 2) {
+        // bf16: the raw k, q, v rows r = -(WM-1) .. 63 of the chunk (row slot r + WM - 1) go to
+        // shared memory by asynchronous copies, zero-filled where a row is absent; the region
+        // is free until the A / P phase
+        constexpr int NRT = CH + WM - 1;
+        for (int idx = tid; idx < 3 * NRT * 16; idx += NT) {
+            const int t = idx / (NRT * 16), rem = idx - t * (NRT * 16), j = rem >> 4, c16 = rem & 15;
+            const int r = j - (WM - 1), p = p0 + r;
+            const TIn* src = t == 0 ? kin : t == 1 ? qin : vin;
+            const int width = t == 2 ? Dv : Dq, col = (t == 2 ? h : hk) * D + 8 * c16;
+            const int ch = (t == 0 ? Dq : t == 1 ? 0 : 2 * Dq) + col;
+            const void* g = src;
+            uint32_t bytes = 0;
+            if (r < n && p >= 0) {
+                g = src + (size_t)(tc0 + r) * width + col;
+                bytes = 16;
+            } else if (r < n && p >= -(A.W - 1)) {
+                g = cbuf + (size_t)(A.W - 1 + p) * A.C + ch;
+                bytes = 16;
+            }
+            cp_async16(sm + P_RAW + (uint32_t)(t * NRT + j) * 256 + c16 * 16, g, bytes);
+        }
+        cp_async_commit();
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
+        cp_async_wait_all();
+        __syncthreads();
+        // SiLU(conv) of output rows r0 .. r0 + 3 of tensor t from its shared-memory tile; each
+        // input row is read and widened once and slides through the window
+        auto conv_rows = [&](int t, auto&& emit) {
+            const unsigned char* tile = sm + P_RAW + (uint32_t)(t * NRT + r0) * 256 + cg * 16;
+            float x[WM + 3][8];
+#pragma unroll
+            for (int j = 0; j < WM + 3; ++j) unpack8_bf16(*reinterpret_cast<const uint4*>(tile + j * 256), x[j]);
+#pragma unroll
+            for (int o = 0; o < 4; ++o) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < WM; ++j) acc = fmaf(w[e][j], x[o + j][e], acc);
+                    y[e] = silu_f(acc);
+                }
+                emit(o, y);
+            }
+        };
+        conv_rows(0, [&](int o, float (&y)[8]) { qk_row(o, y, false); });
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
+        conv_rows(1, [&](int o, float (&y)[8]) { qk_row(o, y, true); });
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chv, A.W);
+        conv_rows(2, [&](int o, float (&y)[8]) { vpark[o] = v_row(o, y); });
+    } else {
+        // fp32: the rows through registers, one tensor at a time
+        ConvRows<TIn, WM> x;
+        x.load(kin, Dq, hk * D + 8 * cg, cbuf, A.C, chk, A.W, tc0, p0, r0, n);
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            float y[8];
+            x.row(w, o, y);
+            qk_row(o, y, false);
+        }
+        x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, chq, A.W, tc0, p0, r0, n);
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            float y[8];
+            x.row(w, o, y);
+            qk_row(o, y, true);
+        }
+        x.load(vin, Dv, h * D + 8 * cg, cbuf, A.C, chv, A.W, tc0, p0, r0, n);
+        ConvRows<TIn, WM>::taps(w, A.conv_w, chv, A.W);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+            float y[8];
+            x.row(w, o, y);
+            vpark[o] = v_row(o, y);
+        }
     }
     // decay prefix G_i = g_0 + ... + g_i: a shuffle scan per warp, then warp 1 adds warp 0's total
     if (tid < 64) {
         const bool in = tid < n;
-        float x = in ? A.ws.g[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
-        sB[tid] = in ? A.ws.beta[(size_t)(tc0 + tid) * A.hv + h] : 0.f;
+        float x = in ? log_decay(A.A_log[h], ga, A.dt_bias[h]) : 0.f;
+        sB[tid] = in ? sigmoid_f(gb) : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -386,10 +584,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
         // (d') V image [token][dv] for MMA3's second product, from the rows parked in registers
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + q * NT, i = idx >> 4, c16 = idx & 15;
-            *reinterpret_cast<uint4*>(sm + P_R4 + (c16 >> 3) * 8192 + tc::sw128_chunk(i, c16 & 7)) = vpark[q];
-        }
+        for (int o = 0; o < 4; ++o)
+            *reinterpret_cast<uint4*>(sm + P_R4 + (cg >> 3) * 8192 + tc::sw128_chunk(r0 + o, cg & 7)) = vpark[o];
         tc::fence_proxy_async();
         sync_all();
 
@@ -700,24 +896,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 
 size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (size_t)hqk * KIMG_BYTES; }
 
-template <typename TIn, typename TOut>
-cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st)
+template <typename TIn>
+cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st)
 {
-    auto prep = chunk_prep_kernel<TIn>;
+    auto prep = A.W <= 4 ? chunk_prep_kernel<TIn, 4> : chunk_prep_kernel<TIn, 8>;
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-    if (e != cudaSuccess) return e;
-    auto state = chunk_state_kernel<TIn, TOut>;
-    e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
     if (e != cudaSuccess) return e;
     const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
     prep<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A);
+    return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_chunk_state(const PrefillArgs& A, cudaStream_t st)
+{
+    auto state = chunk_state_kernel<TIn, TOut>;
+    cudaError_t e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+    if (e != cudaSuccess) return e;
     state<<<A.n * A.hv, NT, S_SMEM, st>>>(A);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_chunk<float, float>(const PrefillArgs&, cudaStream_t);
-template cudaError_t launch_chunk<float, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
-template cudaError_t launch_chunk<__nv_bfloat16, float>(const PrefillArgs&, cudaStream_t);
-template cudaError_t launch_chunk<__nv_bfloat16, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_prep<float>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_prep<__nv_bfloat16>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_state<float, float>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_state<float, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_state<__nv_bfloat16, float>(const PrefillArgs&, cudaStream_t);
+template cudaError_t launch_chunk_state<__nv_bfloat16, __nv_bfloat16>(const PrefillArgs&, cudaStream_t);
 
 }  // namespace gdn

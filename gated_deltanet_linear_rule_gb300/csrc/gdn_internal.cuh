@@ -23,20 +23,17 @@ struct LayerParams {
     bool set() const { return conv_w && A_log && dt_bias && norm_w; }
 };
 
-// Prefill workspace: per-token intermediates of the varlen prefill.  The recurrent path
-// (d < 128) keeps q, k, v in fp32; the chunked tensor-core path (d = 128) in fp16, the
-// precision its MMA operands have anyway.
+// Prefill workspace.  The recurrent path (d < 128) keeps per-token intermediates in fp32;
+// the chunked tensor-core path (d = 128) forms q, k, v and the gates inside its pre-pass
+// and keeps only per-chunk records.
 struct PrefillWorkspace {
     float* qh = nullptr;     // [T][Hqk*dk] normalised q, scaled by dk^-1/2   (recurrent path)
     float* kh = nullptr;     // [T][Hqk*dk] normalised k                      (recurrent path)
     float* vc = nullptr;     // [T][Hv*dv]  conv + SiLU v                     (recurrent path)
-    __half* qh16 = nullptr;  // the same three in fp16                        (chunked path)
-    __half* kh16 = nullptr;
-    __half* vc16 = nullptr;
-    float* g = nullptr;      // [T][Hv]     log decay
-    float* beta = nullptr;   // [T][Hv]
-    float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm
-    float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat
+    float* g = nullptr;      // [T][Hv]     log decay                         (recurrent path)
+    float* beta = nullptr;   // [T][Hv]                                       (recurrent path)
+    float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm (recurrent path)
+    float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat                     (recurrent path)
     int* order = nullptr;    // [T + 64] sequences ranked by length, longest first
     int* chunk_start = nullptr;    // [n + 1] first chunk record of each sequence (chunked path)
     unsigned char* rec = nullptr;  // [chunk_cap][Hv] per-(chunk, v-head) records of the chunked path
@@ -306,9 +303,13 @@ inline int prefill_call_chunks(int total_tokens, int n_seqs) { return (total_tok
 // bytes of one chunk record set (all v-heads and q/k heads of one chunk)
 size_t chunk_record_bytes(int hv, int hqk);
 
-// chunked tensor-core prefill of the delta rule + gated RMSNorm (d_k = d_v = 128); io dtypes
+// chunked tensor-core prefill of the delta rule + gated RMSNorm (d_k = d_v = 128), in two
+// launches: the parallel pre-pass (conv, norms, gates and the chunk-local products; it reads
+// the slots' conv buffers, so it runs before they are updated) and the state pass
+template <typename TIn>
+cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st);
 template <typename TIn, typename TOut>
-cudaError_t launch_chunk(const PrefillArgs& A, cudaStream_t st);
+cudaError_t launch_chunk_state(const PrefillArgs& A, cudaStream_t st);
 void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens, int chunk_cap);
 
 inline SlotCheck slot_check(const Pool& P, int layer)

@@ -8,16 +8,22 @@
 // Kernels (all on the caller's stream, no host synchronisation):
 //   1. validate   one CTA: cu_seqlens 0-based, non-decreasing, ending at total_tokens;
 //                 slot ids allocated and distinct.  The verdict gates every later kernel.
+// d_k = d_v = 128 (the chunked tensor-core path, gdn_chunk.cu):
+//   2. chunk pre-pass  conv, norms, gates and the chunk-local products, one CTA per
+//                 (chunk, v-head); it reads the slots' old conv buffers
+//   3. conv_tail  one CTA per sequence: the slot's conv buffer becomes the last W-1 raw
+//                 inputs (after the pre-pass has read the old buffer)
+//   4. chunk state pass  one CTA per (sequence, v-head), output and final state
+// d < 128 (the recurrent path):
 //   2. prep       one CTA per token: conv + SiLU over all C channels (the left context
 //                 before a sequence's first token comes from its slot's conv buffer),
 //                 L2 scales of q and k, k.q per q/k head, gates per v-head.
-//   3. conv_tail  one CTA per sequence: the slot's conv buffer becomes the last W-1 raw
-//                 inputs (after prep has read the old buffer).
+//   3. conv_tail  as above
 //   4. recurrent  one CTA per (sequence, v-head, row tile of S): the tile of S stays in
 //                 registers across the whole sequence, token after token.
 //   5. epilogue   gated RMSNorm per (token, v-head).
-// Kernels 2, 4 and 5 use the decode kernel's arithmetic in the same order, so a prefill
-// of L tokens equals L decode steps bit for bit.
+// On the recurrent path kernels 2, 4 and 5 use the decode kernel's arithmetic in the same
+// order, so a prefill of L tokens equals L decode steps bit for bit.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -124,175 +130,12 @@ __global__ void __launch_bounds__(256) prep_kernel(PrefillArgs A)
         A.ws.beta[(size_t)t * A.hv + h] = sigmoid_f(to_f(bin[(size_t)t * A.hv + h]));
     }
     __syncthreads();
-    if (A.D == 128) {  // chunked path: fp16 rows
-        for (int c = threadIdx.x; c < C; c += blockDim.x) {
-            if (c < Dq) A.ws.qh16[(size_t)t * Dq + c] = __float2half_rn(y[c] * scale[c / D]);
-            else if (c < 2 * Dq) A.ws.kh16[(size_t)t * Dq + (c - Dq)] = __float2half_rn(y[c] * scale[c / D]);
-            else A.ws.vc16[(size_t)t * (A.hv * D) + (c - 2 * Dq)] = __float2half_rn(y[c]);
-        }
-        return;
-    }
     for (int hk = threadIdx.x; hk < A.hqk; hk += blockDim.x)
         A.kq[(size_t)t * A.hqk + hk] = dots[hk] * scale[hk] * scale[A.hqk + hk];
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
         if (c < Dq) A.ws.qh[(size_t)t * Dq + c] = y[c] * scale[c / D];
         else if (c < 2 * Dq) A.ws.kh[(size_t)t * Dq + (c - Dq)] = y[c] * scale[c / D];
         else A.ws.vc[(size_t)t * (A.hv * D) + (c - 2 * Dq)] = y[c];
-    }
-}
-
-// 8 io values of one row -> float (16-B or 32-B load)
-template <typename T> __device__ __forceinline__ void load8_io(const T* p, float* v);
-template <> __device__ __forceinline__ void load8_io<float>(const float* p, float* v)
-{
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <> __device__ __forceinline__ void load8_io<__nv_bfloat16>(const __nv_bfloat16* p, float* v)
-{
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        v[2 * q] = f.x;
-        v[2 * q + 1] = f.y;
-    }
-}
-
-// 8 io values through the read-only data path (the inputs are not written by this kernel)
-template <typename T> __device__ __forceinline__ void load8_ro(const T* p, float* v);
-template <> __device__ __forceinline__ void load8_ro<float>(const float* p, float* v)
-{
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <> __device__ __forceinline__ void load8_ro<__nv_bfloat16>(const __nv_bfloat16* p, float* v)
-{
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        v[2 * q] = f.x;
-        v[2 * q + 1] = f.y;
-    }
-}
-
-// Prep for the chunked path (d = 128, conv width W <= 4): a thread owns 8 consecutive channels
-// over a block of 32 tokens, keeps the conv window and weights in registers, and normalises
-// q / k heads (128 channels = 16 threads) with half-warp shuffles.  fp16 rows out; gates from
-// the CTAs of the first channel block.
-constexpr int kPrepTokens = 32;
-
-template <typename TIn, int W>
-__global__ void __launch_bounds__(256) prep_chunked_kernel(PrefillArgs A)
-{
-    if (!*A.ws.valid) return;
-    const int D = 128, Dq = A.hqk * D, Dv = A.hv * D, C = A.C;
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
-    const int c8 = g * 8;
-    const int tb0 = blockIdx.y * kPrepTokens, tb1 = min(A.T, tb0 + kPrepTokens);
-    const bool active = c8 < C;
-
-    // gates of this token block
-    if (blockIdx.x == 0) {
-        const TIn* ain = static_cast<const TIn*>(A.a);
-        const TIn* bin = static_cast<const TIn*>(A.b);
-        for (int idx = threadIdx.x; idx < (tb1 - tb0) * A.hv; idx += blockDim.x) {
-            const int t = tb0 + idx / A.hv, h = idx % A.hv;
-            A.ws.g[(size_t)t * A.hv + h] = log_decay(A.A_log[h], to_f(ain[(size_t)t * A.hv + h]), A.dt_bias[h]);
-            A.ws.beta[(size_t)t * A.hv + h] = sigmoid_f(to_f(bin[(size_t)t * A.hv + h]));
-        }
-    }
-    if (tb0 >= tb1) return;
-
-    // channel kind and source row of these 8 channels
-    const TIn* src;
-    int width, col;
-    __half* dst;
-    int kind;  // 0 = q, 1 = k, 2 = v
-    if (c8 < Dq) { src = static_cast<const TIn*>(A.q); width = Dq; col = c8; dst = A.ws.qh16; kind = 0; }
-    else if (c8 < 2 * Dq) { src = static_cast<const TIn*>(A.k); width = Dq; col = c8 - Dq; dst = A.ws.kh16; kind = 1; }
-    else { src = static_cast<const TIn*>(A.v); width = Dv; col = c8 - 2 * Dq; dst = A.ws.vc16; kind = 2; }
-    if (!active) { src = static_cast<const TIn*>(A.q); width = Dq; col = 0; dst = nullptr; kind = 2; }
-
-    float w[8][W];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int j = 0; j < W; ++j) w[e][j] = active ? A.conv_w[(size_t)(c8 + e) * W + j] : 0.f;
-
-    // the sequence of the first token, and the W-1 inputs before it
-    int s = 0;
-    {
-        int lo = 0, hi = A.n;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (A.cu[mid] <= tb0) lo = mid;
-            else hi = mid;
-        }
-        s = lo;
-    }
-    float win[W > 1 ? W - 1 : 1][8];  // win[0] = oldest
-    auto load_window = [&](int t) {   // inputs before token t of sequence s
-        const int pos = t - A.cu[s];
-        const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
-                                                                    A.slot_bytes + A.state_bytes);
-#pragma unroll
-        for (int j = 0; j < W - 1; ++j) {
-            const int pp = pos - (W - 1) + j;  // position of window entry j
-            if (pp >= 0) load8_io<TIn>(src + (size_t)(t - (W - 1) + j) * width + col, win[j]);
-            else load8_io<TIn>(cbuf + (size_t)(W - 1 + pp) * C + c8, win[j]);
-        }
-    };
-    while (s + 1 < A.n && A.cu[s + 1] <= tb0) ++s;
-    if (active) load_window(tb0);
-
-    // inputs are read through the read-only path one token ahead of their use, so the next
-    // load is in flight while this token is computed and stored
-    float xn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (active) load8_ro<TIn>(src + (size_t)tb0 * width + col, xn);
-    for (int t = tb0; t < tb1; ++t) {
-        if (t >= A.cu[s + 1]) {  // a new sequence starts here (skip empty ones)
-            while (s + 1 < A.n && A.cu[s + 1] <= t) ++s;
-            if (active) load_window(t);
-        }
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = xn[e];
-        if (active && t + 1 < tb1) load8_ro<TIn>(src + (size_t)(t + 1) * width + col, xn);
-        float y[8];
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j) acc = fmaf(w[e][j], win[j][e], acc);
-            acc = fmaf(w[e][W - 1], x[e], acc);
-            y[e] = silu_f(acc);
-            ss = fmaf(y[e], y[e], ss);
-        }
-#pragma unroll
-        for (int j = 0; j + 1 < W - 1; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
-        if (W > 1) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) win[W - 2][e] = x[e];
-        }
-        // q / k heads: sum of squares over the 16 threads of the head
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float sc = kind == 0 ? rsqrtf(ss + A.l2_eps) * rsqrtf((float)D) : kind == 1 ? rsqrtf(ss + A.l2_eps) : 1.f;
-        if (active) {
-            uint4 o;
-            o.x = pack_half2(y[0] * sc, y[1] * sc);
-            o.y = pack_half2(y[2] * sc, y[3] * sc);
-            o.z = pack_half2(y[4] * sc, y[5] * sc);
-            o.w = pack_half2(y[6] * sc, y[7] * sc);
-            *reinterpret_cast<uint4*>(dst + (size_t)t * width + col) = o;
-        }
     }
 }
 
@@ -406,6 +249,14 @@ template <typename TIn, typename TOut>
 cudaError_t run(const PrefillArgs& A, cudaStream_t st)
 {
     validate_kernel<<<1, 256, 0, st>>>(A);
+    if (A.T > 0 && A.D == 128) {
+        cudaError_t e = launch_chunk_prep<TIn>(A, st);  // reads the conv buffers ...
+        if (e != cudaSuccess) return e;
+        conv_tail_kernel<TIn><<<dim3(A.n, (A.C + 255) / 256), 256, 0, st>>>(A);  // ... then they advance
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_chunk_state<TIn, TOut>(A, st);
+    }
     if (A.T > 0) {
         const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);
         if (smem > 48 * 1024) {
@@ -413,24 +264,9 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
                 cudaFuncSetAttribute(prep_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
         }
-        if (A.D == 128 && A.W <= 4 && A.C % 8 == 0) {
-            dim3 grid((A.C / 8 + 255) / 256, (A.T + kPrepTokens - 1) / kPrepTokens);
-            switch (A.W) {
-                case 1: prep_chunked_kernel<TIn, 1><<<grid, 256, 0, st>>>(A); break;
-                case 2: prep_chunked_kernel<TIn, 2><<<grid, 256, 0, st>>>(A); break;
-                case 3: prep_chunked_kernel<TIn, 3><<<grid, 256, 0, st>>>(A); break;
-                default: prep_chunked_kernel<TIn, 4><<<grid, 256, 0, st>>>(A); break;
-            }
-        } else {
-            prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
-        }
+        prep_kernel<TIn><<<A.T, 256, smem, st>>>(A);
     }
     conv_tail_kernel<TIn><<<dim3(A.n, (A.C + 255) / 256), 256, 0, st>>>(A);
-    if (A.T > 0 && A.D == 128) {
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_chunk<TIn, TOut>(A, st);
-    }
     if (A.T > 0) {
         const int rows = std::min(A.D, 8 * (32 / (A.D / 16)));
         dim3 grid(A.n, A.hv, A.D / rows);
@@ -454,15 +290,12 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
 {
     const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
     size_t b = 0;
-    if (prefill_chunked(s)) {
-        b += align256((size_t)T * Dq * 2) * 2;        // qh16, kh16
-        b += align256((size_t)T * Dv * 2);            // vc16
-    } else {
+    if (!prefill_chunked(s)) {
         b += align256((size_t)T * Dq * 4) * 2;        // qh, kh
         b += align256((size_t)T * Dv * 4) * 2;        // vc, o
         b += align256((size_t)T * s.hqk * 4);         // k.q
+        b += align256((size_t)T * s.hv * 4) * 2;      // g, beta
     }
-    b += align256((size_t)T * s.hv * 4) * 2;          // g, beta
     b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
     b += align256((size_t)(prefill_max_seqs(T) + 1) * 4);  // chunk starts
     b += (size_t)chunk_cap * chunk_record_bytes(s.hv, s.hqk);  // chunk records (multiple of 256)
@@ -479,19 +312,15 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
         p += align256(bytes);
         return r;
     };
-    if (prefill_chunked(s)) {
-        ws.qh16 = reinterpret_cast<__half*>(take((size_t)T * Dq * 2));
-        ws.kh16 = reinterpret_cast<__half*>(take((size_t)T * Dq * 2));
-        ws.vc16 = reinterpret_cast<__half*>(take((size_t)T * Dv * 2));
-    } else {
+    if (!prefill_chunked(s)) {
         ws.qh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
         ws.kh = reinterpret_cast<float*>(take((size_t)T * Dq * 4));
         ws.vc = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
         ws.o = reinterpret_cast<float*>(take((size_t)T * Dv * 4));
         ws.kq = reinterpret_cast<float*>(take((size_t)T * s.hqk * 4));
+        ws.g = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
+        ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     }
-    ws.g = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
-    ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
     ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
     ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 82432));

@@ -180,3 +180,29 @@ def test_prefill_chunked_d128_random_state_weak_decay_split():
     print(f"chunked weak decay: out {r1:.2e} split {r2:.2e} S {rS:.2e} split S {rS2:.2e}")
     assert max(r1, r2, rS, rS2) <= PREFILL_TOL
     L.close()
+
+
+@pytest.mark.parametrize("W", [2, 6])
+def test_prefill_chunked_d128_conv_width_and_buffer(W):
+    """d = 128 with conv width W = 2 (fewer taps than the 4-tap fast path) and W = 6 (the 8-tap path), from
+    non-zero slot conv buffers and N(0, 0.1) states: the chunked pre-pass takes the W-1 positions before each
+    sequence from its slot's conv buffer, including sequences shorter than W-1; the buffers then advance."""
+    lengths = [1, 2, 70, 129, 5]
+    n = len(lengths)
+    L = Layer(14, 1, 2, 128, conv_w=W, io="bf16", out="f32", num_slots=8, max_prefill_tokens=sum(lengths))
+    slots = [L.pool.alloc() for _ in range(n)]
+    S0 = np.stack([synth.initial_state(14, 0, j, 2, 128, 128) for j in range(n)]).astype(np.float64)
+    conv0 = np.stack([synth.initial_convbuf(14, 0, j, W, L.C, "bf16") for j in range(n)]).astype(np.float64)
+    for j, s in enumerate(slots):
+        L.set_state(0, s, S0[j], conv0[j])
+    inp, cu = synth.varlen_inputs(14, 0, lengths, 1, 2, 128, 128, "bf16")
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    ref = L.oracle_run(0, cu, inp, S0, conv0)
+    r_out = relerr(o, ref["out"])
+    r_S = max(relerr(L.get_state(0, s)[0], ref["S"][j]) for j, s in enumerate(slots))
+    print(f"chunked d128 W={W}: out {r_out:.2e}, S {r_S:.2e}")
+    assert r_out <= PREFILL_TOL and r_S <= PREFILL_TOL
+    for j, s in enumerate(slots):
+        assert np.array_equal(L.get_state(0, s)[1], ref["convbuf"][j])
+    assert L.pool.device_status() == 0
+    L.close()
