@@ -54,7 +54,7 @@ constexpr uint32_t REC_A4 = 0;       // [W; Q'] K-major image: 2 K-tiles x 128 r
 constexpr uint32_t REC_U = 32768;    // U image [token][dv]: two 64-wide halves 8 KiB apart
 constexpr uint32_t REC_O0 = 49152;   // P U image, same layout
 constexpr uint32_t REC_SC = 65536;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
-constexpr uint32_t REC_GZ = 66048;   // output gates silu(z) * w_n, fp16 [token][dv] row-major (16 KiB)
+constexpr uint32_t REC_GZ = 66048;   // output gates silu(z) * w_n, fp16 [token][dv], two 64-wide halves 8 KiB apart
 constexpr uint32_t REC_BYTES = 82432;
 constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token][dk], halves 8 KiB apart
 
@@ -69,27 +69,20 @@ constexpr uint32_t P_SMALL = 99584;
 constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
 constexpr int FS = 65;                // fp32 matrix row stride (conflict-free row reads)
 
-// state-pass shared memory
-constexpr uint32_t S_BUF = 83968;     // one prefetch buffer: record (A4 | U | O0) | K image | scalars
-constexpr uint32_t B_A4 = 0, B_U = 32768, B_O0 = 49152, B_K = 65536, B_SC = 81920;
-constexpr uint32_t S_S0 = 2 * S_BUF;  // S0 in fp16, K-major: 2 K-tiles x 128 rows
-constexpr uint32_t S_A6 = S_S0 + 32768;  // Delta~ image [token][dv], halves 8 KiB apart
-constexpr uint32_t S_SMALL = S_A6 + 16384;
-constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, norm weight, sums) + slack
+// state-pass shared memory (one CTA per (sequence, v-head, d_v half))
+constexpr uint32_t B_A4 = 0, B_K = 32768, B_U = 49152, B_O0 = 57344, B_GZ = 65536, B_SC = 73728;
+constexpr uint32_t S_TX = 32768 + 16384 + 3 * 8192 + 512;  // bytes of one prefetch
+constexpr uint32_t S_BUF = 75776;     // one prefetch buffer: [W; Q'] | K image | U, P U, gates halves | scalars
+constexpr uint32_t S_S0 = 2 * S_BUF;  // S0^T(:, half) in fp16, MN-major: 128 rows (d_k) of 64 d_v
+constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) [token][64 d_v]
+constexpr uint32_t S_SMALL = S_A6 + 8192;
+constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, sums) + slack
 
 __device__ __forceinline__ void sync_all()
 {
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-}
-
-__device__ __forceinline__ void load8(const float* p, float* v)
-{
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // 8 fp16 values of a 16-B chunk -> float
@@ -450,7 +443,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     if (tid == 0)
         tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
     {
-        uint4* gzo = reinterpret_cast<uint4*>(rec + REC_GZ);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
@@ -463,7 +455,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             w.y = pack_half2(g8[2], g8[3]);
             w.z = pack_half2(g8[4], g8[5]);
             w.w = pack_half2(g8[6], g8[7]);
-            gzo[idx] = w;
+            *reinterpret_cast<uint4*>(rec + REC_GZ + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = w;
         }
     }
     mma_done();
@@ -668,11 +660,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
 }
 
 // ================================================================== state pass ====
-// 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
-
-template <typename TIn> struct ZRow {
-    static constexpr int kWords = 64 * sizeof(TIn) / 16;  // 16-B words of 64 inputs
-};
+// One CTA per (sequence, v-head, d_v half); the two halves of a (sequence, v-head) form a
+// cluster of two.  A CTA keeps S^T restricted to its half, [d_k][64 d_v], in TMEM columns
+// [0, 64) (lane = d_k), so both products of the chain have M = 128 and N = 64:
+//     MMA4  [W; Q'] x S0^T(:, half)   -> columns [64, 128): W S0^T rows 0-63, Q' S0^T rows 64-127
+//     MMA6  S^T(:, half) += K^T x Delta~(:, half)   (K^T and Delta~ read MN-major)
+// The gated RMSNorm of an output row needs its sum of squares over all of d_v: each CTA sends
+// its half's 64 per-token sums into the other CTA's shared memory and arrives on that CTA's
+// mbarrier (distributed shared memory); the output rows are finished one chunk later, while
+// the next MMA4 runs.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
+// 32 (w / 4) .. + 31.
 
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
@@ -681,18 +678,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     unsigned char* sm = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_SMALL);  // [2] record buffers
     uint64_t* bar = full + 2;                                    // MMA completion
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
-    float* s_normw = reinterpret_cast<float*>(sm + S_SMALL + 64);  // [128]
-    float* s_ss = s_normw + 128;                                   // [2][64] partial sums of O^2
+    uint64_t* peer_bar = bar + 1;                                // [2] the other half's sums, by chunk parity
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_bar + 2);
+    float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 64);   // [2][2][64] sums of O^2: chunk parity, column half
+    float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
 
+    // both CTAs of a cluster take these exits together (they depend on the sequence only)
     if (!*A.ws.valid) return;
-    const int s = A.ws.order[blockIdx.x / A.hv], h = blockIdx.x % A.hv;
+    const int half = blockIdx.x & 1, pair = blockIdx.x >> 1;
+    const int s = A.ws.order[pair / A.hv], h = pair % A.hv;
     const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
     if (L <= 0) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2, row = qd * 32 + lane;
     const int hk = h / A.r, Dv = A.hv * D;
     const int nch = (L + CH - 1) / CH, gc0 = A.ws.chunk_start[s];
+    const uint32_t peer = cluster_ctarank() ^ 1u;
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
     TOut* out = static_cast<TOut*>(A.out);
@@ -701,11 +702,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         mbar_init(bar, 1);
+        mbar_init(&peer_bar[0], 1);
+        mbar_init(&peer_bar[1], 1);
         fence_mbar_init();
     }
-    if (tid < 128) s_normw[tid] = A.norm_w[tid];
-    if (warp == 0) tc::alloc(tmem_slot, 256);
+    if (warp == 0) tc::alloc(tmem_slot, 128);
     sync_all();
+    cluster_sync_all();  // the other CTA's barriers exist before anything arrives on them
     const uint32_t tm = *tmem_slot;
     uint32_t phase = 0;
     bool ok = true;
@@ -722,9 +725,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES;
         const unsigned char* kimg = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * KIMG_BYTES;
-        mbar_arrive_expect_tx(&full[c & 1], 65536 + 16384 + 512);
-        bulk_g2s(dst + B_A4, rec, 65536, &full[c & 1]);
+        mbar_arrive_expect_tx(&full[c & 1], S_TX);
+        bulk_g2s(dst + B_A4, rec + REC_A4, 32768, &full[c & 1]);
         bulk_g2s(dst + B_K, kimg, 16384, &full[c & 1]);
+        bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, &full[c & 1]);
+        bulk_g2s(dst + B_O0, rec + REC_O0 + half * 8192, 8192, &full[c & 1]);
+        bulk_g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, &full[c & 1]);
         bulk_g2s(dst + B_SC, rec + REC_SC, 512, &full[c & 1]);
         issued = c + 1;
     };
@@ -733,55 +739,66 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         if (nch > 1) prefetch(1);
     }
 
-    // incoming state into TMEM columns [0, 128): lane = d_v row, this warp's column half
-    for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
+    // incoming state: S^T(:, half) into TMEM columns [0, 64); lane = d_k, column j = d_v 64 half + j
+    {
         float v[32];
-        const float* srow = Sg + (size_t)row * D + c0;
+        const int dv0 = half * 64 + 32 * hf;
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) load8(srow + e, v + e);
-        tc::st32(tc::taddr(tm, warp, c0), v);
+        for (int e = 0; e < 32; ++e) v[e] = Sg[(size_t)(dv0 + e) * D + row];
+        tc::st32(tc::taddr(tm, warp, 32 * hf), v);
+        tc::wait_st();
     }
-    tc::wait_st();
     sync_all();
+
+    // The output rows of chunk c wait in registers (O and the gates, this thread's 32 columns)
+    // and are finished while MMA4 of chunk c + 1 runs, when the other CTA's sums for chunk c
+    // have long arrived: the exchange stays off the serial chain.
+    float o[32];
+    uint4 gzr[4];
+    int pend_c = -1;  // chunk whose output rows are pending
+    const int orow = row - 64;
+    auto finish_rows = [&](int pc) -> bool {  // rows >= 64 only; false when the sums never came
+        const bool gotp = mbar_wait_cluster_bounded(&peer_bar[pc & 1], (uint32_t)((pc >> 1) & 1));
+        const int pn = min(CH, L - pc * CH);
+        if (gotp && orow < pn) {
+            const float rs =
+                rms_scale(s_ss[(pc & 1) * 128 + orow] + s_ss[(pc & 1) * 128 + 64 + orow] + peer_ss[(pc & 1) * 64 + orow],
+                          A.norm_eps, D);
+            TOut* dst = out + (size_t)(t0 + pc * CH + orow) * Dv + (size_t)h * D + half * 64 + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float gz[8], y[8];
+                unpack8(gzr[q], gz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = o[8 * q + e] * rs * gz[e];
+                store8<TOut>(dst + 8 * q, y);
+            }
+        }
+        return gotp;
+    };
 
     for (int c = 0; c < nch && ok; ++c) {
         unsigned char* buf = sm + (c & 1) * S_BUF;
-        const int tc0 = t0 + c * CH, n = min(CH, L - c * CH);
-        // the output gates silu(z) * w_n of this thread's row half (rows 64-127 = tokens), computed
-        // by the pre-pass, are fetched early
-        uint4 gz[8];
-        const int orow = row - 64;
-        const size_t obase = (size_t)(tc0 + (orow >= 0 && orow < n ? orow : 0)) * Dv + (size_t)h * D + 64 * hf;
-        if (row >= 64) {
-            const uint4* gp = reinterpret_cast<const uint4*>(A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES +
-                                                             REC_GZ + (size_t)orow * 256 + hf * 128);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) gz[q] = __ldg(gp + q);
-        }
+        // arm this chunk's barrier for the other CTA's 64 sums.  Its stores for chunk c + 2 reuse
+        // the barrier and buffer; they are issued only after it has received this CTA's sums for
+        // chunk c + 1, which are sent after this chunk's sums were consumed.
+        if (tid == 0) mbar_arrive_expect_tx(&peer_bar[c & 1], 256);
         // every thread waits for the record itself; the verdict becomes uniform at the next barrier
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         const float* sc = reinterpret_cast<const float*>(buf + B_SC);
 
-        // S0 (fp16, K-major rows = d_v) for MMA4; S <- e^{G_last} S for MMA6
+        // S0^T (fp16, MN-major: row = d_k) for MMA4; S^T <- e^{G_last} S^T for MMA6
         {
             const float egl = sc[64];
-            float v0[32], v1[32];
-            tc::ld32(tc::taddr(tm, warp, 64 * hf), v0);
-            tc::ld32(tc::taddr(tm, warp, 64 * hf + 32), v1);
+            float v[32];
+            tc::ld32(tc::taddr(tm, warp, 32 * hf), v);
             tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tc::st_chunk<Op>(sm + S_S0 + hf * 16384, row, q, v0 + 8 * q);
-                tc::st_chunk<Op>(sm + S_S0 + hf * 16384, row, 4 + q, v1 + 8 * q);
-            }
+            for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + S_S0, row, 4 * hf + q, v + 8 * q);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                v0[e] *= egl;
-                v1[e] *= egl;
-            }
-            tc::st32(tc::taddr(tm, warp, 64 * hf), v0);
-            tc::st32(tc::taddr(tm, warp, 64 * hf + 32), v1);
+            for (int e = 0; e < 32; ++e) v[e] *= egl;
+            tc::st32(tc::taddr(tm, warp, 32 * hf), v);
             tc::wait_st();
         }
         tc::fence_proxy_async();
@@ -790,78 +807,76 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::fence_after_sync();
         if (!ok) break;
 
-        // MMA4: [W; Q'] x S0^T -> columns [128, 256)
-        if (tid == 0)
-            tc::mma_k(tm + 128, smem_addr(buf + B_A4), 128, smem_addr(sm + S_S0), 128, D, tc::idesc_f16(128, 128), 0);
-        mma_done();
+        // MMA4: [W; Q'] x S0^T(:, half) -> columns [64, 128); the previous chunk's output rows
+        // are finished meanwhile
+        if (tid == 0) {
+            tc::mma_k_mixed(tm + 64, smem_addr(buf + B_A4), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192, D,
+                            tc::idesc_f16(128, 64, 0, 1), 0);
+            tc::commit(bar);
+        }
+        bool gotp = true;
+        if (pend_c >= 0 && row >= 64) gotp = finish_rows(pend_c);
+        {
+            const bool got4 = mbar_wait_bounded(bar, phase, nullptr);
+            phase ^= 1u;
+            if ((!got4 || !gotp) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = __syncthreads_and(got4 && gotp) != 0;
+            tc::fence_after_sync();
+        }
         if (!ok) break;
 
+        float d[32];
+        tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
+        tc::wait_ld();
         if (row < 64) {
             // Delta~_i = gamma_i (U_i - (W S0^T)_i) -> row i of the Delta~ image
-            const int i = row;
-            const float gm = sc[i];
-            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-                float ws_[32];
-                tc::ld32(tc::taddr(tm, warp, 128 + c0), ws_);
-                tc::wait_ld();
+            const float gm = sc[row];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int ch = (c0 & 63) / 8 + q;
-                    float u[8];
-                    unpack8(*reinterpret_cast<const uint4*>(buf + B_U + (c0 >> 6) * 8192 + tc::sw128_chunk(i, ch)), u);
+            for (int q = 0; q < 4; ++q) {
+                float u[8];
+                unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), u);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) u[e] = gm * (u[e] - ws_[8 * q + e]);
-                    tc::st_chunk<Op>(sm + S_A6 + (c0 >> 6) * 8192, i, ch, u);
-                }
+                for (int e = 0; e < 8; ++e) u[e] = gm * (u[e] - d[8 * q + e]);
+                tc::st_chunk<Op>(sm + S_A6, row, 4 * hf + q, u);
             }
-        }
-        // rows 64-127: O_i = (Q' S0^T)_i + (P U)_i over this warp's 64 columns, kept in registers
-        // while MMA6 runs; the other half's sum of squares comes through shared memory
-        float o[64];
-        if (row >= 64) {
-            const int i = orow;
+        } else {
+            // O_i = (Q' S0^T)_i + (P U)_i over this thread's 32 columns, its sum of squares, and
+            // the row's gates, all kept for the next iteration
             float ss = 0.f;
-            float t0v[32], t1v[32];
-            tc::ld32(tc::taddr(tm, warp, 128 + 64 * hf), t0v);
-            tc::ld32(tc::taddr(tm, warp, 128 + 64 * hf + 32), t1v);
-            tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 float pu[8];
-                unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + hf * 8192 + tc::sw128_chunk(i, q)), pu);
+                unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + tc::sw128_chunk(orow, 4 * hf + q)), pu);
+                gzr[q] = *reinterpret_cast<const uint4*>(buf + B_GZ + tc::sw128_chunk(orow, 4 * hf + q));
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float x = (q < 4 ? t0v[8 * q + e] : t1v[8 * (q - 4) + e]) + pu[e];
-                    o[8 * q + e] = x;
-                    ss = fmaf(x, x, ss);
+                    o[8 * q + e] = d[8 * q + e] + pu[e];
+                    ss = fmaf(o[8 * q + e], o[8 * q + e], ss);
                 }
             }
-            s_ss[hf * 64 + i] = ss;
+            s_ss[(c & 1) * 128 + hf * 64 + orow] = ss;
         }
         tc::fence_proxy_async();
         sync_all();
 
-        // MMA6: S += Delta~^T x K (both read MN-major from row-wise images); the output rows'
-        // gated RMSNorm runs while it does
+        // MMA6: S^T(:, half) += K^T x Delta~ (both read MN-major from row-wise images)
         if (tid == 0) {
-            tc::mma_k_mixed(tm, smem_addr(sm + S_A6), 0, 1, 8192, smem_addr(buf + B_K), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 128, 1, 1), 1);
+            tc::mma_k_mixed(tm, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 64, 1, 1), 1);
             tc::commit(bar);
         }
-        if (row >= 64 && orow < n) {
-            const float rs = rms_scale(s_ss[orow] + s_ss[64 + orow], A.norm_eps, D);
-#pragma unroll
-            for (int e8 = 0; e8 < 64; e8 += 8) {
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 gg = __half22float2(reinterpret_cast<const __half2*>(&gz[e8 / 8])[e / 2]);
-                    y[e] = o[e8 + e] * rs * gg.x;
-                    y[e + 1] = o[e8 + e + 1] * rs * gg.y;
-                }
-                store8<TOut>(out + obase + e8, y);
-            }
+        // this half's per-token sums of squares -> the other CTA, by asynchronous stores that
+        // complete on its barrier for this chunk (which it armed for 256 bytes)
+        if (tid >= 32 && tid < 48) {
+            const int j = tid - 32;
+            const float* mine = s_ss + (c & 1) * 128;
+            const float4 a = reinterpret_cast<const float4*>(mine)[j];
+            const float4 b = reinterpret_cast<const float4*>(mine + 64)[j];
+            st_async_cluster_v4(map_to_rank(smem_addr(peer_ss + (c & 1) * 64 + 4 * j), peer),
+                                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w),
+                                map_to_rank(smem_addr(&peer_bar[c & 1]), peer));
         }
+        pend_c = c;
         {
             const bool got6 = mbar_wait_bounded(bar, phase, nullptr);
             phase ^= 1u;
@@ -872,16 +887,20 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         // this buffer is free again: fetch the record two chunks ahead into it
         if (ok && tid == 0 && c + 2 < nch) prefetch(c + 2);
     }
+    if (ok && pend_c >= 0) {
+        bool gotp = true;
+        if (row >= 64) gotp = finish_rows(pend_c);
+        if (!gotp && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        ok = __syncthreads_and(gotp) != 0;
+    }
 
     if (ok) {
-        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-            float v[32];
-            tc::ld32(tc::taddr(tm, warp, c0), v);
-            tc::wait_ld();
-            float* srow = Sg + (size_t)row * D + c0;
+        float v[32];
+        tc::ld32(tc::taddr(tm, warp, 32 * hf), v);
+        tc::wait_ld();
+        const int dv0 = half * 64 + 32 * hf;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(srow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-        }
+        for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = v[e];
     }
     // every prefetched copy must land before the CTA's shared memory goes away
     if (tid == 0) {
@@ -889,7 +908,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
     }
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 256);
+    if (warp == 0) tc::dealloc(tm, 128);
+    // Neither CTA leaves while the other may still write into its shared memory.  Both reach
+    // this barrier: every wait above is bounded and a failed wait ends the loop in both CTAs.
+    cluster_sync_all();
 }
 
 }  // namespace
@@ -913,7 +935,21 @@ cudaError_t launch_chunk_state(const PrefillArgs& A, cudaStream_t st)
     auto state = chunk_state_kernel<TIn, TOut>;
     cudaError_t e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
     if (e != cudaSuccess) return e;
-    state<<<A.n * A.hv, NT, S_SMEM, st>>>(A);
+    // one CTA per (sequence, v-head, d_v half); the two halves form a cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(A.n * A.hv * 2));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = S_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, state, A);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -83,13 +83,17 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
 
 // K = 16 * ksteps GEMM slice loop over operands of K extent 64 * ktiles (each K tile is
 // R rows * 128 B; a_rows / b_rows give the tile pitch of A and B in rows).
+// (The start-address field holds address / 16 in its low 14 bits; shared addresses stay below
+// 256 KiB, so a K slice's descriptor is the base descriptor plus its byte offset / 16.)
 __device__ __forceinline__ void mma_k(uint32_t d_tmem, uint32_t a_saddr, int a_rows, uint32_t b_saddr,
                                            int b_rows, int kdim, uint32_t idesc, uint32_t accumulate)
 {
+    const uint64_t a0 = sdesc(a_saddr), b0 = sdesc(b_saddr);
+#pragma unroll 8
     for (int k16 = 0; k16 < kdim / 16; ++k16) {
         const int kt = k16 >> 2, kin = (k16 & 3) * 32;
-        const uint64_t a = sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
-        const uint64_t b = sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
+        const uint64_t a = a0 + (uint64_t)((kt * a_rows * 128 + kin) >> 4);
+        const uint64_t b = b0 + (uint64_t)((kt * b_rows * 128 + kin) >> 4);
         mma(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
     }
 }
@@ -101,12 +105,13 @@ __device__ __forceinline__ void mma_k_mixed(uint32_t d_tmem, uint32_t a_saddr, i
                                             uint32_t a_lbo, uint32_t b_saddr, int b_rows, uint32_t b_mn,
                                             uint32_t b_lbo, int kdim, uint32_t idesc, uint32_t accumulate)
 {
+    const uint64_t a0 = a_mn ? sdesc_mn(a_saddr, a_lbo) : sdesc(a_saddr);
+    const uint64_t b0 = b_mn ? sdesc_mn(b_saddr, b_lbo) : sdesc(b_saddr);
+#pragma unroll 8
     for (int k16 = 0; k16 < kdim / 16; ++k16) {
         const int kt = k16 >> 2, kin = (k16 & 3) * 32;
-        const uint64_t a = a_mn ? sdesc_mn(a_saddr + (uint32_t)(k16 * 2048), a_lbo)
-                                : sdesc(a_saddr + (uint32_t)(kt * a_rows * 128 + kin));
-        const uint64_t b = b_mn ? sdesc_mn(b_saddr + (uint32_t)(k16 * 2048), b_lbo)
-                                : sdesc(b_saddr + (uint32_t)(kt * b_rows * 128 + kin));
+        const uint64_t a = a0 + (uint64_t)((a_mn ? k16 * 2048 : kt * a_rows * 128 + kin) >> 4);
+        const uint64_t b = b0 + (uint64_t)((b_mn ? k16 * 2048 : kt * b_rows * 128 + kin) >> 4);
         mma(d_tmem, a, b, idesc, (k16 > 0 || accumulate) ? 1u : 0u);
     }
 }
