@@ -38,7 +38,12 @@
 // the N side; Delta~ as the M side) are read MN-major straight from row-wise tiles.
 // Every tcgen05.ld / st is executed by whole warps (they are warp-collective); per-token
 // conditions only guard stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstring>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 #include "gdn_tcgen05.cuh"
@@ -139,14 +144,22 @@ template <typename TIn> __device__ __forceinline__ float raw_at(const Raw8<TIn>&
     return to_f(reinterpret_cast<const TIn*>(r.w)[e]);
 }
 
-// 16-B asynchronous global -> shared copy; src_bytes = 0 writes zeros and reads nothing
-__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes)
+// Tensor maps of the raw bf16 q, k and v rows ([T][width], 2-D, box 128 channels x (64 + WM - 1)
+// rows, no swizzle, zero fill outside the tensor), encoded on the host per call.
+struct PrepMaps {
+    CUtensorMap q, k, v;
+};
+
+// 2-D tiled bulk tensor copy global -> shared (the TMA engine), completing on an mbarrier.
+// x (the channel coordinate) must be a multiple of 8 bf16 (16 B); y may be negative.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // 8 bf16 values of a 16-B word -> float
 __device__ __forceinline__ void unpack8_bf16(uint4 w, float* v)
@@ -186,21 +199,11 @@ struct ConvRows {
     // conv taps of the 8 channels, right-aligned in WM slots
     __device__ __forceinline__ static void taps(float (&w)[8][WM], const float* conv_w, int ch, int W)
     {
-        if (W == WM) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < 8; ++e)
 #pragma unroll
-                for (int j4 = 0; j4 < WM; j4 += 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(conv_w + (size_t)(ch + e) * WM + j4));
-                    w[e][j4] = t.x; w[e][j4 + 1] = t.y; w[e][j4 + 2] = t.z; w[e][j4 + 3] = t.w;
-                }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-#pragma unroll
-                for (int j = 0; j < WM; ++j)
-                    w[e][j] = j >= WM - W ? __ldg(conv_w + (size_t)(ch + e) * W + (j - (WM - W))) : 0.f;
-        }
+            for (int j = 0; j < WM; ++j)
+                w[e][j] = j >= WM - W ? __ldg(conv_w + (size_t)(ch + e) * W + (j - (WM - W))) : 0.f;
     }
 
     // SiLU(conv) of output row r0 + o
@@ -220,7 +223,8 @@ struct ConvRows {
 // 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
 template <typename TIn, int WM>
-__global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
+__global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant__ PrefillArgs A,
+                                                           const __grid_constant__ PrepMaps M)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
@@ -231,7 +235,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     float* sGam = sEG + 64;
     float* sMisc = sGam + 64;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sMisc + 8);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+    uint64_t* sbar = bar + 1;  // raw rows staged
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
     float* FA = reinterpret_cast<float*>(sm + P_R4);
     float* FT = reinterpret_cast<float*>(sm + P_R5);
     float* X = reinterpret_cast<float*>(sm + P_AT);
@@ -257,9 +262,20 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
                                                                 A.slot_bytes + A.state_bytes);
 
+    constexpr int NRT = CH + WM - 1;  // raw rows of a tensor: r = -(WM-1) .. 63 (row slot r + WM - 1)
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(sbar, 1);
         fence_mbar_init();
+        if constexpr (sizeof(TIn) == 2) {
+            // raw bf16 k, q, v rows of the chunk by three tensor copies; rows past the tensor are
+            // zero, rows of a neighbouring sequence are replaced or never used (below)
+            mbar_arrive_expect_tx(sbar, 3 * NRT * 256);
+            const int y0 = tc0 - (WM - 1);
+            tma_load_2d(sm + P_RAW, &M.k, hk * D, y0, sbar);
+            tma_load_2d(sm + P_RAW + NRT * 256, &M.q, hk * D, y0, sbar);
+            tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h * D, y0, sbar);
+        }
     }
     if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
@@ -289,10 +305,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     const TIn* kin = static_cast<const TIn*>(A.k);
     const TIn* vin = static_cast<const TIn*>(A.v);
     const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg, chv = 2 * Dq + h * D + 8 * cg;
-    float ga = 0.f, gb = 0.f;  // raw gate inputs a, b of token tid (tid < n)
+    TIn ga = TIn(0.f), gb = TIn(0.f);  // raw gate inputs a, b of token tid (tid < n), widened when used
     if (tid < n) {
-        ga = to_f(static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h]);
-        gb = to_f(static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h]);
+        ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
+        gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
     }
     // z of the chunk (the output gates are formed while MMA1 runs)
     constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
@@ -338,31 +354,46 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     };
     uint4 vpark[4];  // v rows r0 .. r0 + 3, channels 8 cg .. 8 cg + 7, fp16
     if constexpr (sizeof(TIn) == 2) {
-        // bf16: the raw k, q, v rows r = -(WM-1) .. 63 of the chunk (row slot r + WM - 1) go to
-        // shared memory by asynchronous copies, zero-filled where a row is absent; the region
-        // is free until the A / P phase
-        constexpr int NRT = CH + WM - 1;
-        for (int idx = tid; idx < 3 * NRT * 16; idx += NT) {
-            const int t = idx / (NRT * 16), rem = idx - t * (NRT * 16), j = rem >> 4, c16 = rem & 15;
-            const int r = j - (WM - 1), p = p0 + r;
-            const TIn* src = t == 0 ? kin : t == 1 ? qin : vin;
-            const int width = t == 2 ? Dv : Dq, col = (t == 2 ? h : hk) * D + 8 * c16;
-            const int ch = (t == 0 ? Dq : t == 1 ? 0 : 2 * Dq) + col;
-            const void* g = src;
-            uint32_t bytes = 0;
-            if (r < n && p >= 0) {
-                g = src + (size_t)(tc0 + r) * width + col;
-                bytes = 16;
-            } else if (r < n && p >= -(A.W - 1)) {
-                g = cbuf + (size_t)(A.W - 1 + p) * A.C + ch;
-                bytes = 16;
+        // bf16: the raw k, q, v rows r = -(WM-1) .. 63 of the chunk (row slot r + WM - 1) arrive
+        // by the tensor copies issued above; meanwhile the conv taps of the three tensors go to
+        // shared memory, right-aligned in WM slots ([tensor][channel][WM]).  A sequence's first
+        // chunk then replaces its rows r < 0 by the slot's conv buffer (zero before it).
+        float* s_taps = reinterpret_cast<float*>(sm + P_RAW + 3 * NRT * 256);
+        {
+            constexpr int KT = 3 * D * WM / NT;  // taps per thread, all loads issued before any store
+            float tv[KT];
+#pragma unroll
+            for (int k = 0; k < KT; ++k) {
+                const int idx = tid + k * NT;
+                const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
+                const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + chl;
+                tv[k] = j >= WM - A.W ? __ldg(A.conv_w + (size_t)ch * A.W + (j - (WM - A.W))) : 0.f;
             }
-            cp_async16(sm + P_RAW + (uint32_t)(t * NRT + j) * 256 + c16 * 16, g, bytes);
+#pragma unroll
+            for (int k = 0; k < KT; ++k) s_taps[tid + k * NT] = tv[k];
         }
-        cp_async_commit();
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
-        cp_async_wait_all();
-        __syncthreads();
+        const bool staged = mbar_wait_bounded(sbar, 0, nullptr);
+        if (!staged && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        for (int idx = tid; p0 == 0 && idx < 3 * (WM - 1) * 16; idx += NT) {
+            const int t = idx / ((WM - 1) * 16), rem = idx - t * ((WM - 1) * 16), j = rem >> 4, c16 = rem & 15;
+            const int p = j - (WM - 1);  // position before the sequence's first token
+            const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + 8 * c16;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (p >= -(A.W - 1))
+                x = *reinterpret_cast<const uint4*>(cbuf + (size_t)(A.W - 1 + p) * A.C + ch);
+            *reinterpret_cast<uint4*>(sm + P_RAW + (uint32_t)(t * NRT + j) * 256 + c16 * 16) = x;
+        }
+        ok = __syncthreads_and(staged) != 0;
+        auto load_taps = [&](int t) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int j4 = 0; j4 < WM; j4 += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(s_taps + (t * D + 8 * cg + e) * WM + j4);
+                    w[e][j4] = v4.x; w[e][j4 + 1] = v4.y; w[e][j4 + 2] = v4.z; w[e][j4 + 3] = v4.w;
+                }
+        };
+        load_taps(0);
         // SiLU(conv) of output rows r0 .. r0 + 3 of tensor t from its shared-memory tile; each
         // input row is read and widened once and slides through the window
         auto conv_rows = [&](int t, auto&& emit) {
@@ -384,9 +415,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
             }
         };
         conv_rows(0, [&](int o, float (&y)[8]) { qk_row(o, y, false); });
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
+        load_taps(1);
         conv_rows(1, [&](int o, float (&y)[8]) { qk_row(o, y, true); });
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chv, A.W);
+        load_taps(2);
         conv_rows(2, [&](int o, float (&y)[8]) { vpark[o] = v_row(o, y); });
     } else {
         // fp32: the rows through registers, one tensor at a time
@@ -419,8 +450,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(PrefillArgs A)
     // decay prefix G_i = g_0 + ... + g_i: a shuffle scan per warp, then warp 1 adds warp 0's total
     if (tid < 64) {
         const bool in = tid < n;
-        float x = in ? log_decay(A.A_log[h], ga, A.dt_bias[h]) : 0.f;
-        sB[tid] = in ? sigmoid_f(gb) : 0.f;
+        float x = in ? log_decay(A.A_log[h], to_f(ga), A.dt_bias[h]) : 0.f;
+        sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -918,14 +949,52 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 
 size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (size_t)hqk * KIMG_BYTES; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+
+// [rows][width] bf16 rows at base, read as boxes of 128 channels x box_rows rows
+cudaError_t encode_rows_map(CUtensorMap* m, const void* base, int width, int rows, int box_rows)
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode_tiled) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                                      box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 template <typename TIn>
 cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st)
 {
-    auto prep = A.W <= 4 ? chunk_prep_kernel<TIn, 4> : chunk_prep_kernel<TIn, 8>;
+    const int WM = A.W <= 4 ? 4 : 8;
+    auto prep = WM == 4 ? chunk_prep_kernel<TIn, 4> : chunk_prep_kernel<TIn, 8>;
     cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
+    PrepMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (sizeof(TIn) == 2) {  // bf16 rows come in by tensor copies
+        const int Dq = A.hqk * D, Dv = A.hv * D;
+        if ((e = encode_rows_map(&maps.q, A.q, Dq, A.T, CH + WM - 1)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&maps.k, A.k, Dq, A.T, CH + WM - 1)) != cudaSuccess) return e;
+        if ((e = encode_rows_map(&maps.v, A.v, Dv, A.T, CH + WM - 1)) != cudaSuccess) return e;
+    }
     const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
-    prep<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A);
+    prep<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A, maps);
     return cudaGetLastError();
 }
 
