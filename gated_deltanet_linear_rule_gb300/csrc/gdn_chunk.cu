@@ -161,18 +161,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// 8 bf16 values of a 16-B word -> float
-__device__ __forceinline__ void unpack8_bf16(uint4 w, float* v)
-{
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        v[2 * q] = f.x;
-        v[2 * q + 1] = f.y;
-    }
-}
-
 // One tensor (q, k or v) of a chunk, as a thread of the pre-pass sees it: 8 channels
 // (column col of the input rows of width `width`, channel ch of the conv's C channels) over
 // the output rows r0 .. r0 + 3.  The causal conv of width W <= WM is evaluated as a
@@ -328,17 +316,22 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // q or k row r0 + o from its conv output y: normalise, round, store
     auto qk_row = [&](int o, float (&y)[8], bool is_q) {
         const int i = r0 + o;
-        float ss = 0.f;
+        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
+        for (int e = 0; e < 8; e += 2) s2 = fma2(make_float2(y[e], y[e + 1]), make_float2(y[e], y[e + 1]), s2);
+        float ss = s2.x + s2.y;
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float sc = i < n ? (is_q ? rsqrtf(ss + A.l2_eps) * rsqrtf((float)D) : rsqrtf(ss + A.l2_eps)) : 0.f;
+        const float2 sc2 = make_float2(sc, sc);
+        float2 z2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) z2[e] = mul2(make_float2(y[2 * e], y[2 * e + 1]), sc2);
         uint4 pk;
-        pk.x = pack_half2(y[0] * sc, y[1] * sc);
-        pk.y = pack_half2(y[2] * sc, y[3] * sc);
-        pk.z = pack_half2(y[4] * sc, y[5] * sc);
-        pk.w = pack_half2(y[6] * sc, y[7] * sc);
+        pk.x = pack_half2(z2[0].x, z2[0].y);
+        pk.y = pack_half2(z2[1].x, z2[1].y);
+        pk.z = pack_half2(z2[2].x, z2[2].y);
+        pk.w = pack_half2(z2[3].x, z2[3].y);
         const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
         *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
         if (!is_q && write_k) *reinterpret_cast<uint4*>(kimg + (cg >> 3) * 8192 + tc::sw128_chunk(i, cg & 7)) = pk;
@@ -384,13 +377,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             *reinterpret_cast<uint4*>(sm + P_RAW + (uint32_t)(t * NRT + j) * 256 + c16 * 16) = x;
         }
         ok = __syncthreads_and(staged) != 0;
+        float2 w2[4][WM];  // taps of channel pairs (8 cg + 2 p, 8 cg + 2 p + 1)
         auto load_taps = [&](int t) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int pr = 0; pr < 4; ++pr)
 #pragma unroll
                 for (int j4 = 0; j4 < WM; j4 += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4*>(s_taps + (t * D + 8 * cg + e) * WM + j4);
-                    w[e][j4] = v4.x; w[e][j4 + 1] = v4.y; w[e][j4 + 2] = v4.z; w[e][j4 + 3] = v4.w;
+                    const float* base = s_taps + (t * D + 8 * cg + 2 * pr) * WM + j4;
+                    const float4 a4 = *reinterpret_cast<const float4*>(base);
+                    const float4 b4 = *reinterpret_cast<const float4*>(base + WM);
+                    w2[pr][j4] = make_float2(a4.x, b4.x);
+                    w2[pr][j4 + 1] = make_float2(a4.y, b4.y);
+                    w2[pr][j4 + 2] = make_float2(a4.z, b4.z);
+                    w2[pr][j4 + 3] = make_float2(a4.w, b4.w);
                 }
         };
         load_taps(0);
@@ -398,18 +397,25 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         // input row is read and widened once and slides through the window
         auto conv_rows = [&](int t, auto&& emit) {
             const unsigned char* tile = sm + P_RAW + (uint32_t)(t * NRT + r0) * 256 + cg * 16;
-            float x[WM + 3][8];
+            float2 x2[WM + 3][4];
 #pragma unroll
-            for (int j = 0; j < WM + 3; ++j) unpack8_bf16(*reinterpret_cast<const uint4*>(tile + j * 256), x[j]);
+            for (int j = 0; j < WM + 3; ++j) {
+                const uint4 u = *reinterpret_cast<const uint4*>(tile + j * 256);
+                const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) x2[j][pr] = __bfloat1622float2(hb[pr]);
+            }
 #pragma unroll
             for (int o = 0; o < 4; ++o) {
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float acc = 0.f;
+                for (int pr = 0; pr < 4; ++pr) {
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < WM; ++j) acc = fmaf(w[e][j], x[o + j][e], acc);
-                    y[e] = silu_f(acc);
+                    for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + j][pr], acc);
+                    const float2 yy = silu2(acc);
+                    y[2 * pr] = yy.x;
+                    y[2 * pr + 1] = yy.y;
                 }
                 emit(o, y);
             }
@@ -478,14 +484,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
             const TIn* zv = reinterpret_cast<const TIn*>(zpark[q]);
-            float g8[8];
+            float2 g2[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) g8[e] = i < n ? silu_f(to_f(zv[e])) * A.norm_w[c8 + e] : 0.f;
+            for (int e = 0; e < 4; ++e)
+                g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))),
+                             make_float2(A.norm_w[c8 + 2 * e], A.norm_w[c8 + 2 * e + 1]));
             uint4 w;
-            w.x = pack_half2(g8[0], g8[1]);
-            w.y = pack_half2(g8[2], g8[3]);
-            w.z = pack_half2(g8[4], g8[5]);
-            w.w = pack_half2(g8[6], g8[7]);
+            w.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
+            w.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
+            w.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
+            w.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
             *reinterpret_cast<uint4*>(rec + REC_GZ + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = w;
         }
     }
