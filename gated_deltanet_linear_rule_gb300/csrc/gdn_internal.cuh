@@ -404,6 +404,15 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
                            const void* b, const void* z, void* out, cudaStream_t st);
 
+// the row tensors of a prefill call are read and written in 16-B pieces (and by tensor copies)
+inline bool rows_aligned16(const void* q, const void* k, const void* v, const void* z, const void* out)
+{
+    const uintptr_t m = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(z) |
+                        reinterpret_cast<uintptr_t>(out);
+    return (m & 15u) == 0;
+}
+
 // workspace of a prefill call of up to max_tokens tokens and chunk_cap chunk records
 size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens, int chunk_cap);
 // sequences a call may carry for a workspace of max_tokens tokens

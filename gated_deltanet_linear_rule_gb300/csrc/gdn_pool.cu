@@ -278,6 +278,7 @@ int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const 
     if (n_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (!cu_seqlens_dev || !slot_ids_dev) return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0 && !gdn::rows_aligned16(q, k, v, z, out)) return GDN_ERR_INVALID_ARG;
     if (!P->params[(size_t)layer].set()) return GDN_ERR_NO_PARAMS;
     if (total_tokens > P->shape.max_prefill_tokens) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs > gdn::prefill_max_seqs(P->shape.max_prefill_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;

@@ -439,6 +439,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     if (n_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (!cu_seqlens_dev || !slot_ids_dev) return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !a || !b || !z || !out)) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0 && !rows_aligned16(q, k, v, z, out)) return GDN_ERR_INVALID_ARG;
     const gdn_shape& s = *shape;
     if (s.hqk <= 0 || s.hv <= 0 || s.hv % s.hqk != 0 || s.conv_w < 1 || s.conv_w > 8) return GDN_ERR_INVALID_ARG;
     if (s.io_dtype < 0 || s.io_dtype > 1 || s.out_dtype < 0 || s.out_dtype > 1) return GDN_ERR_INVALID_ARG;

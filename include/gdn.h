@@ -179,9 +179,12 @@ int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, in
  * gdn_decode_step reads them (the System Design page, "GDN Kernel Dispatch
  * Detail": prefill, then "Update temporal_state").  total_tokens must equal
  * cu_seqlens_dev[n_seqs] and not exceed the pool's max_prefill_tokens; slot
- * ids must be allocated and distinct.  Uses the pool's workspace: calls on one
- * pool must not overlap on the GPU.
- * Errors: INVALID_ARG, NO_PARAMS, UNSUPPORTED_SHAPE (too many tokens), CUDA. */
+ * ids must be allocated and distinct.  q, k, v, z and out are row-major
+ * [total_tokens][width] device buffers whose base addresses are 16-B aligned
+ * (they are moved in 16-B pieces and, at d = 128 in bf16, by tensor copies).
+ * Uses the pool's workspace: calls on one pool must not overlap on the GPU.
+ * Errors: INVALID_ARG (incl. a misaligned row buffer), NO_PARAMS,
+ * UNSUPPORTED_SHAPE (too many tokens), CUDA. */
 int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);

@@ -74,3 +74,15 @@ def test_null_arguments_are_rejected(lib):
     assert lib.gdn_prefill_varlen(None, 0, None, None, 1, 1, *([None] * 8)) == -1
     assert lib.gdn_last_device_status(None, None) == -1
     assert lib.gdn_pool_get_info(None, None) == -1
+
+
+def test_noalloc_prefill_rejects_misaligned_rows_before_any_gpu_work(lib):
+    """Row buffers are moved in 16-B pieces (and by tensor copies at d = 128): a base address that is not
+    16-B aligned is refused by the host checks.  The pointers here are never dereferenced."""
+    f = lib.gdn_prefill_varlen_noalloc
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    good, bad = P(0x100000), P(0x100008)
+    args = lambda q: (ctypes.byref(_shape()), good, good, good, good, good, 4, good, good, 1, 64,
+                      q, good, good, good, good, good, good, None, None)
+    assert f(*args(bad)) == -1
