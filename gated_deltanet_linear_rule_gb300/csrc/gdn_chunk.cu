@@ -67,12 +67,12 @@ constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token
 constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1), then [W; Q'] (record)
 constexpr uint32_t P_AP = 32768;      // [P; P]
 constexpr uint32_t P_AT = 49152;      // inverse scratch, then [T2; T1], then the P U image
-constexpr uint32_t P_R4 = 65536;      // A (fp32, stride 65), then the V image, then the U image
-constexpr uint32_t P_R5 = 82944;      // T (fp32, stride 65), then the W image
+constexpr uint32_t P_R4 = 65536;      // A (fp32, stride 68), then the V image, then the U image
+constexpr uint32_t P_R5 = 82944;      // T (fp32, stride 68), then the W image
 constexpr uint32_t P_RAW = P_AP;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
-constexpr uint32_t P_SMALL = 99584;
+constexpr uint32_t P_SMALL = 100352;
 constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
-constexpr int FS = 65;                // fp32 matrix row stride (conflict-free row reads)
+constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
 // state-pass shared memory (one CTA per (sequence, v-head, d_v half))
 constexpr uint32_t B_A4 = 0, B_K = 32768, B_U = 49152, B_O0 = 57344, B_GZ = 65536, B_SC = 73728;
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
-    float* sGraw = reinterpret_cast<float*>(sm + P_SMALL);
-    float* sG = sGraw + 64;
+    float* sBEG = reinterpret_cast<float*>(sm + P_SMALL);  // beta_j e^{G_j}
+    float* sG = sBEG + 64;
     float* sB = sG + 64;
     float* sEG = sB + 64;
     float* sGam = sEG + 64;
@@ -472,6 +472,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     if (tid < 64) {
         const float gl = sG[n - 1];
         sEG[tid] = expf(sG[tid]);
+        sBEG[tid] = sB[tid] * sEG[tid];
         sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
         if (tid == 0) sMisc[0] = expf(gl);
     }
@@ -500,6 +501,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     mma_done();
     if (ok) {
         // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127; columns 32*hf ..
+        //     The entries of A on and above the diagonal are never read (only strictly lower
+        //     blocks enter the inverse), so A is written unmasked; rows past the chunk's end are
+        //     zero through beta = 0 (A) and q = 0 (P).
         {
             const int row = qd * 32 + lane, i = row & 63, c0 = 32 * hf;
             const float Gi = sG[i];
@@ -509,16 +513,24 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             if (row < 64) {
                 const float bi = sB[i];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = c0 + e;
-                    FA[i * FS + j] = (j < i && i < n) ? bi * __expf(Gi - sG[j]) * v[e] : 0.f;
+                for (int e4 = 0; e4 < 32; e4 += 4) {
+                    const float4 g = *reinterpret_cast<const float4*>(sG + c0 + e4);
+                    float4 a;
+                    a.x = bi * __expf(Gi - g.x) * v[e4];
+                    a.y = bi * __expf(Gi - g.y) * v[e4 + 1];
+                    a.z = bi * __expf(Gi - g.z) * v[e4 + 2];
+                    a.w = bi * __expf(Gi - g.w) * v[e4 + 3];
+                    *reinterpret_cast<float4*>(FA + i * FS + c0 + e4) = a;
                 }
             } else {
                 float p[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = c0 + e;
-                    p[e] = (j <= i && i < n) ? __expf(Gi - sG[j]) * v[e] : 0.f;
+                for (int e4 = 0; e4 < 32; e4 += 4) {
+                    const float4 g = *reinterpret_cast<const float4*>(sG + c0 + e4);
+                    const float gg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        p[e4 + e] = (c0 + e4 + e <= i) ? __expf(Gi - gg[e]) * v[e4 + e] : 0.f;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -531,6 +543,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 
         // (d) T = (I + A)^-1, blocked.  16-wide diagonal blocks by forward substitution
         //     (one column per thread; zero above the diagonal and in the upper blocks) ...
+        //     Rows of A and T are read 4 entries at a time; T's zeros above the diagonal are
+        //     exact, so the merge sums below run over whole blocks.
         if (tid < 64) {
             const int b = tid >> 4, j = tid & 15, o = 16 * b;
             float x[16];
@@ -538,7 +552,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             for (int i = 0; i < 16; ++i) {
                 float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int k = 0; k < i; ++k) acc -= FA[(o + i) * FS + o + k] * x[k];
+                for (int k4 = 0; k4 < i; k4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(FA + (o + i) * FS + o + k4);
+                    const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int k = k4; k < k4 + 4 && k < i; ++k) acc -= aa[k - k4] * x[k];
+                }
                 x[i] = acc;
             }
 #pragma unroll
@@ -556,9 +575,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         {
             const int i = (tid >> 4) & 15, j = tid & 15;
             float a0 = 0.f, a1 = 0.f;
-            for (int k = j; k < 16; ++k) {
-                a0 += FA[(16 + i) * FS + k] * FT[k * FS + j];
-                a1 += FA[(48 + i) * FS + 32 + k] * FT[(32 + k) * FS + 32 + j];
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 f0 = *reinterpret_cast<const float4*>(FA + (16 + i) * FS + k4);
+                const float4 f1 = *reinterpret_cast<const float4*>(FA + (48 + i) * FS + 32 + k4);
+                const float g0[4] = {f0.x, f0.y, f0.z, f0.w}, g1[4] = {f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    a0 = fmaf(g0[k], FT[(k4 + k) * FS + j], a0);
+                    a1 = fmaf(g1[k], FT[(32 + k4 + k) * FS + 32 + j], a1);
+                }
             }
             X[i * 17 + j] = a0;
             X[(16 + i) * 17 + j] = a1;
@@ -567,9 +593,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         {
             const int i = (tid >> 4) & 15, j = tid & 15;
             float a0 = 0.f, a1 = 0.f;
-            for (int k = 0; k <= i; ++k) {
-                a0 += FT[(16 + i) * FS + 16 + k] * X[k * 17 + j];
-                a1 += FT[(48 + i) * FS + 48 + k] * X[(16 + k) * 17 + j];
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 f0 = *reinterpret_cast<const float4*>(FT + (16 + i) * FS + 16 + k4);
+                const float4 f1 = *reinterpret_cast<const float4*>(FT + (48 + i) * FS + 48 + k4);
+                const float g0[4] = {f0.x, f0.y, f0.z, f0.w}, g1[4] = {f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    a0 = fmaf(g0[k], X[(k4 + k) * 17 + j], a0);
+                    a1 = fmaf(g1[k], X[(16 + k4 + k) * 17 + j], a1);
+                }
             }
             FT[(16 + i) * FS + j] = -a0;
             FT[(48 + i) * FS + 32 + j] = -a1;
@@ -579,10 +612,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         {
             const int i0 = tid >> 5, j = tid & 31;
             float a[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = j; k < 32; ++k) {
-                const float t = FT[k * FS + j];
+#pragma unroll 2
+            for (int k4 = 0; k4 < 32; k4 += 4) {
+                float t[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) a[q] += FA[(32 + i0 + 8 * q) * FS + k] * t;
+                for (int k = 0; k < 4; ++k) t[k] = FT[(k4 + k) * FS + j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 f = *reinterpret_cast<const float4*>(FA + (32 + i0 + 8 * q) * FS + k4);
+                    a[q] = fmaf(f.x, t[0], a[q]);
+                    a[q] = fmaf(f.y, t[1], a[q]);
+                    a[q] = fmaf(f.z, t[2], a[q]);
+                    a[q] = fmaf(f.w, t[3], a[q]);
+                }
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) X[(i0 + 8 * q) * 33 + j] = a[q];
@@ -591,11 +633,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         {
             const int i0 = tid >> 5, j = tid & 31;
             float a[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k <= i0 + 24; ++k) {
-                const float x = X[k * 33 + j];
+#pragma unroll 2
+            for (int k4 = 0; k4 < 32; k4 += 4) {
+                float x[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (k <= i0 + 8 * q) a[q] += FT[(32 + i0 + 8 * q) * FS + 32 + k] * x;
+                for (int k = 0; k < 4; ++k) x[k] = X[(k4 + k) * 33 + j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 f = *reinterpret_cast<const float4*>(FT + (32 + i0 + 8 * q) * FS + 32 + k4);
+                    a[q] = fmaf(f.x, x[0], a[q]);
+                    a[q] = fmaf(f.y, x[1], a[q]);
+                    a[q] = fmaf(f.z, x[2], a[q]);
+                    a[q] = fmaf(f.w, x[3], a[q]);
+                }
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) FT[(32 + i0 + 8 * q) * FS + j] = -a[q];
@@ -604,12 +654,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one 8-column chunk per item
         for (int idx = tid; idx < 128 * 8; idx += NT) {
             const int r = idx >> 3, c8 = idx & 7, i = r & 63;
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = c8 * 8 + e;
-                v[e] = FT[i * FS + j] * (r < 64 ? sB[j] : sB[j] * sEG[j]);
-            }
+            const float* sc = (r < 64 ? sB : sBEG) + c8 * 8;
+            const float4 t0 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8);
+            const float4 t1 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8 + 4);
+            const float4 s0 = *reinterpret_cast<const float4*>(sc), s1 = *reinterpret_cast<const float4*>(sc + 4);
+            float v[8] = {t0.x * s0.x, t0.y * s0.y, t0.z * s0.z, t0.w * s0.w,
+                          t1.x * s1.x, t1.y * s1.y, t1.z * s1.z, t1.w * s1.w};
             tc::st_chunk<Op>(sm + P_AT, r, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
