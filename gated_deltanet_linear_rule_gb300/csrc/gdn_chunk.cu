@@ -251,6 +251,38 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                                                                 A.slot_bytes + A.state_bytes);
 
     constexpr int NRT = CH + WM - 1;  // raw rows of a tensor: r = -(WM-1) .. 63 (row slot r + WM - 1)
+    const int rb = tid >> 4, cg = tid & 15, r0 = 4 * rb, p0 = c * CH;
+    // global loads that nothing waits for yet go out first: the gate inputs a, b of token tid,
+    // the chunk's z rows (output gates, formed while MMA1 runs) and the conv taps
+    TIn ga = TIn(0.f), gb = TIn(0.f);
+    if (tid < n) {
+        ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
+        gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
+    }
+    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
+    uint4 zpark[4][ZW];
+    {
+        const TIn* zin = static_cast<const TIn*>(A.z);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
+#pragma unroll
+            for (int wd = 0; wd < ZW; ++wd)
+                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    constexpr int KT = 3 * D * WM / NT;  // conv taps per thread (bf16 path: [tensor][channel][WM] in shared memory)
+    float tv[KT];
+    if constexpr (sizeof(TIn) == 2) {
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+            const int idx = tid + k * NT;
+            const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
+            const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + chl;
+            tv[k] = j >= WM - A.W ? __ldg(A.conv_w + (size_t)ch * A.W + (j - (WM - A.W))) : 0.f;
+        }
+    }
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(sbar, 1);
@@ -279,62 +311,80 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_after_sync();
     };
 
+    // gates and the decay prefix G_i = g_0 + ... + g_i, by warps 0 and 1 while the rows are in
+    // flight: a shuffle scan per warp, then warp 1 adds warp 0's total
+    if (tid < 64) {
+        const bool in = tid < n;
+        float x = in ? log_decay(A.A_log[h], to_f(ga), A.dt_bias[h]) : 0.f;
+        sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        sG[tid] = x;
+        named_bar_sync(1, 64);
+        if (tid >= 32) sG[tid] += sG[31];
+        named_bar_sync(1, 64);
+        const float gl = sG[n - 1];
+        sEG[tid] = expf(sG[tid]);
+        sBEG[tid] = sB[tid] * sEG[tid];
+        sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
+        if (tid == 0) sMisc[0] = expf(gl);
+    }
+
     // (a) conv1d + SiLU of the chunk's q, k and v rows from the raw inputs (the W-1 rows
     //     before a sequence's first token from its slot's conv buffer), L2 norms of q and k
     //     (q also scaled by dk^-1/2), fp16 rounding; the gates of the chunk's tokens.
     //     Thread (rb, cg) = (tid / 16, tid % 16) owns rows 4 rb .. 4 rb + 3 and channels
     //     8 cg .. 8 cg + 7 of each tensor; a row's 16 threads are one half-warp, which sums
-    //     the row's squares by shuffles.  q, k go to the [K; Q] tile (k also to the K image);
+    //     the squares of two rows at a time by shuffles.  q, k go to the [K; Q] tile (k also to the K image);
     //     v is parked in registers until the inverse has freed its shared-memory space.
     //     bf16 rows are staged in shared memory by asynchronous copies; fp32 rows pass
     //     through registers, one tensor at a time.
-    const int rb = tid >> 4, cg = tid & 15, r0 = 4 * rb, p0 = c * CH;
     const TIn* qin = static_cast<const TIn*>(A.q);
     const TIn* kin = static_cast<const TIn*>(A.k);
     const TIn* vin = static_cast<const TIn*>(A.v);
     const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg, chv = 2 * Dq + h * D + 8 * cg;
-    TIn ga = TIn(0.f), gb = TIn(0.f);  // raw gate inputs a, b of token tid (tid < n), widened when used
-    if (tid < n) {
-        ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
-        gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
-    }
-    // z of the chunk (the output gates are formed while MMA1 runs)
-    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
-    uint4 zpark[4][ZW];
-    {
-        const TIn* zin = static_cast<const TIn*>(A.z);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
-#pragma unroll
-            for (int wd = 0; wd < ZW; ++wd)
-                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
     float w[8][WM];
-    // q or k row r0 + o from its conv output y: normalise, round, store
-    auto qk_row = [&](int o, float (&y)[8], bool is_q) {
-        const int i = r0 + o;
-        float2 s2 = make_float2(0.f, 0.f);
+    // q or k rows r0 + o, r0 + o + 1 from their conv outputs: normalise, round, store.  The two
+    // rows' sums of squares over the row's 16 threads take five shuffles: lanes with bit 3 clear
+    // keep row o's partial and hand row o + 1's to the lane 8 away (which does the opposite),
+    // a butterfly over bits 2..0 completes each sum (bitwise equal in every lane of the group),
+    // and one more exchange brings the other row's scale.
+    auto qk_rows2 = [&](int o, const float (&y0)[8], const float (&y1)[8], bool is_q) {
+        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) s2 = fma2(make_float2(y[e], y[e + 1]), make_float2(y[e], y[e + 1]), s2);
-        float ss = s2.x + s2.y;
+        for (int e = 0; e < 8; e += 2) {
+            a2 = fma2(make_float2(y0[e], y0[e + 1]), make_float2(y0[e], y0[e + 1]), a2);
+            b2 = fma2(make_float2(y1[e], y1[e + 1]), make_float2(y1[e], y1[e + 1]), b2);
+        }
+        const float s0 = a2.x + a2.y, s1 = b2.x + b2.y;
+        const bool hi = (lane & 8) != 0;
+        float t = (hi ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi ? s0 : s1, 8);
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float sc = i < n ? (is_q ? rsqrtf(ss + A.l2_eps) * rsqrtf((float)D) : rsqrtf(ss + A.l2_eps)) : 0.f;
-        const float2 sc2 = make_float2(sc, sc);
-        float2 z2[4];
+        for (int off = 4; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        const float mine = is_q ? rsqrtf(t + A.l2_eps) * rsqrtf((float)D) : rsqrtf(t + A.l2_eps);
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
+        const float sc[2] = {(r0 + o < n) ? (hi ? other : mine) : 0.f, (r0 + o + 1 < n) ? (hi ? mine : other) : 0.f};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) z2[e] = mul2(make_float2(y[2 * e], y[2 * e + 1]), sc2);
-        uint4 pk;
-        pk.x = pack_half2(z2[0].x, z2[0].y);
-        pk.y = pack_half2(z2[1].x, z2[1].y);
-        pk.z = pack_half2(z2[2].x, z2[2].y);
-        pk.w = pack_half2(z2[3].x, z2[3].y);
-        const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
-        *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
-        if (!is_q && write_k) *reinterpret_cast<uint4*>(kimg + (cg >> 3) * 8192 + tc::sw128_chunk(i, cg & 7)) = pk;
+        for (int rr = 0; rr < 2; ++rr) {
+            const float* y = rr == 0 ? y0 : y1;
+            const float2 sc2 = make_float2(sc[rr], sc[rr]);
+            float2 z2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) z2[e] = mul2(make_float2(y[2 * e], y[2 * e + 1]), sc2);
+            uint4 pk;
+            pk.x = pack_half2(z2[0].x, z2[0].y);
+            pk.y = pack_half2(z2[1].x, z2[1].y);
+            pk.z = pack_half2(z2[2].x, z2[2].y);
+            pk.w = pack_half2(z2[3].x, z2[3].y);
+            const int i = r0 + o + rr;
+            const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
+            *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
+            if (!is_q && write_k)
+                *reinterpret_cast<uint4*>(kimg + (cg >> 3) * 8192 + tc::sw128_chunk(i, cg & 7)) = pk;
+        }
     };
     auto v_row = [&](int o, const float (&y)[8]) {
         const bool in = r0 + o < n;
@@ -352,19 +402,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         // shared memory, right-aligned in WM slots ([tensor][channel][WM]).  A sequence's first
         // chunk then replaces its rows r < 0 by the slot's conv buffer (zero before it).
         float* s_taps = reinterpret_cast<float*>(sm + P_RAW + 3 * NRT * 256);
-        {
-            constexpr int KT = 3 * D * WM / NT;  // taps per thread, all loads issued before any store
-            float tv[KT];
 #pragma unroll
-            for (int k = 0; k < KT; ++k) {
-                const int idx = tid + k * NT;
-                const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
-                const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + chl;
-                tv[k] = j >= WM - A.W ? __ldg(A.conv_w + (size_t)ch * A.W + (j - (WM - A.W))) : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < KT; ++k) s_taps[tid + k * NT] = tv[k];
-        }
+        for (int k = 0; k < KT; ++k) s_taps[tid + k * NT] = tv[k];
         const bool staged = mbar_wait_bounded(sbar, 0, nullptr);
         if (!staged && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         for (int idx = tid; p0 == 0 && idx < 3 * (WM - 1) * 16; idx += NT) {
@@ -406,43 +445,50 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 for (int pr = 0; pr < 4; ++pr) x2[j][pr] = __bfloat1622float2(hb[pr]);
             }
 #pragma unroll
-            for (int o = 0; o < 4; ++o) {
-                float y[8];
+            for (int o = 0; o < 4; o += 2) {
+                float y[2][8];
 #pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    float2 acc = make_float2(0.f, 0.f);
+                for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-                    for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + j][pr], acc);
-                    const float2 yy = silu2(acc);
-                    y[2 * pr] = yy.x;
-                    y[2 * pr + 1] = yy.y;
-                }
-                emit(o, y);
+                    for (int pr = 0; pr < 4; ++pr) {
+                        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + rr + j][pr], acc);
+                        const float2 yy = silu2(acc);
+                        y[rr][2 * pr] = yy.x;
+                        y[rr][2 * pr + 1] = yy.y;
+                    }
+                emit(o, y[0], y[1]);
             }
         };
-        conv_rows(0, [&](int o, float (&y)[8]) { qk_row(o, y, false); });
+        conv_rows(0, [&](int o, const float (&y0)[8], const float (&y1)[8]) { qk_rows2(o, y0, y1, false); });
         load_taps(1);
-        conv_rows(1, [&](int o, float (&y)[8]) { qk_row(o, y, true); });
+        conv_rows(1, [&](int o, const float (&y0)[8], const float (&y1)[8]) { qk_rows2(o, y0, y1, true); });
         load_taps(2);
-        conv_rows(2, [&](int o, float (&y)[8]) { vpark[o] = v_row(o, y); });
+        conv_rows(2, [&](int o, const float (&y0)[8], const float (&y1)[8]) {
+            vpark[o] = v_row(o, y0);
+            vpark[o + 1] = v_row(o + 1, y1);
+        });
     } else {
         // fp32: the rows through registers, one tensor at a time
         ConvRows<TIn, WM> x;
         x.load(kin, Dq, hk * D + 8 * cg, cbuf, A.C, chk, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
 #pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            float y[8];
-            x.row(w, o, y);
-            qk_row(o, y, false);
+        for (int o = 0; o < 4; o += 2) {
+            float y0[8], y1[8];
+            x.row(w, o, y0);
+            x.row(w, o + 1, y1);
+            qk_rows2(o, y0, y1, false);
         }
         x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, chq, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
 #pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            float y[8];
-            x.row(w, o, y);
-            qk_row(o, y, true);
+        for (int o = 0; o < 4; o += 2) {
+            float y0[8], y1[8];
+            x.row(w, o, y0);
+            x.row(w, o + 1, y1);
+            qk_rows2(o, y0, y1, true);
         }
         x.load(vin, Dv, h * D + 8 * cg, cbuf, A.C, chv, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chv, A.W);
@@ -453,29 +499,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             vpark[o] = v_row(o, y);
         }
     }
-    // decay prefix G_i = g_0 + ... + g_i: a shuffle scan per warp, then warp 1 adds warp 0's total
-    if (tid < 64) {
-        const bool in = tid < n;
-        float x = in ? log_decay(A.A_log[h], to_f(ga), A.dt_bias[h]) : 0.f;
-        sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        sG[tid] = x;
-    }
     tc::fence_proxy_async();
     sync_all();
-    if (tid >= 32 && tid < 64) sG[tid] += sG[31];
-    __syncthreads();
-    if (tid < 64) {
-        const float gl = sG[n - 1];
-        sEG[tid] = expf(sG[tid]);
-        sBEG[tid] = sB[tid] * sEG[tid];
-        sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
-        if (tid == 0) sMisc[0] = expf(gl);
-    }
 
     // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n go straight to the record
     if (tid == 0)
