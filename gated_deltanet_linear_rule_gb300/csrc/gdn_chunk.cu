@@ -25,8 +25,8 @@
 //     MMA1  [K; Q]  x K^T          -> K K^T (rows 0-63), Q K^T (rows 64-127)     128 x 64  x 128
 //     blocked triangular inverse of I + A on the CUDA cores (16-wide diagonal blocks, then
 //     16 -> 32 -> 64 by  T_21 = -T_22 A_21 T_11)
-//     MMA3  [T2; T1] x K,  [T2; T1] x V  -> W (rows 64-127), U (rows 0-63)       2 x 128 x 128 x 64
-//     MMA5  [P; P] x W,  [P; P] x U      -> P W, P U                             2 x 128 x 128 x 64
+//     MMA3  [T2; 0] x V + [0; T1] x K   -> U (rows 0-63), W (rows 64-127)       128 x 128 x 128
+//     MMA5  [P; 0] x W + [0; P] x U     -> P W (rows 0-63), P U (rows 64-127)   128 x 128 x 128
 //   and writes per (chunk, v-head) a record: the [W; Q'] operand image, U and P U images, the
 //   decay factors and the output gates silu(z) * w_n; per (chunk, q/k head) the K image.
 // State pass (chunk_state_kernel, double-buffered bulk copies of the records):
@@ -65,12 +65,18 @@ constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token
 
 // pre-pass shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1), then [W; Q'] (record)
-constexpr uint32_t P_AP = 32768;      // [P; P]
-constexpr uint32_t P_AT = 49152;      // inverse scratch, then [T2; T1], then the P U image
-constexpr uint32_t P_R4 = 65536;      // A (fp32, stride 68), then the V image, then the U image
-constexpr uint32_t P_R5 = 82944;      // T (fp32, stride 68), then the W image
-constexpr uint32_t P_RAW = P_AP;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
-constexpr uint32_t P_SMALL = 100352;
+// Five 8 KiB blocks T2 | Z | P | Z | T1 (64 rows of 64 fp16, swizzled; Z zero) hold the
+// 128-row left operands of the block-diagonal products: [T2; Z] at P_T2, [Z; P] at P_Z0,
+// [P; Z] at P_P and [Z; T1] at P_Z1.
+constexpr uint32_t P_T2 = 32768;      // T diag(beta)
+constexpr uint32_t P_Z0 = 40960;
+constexpr uint32_t P_P = 49152;       // P
+constexpr uint32_t P_Z1 = 57344;
+constexpr uint32_t P_T1 = 65536;      // inverse scratch, then T diag(beta e^G)
+constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image
+constexpr uint32_t P_R5 = 91136;      // T (fp32, stride 68), then the W image
+constexpr uint32_t P_RAW = P_T2;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
+constexpr uint32_t P_SMALL = 108544;
 constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
 constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
     float* FA = reinterpret_cast<float*>(sm + P_R4);
     float* FT = reinterpret_cast<float*>(sm + P_R5);
-    float* X = reinterpret_cast<float*>(sm + P_AT);
+    float* X = reinterpret_cast<float*>(sm + P_T1);
 
     if (!*A.ws.valid) return;
     const int gc = blockIdx.x / A.hv, h = blockIdx.x % A.hv;
@@ -255,9 +261,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // global loads that nothing waits for yet go out first: the gate inputs a, b of token tid,
     // the chunk's z rows (output gates, formed while MMA1 runs) and the conv taps
     TIn ga = TIn(0.f), gb = TIn(0.f);
-    if (tid < n) {
-        ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
-        gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
+    float a_log = 0.f, dt_b = 0.f;
+    if (tid < 64) {
+        a_log = __ldg(A.A_log + h);
+        dt_b = __ldg(A.dt_bias + h);
+        if (tid < n) {
+            ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
+            gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
+        }
     }
     constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
     uint4 zpark[4][ZW];
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h * D, y0, sbar);
         }
     }
-    if (warp == 0) tc::alloc(tmem_slot, 256);
+    if (warp == 0) tc::alloc(tmem_slot, 128);
     sync_all();
     const uint32_t tm = *tmem_slot;
     uint32_t phase = 0;
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // flight: a shuffle scan per warp, then warp 1 adds warp 0's total
     if (tid < 64) {
         const bool in = tid < n;
-        float x = in ? log_decay(A.A_log[h], to_f(ga), A.dt_bias[h]) : 0.f;
+        float x = in ? log_decay(a_log, to_f(ga), dt_b) : 0.f;
         sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -399,11 +410,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     if constexpr (sizeof(TIn) == 2) {
         // bf16: the raw k, q, v rows r = -(WM-1) .. 63 of the chunk (row slot r + WM - 1) arrive
         // by the tensor copies issued above; meanwhile the conv taps of the three tensors go to
-        // shared memory, right-aligned in WM slots ([tensor][channel][WM]).  A sequence's first
-        // chunk then replaces its rows r < 0 by the slot's conv buffer (zero before it).
+        // shared memory, right-aligned in WM slots ([tensor][tap][channel], so that a thread's 8
+        // channels are two conflict-free 16-B reads).  A sequence's first chunk then replaces
+        // its rows r < 0 by the slot's conv buffer (zero before it).
         float* s_taps = reinterpret_cast<float*>(sm + P_RAW + 3 * NRT * 256);
 #pragma unroll
-        for (int k = 0; k < KT; ++k) s_taps[tid + k * NT] = tv[k];
+        for (int k = 0; k < KT; ++k) {  // [tensor][tap][channel]: a tap's channels are contiguous
+            const int idx = tid + k * NT;
+            const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
+            s_taps[(t * WM + j) * D + chl] = tv[k];
+        }
         const bool staged = mbar_wait_bounded(sbar, 0, nullptr);
         if (!staged && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         for (int idx = tid; p0 == 0 && idx < 3 * (WM - 1) * 16; idx += NT) {
@@ -419,17 +435,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         float2 w2[4][WM];  // taps of channel pairs (8 cg + 2 p, 8 cg + 2 p + 1)
         auto load_taps = [&](int t) {
 #pragma unroll
-            for (int pr = 0; pr < 4; ++pr)
-#pragma unroll
-                for (int j4 = 0; j4 < WM; j4 += 4) {
-                    const float* base = s_taps + (t * D + 8 * cg + 2 * pr) * WM + j4;
-                    const float4 a4 = *reinterpret_cast<const float4*>(base);
-                    const float4 b4 = *reinterpret_cast<const float4*>(base + WM);
-                    w2[pr][j4] = make_float2(a4.x, b4.x);
-                    w2[pr][j4 + 1] = make_float2(a4.y, b4.y);
-                    w2[pr][j4 + 2] = make_float2(a4.z, b4.z);
-                    w2[pr][j4 + 3] = make_float2(a4.w, b4.w);
-                }
+            for (int j = 0; j < WM; ++j) {
+                const float* base = s_taps + (t * WM + j) * D + 8 * cg;
+                const float4 a4 = *reinterpret_cast<const float4*>(base);
+                const float4 b4 = *reinterpret_cast<const float4*>(base + 4);
+                w2[0][j] = make_float2(a4.x, a4.y);
+                w2[1][j] = make_float2(a4.z, a4.w);
+                w2[2][j] = make_float2(b4.x, b4.y);
+                w2[3][j] = make_float2(b4.z, b4.w);
+            }
         };
         load_taps(0);
         // SiLU(conv) of output rows r0 .. r0 + 3 of tensor t from its shared-memory tile; each
@@ -503,8 +517,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     sync_all();
 
     // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n go straight to the record
+    //     and the two zero blocks are cleared (the staging area they lie in is dead)
     if (tid == 0)
         tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<uint4*>(sm + P_Z0 + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + P_Z1 + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
     {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -525,7 +545,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     }
     mma_done();
     if (ok) {
-        // (c) A (fp32) from rows 0-63, P (both halves of [P; P]) from rows 64-127; columns 32*hf ..
+        // (c) A (fp32) from rows 0-63, P from rows 64-127; columns 32*hf ..
         //     The entries of A on and above the diagonal are never read (only strictly lower
         //     blocks enter the inverse), so A is written unmasked; rows past the chunk's end are
         //     zero through beta = 0 (A) and q = 0 (P).
@@ -558,10 +578,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                         p[e4 + e] = (c0 + e4 + e <= i) ? __expf(Gi - gg[e]) * v[e4 + e] : 0.f;
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    tc::st_chunk<Op>(sm + P_AP, i, c0 / 8 + q, p + 8 * q);
-                    tc::st_chunk<Op>(sm + P_AP, 64 + i, c0 / 8 + q, p + 8 * q);
-                }
+                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
             }
         }
         __syncthreads();
@@ -676,16 +693,17 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             for (int q = 0; q < 4; ++q) FT[(32 + i0 + 8 * q) * FS + j] = -a[q];
         }
         __syncthreads();
-        //     [T2; T1] = [T diag(beta); T diag(beta e^G)], one 8-column chunk per item
+        //     T2 = T diag(beta), T1 = T diag(beta e^G), one 8-column chunk per item; a warp
+        //     takes 32 consecutive rows of one chunk column (conflict-free row reads)
         for (int idx = tid; idx < 128 * 8; idx += NT) {
-            const int r = idx >> 3, c8 = idx & 7, i = r & 63;
+            const int r = idx & 127, c8 = idx >> 7, i = r & 63;
             const float* sc = (r < 64 ? sB : sBEG) + c8 * 8;
             const float4 t0 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8);
             const float4 t1 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8 + 4);
             const float4 s0 = *reinterpret_cast<const float4*>(sc), s1 = *reinterpret_cast<const float4*>(sc + 4);
             float v[8] = {t0.x * s0.x, t0.y * s0.y, t0.z * s0.z, t0.w * s0.w,
                           t1.x * s1.x, t1.y * s1.y, t1.z * s1.z, t1.w * s1.w};
-            tc::st_chunk<Op>(sm + P_AT, r, c8, v);
+            tc::st_chunk<Op>(sm + (r < 64 ? P_T2 : P_T1), i, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
         // (d') V image [token][dv] for MMA3's second product, from the rows parked in registers
@@ -695,24 +713,24 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_proxy_async();
         sync_all();
 
-        // (e) MMA3: [T2; T1] x K (K read MN-major from the [K; Q] tile) and [T2; T1] x V
+        // (e) MMA3, block diagonal: [T2; Z] x V + [Z; T1] x K (V and K read MN-major; K from
+        //     the [K; Q] tile) -> U in rows 0-63, W in rows 64-127
         if (tid == 0) {
-            tc::mma_k_mixed(tm, smem_addr(sm + P_AT), 128, 0, 0, smem_addr(sm + P_A1), 0, 1, 16384, CH,
+            tc::mma_k_mixed(tm, smem_addr(sm + P_T2), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 0);
-            tc::mma_k_mixed(tm + 128, smem_addr(sm + P_AT), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 128, 0, 1), 0);
+            tc::mma_k_mixed(tm, smem_addr(sm + P_Z1), 128, 0, 0, smem_addr(sm + P_A1), 0, 1, 16384, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 1);
         }
         mma_done();
     }
     if (ok) {
-        // (f) W (rows 64-127 of the first product) -> the record's [W; Q'] rows 0-63 and the
-        //     MN-major W image; U (rows 0-63 of the second product) -> the U image (over the dead
-        //     V image) and the record's U image
+        // (f) U (rows 0-63) -> the U image (over the dead V image) and the record's U image;
+        //     W (rows 64-127) -> the record's [W; Q'] rows 0-63 and the MN-major W image
         {
             const int row = qd * 32 + lane, i = row & 63;
             for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float v[32];
-                tc::ld32(tc::taddr(tm, warp, (row < 64 ? 128 : 0) + c0), v);
+                tc::ld32(tc::taddr(tm, warp, c0), v);
                 tc::wait_ld();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -730,38 +748,37 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_proxy_async();
         sync_all();
 
-        // (g) MMA5: [P; P] x W and [P; P] x U (both MN-major images)
+        // (g) MMA5, block diagonal: [P; Z] x W + [Z; P] x U (both MN-major images) -> P W in
+        //     rows 0-63, P U in rows 64-127
         if (tid == 0) {
-            tc::mma_k_mixed(tm, smem_addr(sm + P_AP), 128, 0, 0, smem_addr(sm + P_R5), 0, 1, 8192, CH,
+            tc::mma_k_mixed(tm, smem_addr(sm + P_P), 128, 0, 0, smem_addr(sm + P_R5), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 0);
-            tc::mma_k_mixed(tm + 128, smem_addr(sm + P_AP), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 128, 0, 1), 0);
+            tc::mma_k_mixed(tm, smem_addr(sm + P_Z0), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
+                            tc::idesc_f16(128, 128, 0, 1), 1);
         }
         mma_done();
     }
     if (ok) {
-        // (h) rows 64-127: Q' = e^G Q - P W -> the record's [W; Q'] rows 64-127 (Q read from the
-        //     [K; Q] tile);  P U -> the record's P U image.  Every record part is written to global
-        //     memory as it is produced.
-        const int row = qd * 32 + lane;
-        if (row >= 64) {
-            const int i = row - 64;
-            const float eg = sEG[i];
-            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-                float pw[32], pu[32];
-                tc::ld32(tc::taddr(tm, warp, c0), pw);
-                tc::ld32(tc::taddr(tm, warp, 128 + c0), pu);
-                tc::wait_ld();
+        // (h) rows 0-63: Q' = e^G Q - P W -> the record's [W; Q'] rows 64-127 (Q read from the
+        //     [K; Q] tile); rows 64-127: P U -> the record's P U image.  Every record part is
+        //     written to global memory as it is produced.
+        const int row = qd * 32 + lane, i = row & 63;
+        const float eg = sEG[i];
+        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
+            float d[32];
+            tc::ld32(tc::taddr(tm, warp, c0), d);
+            tc::wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int ch = (c0 & 63) / 8 + q;
-                    unsigned char* qa = sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch);
+            for (int q = 0; q < 4; ++q) {
+                const int ch = (c0 & 63) / 8 + q;
+                if (row < 64) {
                     float qv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(qa), qv);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - pw[8 * q + e];
+                    for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
                     tc::st_chunk<Op>(rec + REC_A4 + (c0 >> 6) * 16384, 64 + i, ch, qv);
-                    tc::st_chunk<Op>(rec + REC_O0 + (c0 >> 6) * 8192, i, ch, pu + 8 * q);
+                } else {
+                    tc::st_chunk<Op>(rec + REC_O0 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
                 }
             }
         }
@@ -770,7 +787,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         if (tid == 0) sc[64] = sMisc[0];
     }
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 256);
+    if (warp == 0) tc::dealloc(tm, 128);
 }
 
 // ================================================================== state pass ====
