@@ -516,8 +516,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     tc::fence_proxy_async();
     sync_all();
 
-    // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n go straight to the record
-    //     and the two zero blocks are cleared (the staging area they lie in is dead)
+    // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n are formed (into the T
+    //     area, from where one bulk copy takes them to the record) and the two zero blocks are
+    //     cleared (the staging area they lie in is dead).  Every record part is assembled in
+    //     shared memory and leaves by bulk copies.
     if (tid == 0)
         tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
 #pragma unroll
@@ -540,10 +542,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             w.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
             w.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
             w.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
-            *reinterpret_cast<uint4*>(rec + REC_GZ + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = w;
+            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = w;
         }
     }
+    tc::fence_proxy_async();
     mma_done();
+    if (tid == 0) {
+        bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
+        bulk_commit();
+    }
     if (ok) {
         // (c) A (fp32) from rows 0-63, P from rows 64-127; columns 32*hf ..
         //     The entries of A on and above the diagonal are never read (only strictly lower
@@ -581,6 +588,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
             }
         }
+        if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the T area
         __syncthreads();
 
         // (d) T = (I + A)^-1, blocked.  16-wide diagonal blocks by forward substitution
@@ -724,8 +732,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         mma_done();
     }
     if (ok) {
-        // (f) U (rows 0-63) -> the U image (over the dead V image) and the record's U image;
-        //     W (rows 64-127) -> the record's [W; Q'] rows 0-63 and the MN-major W image
+        // (f) U (rows 0-63) -> the U image (over the dead V image); W (rows 64-127) -> the
+        //     W image; both images are also the record's U part and [W; Q'] rows 0-63
         {
             const int row = qd * 32 + lane, i = row & 63;
             for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
@@ -735,13 +743,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
-                    if (row >= 64) {
-                        tc::st_chunk<Op>(rec + REC_A4 + (c0 >> 6) * 16384, i, ch, v + 8 * q);
-                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
-                    } else {
-                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, v + 8 * q);
-                        tc::st_chunk<Op>(rec + REC_U + (c0 >> 6) * 8192, i, ch, v + 8 * q);
-                    }
+                    tc::st_chunk<Op>(sm + (row >= 64 ? P_R5 : P_R4) + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                 }
             }
         }
@@ -749,19 +751,23 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         sync_all();
 
         // (g) MMA5, block diagonal: [P; Z] x W + [Z; P] x U (both MN-major images) -> P W in
-        //     rows 0-63, P U in rows 64-127
+        //     rows 0-63, P U in rows 64-127; meanwhile the images go to the record
         if (tid == 0) {
             tc::mma_k_mixed(tm, smem_addr(sm + P_P), 128, 0, 0, smem_addr(sm + P_R5), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 0);
             tc::mma_k_mixed(tm, smem_addr(sm + P_Z0), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 1);
+            bulk_s2g(rec + REC_A4, sm + P_R5, 8192);
+            bulk_s2g(rec + REC_A4 + 16384, sm + P_R5 + 8192, 8192);
+            bulk_s2g(rec + REC_U, sm + P_R4, 16384);
+            bulk_commit();
+            bulk_wait_read_all();  // (h) writes the P U rows over the U image
         }
         mma_done();
     }
     if (ok) {
-        // (h) rows 0-63: Q' = e^G Q - P W -> the record's [W; Q'] rows 64-127 (Q read from the
-        //     [K; Q] tile); rows 64-127: P U -> the record's P U image.  Every record part is
-        //     written to global memory as it is produced.
+        // (h) rows 0-63: Q' = e^G Q - P W, written over Q in the [K; Q] tile (the same thread
+        //     reads Q first); rows 64-127: P U over the U image.  Then both go to the record.
         const int row = qd * 32 + lane, i = row & 63;
         const float eg = sEG[i];
         for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
@@ -772,20 +778,30 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             for (int q = 0; q < 4; ++q) {
                 const int ch = (c0 & 63) / 8 + q;
                 if (row < 64) {
+                    unsigned char* qa = sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch);
                     float qv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
+                    unpack8(*reinterpret_cast<const uint4*>(qa), qv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
-                    tc::st_chunk<Op>(rec + REC_A4 + (c0 >> 6) * 16384, 64 + i, ch, qv);
+                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv);
                 } else {
-                    tc::st_chunk<Op>(rec + REC_O0 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
+                    tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
                 }
             }
+        }
+        tc::fence_proxy_async();
+        sync_all();
+        if (tid == 0) {
+            bulk_s2g(rec + REC_A4 + 8192, sm + P_A1 + 8192, 8192);
+            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_A1 + 16384 + 8192, 8192);
+            bulk_s2g(rec + REC_O0, sm + P_R4, 16384);
+            bulk_commit();
         }
         float* sc = reinterpret_cast<float*>(rec + REC_SC);
         if (tid < 64) sc[tid] = sGam[tid];
         if (tid == 0) sc[64] = sMisc[0];
     }
+    if (tid == 0) bulk_wait_read_all();  // shared memory outlives every copy reading it
     sync_all();
     if (warp == 0) tc::dealloc(tm, 128);
 }
