@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     //     (q also scaled by dk^-1/2), fp16 rounding; the gates of the chunk's tokens.
     //     Thread (rb, cg) = (tid / 16, tid % 16) owns rows 4 rb .. 4 rb + 3 and channels
     //     8 cg .. 8 cg + 7 of each tensor; a row's 16 threads are one half-warp, which sums
-    //     the squares of two rows at a time by shuffles.  q, k go to the [K; Q] tile (k also to the K image);
+    //     the squares of two rows at a time by shuffles.  q, k go to the [K; Q] tile;
     //     v is parked in registers until the inverse has freed its shared-memory space.
     //     bf16 rows are staged in shared memory by asynchronous copies; fp32 rows pass
     //     through registers, one tensor at a time.
@@ -393,8 +393,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             const int i = r0 + o + rr;
             const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
             *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
-            if (!is_q && write_k)
-                *reinterpret_cast<uint4*>(kimg + (cg >> 3) * 8192 + tc::sw128_chunk(i, cg & 7)) = pk;
         }
     };
     auto v_row = [&](int o, const float (&y)[8]) {
@@ -515,6 +513,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     }
     tc::fence_proxy_async();
     sync_all();
+    if (tid == 0 && write_k) {  // the K rows of both K-tiles are the (chunk, q/k head) K image
+        bulk_s2g(kimg, sm + P_A1, 8192);
+        bulk_s2g(kimg + 8192, sm + P_A1 + 16384, 8192);
+        bulk_commit();
+    }
 
     // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n are formed (into the T
     //     area, from where one bulk copy takes them to the record) and the two zero blocks are
