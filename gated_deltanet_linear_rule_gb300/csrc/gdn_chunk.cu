@@ -214,7 +214,9 @@ struct ConvRows {
 };
 
 // ===================================================================== pre-pass ====
-// 8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
+// One CTA per (chunk, q/k head): the q / k conv, norms, the K image and [K; Q] x K^T are
+// shared by the r = Hv / Hqk v-heads of the q/k head, which the CTA then takes one after the
+// other.  8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
 template <typename TIn, int WM>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant__ PrefillArgs A,
@@ -229,14 +231,14 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     float* sGam = sEG + 64;
     float* sMisc = sGam + 64;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sMisc + 8);
-    uint64_t* sbar = bar + 1;  // raw rows staged
+    uint64_t* sbar = bar + 1;  // raw rows staged (one phase per batch of tensor copies)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
     float* FA = reinterpret_cast<float*>(sm + P_R4);
     float* FT = reinterpret_cast<float*>(sm + P_R5);
     float* X = reinterpret_cast<float*>(sm + P_T1);
 
     if (!*A.ws.valid) return;
-    const int gc = blockIdx.x / A.hv, h = blockIdx.x % A.hv;
+    const int gc = blockIdx.x / A.hqk, hk = blockIdx.x % A.hqk;
     if (gc >= A.ws.chunk_start[A.n]) return;
     int lo = 0, hi = A.n;  // the sequence of chunk gc: largest s with chunk_start[s] <= gc
     while (hi - lo > 1) {
@@ -249,30 +251,36 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const int n = min(CH, A.cu[s + 1] - tc0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2;
-    const int hk = h / A.r, Dq = A.hqk * D, Dv = A.hv * D;
-    const bool write_k = (h % A.r) == 0;
-    unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
+    const int h0 = hk * A.r, Dq = A.hqk * D, Dv = A.hv * D;
     unsigned char* kimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * KIMG_BYTES;
     const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
                                                                 A.slot_bytes + A.state_bytes);
 
     constexpr int NRT = CH + WM - 1;  // raw rows of a tensor: r = -(WM-1) .. 63 (row slot r + WM - 1)
     const int rb = tid >> 4, cg = tid & 15, r0 = 4 * rb, p0 = c * CH;
-    // global loads that nothing waits for yet go out first: the gate inputs a, b of token tid,
-    // the chunk's z rows (output gates, formed while MMA1 runs) and the conv taps
+    const TIn* qin = static_cast<const TIn*>(A.q);
+    const TIn* kin = static_cast<const TIn*>(A.k);
+    const TIn* vin = static_cast<const TIn*>(A.v);
+    const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg;
+
+    // Per-head inputs nothing waits for yet are loaded one head ahead: the gate inputs a, b of
+    // token tid and the head's A_log, dt_bias (warps 0 and 1), the chunk's z rows, and (bf16)
+    // the head's v conv taps.
     TIn ga = TIn(0.f), gb = TIn(0.f);
     float a_log = 0.f, dt_b = 0.f;
-    if (tid < 64) {
-        a_log = __ldg(A.A_log + h);
-        dt_b = __ldg(A.dt_bias + h);
-        if (tid < n) {
-            ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
-            gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
-        }
-    }
     constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
     uint4 zpark[4][ZW];
-    {
+    constexpr int KV = D * WM / NT;  // v taps per thread
+    float tvv[KV];
+    auto prefetch_head = [&](int h) {
+        if (tid < 64) {
+            a_log = __ldg(A.A_log + h);
+            dt_b = __ldg(A.dt_bias + h);
+            if (tid < n) {
+                ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
+                gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
+            }
+        }
         const TIn* zin = static_cast<const TIn*>(A.z);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -282,35 +290,43 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
                                      : make_uint4(0u, 0u, 0u, 0u);
         }
-    }
-    constexpr int KT = 3 * D * WM / NT;  // conv taps per thread (bf16 path: [tensor][channel][WM] in shared memory)
+        if constexpr (sizeof(TIn) == 2) {
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int idx = tid + k * NT, chl = idx / WM, j = idx - chl * WM;
+                tvv[k] = j >= WM - A.W ? __ldg(A.conv_w + (size_t)(2 * Dq + h * D + chl) * A.W + (j - (WM - A.W))) : 0.f;
+            }
+        }
+    };
+    prefetch_head(h0);
+    constexpr int KT = 2 * D * WM / NT;  // q / k conv taps per thread (bf16)
     float tv[KT];
     if constexpr (sizeof(TIn) == 2) {
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
             const int idx = tid + k * NT;
             const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
-            const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + chl;
+            const int ch = (t == 0 ? Dq + hk * D : hk * D) + chl;
             tv[k] = j >= WM - A.W ? __ldg(A.conv_w + (size_t)ch * A.W + (j - (WM - A.W))) : 0.f;
         }
     }
+    const int y0 = tc0 - (WM - 1);
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(sbar, 1);
         fence_mbar_init();
         if constexpr (sizeof(TIn) == 2) {
-            // raw bf16 k, q, v rows of the chunk by three tensor copies; rows past the tensor are
-            // zero, rows of a neighbouring sequence are replaced or never used (below)
+            // raw bf16 k, q and the first head's v rows of the chunk by three tensor copies; rows
+            // past the tensor are zero, rows of a neighbouring sequence are replaced or never used
             mbar_arrive_expect_tx(sbar, 3 * NRT * 256);
-            const int y0 = tc0 - (WM - 1);
             tma_load_2d(sm + P_RAW, &M.k, hk * D, y0, sbar);
             tma_load_2d(sm + P_RAW + NRT * 256, &M.q, hk * D, y0, sbar);
-            tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h * D, y0, sbar);
+            tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h0 * D, y0, sbar);
         }
     }
-    if (warp == 0) tc::alloc(tmem_slot, 128);
+    if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
-    const uint32_t tm = *tmem_slot;
+    const uint32_t tm = *tmem_slot;  // columns [0, 128): MMA3 / MMA5 of a head; [128, 192): MMA1
     uint32_t phase = 0;
     bool ok = true;
     auto mma_done = [&]() {
@@ -322,65 +338,64 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_after_sync();
     };
 
-    // gates and the decay prefix G_i = g_0 + ... + g_i, by warps 0 and 1 while the rows are in
-    // flight: a shuffle scan per warp, then warp 1 adds warp 0's total
-    if (tid < 64) {
-        const bool in = tid < n;
-        float x = in ? log_decay(a_log, to_f(ga), dt_b) : 0.f;
-        sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
+    // gates of head h and the decay prefix G_i = g_0 + ... + g_i, by warps 0 and 1: a shuffle
+    // scan per warp, then warp 1 adds warp 0's total
+    auto scan = [&]() {
+        if (tid < 64) {
+            const bool in = tid < n;
+            float x = in ? log_decay(a_log, to_f(ga), dt_b) : 0.f;
+            sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            sG[tid] = x;
+            named_bar_sync(1, 64);
+            if (tid >= 32) sG[tid] += sG[31];
+            named_bar_sync(1, 64);
+            const float gl = sG[n - 1];
+            sEG[tid] = expf(sG[tid]);
+            sBEG[tid] = sB[tid] * sEG[tid];
+            sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
+            if (tid == 0) sMisc[0] = expf(gl);
         }
-        sG[tid] = x;
-        named_bar_sync(1, 64);
-        if (tid >= 32) sG[tid] += sG[31];
-        named_bar_sync(1, 64);
-        const float gl = sG[n - 1];
-        sEG[tid] = expf(sG[tid]);
-        sBEG[tid] = sB[tid] * sEG[tid];
-        sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
-        if (tid == 0) sMisc[0] = expf(gl);
-    }
+    };
+    scan();
 
-    // (a) conv1d + SiLU of the chunk's q, k and v rows from the raw inputs (the W-1 rows
-    //     before a sequence's first token from its slot's conv buffer), L2 norms of q and k
-    //     (q also scaled by dk^-1/2), fp16 rounding; the gates of the chunk's tokens.
-    //     Thread (rb, cg) = (tid / 16, tid % 16) owns rows 4 rb .. 4 rb + 3 and channels
-    //     8 cg .. 8 cg + 7 of each tensor; a row's 16 threads are one half-warp, which sums
-    //     the squares of two rows at a time by shuffles.  q, k go to the [K; Q] tile;
-    //     v is parked in registers until the inverse has freed its shared-memory space.
-    //     bf16 rows are staged in shared memory by asynchronous copies; fp32 rows pass
-    //     through registers, one tensor at a time.
-    const TIn* qin = static_cast<const TIn*>(A.q);
-    const TIn* kin = static_cast<const TIn*>(A.k);
-    const TIn* vin = static_cast<const TIn*>(A.v);
-    const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg, chv = 2 * Dq + h * D + 8 * cg;
+    // (a) conv1d + SiLU of the chunk's q, k rows and the first head's v rows from the raw inputs
+    //     (the W-1 rows before a sequence's first token from its slot's conv buffer), L2 norms of
+    //     q and k (q also scaled by dk^-1/2), fp16 rounding.  Thread (rb, cg) = (tid / 16,
+    //     tid % 16) owns rows 4 rb .. 4 rb + 3 and channels 8 cg .. 8 cg + 7 of each tensor; a
+    //     row's 16 threads are one half-warp, which sums the squares of two rows at a time by
+    //     shuffles.  q, k go to the [K; Q] tile; v is parked in registers until the inverse has
+    //     freed its shared-memory space.  bf16 rows are staged in shared memory by tensor
+    //     copies; fp32 rows pass through registers, one tensor at a time.
     float w[8][WM];
     // q or k rows r0 + o, r0 + o + 1 from their conv outputs: normalise, round, store.  The two
     // rows' sums of squares over the row's 16 threads take five shuffles: lanes with bit 3 clear
     // keep row o's partial and hand row o + 1's to the lane 8 away (which does the opposite),
     // a butterfly over bits 2..0 completes each sum (bitwise equal in every lane of the group),
     // and one more exchange brings the other row's scale.
-    auto qk_rows2 = [&](int o, const float (&y0)[8], const float (&y1)[8], bool is_q) {
+    auto qk_rows2 = [&](int o, const float (&y0_)[8], const float (&y1_)[8], bool is_q) {
         float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-            a2 = fma2(make_float2(y0[e], y0[e + 1]), make_float2(y0[e], y0[e + 1]), a2);
-            b2 = fma2(make_float2(y1[e], y1[e + 1]), make_float2(y1[e], y1[e + 1]), b2);
+            a2 = fma2(make_float2(y0_[e], y0_[e + 1]), make_float2(y0_[e], y0_[e + 1]), a2);
+            b2 = fma2(make_float2(y1_[e], y1_[e + 1]), make_float2(y1_[e], y1_[e + 1]), b2);
         }
         const float s0 = a2.x + a2.y, s1 = b2.x + b2.y;
-        const bool hi = (lane & 8) != 0;
-        float t = (hi ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi ? s0 : s1, 8);
+        const bool hi8 = (lane & 8) != 0;
+        float t = (hi8 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi8 ? s0 : s1, 8);
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
         const float mine = is_q ? rsqrtf(t + A.l2_eps) * rsqrtf((float)D) : rsqrtf(t + A.l2_eps);
         const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
-        const float sc[2] = {(r0 + o < n) ? (hi ? other : mine) : 0.f, (r0 + o + 1 < n) ? (hi ? mine : other) : 0.f};
+        const float sc[2] = {(r0 + o < n) ? (hi8 ? other : mine) : 0.f,
+                             (r0 + o + 1 < n) ? (hi8 ? mine : other) : 0.f};
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            const float* y = rr == 0 ? y0 : y1;
+            const float* y = rr == 0 ? y0_ : y1_;
             const float2 sc2 = make_float2(sc[rr], sc[rr]);
             float2 z2[4];
 #pragma unroll
@@ -405,82 +420,95 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         return pk;
     };
     uint4 vpark[4];  // v rows r0 .. r0 + 3, channels 8 cg .. 8 cg + 7, fp16
+    // bf16: taps of channel pairs (8 cg + 2 p, 8 cg + 2 p + 1) from a [tap][channel] table
+    float2 w2[4][WM];
+    auto load_taps = [&](const float* table) {
+#pragma unroll
+        for (int j = 0; j < WM; ++j) {
+            const float* base = table + j * D + 8 * cg;
+            const float4 a4 = *reinterpret_cast<const float4*>(base);
+            const float4 b4 = *reinterpret_cast<const float4*>(base + 4);
+            w2[0][j] = make_float2(a4.x, a4.y);
+            w2[1][j] = make_float2(a4.z, a4.w);
+            w2[2][j] = make_float2(b4.x, b4.y);
+            w2[3][j] = make_float2(b4.z, b4.w);
+        }
+    };
+    // bf16: SiLU(conv) of output rows r0 .. r0 + 3 from a staged tile (row slot r + WM - 1 holds
+    // row r); each input row is read and widened once and slides through the window
+    auto conv_rows = [&](const unsigned char* tile_base, auto&& emit) {
+        const unsigned char* tile = tile_base + (uint32_t)r0 * 256 + cg * 16;
+        float2 x2[WM + 3][4];
+#pragma unroll
+        for (int j = 0; j < WM + 3; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(tile + j * 256);
+            const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int pr = 0; pr < 4; ++pr) x2[j][pr] = __bfloat1622float2(hb[pr]);
+        }
+#pragma unroll
+        for (int o = 0; o < 4; o += 2) {
+            float y[2][8];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + rr + j][pr], acc);
+                    const float2 yy = silu2(acc);
+                    y[rr][2 * pr] = yy.x;
+                    y[rr][2 * pr + 1] = yy.y;
+                }
+            emit(o, y[0], y[1]);
+        }
+    };
+    auto v_emit = [&](int o, const float (&y0_)[8], const float (&y1_)[8]) {
+        vpark[o] = v_row(o, y0_);
+        vpark[o + 1] = v_row(o + 1, y1_);
+    };
+    // a sequence's first chunk: rows r < 0 of a staged tile from the slot's conv buffer (zero
+    // before it); channel base ch0 of the conv's C channels
+    auto halo = [&](unsigned char* tile_base, int ch0, int idx) {
+        const int j = idx >> 4, c16 = idx & 15, p = j - (WM - 1);
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (p >= -(A.W - 1)) x = *reinterpret_cast<const uint4*>(cbuf + (size_t)(A.W - 1 + p) * A.C + ch0 + 8 * c16);
+        *reinterpret_cast<uint4*>(tile_base + (uint32_t)j * 256 + c16 * 16) = x;
+    };
+    // bf16: the v taps of a head (prefetched) into a [tap][channel] table
+    auto store_vtaps = [&](float* table) {
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + k * NT, chl = idx / WM, j = idx - chl * WM;
+            table[j * D + chl] = tvv[k];
+        }
+    };
     if constexpr (sizeof(TIn) == 2) {
-        // bf16: the raw k, q, v rows r = -(WM-1) .. 63 of the chunk (row slot r + WM - 1) arrive
-        // by the tensor copies issued above; meanwhile the conv taps of the three tensors go to
-        // shared memory, right-aligned in WM slots ([tensor][tap][channel], so that a thread's 8
-        // channels are two conflict-free 16-B reads).  A sequence's first chunk then replaces
-        // its rows r < 0 by the slot's conv buffer (zero before it).
+        // q, k and the first head's v rows arrive by the copies issued above; meanwhile the
+        // taps go to shared memory, right-aligned in WM slots ([tensor][tap][channel], so that
+        // a thread's 8 channels of a tap are two conflict-free 16-B reads)
         float* s_taps = reinterpret_cast<float*>(sm + P_RAW + 3 * NRT * 256);
 #pragma unroll
-        for (int k = 0; k < KT; ++k) {  // [tensor][tap][channel]: a tap's channels are contiguous
+        for (int k = 0; k < KT; ++k) {
             const int idx = tid + k * NT;
             const int t = idx / (D * WM), rem = idx - t * (D * WM), chl = rem / WM, j = rem - chl * WM;
             s_taps[(t * WM + j) * D + chl] = tv[k];
         }
+        store_vtaps(s_taps + 2 * WM * D);
         const bool staged = mbar_wait_bounded(sbar, 0, nullptr);
         if (!staged && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         for (int idx = tid; p0 == 0 && idx < 3 * (WM - 1) * 16; idx += NT) {
-            const int t = idx / ((WM - 1) * 16), rem = idx - t * ((WM - 1) * 16), j = rem >> 4, c16 = rem & 15;
-            const int p = j - (WM - 1);  // position before the sequence's first token
-            const int ch = (t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h * D) + 8 * c16;
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (p >= -(A.W - 1))
-                x = *reinterpret_cast<const uint4*>(cbuf + (size_t)(A.W - 1 + p) * A.C + ch);
-            *reinterpret_cast<uint4*>(sm + P_RAW + (uint32_t)(t * NRT + j) * 256 + c16 * 16) = x;
+            const int t = idx / ((WM - 1) * 16);
+            halo(sm + P_RAW + t * NRT * 256, t == 0 ? Dq + hk * D : t == 1 ? hk * D : 2 * Dq + h0 * D,
+                 idx - t * ((WM - 1) * 16));
         }
         ok = __syncthreads_and(staged) != 0;
-        float2 w2[4][WM];  // taps of channel pairs (8 cg + 2 p, 8 cg + 2 p + 1)
-        auto load_taps = [&](int t) {
-#pragma unroll
-            for (int j = 0; j < WM; ++j) {
-                const float* base = s_taps + (t * WM + j) * D + 8 * cg;
-                const float4 a4 = *reinterpret_cast<const float4*>(base);
-                const float4 b4 = *reinterpret_cast<const float4*>(base + 4);
-                w2[0][j] = make_float2(a4.x, a4.y);
-                w2[1][j] = make_float2(a4.z, a4.w);
-                w2[2][j] = make_float2(b4.x, b4.y);
-                w2[3][j] = make_float2(b4.z, b4.w);
-            }
-        };
-        load_taps(0);
-        // SiLU(conv) of output rows r0 .. r0 + 3 of tensor t from its shared-memory tile; each
-        // input row is read and widened once and slides through the window
-        auto conv_rows = [&](int t, auto&& emit) {
-            const unsigned char* tile = sm + P_RAW + (uint32_t)(t * NRT + r0) * 256 + cg * 16;
-            float2 x2[WM + 3][4];
-#pragma unroll
-            for (int j = 0; j < WM + 3; ++j) {
-                const uint4 u = *reinterpret_cast<const uint4*>(tile + j * 256);
-                const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-                for (int pr = 0; pr < 4; ++pr) x2[j][pr] = __bfloat1622float2(hb[pr]);
-            }
-#pragma unroll
-            for (int o = 0; o < 4; o += 2) {
-                float y[2][8];
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                    for (int pr = 0; pr < 4; ++pr) {
-                        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + rr + j][pr], acc);
-                        const float2 yy = silu2(acc);
-                        y[rr][2 * pr] = yy.x;
-                        y[rr][2 * pr + 1] = yy.y;
-                    }
-                emit(o, y[0], y[1]);
-            }
-        };
-        conv_rows(0, [&](int o, const float (&y0)[8], const float (&y1)[8]) { qk_rows2(o, y0, y1, false); });
-        load_taps(1);
-        conv_rows(1, [&](int o, const float (&y0)[8], const float (&y1)[8]) { qk_rows2(o, y0, y1, true); });
-        load_taps(2);
-        conv_rows(2, [&](int o, const float (&y0)[8], const float (&y1)[8]) {
-            vpark[o] = v_row(o, y0);
-            vpark[o + 1] = v_row(o + 1, y1);
-        });
+        load_taps(s_taps);
+        conv_rows(sm + P_RAW, [&](int o, const float (&y0_)[8], const float (&y1_)[8]) { qk_rows2(o, y0_, y1_, false); });
+        load_taps(s_taps + WM * D);
+        conv_rows(sm + P_RAW + NRT * 256, [&](int o, const float (&y0_)[8], const float (&y1_)[8]) { qk_rows2(o, y0_, y1_, true); });
+        load_taps(s_taps + 2 * WM * D);
+        conv_rows(sm + P_RAW + 2 * NRT * 256, v_emit);
     } else {
         // fp32: the rows through registers, one tensor at a time
         ConvRows<TIn, WM> x;
@@ -488,49 +516,48 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
 #pragma unroll
         for (int o = 0; o < 4; o += 2) {
-            float y0[8], y1[8];
-            x.row(w, o, y0);
-            x.row(w, o + 1, y1);
-            qk_rows2(o, y0, y1, false);
+            float y0_[8], y1_[8];
+            x.row(w, o, y0_);
+            x.row(w, o + 1, y1_);
+            qk_rows2(o, y0_, y1_, false);
         }
         x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, chq, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
 #pragma unroll
         for (int o = 0; o < 4; o += 2) {
-            float y0[8], y1[8];
-            x.row(w, o, y0);
-            x.row(w, o + 1, y1);
-            qk_rows2(o, y0, y1, true);
-        }
-        x.load(vin, Dv, h * D + 8 * cg, cbuf, A.C, chv, A.W, tc0, p0, r0, n);
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chv, A.W);
-#pragma unroll
-        for (int o = 0; o < 4; ++o) {
-            float y[8];
-            x.row(w, o, y);
-            vpark[o] = v_row(o, y);
+            float y0_[8], y1_[8];
+            x.row(w, o, y0_);
+            x.row(w, o + 1, y1_);
+            qk_rows2(o, y0_, y1_, true);
         }
     }
+    // fp32: v rows of head h through registers
+    auto conv_v_f32 = [&](int h) {
+        if constexpr (sizeof(TIn) != 2) {
+            ConvRows<TIn, WM> x;
+            x.load(vin, Dv, h * D + 8 * cg, cbuf, A.C, 2 * Dq + h * D + 8 * cg, A.W, tc0, p0, r0, n);
+            ConvRows<TIn, WM>::taps(w, A.conv_w, 2 * Dq + h * D + 8 * cg, A.W);
+#pragma unroll
+            for (int o = 0; o < 4; ++o) {
+                float y[8];
+                x.row(w, o, y);
+                vpark[o] = v_row(o, y);
+            }
+        }
+    };
+    conv_v_f32(h0);
     tc::fence_proxy_async();
     sync_all();
-    if (tid == 0 && write_k) {  // the K rows of both K-tiles are the (chunk, q/k head) K image
+    if (tid == 0) {  // the K rows of both K-tiles are the (chunk, q/k head) K image
         bulk_s2g(kimg, sm + P_A1, 8192);
         bulk_s2g(kimg + 8192, sm + P_A1 + 16384, 8192);
         bulk_commit();
     }
 
-    // (b) MMA1: [K; Q] x K^T; meanwhile the output gates silu(z) * w_n are formed (into the T
-    //     area, from where one bulk copy takes them to the record) and the two zero blocks are
-    //     cleared (the staging area they lie in is dead).  Every record part is assembled in
-    //     shared memory and leaves by bulk copies.
-    if (tid == 0)
-        tc::mma_k(tm, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<uint4*>(sm + P_Z0 + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm + P_Z1 + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    {
+    // the output gates silu(z) * w_n of the head into the W area, from where one bulk copy
+    // takes them to the record.  Every record part is assembled in shared memory and leaves
+    // by bulk copies.
+    auto gates = [&]() {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
@@ -540,22 +567,62 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             for (int e = 0; e < 4; ++e)
                 g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))),
                              make_float2(A.norm_w[c8 + 2 * e], A.norm_w[c8 + 2 * e + 1]));
-            uint4 w;
-            w.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
-            w.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
-            w.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
-            w.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
-            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = w;
+            uint4 wv;
+            wv.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
+            wv.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
+            wv.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
+            wv.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
+            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = wv;
         }
-    }
-    tc::fence_proxy_async();
+        tc::fence_proxy_async();
+    };
+    auto zero_block = [&](uint32_t off) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) *reinterpret_cast<uint4*>(sm + off + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    };
+
+    // (b) MMA1: [K; Q] x K^T into columns [128, 192); meanwhile the first head's gates are formed
+    //     and the two zero blocks are cleared (the staging area they lie in is dead)
+    if (tid == 0)
+        tc::mma_k(tm + 128, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
+    zero_block(P_Z0);
+    zero_block(P_Z1);
+    gates();
     mma_done();
-    if (tid == 0) {
-        bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
-        bulk_commit();
-    }
-    if (ok) {
-        // (c) A (fp32) from rows 0-63, P from rows 64-127; columns 32*hf ..
+
+    for (int jh = 0; jh < A.r && ok; ++jh) {
+        const int h = h0 + jh;
+        unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
+        if (jh > 0) {
+            // the head's v rows were staged at P_T2 by a copy issued after the previous head's
+            // MMA5 (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which is
+            // cleared again once the rows are consumed.
+            scan();
+            if constexpr (sizeof(TIn) == 2) {
+                float* vt = reinterpret_cast<float*>(sm + P_T2 + NRT * 256);
+                store_vtaps(vt);
+                const bool staged = mbar_wait_bounded(sbar, (uint32_t)(jh & 1), nullptr);
+                if (!staged && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+                for (int idx = tid; p0 == 0 && idx < (WM - 1) * 16; idx += NT) halo(sm + P_T2, 2 * Dq + h * D, idx);
+                ok = __syncthreads_and(staged) != 0;
+                if (!ok) break;
+                load_taps(vt);
+                conv_rows(sm + P_T2, v_emit);
+                __syncthreads();
+                zero_block(P_Z0);
+            } else {
+                conv_v_f32(h);
+            }
+            gates();
+            sync_all();
+        }
+        if (tid == 0) {
+            bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
+            bulk_commit();
+        }
+        if (jh + 1 < A.r) prefetch_head(h + 1);
+
+        // (c) A (fp32) from rows 0-63, P from rows 64-127 of [K; Q] x K^T; columns 32*hf ..
         //     The entries of A on and above the diagonal are never read (only strictly lower
         //     blocks enter the inverse), so A is written unmasked; rows past the chunk's end are
         //     zero through beta = 0 (A) and q = 0 (P).
@@ -563,7 +630,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             const int row = qd * 32 + lane, i = row & 63, c0 = 32 * hf;
             const float Gi = sG[i];
             float v[32];
-            tc::ld32(tc::taddr(tm, warp, c0), v);
+            tc::ld32(tc::taddr(tm, warp, 128 + c0), v);
             tc::wait_ld();
             if (row < 64) {
                 const float bi = sB[i];
@@ -591,9 +658,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
             }
         }
-        if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the T area
+        if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the W area
         __syncthreads();
-
         // (d) T = (I + A)^-1, blocked.  16-wide diagonal blocks by forward substitution
         //     (one column per thread; zero above the diagonal and in the upper blocks) ...
         //     Rows of A and T are read 4 entries at a time; T's zeros above the diagonal are
@@ -733,8 +799,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                             tc::idesc_f16(128, 128, 0, 1), 1);
         }
         mma_done();
-    }
-    if (ok) {
+        if (!ok) break;
+
         // (f) U (rows 0-63) -> the U image (over the dead V image); W (rows 64-127) -> the
         //     W image; both images are also the record's U part and [W; Q'] rows 0-63
         {
@@ -764,49 +830,59 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             bulk_s2g(rec + REC_A4 + 16384, sm + P_R5 + 8192, 8192);
             bulk_s2g(rec + REC_U, sm + P_R4, 16384);
             bulk_commit();
-            bulk_wait_read_all();  // (h) writes the P U rows over the U image
+            bulk_wait_read_all();  // (h) writes over both images
         }
         mma_done();
-    }
-    if (ok) {
-        // (h) rows 0-63: Q' = e^G Q - P W, written over Q in the [K; Q] tile (the same thread
-        //     reads Q first); rows 64-127: P U over the U image.  Then both go to the record.
-        const int row = qd * 32 + lane, i = row & 63;
-        const float eg = sEG[i];
-        for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-            float d[32];
-            tc::ld32(tc::taddr(tm, warp, c0), d);
-            tc::wait_ld();
+        if (!ok) break;
+        if constexpr (sizeof(TIn) == 2) {
+            // the next head's v rows go to P_T2 while this one finishes (T2, Z0 and P are dead)
+            if (tid == 0 && jh + 1 < A.r) {
+                mbar_arrive_expect_tx(sbar, NRT * 256);
+                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
+            }
+        }
+
+        // (h) rows 0-63: Q' = e^G Q - P W into the W area; rows 64-127: P U over the U image.
+        //     Then both go to the record.
+        {
+            const int row = qd * 32 + lane, i = row & 63;
+            const float eg = sEG[i];
+            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
+                float d[32];
+                tc::ld32(tc::taddr(tm, warp, c0), d);
+                tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int ch = (c0 & 63) / 8 + q;
-                if (row < 64) {
-                    unsigned char* qa = sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch);
-                    float qv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(qa), qv);
+                for (int q = 0; q < 4; ++q) {
+                    const int ch = (c0 & 63) / 8 + q;
+                    if (row < 64) {
+                        float qv[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
-                    tc::st_chunk<Op>(sm + P_A1 + (c0 >> 6) * 16384, 64 + i, ch, qv);
-                } else {
-                    tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
+                        for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
+                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, qv);
+                    } else {
+                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
+                    }
                 }
             }
         }
         tc::fence_proxy_async();
         sync_all();
         if (tid == 0) {
-            bulk_s2g(rec + REC_A4 + 8192, sm + P_A1 + 8192, 8192);
-            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_A1 + 16384 + 8192, 8192);
+            bulk_s2g(rec + REC_A4 + 8192, sm + P_R5, 8192);
+            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_R5 + 8192, 8192);
             bulk_s2g(rec + REC_O0, sm + P_R4, 16384);
             bulk_commit();
         }
-        float* sc = reinterpret_cast<float*>(rec + REC_SC);
-        if (tid < 64) sc[tid] = sGam[tid];
-        if (tid == 0) sc[64] = sMisc[0];
+        float* scr = reinterpret_cast<float*>(rec + REC_SC);
+        if (tid < 64) scr[tid] = sGam[tid];
+        if (tid == 0) scr[64] = sMisc[0];
+        if (tid == 0) bulk_wait_read_all();  // the next head reuses the W and U areas
+        sync_all();
     }
     if (tid == 0) bulk_wait_read_all();  // shared memory outlives every copy reading it
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 128);
+    if (warp == 0) tc::dealloc(tm, 256);
 }
 
 // ================================================================== state pass ====
@@ -1113,7 +1189,7 @@ cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st)
         if ((e = encode_rows_map(&maps.v, A.v, Dv, A.T, CH + WM - 1)) != cudaSuccess) return e;
     }
     const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
-    prep<<<max_chunks * A.hv, NT, P_SMEM, st>>>(A, maps);
+    prep<<<max_chunks * A.hqk, NT, P_SMEM, st>>>(A, maps);
     return cudaGetLastError();
 }
 

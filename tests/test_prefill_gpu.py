@@ -206,3 +206,28 @@ def test_prefill_chunked_d128_conv_width_and_buffer(W):
         assert np.array_equal(L.get_state(0, s)[1], ref["convbuf"][j])
     assert L.pool.device_status() == 0
     L.close()
+
+
+@pytest.mark.parametrize("hqk,hv", [(2, 2), (1, 4)])
+def test_prefill_chunked_d128_gqa_ratios(hqk, hv):
+    """d = 128 with GQA ratio 1 and 4: the pre-pass shares a q/k head's conv, norms and [K; Q] x K^T between
+    the ratio's v-heads, which it takes one after the other; a random state and conv buffer to start from."""
+    lengths = [70, 3, 129]
+    n = len(lengths)
+    L = Layer(15, hqk, hv, 128, io="bf16", out="f32", num_slots=4, max_prefill_tokens=sum(lengths))
+    slots = [L.pool.alloc() for _ in range(n)]
+    S0 = np.stack([synth.initial_state(15, 0, j, hv, 128, 128) for j in range(n)]).astype(np.float64)
+    conv0 = np.stack([synth.initial_convbuf(15, 0, j, 4, L.C, "bf16") for j in range(n)]).astype(np.float64)
+    for j, s in enumerate(slots):
+        L.set_state(0, s, S0[j], conv0[j])
+    inp, cu = synth.varlen_inputs(15, 0, lengths, hqk, hv, 128, 128, "bf16")
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    ref = L.oracle_run(0, cu, inp, S0, conv0)
+    r_out = relerr(o, ref["out"])
+    r_S = max(relerr(L.get_state(0, s)[0], ref["S"][j]) for j, s in enumerate(slots))
+    print(f"chunked d128 GQA {hv // hqk}: out {r_out:.2e}, S {r_S:.2e}")
+    assert r_out <= PREFILL_TOL and r_S <= PREFILL_TOL
+    for j, s in enumerate(slots):
+        assert np.array_equal(L.get_state(0, s)[1], ref["convbuf"][j])
+    assert L.pool.device_status() == 0
+    L.close()
