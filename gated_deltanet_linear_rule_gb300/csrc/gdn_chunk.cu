@@ -594,8 +594,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         const int h = h0 + jh;
         unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
         if (jh > 0) {
-            // the head's v rows were staged at P_T2 by a copy issued after the previous head's
-            // MMA5 (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which is
+            // the head's v rows were staged at P_T2 by a copy issued at the end of the previous
+            // head (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which is
             // cleared again once the rows are consumed.
             scan();
             if constexpr (sizeof(TIn) == 2) {
@@ -609,10 +609,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 load_taps(vt);
                 conv_rows(sm + P_T2, v_emit);
                 __syncthreads();
-                zero_block(P_Z0);
             } else {
                 conv_v_f32(h);
             }
+            zero_block(P_Z0);  // it held the previous head's Q' half (and, in bf16, these v rows)
             gates();
             sync_all();
         }
@@ -830,20 +830,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             bulk_s2g(rec + REC_A4 + 16384, sm + P_R5 + 8192, 8192);
             bulk_s2g(rec + REC_U, sm + P_R4, 16384);
             bulk_commit();
-            bulk_wait_read_all();  // (h) writes over both images
         }
         mma_done();
         if (!ok) break;
-        if constexpr (sizeof(TIn) == 2) {
-            // the next head's v rows go to P_T2 while this one finishes (T2, Z0 and P are dead)
-            if (tid == 0 && jh + 1 < A.r) {
-                mbar_arrive_expect_tx(sbar, NRT * 256);
-                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
-            }
-        }
 
-        // (h) rows 0-63: Q' = e^G Q - P W into the W area; rows 64-127: P U over the U image.
-        //     Then both go to the record.
+        // (h) rows 0-63: Q' = e^G Q - P W, its two 64-wide halves into the dead T2 and Z0
+        //     blocks; rows 64-127: P U, halves into the dead P and T1 blocks (the W and U images
+        //     are still being copied out).  Then both go to the record.
         {
             const int row = qd * 32 + lane, i = row & 63;
             const float eg = sEG[i];
@@ -859,9 +852,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                         unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
-                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, qv);
+                        tc::st_chunk<Op>(sm + (c0 < 64 ? P_T2 : P_Z0), i, ch, qv);
                     } else {
-                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
+                        tc::st_chunk<Op>(sm + (c0 < 64 ? P_P : P_T1), i, ch, d + 8 * q);
                     }
                 }
             }
@@ -869,15 +862,25 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_proxy_async();
         sync_all();
         if (tid == 0) {
-            bulk_s2g(rec + REC_A4 + 8192, sm + P_R5, 8192);
-            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_R5 + 8192, 8192);
-            bulk_s2g(rec + REC_O0, sm + P_R4, 16384);
+            bulk_s2g(rec + REC_A4 + 8192, sm + P_T2, 8192);
+            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_Z0, 8192);
+            bulk_s2g(rec + REC_O0, sm + P_P, 8192);
+            bulk_s2g(rec + REC_O0 + 8192, sm + P_T1, 8192);
             bulk_commit();
         }
         float* scr = reinterpret_cast<float*>(rec + REC_SC);
         if (tid < 64) scr[tid] = sGam[tid];
         if (tid == 0) scr[64] = sMisc[0];
-        if (tid == 0) bulk_wait_read_all();  // the next head reuses the W and U areas
+        if (tid == 0) {
+            bulk_wait_read_all();  // the next head reuses every area
+            if constexpr (sizeof(TIn) == 2) {
+                // the next head's v rows go to P_T2 (over T2, Z0 and the start of P)
+                if (jh + 1 < A.r) {
+                    mbar_arrive_expect_tx(sbar, NRT * 256);
+                    tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
+                }
+            }
+        }
         sync_all();
     }
     if (tid == 0) bulk_wait_read_all();  // shared memory outlives every copy reading it
