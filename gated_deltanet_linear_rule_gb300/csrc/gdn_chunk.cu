@@ -77,7 +77,7 @@ constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, 
 constexpr uint32_t P_R5 = 91136;      // T (fp32, stride 68), then the W image
 constexpr uint32_t P_RAW = P_T2;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
 constexpr uint32_t P_SMALL = 108544;
-constexpr size_t P_SMEM = P_SMALL + 2048 + 1024;  // small area (1.3 KB) + alignment slack
+constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.7 KB) + alignment slack
 constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
 // state-pass shared memory (one CTA per (sequence, v-head, d_v half))
@@ -224,13 +224,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
-    float* sBEG = reinterpret_cast<float*>(sm + P_SMALL);  // beta_j e^{G_j}
-    float* sG = sBEG + 64;
-    float* sB = sG + 64;
-    float* sEG = sB + 64;
-    float* sGam = sEG + 64;
-    float* sMisc = sGam + 64;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sMisc + 8);
+    // two sets (by head parity) of per-token gate arrays, 5 x 64 floats each: beta e^G, G,
+    // beta, e^G, gamma = e^{G_last - G}; then e^{G_last} per set
+    float* sSet = reinterpret_cast<float*>(sm + P_SMALL);
+    float* sMisc2 = sSet + 640;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sSet + 656);
     uint64_t* sbar = bar + 1;  // raw rows staged (one phase per batch of tensor copies)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
     float* FA = reinterpret_cast<float*>(sm + P_R4);
@@ -272,15 +270,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     uint4 zpark[4][ZW];
     constexpr int KV = D * WM / NT;  // v taps per thread
     float tvv[KV];
-    auto prefetch_head = [&](int h) {
-        if (tid < 64) {
+    // gate inputs of head h for the threads of warp pair `pair` (token tid % 64)
+    auto load_gate_inputs = [&](int h, int pair) {
+        if ((tid >> 6) == pair) {
+            const int t = tid & 63;
             a_log = __ldg(A.A_log + h);
             dt_b = __ldg(A.dt_bias + h);
-            if (tid < n) {
-                ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + tid) * A.hv + h];
-                gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + tid) * A.hv + h];
+            if (t < n) {
+                ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + t) * A.hv + h];
+                gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + t) * A.hv + h];
             }
         }
+    };
+    auto prefetch_head = [&](int h) {
         const TIn* zin = static_cast<const TIn*>(A.z);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -299,6 +301,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
     };
     prefetch_head(h0);
+    load_gate_inputs(h0, 0);
+    if (A.r > 1) load_gate_inputs(h0 + 1, 1);
     constexpr int KT = 2 * D * WM / NT;  // q / k conv taps per thread (bf16)
     float tv[KT];
     if constexpr (sizeof(TIn) == 2) {
@@ -338,30 +342,39 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_after_sync();
     };
 
-    // gates of head h and the decay prefix G_i = g_0 + ... + g_i, by warps 0 and 1: a shuffle
-    // scan per warp, then warp 1 adds warp 0's total
-    auto scan = [&]() {
-        if (tid < 64) {
-            const bool in = tid < n;
+    // gates of a head and the decay prefix G_i = g_0 + ... + g_i into set k, by the 64 threads of
+    // warp pair `pair` (which hold the head's gate inputs): a shuffle scan per warp, then the
+    // second warp adds the first's total.  Heads 0 and 1 are scanned at the start by pairs 0
+    // and 1; a head after that by pair 0 when its turn comes.
+    auto scan_set = [&](int k, int pair) {
+        if ((tid >> 6) == pair) {
+            const int t = tid & 63;
+            float* G = sSet + k * 320 + 64;
+            float* B = G + 64;
+            float* EG = B + 64;
+            float* GAM = EG + 64;
+            float* BEG = G - 64;
+            const bool in = t < n;
             float x = in ? log_decay(a_log, to_f(ga), dt_b) : 0.f;
-            sB[tid] = in ? sigmoid_f(to_f(gb)) : 0.f;
+            B[t] = in ? sigmoid_f(to_f(gb)) : 0.f;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, off);
                 if (lane >= off) x += y;
             }
-            sG[tid] = x;
-            named_bar_sync(1, 64);
-            if (tid >= 32) sG[tid] += sG[31];
-            named_bar_sync(1, 64);
-            const float gl = sG[n - 1];
-            sEG[tid] = expf(sG[tid]);
-            sBEG[tid] = sB[tid] * sEG[tid];
-            sGam[tid] = tid < n ? expf(gl - sG[tid]) : 0.f;
-            if (tid == 0) sMisc[0] = expf(gl);
+            G[t] = x;
+            named_bar_sync(1 + pair, 64);
+            if (t >= 32) G[t] += G[31];
+            named_bar_sync(1 + pair, 64);
+            const float gl = G[n - 1];
+            EG[t] = expf(G[t]);
+            BEG[t] = B[t] * EG[t];
+            GAM[t] = t < n ? expf(gl - G[t]) : 0.f;
+            if (t == 0) sMisc2[k * 8] = expf(gl);
         }
     };
-    scan();
+    scan_set(0, 0);
+    if (A.r > 1) scan_set(1, 1);
 
     // (a) conv1d + SiLU of the chunk's q, k rows and the first head's v rows from the raw inputs
     //     (the W-1 rows before a sequence's first token from its slot's conv buffer), L2 norms of
@@ -593,11 +606,18 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     for (int jh = 0; jh < A.r && ok; ++jh) {
         const int h = h0 + jh;
         unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
+        const int cs = jh & 1;  // this head's gate arrays
+        float* sBEG = sSet + cs * 320;
+        float* sG = sBEG + 64;
+        float* sB = sG + 64;
+        float* sEG = sB + 64;
+        float* sGam = sEG + 64;
+        const float* sMisc = sMisc2 + cs * 8;
         if (jh > 0) {
             // the head's v rows were staged at P_T2 by a copy issued at the end of the previous
             // head (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which is
             // cleared again once the rows are consumed.
-            scan();
+            if (jh > 1) scan_set(cs, 0);
             if constexpr (sizeof(TIn) == 2) {
                 float* vt = reinterpret_cast<float*>(sm + P_T2 + NRT * 256);
                 store_vtaps(vt);
@@ -620,7 +640,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
             bulk_commit();
         }
-        if (jh + 1 < A.r) prefetch_head(h + 1);
+        if (jh + 1 < A.r) {
+            prefetch_head(h + 1);
+            if (jh + 1 > 1) load_gate_inputs(h + 1, 0);
+        }
 
         // (c) A (fp32) from rows 0-63, P from rows 64-127 of [K; Q] x K^T; columns 32*hf ..
         //     The entries of A on and above the diagonal are never read (only strictly lower
