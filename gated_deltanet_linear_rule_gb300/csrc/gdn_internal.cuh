@@ -447,7 +447,8 @@ template <typename TIn>
 cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st);
 template <typename TIn, typename TOut>
 cudaError_t launch_chunk_state(const PrefillArgs& A, cudaStream_t st);
-void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens, int chunk_cap);
+// lays the parts out from ws.base; false if they would not fit in ws.bytes
+bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int max_tokens, int chunk_cap);
 
 inline SlotCheck slot_check(const Pool& P, int layer)
 {

@@ -130,7 +130,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
         const int cap = gdn::prefill_pool_chunk_cap(P->shape, P->shape.max_prefill_tokens);
         P->ws.bytes = gdn::prefill_workspace_bytes(P->shape, P->shape.max_prefill_tokens, cap);
         if (cudaMalloc(&P->ws.base, P->ws.bytes) != cudaSuccess) rc = GDN_ERR_CUDA;
-        else gdn::prefill_workspace_carve(P->ws, P->shape, P->shape.max_prefill_tokens, cap);
+        else if (!gdn::prefill_workspace_carve(P->ws, P->shape, P->shape.max_prefill_tokens, cap)) rc = GDN_ERR_CUDA;
     }
     if (rc == GDN_OK) {
         if (enqueue_zero(P->base, P->total_bytes, 0, P->num_sms) != cudaSuccess) rc = GDN_ERR_CUDA;

@@ -303,7 +303,7 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
     return b;
 }
 
-void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, int chunk_cap)
+bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, int chunk_cap)
 {
     const size_t Dq = (size_t)s.hqk * s.dk, Dv = (size_t)s.hv * s.dv;
     char* p = static_cast<char*>(ws.base);
@@ -323,10 +323,12 @@ void prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
     }
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
     ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
-    ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hv * 82432));
-    ws.kimg = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * s.hqk * 16384));
+    ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * chunk_record_bytes(s.hv, 0)));
+    ws.kimg = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * chunk_record_bytes(0, s.hqk)));
     ws.chunk_cap = chunk_cap;
     ws.valid = reinterpret_cast<int*>(take(256));
+    // the parts must fit the bytes prefill_workspace_bytes sized
+    return (size_t)(p - static_cast<char*>(ws.base)) <= ws.bytes;
 }
 
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
@@ -458,7 +460,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     PrefillWorkspace ws;
     ws.base = scratch;
     ws.bytes = ws_bytes;
-    prefill_workspace_carve(ws, s, total_tokens, chunk_cap);
+    if (!prefill_workspace_carve(ws, s, total_tokens, chunk_cap)) return GDN_ERR_CUDA;
     unsigned char* live = static_cast<unsigned char*>(scratch) + ws_bytes;
     unsigned int* status = status_dev ? status_dev : reinterpret_cast<unsigned int*>(live + live_bytes);
 
