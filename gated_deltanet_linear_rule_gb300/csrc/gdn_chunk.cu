@@ -385,40 +385,48 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     //     freed its shared-memory space.  bf16 rows are staged in shared memory by tensor
     //     copies; fp32 rows pass through registers, one tensor at a time.
     float w[8][WM];
-    // q or k rows r0 + o, r0 + o + 1 from their conv outputs: normalise, round, store.  The two
-    // rows' sums of squares over the row's 16 threads take five shuffles: lanes with bit 3 clear
-    // keep row o's partial and hand row o + 1's to the lane 8 away (which does the opposite),
-    // a butterfly over bits 2..0 completes each sum (bitwise equal in every lane of the group),
-    // and one more exchange brings the other row's scale.
-    auto qk_rows2 = [&](int o, const float (&y0_)[8], const float (&y1_)[8], bool is_q) {
-        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+    // q or k rows r0 .. r0 + 3 from their conv outputs: normalise, round, store.  The four rows'
+    // sums of squares over the row's 16 threads take five dependent shuffles: across lane bit 3
+    // each lane keeps one pair of rows and hands over the other pair, across bit 2 one row of
+    // the pair, and a butterfly over bits 1..0 completes each row's sum (bitwise equal in the
+    // four lanes that hold it); four independent shuffles then bring every row's scale.
+    auto qk_rows4 = [&](const float (&y)[4][8], bool is_q) {
+        float sq[4];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            a2 = fma2(make_float2(y0_[e], y0_[e + 1]), make_float2(y0_[e], y0_[e + 1]), a2);
-            b2 = fma2(make_float2(y1_[e], y1_[e + 1]), make_float2(y1_[e], y1_[e + 1]), b2);
+        for (int r = 0; r < 4; ++r) {
+            float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) a2 = fma2(make_float2(y[r][e], y[r][e + 1]), make_float2(y[r][e], y[r][e + 1]), a2);
+            sq[r] = a2.x + a2.y;
         }
-        const float s0 = a2.x + a2.y, s1 = b2.x + b2.y;
-        const bool hi8 = (lane & 8) != 0;
-        float t = (hi8 ? s1 : s0) + __shfl_xor_sync(0xffffffffu, hi8 ? s0 : s1, 8);
+        const bool b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+        const float k0 = b3 ? sq[2] : sq[0], k1 = b3 ? sq[3] : sq[1];
+        const float t0 = k0 + __shfl_xor_sync(0xffffffffu, b3 ? sq[0] : sq[2], 8);
+        const float t1 = k1 + __shfl_xor_sync(0xffffffffu, b3 ? sq[1] : sq[3], 8);
+        float u = (b2 ? t1 : t0) + __shfl_xor_sync(0xffffffffu, b2 ? t0 : t1, 4);
+        u += __shfl_xor_sync(0xffffffffu, u, 2);
+        u += __shfl_xor_sync(0xffffffffu, u, 1);
+        // this lane now holds row 2 b3 + b2
+        const float mine = is_q ? rsqrtf(u + A.l2_eps) * rsqrtf((float)D) : rsqrtf(u + A.l2_eps);
+        float sc[4];
 #pragma unroll
-        for (int off = 4; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-        const float mine = is_q ? rsqrtf(t + A.l2_eps) * rsqrtf((float)D) : rsqrtf(t + A.l2_eps);
-        const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
-        const float sc[2] = {(r0 + o < n) ? (hi8 ? other : mine) : 0.f,
-                             (r0 + o + 1 < n) ? (hi8 ? mine : other) : 0.f};
+        for (int r = 0; r < 4; ++r) {
+            const int src = (lane & ~12) | ((r >> 1) << 3) | ((r & 1) << 2);
+            const float v = __shfl_sync(0xffffffffu, mine, src);
+            sc[r] = r0 + r < n ? v : 0.f;
+        }
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const float* y = rr == 0 ? y0_ : y1_;
-            const float2 sc2 = make_float2(sc[rr], sc[rr]);
+        for (int r = 0; r < 4; ++r) {
+            const float2 sc2 = make_float2(sc[r], sc[r]);
             float2 z2[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) z2[e] = mul2(make_float2(y[2 * e], y[2 * e + 1]), sc2);
+            for (int e = 0; e < 4; ++e) z2[e] = mul2(make_float2(y[r][2 * e], y[r][2 * e + 1]), sc2);
             uint4 pk;
             pk.x = pack_half2(z2[0].x, z2[0].y);
             pk.y = pack_half2(z2[1].x, z2[1].y);
             pk.z = pack_half2(z2[2].x, z2[2].y);
             pk.w = pack_half2(z2[3].x, z2[3].y);
-            const int i = r0 + o + rr;
+            const int i = r0 + r;
             const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
             *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
         }
@@ -459,26 +467,23 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 #pragma unroll
             for (int pr = 0; pr < 4; ++pr) x2[j][pr] = __bfloat1622float2(hb[pr]);
         }
+        float y[4][8];
 #pragma unroll
-        for (int o = 0; o < 4; o += 2) {
-            float y[2][8];
+        for (int o = 0; o < 4; ++o)
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
+            for (int pr = 0; pr < 4; ++pr) {
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + rr + j][pr], acc);
-                    const float2 yy = silu2(acc);
-                    y[rr][2 * pr] = yy.x;
-                    y[rr][2 * pr + 1] = yy.y;
-                }
-            emit(o, y[0], y[1]);
-        }
+                for (int j = 0; j < WM; ++j) acc = fma2(w2[pr][j], x2[o + j][pr], acc);
+                const float2 yy = silu2(acc);
+                y[o][2 * pr] = yy.x;
+                y[o][2 * pr + 1] = yy.y;
+            }
+        emit(y);
     };
-    auto v_emit = [&](int o, const float (&y0_)[8], const float (&y1_)[8]) {
-        vpark[o] = v_row(o, y0_);
-        vpark[o + 1] = v_row(o + 1, y1_);
+    auto v_emit = [&](const float (&y)[4][8]) {
+#pragma unroll
+        for (int o = 0; o < 4; ++o) vpark[o] = v_row(o, y[o]);
     };
     // a sequence's first chunk: rows r < 0 of a staged tile from the slot's conv buffer (zero
     // before it); channel base ch0 of the conv's C channels
@@ -517,9 +522,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
         ok = __syncthreads_and(staged) != 0;
         load_taps(s_taps);
-        conv_rows(sm + P_RAW, [&](int o, const float (&y0_)[8], const float (&y1_)[8]) { qk_rows2(o, y0_, y1_, false); });
+        conv_rows(sm + P_RAW, [&](const float (&y)[4][8]) { qk_rows4(y, false); });
         load_taps(s_taps + WM * D);
-        conv_rows(sm + P_RAW + NRT * 256, [&](int o, const float (&y0_)[8], const float (&y1_)[8]) { qk_rows2(o, y0_, y1_, true); });
+        conv_rows(sm + P_RAW + NRT * 256, [&](const float (&y)[4][8]) { qk_rows4(y, true); });
         load_taps(s_taps + 2 * WM * D);
         conv_rows(sm + P_RAW + 2 * NRT * 256, v_emit);
     } else {
@@ -527,21 +532,19 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         ConvRows<TIn, WM> x;
         x.load(kin, Dq, hk * D + 8 * cg, cbuf, A.C, chk, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
+        {
+            float y[4][8];
 #pragma unroll
-        for (int o = 0; o < 4; o += 2) {
-            float y0_[8], y1_[8];
-            x.row(w, o, y0_);
-            x.row(w, o + 1, y1_);
-            qk_rows2(o, y0_, y1_, false);
+            for (int o = 0; o < 4; ++o) x.row(w, o, y[o]);
+            qk_rows4(y, false);
         }
         x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, chq, A.W, tc0, p0, r0, n);
         ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
+        {
+            float y[4][8];
 #pragma unroll
-        for (int o = 0; o < 4; o += 2) {
-            float y0_[8], y1_[8];
-            x.row(w, o, y0_);
-            x.row(w, o + 1, y1_);
-            qk_rows2(o, y0_, y1_, true);
+            for (int o = 0; o < 4; ++o) x.row(w, o, y[o]);
+            qk_rows4(y, true);
         }
     }
     // fp32: v rows of head h through registers
