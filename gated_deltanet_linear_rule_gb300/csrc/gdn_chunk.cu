@@ -73,8 +73,8 @@ constexpr uint32_t P_Z0 = 40960;
 constexpr uint32_t P_P = 49152;       // P
 constexpr uint32_t P_Z1 = 57344;
 constexpr uint32_t P_T1 = 65536;      // inverse scratch, then T diag(beta e^G)
-constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image
-constexpr uint32_t P_R5 = 91136;      // T (fp32, stride 68), then the W image
+constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image, then Q'
+constexpr uint32_t P_R5 = 91136;      // gates, then T (fp32, stride 68), then the W image, then P U
 constexpr uint32_t P_RAW = P_T2;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
 constexpr uint32_t P_SMALL = 108544;
 constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.7 KB) + alignment slack
@@ -94,6 +94,12 @@ __device__ __forceinline__ void sync_all()
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+}
+
+// arrive on named barrier `id` (of `threads` threads) without waiting for it
+__device__ __forceinline__ void named_bar_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // 8 fp16 values of a 16-B chunk -> float
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             if (t == 0) sMisc2[k * 8] = expf(gl);
         }
     };
+
     scan_set(0, 0);
     if (A.r > 1) scan_set(1, 1);
 
@@ -574,15 +581,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // takes them to the record.  Every record part is assembled in shared memory and leaves
     // by bulk copies.
     auto gates = [&]() {
+        float2 nw[4];  // the norm weights of this thread's 8 channels (the same for every q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) nw[e] = make_float2(__ldg(A.norm_w + 8 * cg + 2 * e), __ldg(A.norm_w + 8 * cg + 2 * e + 1));
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
             const TIn* zv = reinterpret_cast<const TIn*>(zpark[q]);
             float2 g2[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))),
-                             make_float2(A.norm_w[c8 + 2 * e], A.norm_w[c8 + 2 * e + 1]));
+            for (int e = 0; e < 4; ++e) g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))), nw[e]);
             uint4 wv;
             wv.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
             wv.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
@@ -617,9 +625,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         float* sGam = sEG + 64;
         const float* sMisc = sMisc2 + cs * 8;
         if (jh > 0) {
-            // the head's v rows were staged at P_T2 by a copy issued at the end of the previous
-            // head (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which is
-            // cleared again once the rows are consumed.
+            // the head's v rows were staged at P_T2 by a copy issued once the previous head's MMA5
+            // was done (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which
+            // is cleared again once the rows are consumed.
             if (jh > 1) scan_set(cs, 0);
             if constexpr (sizeof(TIn) == 2) {
                 float* vt = reinterpret_cast<float*>(sm + P_T2 + NRT * 256);
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             } else {
                 conv_v_f32(h);
             }
-            zero_block(P_Z0);  // it held the previous head's Q' half (and, in bf16, these v rows)
+            if constexpr (sizeof(TIn) == 2) zero_block(P_Z0);  // it held these v rows
             gates();
             sync_all();
         }
@@ -852,17 +860,33 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                             tc::idesc_f16(128, 128, 0, 1), 0);
             tc::mma_k_mixed(tm, smem_addr(sm + P_Z0), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 1);
+            tc::commit(bar);
             bulk_s2g(rec + REC_A4, sm + P_R5, 8192);
             bulk_s2g(rec + REC_A4 + 16384, sm + P_R5 + 8192, 8192);
             bulk_s2g(rec + REC_U, sm + P_R4, 16384);
             bulk_commit();
+            bulk_wait_read_all();  // (h) writes over both images
         }
-        mma_done();
+        {
+            const bool got = mbar_wait_bounded(bar, phase, nullptr);
+            phase ^= 1u;
+            if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = __syncthreads_and(got) != 0;
+            tc::fence_after_sync();
+        }
         if (!ok) break;
+        if constexpr (sizeof(TIn) == 2) {
+            // the next head's v rows go to P_T2 (over T2, Z0 and the start of P, all dead once
+            // MMA5 is done), so that they arrive while this head finishes
+            if (tid == 0 && jh + 1 < A.r) {
+                mbar_arrive_expect_tx(sbar, NRT * 256);
+                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
+            }
+        }
 
-        // (h) rows 0-63: Q' = e^G Q - P W, its two 64-wide halves into the dead T2 and Z0
-        //     blocks; rows 64-127: P U, halves into the dead P and T1 blocks (the W and U images
-        //     are still being copied out).  Then both go to the record.
+        // (h) rows 0-63: Q' = e^G Q - P W, its two 64-wide halves into the U image area;
+        //     rows 64-127: P U, halves into the W image area (both images are in the record
+        //     by now).  Then both go to the record.
         {
             const int row = qd * 32 + lane, i = row & 63;
             const float eg = sEG[i];
@@ -878,9 +902,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                         unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
-                        tc::st_chunk<Op>(sm + (c0 < 64 ? P_T2 : P_Z0), i, ch, qv);
+                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, qv);
                     } else {
-                        tc::st_chunk<Op>(sm + (c0 < 64 ? P_P : P_T1), i, ch, d + 8 * q);
+                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
                     }
                 }
             }
@@ -888,25 +912,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::fence_proxy_async();
         sync_all();
         if (tid == 0) {
-            bulk_s2g(rec + REC_A4 + 8192, sm + P_T2, 8192);
-            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_Z0, 8192);
-            bulk_s2g(rec + REC_O0, sm + P_P, 8192);
-            bulk_s2g(rec + REC_O0 + 8192, sm + P_T1, 8192);
+            bulk_s2g(rec + REC_A4 + 8192, sm + P_R4, 8192);
+            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_R4 + 8192, 8192);
+            bulk_s2g(rec + REC_O0, sm + P_R5, 16384);
             bulk_commit();
         }
         float* scr = reinterpret_cast<float*>(rec + REC_SC);
         if (tid < 64) scr[tid] = sGam[tid];
         if (tid == 0) scr[64] = sMisc[0];
-        if (tid == 0) {
-            bulk_wait_read_all();  // the next head reuses every area
-            if constexpr (sizeof(TIn) == 2) {
-                // the next head's v rows go to P_T2 (over T2, Z0 and the start of P)
-                if (jh + 1 < A.r) {
-                    mbar_arrive_expect_tx(sbar, NRT * 256);
-                    tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
-                }
-            }
-        }
+        if (tid == 0) bulk_wait_read_all();  // the next head reuses every area
         sync_all();
     }
     if (tid == 0) bulk_wait_read_all();  // shared memory outlives every copy reading it
@@ -932,9 +946,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_SMALL);  // [2] record buffers
-    uint64_t* bar = full + 2;                                    // MMA completion
+    uint64_t* bar = full + 2;                                    // MMA4 completion (one phase per chunk)
     uint64_t* peer_bar = bar + 1;                                // [2] the other half's sums, by chunk parity
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_bar + 2);
+    uint64_t* bar6 = peer_bar + 3;                               // MMA6 completion (one phase per chunk)
     float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 64);   // [2][2][64] sums of O^2: chunk parity, column half
     float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
 
@@ -957,6 +972,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
         mbar_init(bar, 1);
+        mbar_init(bar6, 1);
         mbar_init(&peer_bar[0], 1);
         mbar_init(&peer_bar[1], 1);
         fence_mbar_init();
@@ -965,17 +981,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     sync_all();
     cluster_sync_all();  // the other CTA's barriers exist before anything arrives on them
     const uint32_t tm = *tmem_slot;
-    uint32_t phase = 0;
     bool ok = true;
-    auto mma_done = [&]() {
-        if (tid == 0) tc::commit(bar);
-        const bool got = mbar_wait_bounded(bar, phase, nullptr);
-        phase ^= 1u;
-        if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-        ok = __syncthreads_and(got) != 0;
-        tc::fence_after_sync();
-    };
-    int issued = 0;  // records prefetched so far (thread 0)
+    constexpr int PF = 64;  // the thread that fetches the records (warp 2 works on output rows)
+    int issued = 0;         // records fetched so far (thread PF)
     auto prefetch = [&](int c) {
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES;
@@ -989,7 +997,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         bulk_g2s(dst + B_SC, rec + REC_SC, 512, &full[c & 1]);
         issued = c + 1;
     };
-    if (tid == 0) {
+    if (tid == PF) {
         prefetch(0);
         if (nch > 1) prefetch(1);
     }
@@ -1032,71 +1040,115 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         return gotp;
     };
 
-    for (int c = 0; c < nch && ok; ++c) {
+    // The barrier for the other CTA's 64 sums of chunk c is armed (for 256 bytes) before the
+    // loop for chunks 0 and 1, and for chunk c + 2 by thread PF once it has seen the sums of
+    // chunk c arrive (never after a failed wait).  The other CTA's stores for chunk c + 2 are issued only after it has
+    // received this CTA's sums for chunk c + 1, which are sent after those of chunk c were
+    // consumed, so a phase is never armed or completed twice.
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&peer_bar[0], 256);
+        if (nch > 1) mbar_arrive_expect_tx(&peer_bar[1], 256);
+    }
+    sync_all();
+    // Per chunk, only W S0^T -> Delta~ lies between the two products.  The decay of S, the
+    // previous chunk's output rows, the output rows of this chunk and the sum exchange all run
+    // while one of the products executes.  Warps 0, 1, 4, 5 hold rows 0-63 of MMA4 (W S0^T) and
+    // build Delta~; warps 2, 3, 6, 7 hold rows 64-127 (Q' S0^T) and produce the output.  MMA4
+    // and MMA6 complete on barriers of their own, one phase per chunk: the output warps may
+    // still be waiting for MMA4 when MMA6 is done, and a shared barrier would by then have
+    // moved two phases past them.  Per-thread verdicts of the bounded waits become uniform at
+    // the barrier opening the next chunk, the only full barrier of the loop (so the loop runs
+    // on c alone).  A barrier phase is armed only once the previous phase was seen complete.
+    for (int c = 0; c < nch; ++c) {
         unsigned char* buf = sm + (c & 1) * S_BUF;
-        // arm this chunk's barrier for the other CTA's 64 sums.  Its stores for chunk c + 2 reuse
-        // the barrier and buffer; they are issued only after it has received this CTA's sums for
-        // chunk c + 1, which are sent after this chunk's sums were consumed.
-        if (tid == 0) mbar_arrive_expect_tx(&peer_bar[c & 1], 256);
-        // every thread waits for the record itself; the verdict becomes uniform at the next barrier
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         const float* sc = reinterpret_cast<const float*>(buf + B_SC);
 
-        // S0^T (fp16, MN-major: row = d_k) for MMA4; S^T <- e^{G_last} S^T for MMA6
+        // S0^T (fp16, MN-major: row = d_k) for MMA4; S^T <- e^{G_last} S^T for MMA6 (columns
+        // [0, 64), which MMA4 does not touch; the store completes before MMA6 is issued)
         {
-            const float egl = sc[64];
             float v[32];
             tc::ld32(tc::taddr(tm, warp, 32 * hf), v);
             tc::wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + S_S0, row, 4 * hf + q, v + 8 * q);
+            const float egl = sc[64];
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] *= egl;
             tc::st32(tc::taddr(tm, warp, 32 * hf), v);
-            tc::wait_st();
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
-        ok = __syncthreads_and(got) != 0;
+        ok = __syncthreads_and(got && ok) != 0;
         tc::fence_after_sync();
         if (!ok) break;
 
-        // MMA4: [W; Q'] x S0^T(:, half) -> columns [64, 128); the previous chunk's output rows
-        // are finished meanwhile
+        // MMA4: [W; Q'] x S0^T(:, half) -> columns [64, 128)
         if (tid == 0) {
             tc::mma_k_mixed(tm + 64, smem_addr(buf + B_A4), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192, D,
                             tc::idesc_f16(128, 64, 0, 1), 0);
             tc::commit(bar);
         }
-        bool gotp = true;
-        if (pend_c >= 0 && row >= 64) gotp = finish_rows(pend_c);
-        {
-            const bool got4 = mbar_wait_bounded(bar, phase, nullptr);
-            phase ^= 1u;
-            if ((!got4 || !gotp) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-            ok = __syncthreads_and(got4 && gotp) != 0;
-            tc::fence_after_sync();
-        }
-        if (!ok) break;
-
         float d[32];
-        tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
-        tc::wait_ld();
         if (row < 64) {
-            // Delta~_i = gamma_i (U_i - (W S0^T)_i) -> row i of the Delta~ image
-            const float gm = sc[row];
+            // Delta~_i = gamma_i U_i - gamma_i (W S0^T)_i -> row i of the Delta~ image, then MMA6;
+            // gamma_i U_i is formed while MMA4 runs
+            float gu[32];
+            {
+                const float gm = sc[row];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), gu + 8 * q);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gu[8 * q + e] *= gm;
+                }
+            }
+            const float ngm = -sc[row];
+            const bool got4 = mbar_wait_bounded(bar, (uint32_t)(c & 1), nullptr);
+            if (!got4 && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = got4;
+            tc::fence_after_sync();
+            tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
+            tc::wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float u[8];
-                unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), u);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) u[e] = gm * (u[e] - d[8 * q + e]);
+                for (int e = 0; e < 8; ++e) u[e] = fmaf(ngm, d[8 * q + e], gu[8 * q + e]);
                 tc::st_chunk<Op>(sm + S_A6, row, 4 * hf + q, u);
             }
+            tc::fence_proxy_async();
+            tc::wait_st();
+            tc::fence_before_sync();
+            named_bar_sync(1, NT);  // the output warps only arrive
+            // MMA6: S^T(:, half) += K^T x Delta~ (both read MN-major from row-wise images).  The
+            // commit is issued even when MMA6 is not, so that every thread's wait has its phase.
+            if (tid == 0) {
+                tc::fence_after_sync();
+                if (ok)
+                    tc::mma_k_mixed(tm, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
+                                    tc::idesc_f16(128, 64, 1, 1), 1);
+                tc::commit(bar6);
+            }
         } else {
+            // the decayed S of rows 64-127 is in TMEM: MMA6 may start as far as these warps go
+            tc::wait_st();
+            tc::fence_before_sync();
+            named_bar_arrive(1, NT);
+            // the previous chunk's output rows, then the next-but-one chunk's sums barrier
+            bool gotp = true;
+            if (pend_c >= 0) gotp = finish_rows(pend_c);
+            if (tid == PF && gotp && pend_c >= 0 && c + 1 < nch) mbar_arrive_expect_tx(&peer_bar[(c + 1) & 1], 256);
+            const bool got4 = mbar_wait_bounded(bar, (uint32_t)(c & 1), nullptr);
+            if ((!got4 || !gotp) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = got4 && gotp;
+            tc::fence_after_sync();
             // O_i = (Q' S0^T)_i + (P U)_i over this thread's 32 columns, its sum of squares, and
-            // the row's gates, all kept for the next iteration
+            // the row's gates, all kept for the next chunk; MMA4's columns stay intact until the
+            // next chunk's MMA4, which is issued after the barrier opening that chunk
+            tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
+            tc::wait_ld();
             float ss = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -1110,38 +1162,29 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 }
             }
             s_ss[(c & 1) * 128 + hf * 64 + orow] = ss;
-        }
-        tc::fence_proxy_async();
-        sync_all();
-
-        // MMA6: S^T(:, half) += K^T x Delta~ (both read MN-major from row-wise images)
-        if (tid == 0) {
-            tc::mma_k_mixed(tm, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 64, 1, 1), 1);
-            tc::commit(bar);
-        }
-        // this half's per-token sums of squares -> the other CTA, by asynchronous stores that
-        // complete on its barrier for this chunk (which it armed for 256 bytes)
-        if (tid >= 32 && tid < 48) {
-            const int j = tid - 32;
-            const float* mine = s_ss + (c & 1) * 128;
-            const float4 a = reinterpret_cast<const float4*>(mine)[j];
-            const float4 b = reinterpret_cast<const float4*>(mine + 64)[j];
-            st_async_cluster_v4(map_to_rank(smem_addr(peer_ss + (c & 1) * 64 + 4 * j), peer),
-                                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w),
-                                map_to_rank(smem_addr(&peer_bar[c & 1]), peer));
+            named_bar_sync(2, NT / 2);  // the four output warps
+            // this half's per-token sums of squares -> the other CTA, by asynchronous stores that
+            // complete on its barrier for this chunk
+            if (tid >= PF && tid < PF + 16) {
+                const int j = tid - PF;
+                const float* mine = s_ss + (c & 1) * 128;
+                const float4 a = reinterpret_cast<const float4*>(mine)[j];
+                const float4 b = reinterpret_cast<const float4*>(mine + 64)[j];
+                st_async_cluster_v4(map_to_rank(smem_addr(peer_ss + (c & 1) * 64 + 4 * j), peer),
+                                    make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w),
+                                    map_to_rank(smem_addr(&peer_bar[c & 1]), peer));
+            }
         }
         pend_c = c;
-        {
-            const bool got6 = mbar_wait_bounded(bar, phase, nullptr);
-            phase ^= 1u;
-            if (!got6 && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-            ok = __syncthreads_and(got6) != 0;
-            tc::fence_after_sync();
-        }
-        // this buffer is free again: fetch the record two chunks ahead into it
-        if (ok && tid == 0 && c + 2 < nch) prefetch(c + 2);
+        const bool got6 = mbar_wait_bounded(bar6, (uint32_t)(c & 1), nullptr);
+        if (!got6 && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        ok = ok && got6;
+        tc::fence_after_sync();
+        // this buffer is free again (its rows were read before barriers 1 and 2, both products
+        // are done): fetch the record two chunks ahead into it
+        if (tid == PF && ok && c + 2 < nch) prefetch(c + 2);
     }
+    ok = __syncthreads_and(ok) != 0;
     if (ok && pend_c >= 0) {
         bool gotp = true;
         if (row >= 64) gotp = finish_rows(pend_c);
@@ -1158,7 +1201,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = v[e];
     }
     // every prefetched copy must land before the CTA's shared memory goes away
-    if (tid == 0) {
+    if (tid == PF) {
         for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
             mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
     }
