@@ -13,26 +13,27 @@
 //     T      = (I + A)^-1                              (unit lower triangular)
 //     W      = T diag(beta e^G) K,     U = T diag(beta) V
 //     P_ij   = e^{G_i - G_j} (q_i . k_j)               (i >= j)
-//     Q'     = diag(e^G) Q - P W,      O0 = P U
-//     Delta  = U - W S0^T,             O  = Q' S0^T + O0
+//     Delta  = U - W S0^T,             O  = diag(e^G) Q S0^T + P Delta
 //     S_end  = e^{G_last} S0 + Delta^T diag(e^{G_last - G_j}) K
-// Everything above the line "Delta = ..." is independent of the incoming state, so it runs
-// in a fully parallel pre-pass, one CTA per (chunk, v-head) over all chunks of all
+// (O is the chunk form of o_t = S_t q_t: S_t = e^{G_t} S0 + sum_{j<=t} e^{G_t - G_j} delta_j
+// k_j^T with delta_j = Delta_j.)  Everything above the line "Delta = ..." is independent of
+// the incoming state, so it runs in a fully parallel pre-pass over all chunks of all
 // sequences at once; only the last two lines form the serial chain, run by one CTA per
-// (sequence, v-head) that keeps S in fp32 tensor memory across its chunks.
+// (sequence, v-head, d_v half) that keeps S in fp32 tensor memory across its chunks.
 //
 // Pre-pass (chunk_prep_kernel, 2 CTAs per SM):
 //     MMA1  [K; Q]  x K^T          -> K K^T (rows 0-63), Q K^T (rows 64-127)     128 x 64  x 128
 //     blocked triangular inverse of I + A on the CUDA cores (16-wide diagonal blocks, then
 //     16 -> 32 -> 64 by  T_21 = -T_22 A_21 T_11)
 //     MMA3  [T2; 0] x V + [0; T1] x K   -> U (rows 0-63), W (rows 64-127)       128 x 128 x 128
-//     MMA5  [P; 0] x W + [0; P] x U     -> P W (rows 0-63), P U (rows 64-127)   128 x 128 x 128
-//   and writes per (chunk, v-head) a record: the [W; Q'] operand image, U and P U images, the
-//   decay factors and the output gates silu(z) * w_n; per (chunk, q/k head) the K image.
+//   and writes per (chunk, v-head) a record: the W, U and P images, the decay factors and the
+//   output gates silu(z) * w_n; per (chunk, q/k head) the K and Q images.
 // State pass (chunk_state_kernel, double-buffered bulk copies of the records):
-//     MMA4  [W; Q'] x S0^T   -> W S0^T (rows 0-63), Q' S0^T (rows 64-127)         128 x 128 x 128
-//     Delta, O = Q' S0^T + P U with the gated RMSNorm fused, output written
+//     MMA4  [W; Q] x S0^T    -> W S0^T (rows 0-63), Q S0^T (rows 64-127)          128 x 128 x 128
+//     Delta
 //     MMA6  S += Delta~^T x K   (S pre-scaled by e^{G_last} in TMEM)              128 x 128 x 64
+//     MMA7  [.; P] x Delta  -> P Delta (rows 64-127), off the chain              128 x 128 x 64
+//     O = diag(e^G) Q S0^T + P Delta with the gated RMSNorm fused, output written
 // Operands are fp16 (11-bit significand; bf16's 8 bits put the chunked result at ~5e-3 of
 // the recurrent definition) with fp32 accumulation.  Transposed operands (K, V, W, U as
 // the N side; Delta~ as the M side) are read MN-major straight from row-wise tiles.
@@ -55,16 +56,17 @@ constexpr int D = 128, CH = 64, NT = 256;
 using Op = __half;
 
 // record of one (chunk, v-head), written by the pre-pass, read by the state pass
-constexpr uint32_t REC_A4 = 0;       // [W; Q'] K-major image: 2 K-tiles x 128 rows
-constexpr uint32_t REC_U = 32768;    // U image [token][dv]: two 64-wide halves 8 KiB apart
-constexpr uint32_t REC_O0 = 49152;   // P U image, same layout
-constexpr uint32_t REC_SC = 65536;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
-constexpr uint32_t REC_GZ = 66048;   // output gates silu(z) * w_n, fp16 [token][dv], two 64-wide halves 8 KiB apart
-constexpr uint32_t REC_BYTES = 82432;
+constexpr uint32_t REC_W = 0;        // W image [token][dk]: two 64-wide halves 8 KiB apart
+constexpr uint32_t REC_U = 16384;    // U image [token][dv], same layout
+constexpr uint32_t REC_GZ = 32768;   // output gates silu(z) * w_n, fp16 [token][dv], same layout
+constexpr uint32_t REC_SC = 49152;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
+constexpr uint32_t REC_P = 49664;    // P image [i][j], 64 x 64
+constexpr uint32_t REC_Q = 57856;    // Q~ = diag(e^G) Q image [token][dk], halves 8 KiB apart
+constexpr uint32_t REC_BYTES = 74240;
 constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token][dk], halves 8 KiB apart
 
 // pre-pass shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1), then [W; Q'] (record)
+constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1 and MMA3; the K and Q images of the record)
 // Five 8 KiB blocks T2 | Z | P | Z | T1 (64 rows of 64 fp16, swizzled; Z zero) hold the
 // 128-row left operands of the block-diagonal products: [T2; Z] at P_T2, [Z; P] at P_Z0,
 // [P; Z] at P_P and [Z; T1] at P_Z1.
@@ -73,20 +75,26 @@ constexpr uint32_t P_Z0 = 40960;
 constexpr uint32_t P_P = 49152;       // P
 constexpr uint32_t P_Z1 = 57344;
 constexpr uint32_t P_T1 = 65536;      // inverse scratch, then T diag(beta e^G)
-constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image, then Q'
-constexpr uint32_t P_R5 = 91136;      // gates, then T (fp32, stride 68), then the W image, then P U
+constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image
+constexpr uint32_t P_R5 = 91136;      // gates, then T (fp32, stride 68), then the W image
 constexpr uint32_t P_RAW = P_T2;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
 constexpr uint32_t P_SMALL = 108544;
 constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.7 KB) + alignment slack
 constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
 // state-pass shared memory (one CTA per (sequence, v-head, d_v half))
-constexpr uint32_t B_A4 = 0, B_K = 32768, B_U = 49152, B_O0 = 57344, B_GZ = 65536, B_SC = 73728;
-constexpr uint32_t S_TX = 32768 + 16384 + 3 * 8192 + 512;  // bytes of one prefetch
-constexpr uint32_t S_BUF = 75776;     // one prefetch buffer: [W; Q'] | K image | U, P U, gates halves | scalars
-constexpr uint32_t S_S0 = 2 * S_BUF;  // S0^T(:, half) in fp16, MN-major: 128 rows (d_k) of 64 d_v
+// One record buffer: the [W; Q] operand (2 K-tiles of 128 rows) | K image | U half | gates
+// half | scalars.  P goes to a slot of its own (two of them, by chunk parity), each after an
+// 8 KiB zero block: MMA7 reads [0; P] as its 128-row operand.
+constexpr uint32_t B_A = 0, B_K = 32768, B_U = 49152, B_GZ = 57344, B_SC = 65536;
+constexpr uint32_t SC_BYTES = 512;   // the scalars fetched: gamma[64], e^{G_last}
+constexpr uint32_t S_TX = 32768 + 16384 + 8192 + 8192 + SC_BYTES;  // bytes fetched into one record buffer
+constexpr uint32_t S_BUF = 66560;
+constexpr uint32_t S_S0 = 2 * S_BUF;     // S0^T(:, half) in fp16, MN-major: 128 rows (d_k) of 64 d_v
 constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) [token][64 d_v]
-constexpr uint32_t S_SMALL = S_A6 + 8192;
+constexpr uint32_t S_DL = S_A6 + 8192;   // [2] Delta(:, half) [token][64 d_v], by chunk parity
+constexpr uint32_t S_PZ = S_DL + 16384;  // [2] zero block | P [i][j], by chunk parity
+constexpr uint32_t S_SMALL = S_PZ + 32768;
 constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, sums) + slack
 
 __device__ __forceinline__ void sync_all()
@@ -692,8 +700,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
             }
         }
+        tc::fence_proxy_async();  // P leaves for the record by a bulk copy
         if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the W area
         __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(rec + REC_P, sm + P_P, 8192);
+            bulk_commit();
+        }
         // (d) T = (I + A)^-1, blocked.  16-wide diagonal blocks by forward substitution
         //     (one column per thread; zero above the diagonal and in the upper blocks) ...
         //     Rows of A and T are read 4 entries at a time; T's zeros above the diagonal are
@@ -825,18 +838,41 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         sync_all();
 
         // (e) MMA3, block diagonal: [T2; Z] x V + [Z; T1] x K (V and K read MN-major; K from
-        //     the [K; Q] tile) -> U in rows 0-63, W in rows 64-127
+        //     the [K; Q] tile) -> U in rows 0-63, W in rows 64-127.  Meanwhile Q~ = diag(e^G) Q
+        //     goes to the record, 16 B per store.
         if (tid == 0) {
             tc::mma_k_mixed(tm, smem_addr(sm + P_T2), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 0);
             tc::mma_k_mixed(tm, smem_addr(sm + P_Z1), 128, 0, 0, smem_addr(sm + P_A1), 0, 1, 16384, CH,
                             tc::idesc_f16(128, 128, 0, 1), 1);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = tid + NT * k, kt = idx >> 9, i = (idx >> 3) & 63, j = idx & 7;
+            float qv[8];
+            unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + kt * 16384 + tc::sw128_chunk(64 + i, j)), qv);
+            const float eg = sEG[i];
+            uint4 w;
+            w.x = pack_half2(eg * qv[0], eg * qv[1]);
+            w.y = pack_half2(eg * qv[2], eg * qv[3]);
+            w.z = pack_half2(eg * qv[4], eg * qv[5]);
+            w.w = pack_half2(eg * qv[6], eg * qv[7]);
+            *reinterpret_cast<uint4*>(rec + REC_Q + kt * 8192 + tc::sw128_chunk(i, j)) = w;
+        }
         mma_done();
         if (!ok) break;
+        if constexpr (sizeof(TIn) == 2) {
+            // the next head's v rows go to P_T2 (over T2, Z0 and the start of P: MMA3 is done
+            // and P has been copied out), so that they arrive while this head finishes
+            if (tid == 0 && jh + 1 < A.r) {
+                bulk_wait_read_all();
+                mbar_arrive_expect_tx(sbar, NRT * 256);
+                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
+            }
+        }
 
         // (f) U (rows 0-63) -> the U image (over the dead V image); W (rows 64-127) -> the
-        //     W image; both images are also the record's U part and [W; Q'] rows 0-63
+        //     W image; both go to the record with the decay factors
         {
             const int row = qd * 32 + lane, i = row & 63;
             for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
@@ -852,69 +888,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
         tc::fence_proxy_async();
         sync_all();
-
-        // (g) MMA5, block diagonal: [P; Z] x W + [Z; P] x U (both MN-major images) -> P W in
-        //     rows 0-63, P U in rows 64-127; meanwhile the images go to the record
         if (tid == 0) {
-            tc::mma_k_mixed(tm, smem_addr(sm + P_P), 128, 0, 0, smem_addr(sm + P_R5), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 128, 0, 1), 0);
-            tc::mma_k_mixed(tm, smem_addr(sm + P_Z0), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
-                            tc::idesc_f16(128, 128, 0, 1), 1);
-            tc::commit(bar);
-            bulk_s2g(rec + REC_A4, sm + P_R5, 8192);
-            bulk_s2g(rec + REC_A4 + 16384, sm + P_R5 + 8192, 8192);
+            bulk_s2g(rec + REC_W, sm + P_R5, 16384);
             bulk_s2g(rec + REC_U, sm + P_R4, 16384);
-            bulk_commit();
-            bulk_wait_read_all();  // (h) writes over both images
-        }
-        {
-            const bool got = mbar_wait_bounded(bar, phase, nullptr);
-            phase ^= 1u;
-            if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-            ok = __syncthreads_and(got) != 0;
-            tc::fence_after_sync();
-        }
-        if (!ok) break;
-        if constexpr (sizeof(TIn) == 2) {
-            // the next head's v rows go to P_T2 (over T2, Z0 and the start of P, all dead once
-            // MMA5 is done), so that they arrive while this head finishes
-            if (tid == 0 && jh + 1 < A.r) {
-                mbar_arrive_expect_tx(sbar, NRT * 256);
-                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
-            }
-        }
-
-        // (h) rows 0-63: Q' = e^G Q - P W, its two 64-wide halves into the U image area;
-        //     rows 64-127: P U, halves into the W image area (both images are in the record
-        //     by now).  Then both go to the record.
-        {
-            const int row = qd * 32 + lane, i = row & 63;
-            const float eg = sEG[i];
-            for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
-                float d[32];
-                tc::ld32(tc::taddr(tm, warp, c0), d);
-                tc::wait_ld();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int ch = (c0 & 63) / 8 + q;
-                    if (row < 64) {
-                        float qv[8];
-                        unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + (c0 >> 6) * 16384 + tc::sw128_chunk(64 + i, ch)), qv);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) qv[e] = eg * qv[e] - d[8 * q + e];
-                        tc::st_chunk<Op>(sm + P_R4 + (c0 >> 6) * 8192, i, ch, qv);
-                    } else {
-                        tc::st_chunk<Op>(sm + P_R5 + (c0 >> 6) * 8192, i, ch, d + 8 * q);
-                    }
-                }
-            }
-        }
-        tc::fence_proxy_async();
-        sync_all();
-        if (tid == 0) {
-            bulk_s2g(rec + REC_A4 + 8192, sm + P_R4, 8192);
-            bulk_s2g(rec + REC_A4 + 16384 + 8192, sm + P_R4 + 8192, 8192);
-            bulk_s2g(rec + REC_O0, sm + P_R5, 16384);
             bulk_commit();
         }
         float* scr = reinterpret_cast<float*>(rec + REC_SC);
@@ -931,13 +907,18 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // ================================================================== state pass ====
 // One CTA per (sequence, v-head, d_v half); the two halves of a (sequence, v-head) form a
 // cluster of two.  A CTA keeps S^T restricted to its half, [d_k][64 d_v], in TMEM columns
-// [0, 64) (lane = d_k), so both products of the chain have M = 128 and N = 64:
-//     MMA4  [W; Q'] x S0^T(:, half)   -> columns [64, 128): W S0^T rows 0-63, Q' S0^T rows 64-127
-//     MMA6  S^T(:, half) += K^T x Delta~(:, half)   (K^T and Delta~ read MN-major)
-// The gated RMSNorm of an output row needs its sum of squares over all of d_v: each CTA sends
-// its half's 64 per-token sums into the other CTA's shared memory and arrives on that CTA's
-// mbarrier (distributed shared memory); the output rows are finished one chunk later, while
-// the next MMA4 runs.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
+// [0, 64) (lane = d_k), so the products have M = 128 and N = 64:
+//     MMA4  [W; Q~] x S0^T(:, half)   -> W S0^T rows 0-63, diag(e^G) Q S0^T rows 64-127
+//     MMA6  S^T(:, half) += K^T x Delta~(:, half)   (Delta~ = diag(gamma) Delta; both MN-major)
+//     MMA7  [0; P] x Delta(:, half)   -> accumulated onto MMA4's rows 64-127: the output O
+// MMA4 of chunk c writes TMEM columns [64, 128) + 64 (c % 2), so that MMA7 of chunk c, issued
+// after MMA4 of chunk c + 1, runs while Delta of chunk c + 1 is formed.  Only MMA4 -> Delta ->
+// MMA6 is serial from chunk to chunk.  The gated RMSNorm of an output row needs its sum of
+// squares over all of d_v, so each CTA sends its half's 64 per-token sums into the other
+// CTA's shared memory and arrives on that CTA's mbarrier (distributed shared memory).  Warps
+// w with w % 4 < 2 hold rows 0-63 (Delta); the others hold rows 64-127 and read the output
+// one chunk behind the chain, finishing its rows one more behind (once the other CTA's sums
+// are in); thread PF of warp 2 fetches the records.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
 // 32 (w / 4) .. + 31.
 
 template <typename TIn, typename TOut>
@@ -946,11 +927,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_SMALL);  // [2] record buffers
-    uint64_t* bar = full + 2;                                    // MMA4 completion (one phase per chunk)
-    uint64_t* peer_bar = bar + 1;                                // [2] the other half's sums, by chunk parity
+    uint64_t* bar4 = full + 2;                                   // MMA4 completion (one phase per chunk)
+    uint64_t* peer_bar = bar4 + 1;                               // [2] the other half's sums, by chunk parity
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_bar + 2);
     uint64_t* bar6 = peer_bar + 3;                               // MMA6 completion (one phase per chunk)
-    float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 64);   // [2][2][64] sums of O^2: chunk parity, column half
+    uint64_t* bar7 = peer_bar + 4;                               // MMA7 completion (one phase per chunk)
+    uint64_t* full_p = peer_bar + 5;                             // [2] P slots
+    float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 128);  // [2][2][64] sums of O^2: chunk parity, column half
     float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
 
     // both CTAs of a cluster take these exits together (they depend on the sequence only)
@@ -971,36 +954,70 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(bar, 1);
+        mbar_init(&full_p[0], 1);
+        mbar_init(&full_p[1], 1);
+        mbar_init(bar4, 1);
         mbar_init(bar6, 1);
+        mbar_init(bar7, 1);
         mbar_init(&peer_bar[0], 1);
         mbar_init(&peer_bar[1], 1);
         fence_mbar_init();
     }
-    if (warp == 0) tc::alloc(tmem_slot, 128);
+    if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
     cluster_sync_all();  // the other CTA's barriers exist before anything arrives on them
     const uint32_t tm = *tmem_slot;
     bool ok = true;
     constexpr int PF = 64;  // the thread that fetches the records (warp 2 works on output rows)
-    int issued = 0;         // records fetched so far (thread PF)
-    auto prefetch = [&](int c) {
+    int main_issued = 0, p_issued = 0;  // fetches so far (thread PF)
+    int mma7_issued = 0;                // MMA7s so far (thread 0)
+    auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
+    auto fetch_main = [&](int c) {  // the record's [W; Q] operand, K image, U, gates and scalars
         unsigned char* dst = sm + (c & 1) * S_BUF;
-        const unsigned char* rec = A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES;
+        const unsigned char* rec = record(c);
         const unsigned char* kimg = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * KIMG_BYTES;
         mbar_arrive_expect_tx(&full[c & 1], S_TX);
-        bulk_g2s(dst + B_A4, rec + REC_A4, 32768, &full[c & 1]);
+        bulk_g2s(dst + B_A, rec + REC_W, 8192, &full[c & 1]);
+        bulk_g2s(dst + B_A + 16384, rec + REC_W + 8192, 8192, &full[c & 1]);
+        bulk_g2s(dst + B_A + 8192, rec + REC_Q, 8192, &full[c & 1]);
+        bulk_g2s(dst + B_A + 16384 + 8192, rec + REC_Q + 8192, 8192, &full[c & 1]);
         bulk_g2s(dst + B_K, kimg, 16384, &full[c & 1]);
         bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_O0, rec + REC_O0 + half * 8192, 8192, &full[c & 1]);
         bulk_g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_SC, rec + REC_SC, 512, &full[c & 1]);
-        issued = c + 1;
+        bulk_g2s(dst + B_SC, rec + REC_SC, SC_BYTES, &full[c & 1]);
+        main_issued = c + 1;
+    };
+    auto fetch_p = [&](int c) {
+        mbar_arrive_expect_tx(&full_p[c & 1], 8192);
+        bulk_g2s(sm + S_PZ + (c & 1) * 16384 + 8192, record(c) + REC_P, 8192, &full_p[c & 1]);
+        p_issued = c + 1;
     };
     if (tid == PF) {
-        prefetch(0);
-        if (nch > 1) prefetch(1);
+        fetch_main(0);
+        fetch_p(0);
+        if (nch > 1) {
+            fetch_main(1);
+            fetch_p(1);
+        }
     }
+    // MMA7 of chunk pc (thread 0): [0; P] x Delta accumulated onto chunk pc's MMA4 columns;
+    // the commit is issued even when the product is not, so that every wait has its phase
+    auto issue_mma7 = [&](int pc, bool go) {
+        const bool gotp = mbar_wait_bounded(&full_p[pc & 1], (uint32_t)((pc >> 1) & 1), nullptr);
+        if (!gotp) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        if (go && gotp)
+            tc::mma_k_mixed(tm + 64 + 64 * (pc & 1), smem_addr(sm + S_PZ + (pc & 1) * 16384), 128, 0, 0,
+                            smem_addr(sm + S_DL + (pc & 1) * 8192), 0, 1, 8192, CH, tc::idesc_f16(128, 64, 0, 1), 1);
+        tc::commit(bar7);
+        mma7_issued = pc + 1;
+    };
+    // the zero halves of MMA7's operands
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int idx = tid + NT * k;  // 16-B chunk of the two 8 KiB zero blocks
+        *reinterpret_cast<uint4*>(sm + S_PZ + (idx >> 9) * 16384 + (idx & 511) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async();
 
     // incoming state: S^T(:, half) into TMEM columns [0, 64); lane = d_k, column j = d_v 64 half + j
     {
@@ -1011,16 +1028,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::st32(tc::taddr(tm, warp, 32 * hf), v);
         tc::wait_st();
     }
-    sync_all();
 
-    // The output rows of chunk c wait in registers (O and the gates, this thread's 32 columns)
-    // and are finished while MMA4 of chunk c + 1 runs, when the other CTA's sums for chunk c
-    // have long arrived: the exchange stays off the serial chain.
+    // output rows (rows >= 64 only, this thread's 32 columns): gzn holds the gates of the chunk
+    // just computed; o / gzr the O_i and gates of the chunk before, waiting for the other CTA's
+    // sums
     float o[32];
-    uint4 gzr[4];
-    int pend_c = -1;  // chunk whose output rows are pending
+    uint4 gzn[4], gzr[4];
     const int orow = row - 64;
-    auto finish_rows = [&](int pc) -> bool {  // rows >= 64 only; false when the sums never came
+    auto finish_rows = [&](int pc) -> bool {  // false when the sums never came
         const bool gotp = mbar_wait_cluster_bounded(&peer_bar[pc & 1], (uint32_t)((pc >> 1) & 1));
         const int pn = min(CH, L - pc * CH);
         if (gotp && orow < pn) {
@@ -1039,26 +1054,49 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         }
         return gotp;
     };
+    // O of chunk pc (MMA4's rows 64-127 plus MMA7), its sums of squares
+    auto complete_rows = [&](int pc) -> bool {
+        const bool got7 = mbar_wait_bounded(bar7, (uint32_t)(pc & 1), nullptr);
+        tc::fence_after_sync();
+        tc::ld32(tc::taddr(tm, warp, 64 + 64 * (pc & 1) + 32 * hf), o);
+        tc::wait_ld();
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) gzr[q] = gzn[q];
+        s_ss[(pc & 1) * 128 + hf * 64 + orow] = ss;
+        return got7;
+    };
+    // this half's per-token sums of squares of chunk pc -> the other CTA, by asynchronous
+    // stores that complete on its barrier for that chunk (16 threads of warp 2)
+    auto send_sums = [&](int pc) {
+        if (tid >= PF && tid < PF + 16) {
+            const int j = tid - PF;
+            const float* mine = s_ss + (pc & 1) * 128;
+            const float4 a = reinterpret_cast<const float4*>(mine)[j];
+            const float4 b = reinterpret_cast<const float4*>(mine + 64)[j];
+            st_async_cluster_v4(map_to_rank(smem_addr(peer_ss + (pc & 1) * 64 + 4 * j), peer),
+                                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w),
+                                map_to_rank(smem_addr(&peer_bar[pc & 1]), peer));
+        }
+    };
 
     // The barrier for the other CTA's 64 sums of chunk c is armed (for 256 bytes) before the
-    // loop for chunks 0 and 1, and for chunk c + 2 by thread PF once it has seen the sums of
-    // chunk c arrive (never after a failed wait).  The other CTA's stores for chunk c + 2 are issued only after it has
-    // received this CTA's sums for chunk c + 1, which are sent after those of chunk c were
-    // consumed, so a phase is never armed or completed twice.
+    // loop for chunks 0 and 1, and for chunk c >= 2 by thread PF in chunk c once it has seen
+    // the sums of chunk c - 2 arrive (never after a failed wait).  The other CTA sends its
+    // sums of chunk c only after it has received this CTA's sums of chunk c - 1, which are
+    // sent after that point, so a phase is never armed or completed twice and a sums slot is
+    // never overwritten before it is read.
     if (tid == 0) {
         mbar_arrive_expect_tx(&peer_bar[0], 256);
         if (nch > 1) mbar_arrive_expect_tx(&peer_bar[1], 256);
     }
     sync_all();
-    // Per chunk, only W S0^T -> Delta~ lies between the two products.  The decay of S, the
-    // previous chunk's output rows, the output rows of this chunk and the sum exchange all run
-    // while one of the products executes.  Warps 0, 1, 4, 5 hold rows 0-63 of MMA4 (W S0^T) and
-    // build Delta~; warps 2, 3, 6, 7 hold rows 64-127 (Q' S0^T) and produce the output.  MMA4
-    // and MMA6 complete on barriers of their own, one phase per chunk: the output warps may
-    // still be waiting for MMA4 when MMA6 is done, and a shared barrier would by then have
-    // moved two phases past them.  Per-thread verdicts of the bounded waits become uniform at
-    // the barrier opening the next chunk, the only full barrier of the loop (so the loop runs
-    // on c alone).  A barrier phase is armed only once the previous phase was seen complete.
+    // MMA4, MMA6 and MMA7 complete on barriers of their own, one phase per chunk, and no
+    // waiter can fall two phases behind one of them.  Per-thread verdicts of the bounded
+    // waits become uniform at the barrier opening the next chunk, the only full barrier of
+    // the loop (so the loop runs on c alone).
     for (int c = 0; c < nch; ++c) {
         unsigned char* buf = sm + (c & 1) * S_BUF;
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
@@ -1084,46 +1122,46 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::fence_after_sync();
         if (!ok) break;
 
-        // MMA4: [W; Q'] x S0^T(:, half) -> columns [64, 128)
+        // MMA4: [W; Q~] x S0^T(:, half) -> columns [64, 128) + 64 (c % 2); then MMA7 of the
+        // chunk before
         if (tid == 0) {
-            tc::mma_k_mixed(tm + 64, smem_addr(buf + B_A4), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192, D,
-                            tc::idesc_f16(128, 64, 0, 1), 0);
-            tc::commit(bar);
+            tc::mma_k_mixed(tm + 64 + 64 * (c & 1), smem_addr(buf + B_A), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192,
+                            D, tc::idesc_f16(128, 64, 0, 1), 0);
+            tc::commit(bar4);
+            if (c >= 1) issue_mma7(c - 1, true);
         }
-        float d[32];
         if (row < 64) {
-            // Delta~_i = gamma_i U_i - gamma_i (W S0^T)_i -> row i of the Delta~ image, then MMA6;
-            // gamma_i U_i is formed while MMA4 runs
-            float gu[32];
-            {
-                const float gm = sc[row];
+            // Delta_i = U_i - (W S0^T)_i and Delta~_i = gamma_i Delta_i -> row i of this chunk's
+            // Delta image and of the Delta~ image, then MMA6
+            float u[32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), gu + 8 * q);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gu[8 * q + e] *= gm;
-                }
-            }
-            const float ngm = -sc[row];
-            const bool got4 = mbar_wait_bounded(bar, (uint32_t)(c & 1), nullptr);
+            for (int q = 0; q < 4; ++q)
+                unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), u + 8 * q);
+            const float gm = sc[row];
+            const bool got4 = mbar_wait_bounded(bar4, (uint32_t)(c & 1), nullptr);
             if (!got4 && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
             ok = got4;
             tc::fence_after_sync();
-            tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
+            float d[32];
+            tc::ld32(tc::taddr(tm, warp, 64 + 64 * (c & 1) + 32 * hf), d);
             tc::wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float u[8];
+                float dl[8], dg[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) u[e] = fmaf(ngm, d[8 * q + e], gu[8 * q + e]);
-                tc::st_chunk<Op>(sm + S_A6, row, 4 * hf + q, u);
+                for (int e = 0; e < 8; ++e) {
+                    dl[e] = u[8 * q + e] - d[8 * q + e];
+                    dg[e] = gm * dl[e];
+                }
+                tc::st_chunk<Op>(sm + S_A6, row, 4 * hf + q, dg);
+                tc::st_chunk<Op>(sm + S_DL + (c & 1) * 8192, row, 4 * hf + q, dl);
             }
             tc::fence_proxy_async();
             tc::wait_st();
             tc::fence_before_sync();
             named_bar_sync(1, NT);  // the output warps only arrive
-            // MMA6: S^T(:, half) += K^T x Delta~ (both read MN-major from row-wise images).  The
-            // commit is issued even when MMA6 is not, so that every thread's wait has its phase.
+            // MMA6: S^T(:, half) += K^T x Delta~; the commit is issued even when the product is
+            // not, so that every wait has its phase
             if (tid == 0) {
                 tc::fence_after_sync();
                 if (ok)
@@ -1132,64 +1170,55 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 tc::commit(bar6);
             }
         } else {
-            // the decayed S of rows 64-127 is in TMEM: MMA6 may start as far as these warps go
+            // the decayed S of rows 64-127 is in TMEM: MMA6 may go ahead as far as these warps
+            // are concerned
             tc::wait_st();
             tc::fence_before_sync();
             named_bar_arrive(1, NT);
-            // the previous chunk's output rows, then the next-but-one chunk's sums barrier
+            // the chunk before last: finished rows out; the next sums barrier phase armed
             bool gotp = true;
-            if (pend_c >= 0) gotp = finish_rows(pend_c);
-            if (tid == PF && gotp && pend_c >= 0 && c + 1 < nch) mbar_arrive_expect_tx(&peer_bar[(c + 1) & 1], 256);
-            const bool got4 = mbar_wait_bounded(bar, (uint32_t)(c & 1), nullptr);
-            if ((!got4 || !gotp) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-            ok = got4 && gotp;
-            tc::fence_after_sync();
-            // O_i = (Q' S0^T)_i + (P U)_i over this thread's 32 columns, its sum of squares, and
-            // the row's gates, all kept for the next chunk; MMA4's columns stay intact until the
-            // next chunk's MMA4, which is issued after the barrier opening that chunk
-            tc::ld32(tc::taddr(tm, warp, 64 + 32 * hf), d);
-            tc::wait_ld();
-            float ss = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float pu[8];
-                unpack8(*reinterpret_cast<const uint4*>(buf + B_O0 + tc::sw128_chunk(orow, 4 * hf + q)), pu);
-                gzr[q] = *reinterpret_cast<const uint4*>(buf + B_GZ + tc::sw128_chunk(orow, 4 * hf + q));
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    o[8 * q + e] = d[8 * q + e] + pu[e];
-                    ss = fmaf(o[8 * q + e], o[8 * q + e], ss);
-                }
+            if (c >= 2) {
+                gotp = finish_rows(c - 2);
+                if (tid == PF && gotp) mbar_arrive_expect_tx(&peer_bar[c & 1], 256);
             }
-            s_ss[(c & 1) * 128 + hf * 64 + orow] = ss;
-            named_bar_sync(2, NT / 2);  // the four output warps
-            // this half's per-token sums of squares -> the other CTA, by asynchronous stores that
-            // complete on its barrier for this chunk
-            if (tid >= PF && tid < PF + 16) {
-                const int j = tid - PF;
-                const float* mine = s_ss + (c & 1) * 128;
-                const float4 a = reinterpret_cast<const float4*>(mine)[j];
-                const float4 b = reinterpret_cast<const float4*>(mine + 64)[j];
-                st_async_cluster_v4(map_to_rank(smem_addr(peer_ss + (c & 1) * 64 + 4 * j), peer),
-                                    make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w),
-                                    map_to_rank(smem_addr(&peer_bar[c & 1]), peer));
+            // the chunk before: its output rows (MMA7 is done with its P slot, which PF refills;
+            // the next chunk's MMA4 overwrites these columns only after the next full barrier)
+            bool got7 = true;
+            if (c >= 1) {
+                got7 = complete_rows(c - 1);
+                if (tid == PF && got7 && c + 1 < nch) fetch_p(c + 1);
             }
+            if ((!gotp || !got7) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+            ok = gotp && got7;
+            // this chunk's gates, read before this buffer is refetched
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                gzn[q] = *reinterpret_cast<const uint4*>(buf + B_GZ + tc::sw128_chunk(orow, 4 * hf + q));
+            named_bar_sync(2, NT / 2);  // the four output warps: sums of chunk c - 1 written, buffer read
+            if (c >= 1) send_sums(c - 1);
         }
-        pend_c = c;
         const bool got6 = mbar_wait_bounded(bar6, (uint32_t)(c & 1), nullptr);
         if (!got6 && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
         ok = ok && got6;
         tc::fence_after_sync();
-        // this buffer is free again (its rows were read before barriers 1 and 2, both products
-        // are done): fetch the record two chunks ahead into it
-        if (tid == PF && ok && c + 2 < nch) prefetch(c + 2);
+        // this buffer is free (MMA4 and MMA6 are done, its rows were read before barriers 1
+        // and 2): fetch the record two chunks ahead into it
+        if (tid == PF && ok && c + 2 < nch) fetch_main(c + 2);
     }
     ok = __syncthreads_and(ok) != 0;
-    if (ok && pend_c >= 0) {
-        bool gotp = true;
-        if (row >= 64) gotp = finish_rows(pend_c);
-        if (!gotp && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
-        ok = __syncthreads_and(gotp) != 0;
+    if (ok) {
+        // MMA7 of the last chunk, then the last two chunks' output rows
+        if (tid == 0) issue_mma7(nch - 1, true);
+        bool gotp = true, got7 = true;
+        if (row >= 64) {
+            if (nch >= 2) gotp = finish_rows(nch - 2);
+            got7 = complete_rows(nch - 1);
+            named_bar_sync(2, NT / 2);
+            send_sums(nch - 1);
+            gotp = finish_rows(nch - 1) && gotp;
+        }
+        if ((!gotp || !got7) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        ok = __syncthreads_and(gotp && got7) != 0;
     }
 
     if (ok) {
@@ -1200,13 +1229,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 #pragma unroll
         for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = v[e];
     }
-    // every prefetched copy must land before the CTA's shared memory goes away
+    // every fetched copy must land, and the last MMA7 be done, before the CTA's shared and
+    // tensor memory go away
+    if (tid == 0 && mma7_issued > 0) mbar_wait_bounded(bar7, (uint32_t)((mma7_issued - 1) & 1), nullptr);
     if (tid == PF) {
-        for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
+        for (int c = (main_issued > 2 ? main_issued - 2 : 0); c < main_issued; ++c)
             mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
+        for (int c = (p_issued > 2 ? p_issued - 2 : 0); c < p_issued; ++c)
+            mbar_wait_bounded(&full_p[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
     }
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 128);
+    if (warp == 0) tc::dealloc(tm, 256);
     // Neither CTA leaves while the other may still write into its shared memory.  Both reach
     // this barrier: every wait above is bounded and a failed wait ends the loop in both CTAs.
     cluster_sync_all();
