@@ -918,8 +918,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // CTA's shared memory and arrives on that CTA's mbarrier (distributed shared memory).  Warps
 // w with w % 4 < 2 hold rows 0-63 (Delta); the others hold rows 64-127 and read the output
 // one chunk behind the chain, finishing its rows one more behind (once the other CTA's sums
-// are in); thread PF of warp 2 fetches the records.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
-// 32 (w / 4) .. + 31.
+// are in); thread PF of warp 2 fetches the records, thread 0 issues the products.  8 warps:
+// warp w reads TMEM lane quarter w % 4 and works on columns 32 (w / 4) .. + 31.
 
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
@@ -972,7 +972,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     int main_issued = 0, p_issued = 0;  // fetches so far (thread PF)
     int mma7_issued = 0;                // MMA7s so far (thread 0)
     auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
-    auto fetch_main = [&](int c) {  // the record's [W; Q] operand, K image, U, gates and scalars
+    auto fetch_main = [&](int c) {  // the record's [W; Q~] operand, K image, U, gates and scalars
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = record(c);
         const unsigned char* kimg = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * KIMG_BYTES;
