@@ -447,6 +447,63 @@ def time_prefill(torch, binding, synth, steps, warmup):
     return statistics.median(times), T
 
 
+def time_mixed(torch, binding, synth, iters=5, warmup=2, m=32, lengths=(8192, 8192)):
+    """The continuous-batching step of the mixed-batch workload (32 decode slots + two new 8192-token
+    prompts per iteration, 16/32 heads, d = 128, bf16 io): gdn_mixed_step against the same work as a
+    decode call followed by a prefill call.  Device time per iteration (median); the prompts' slots
+    are zeroed outside the timed region, as in a recycled slot."""
+    T = sum(lengths)
+    pool = binding.Pool(HQK, HV, D, D, m + len(lengths) + 2, 1, W, "bf16", "bf16", max_prefill_tokens=T)
+    p = synth.layer_params(WORKLOAD_DECODE, 0, HQK, HV, D, D, W)
+    pool.layer_params(0, *(torch.from_numpy(p[k]) for k in ("conv_w", "A_log", "dt_bias", "norm_w")))
+    dec = [pool.alloc() for _ in range(m)]
+    pre = [pool.alloc() for _ in lengths]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(44)
+    for s in dec:
+        pool.state_views(0, s)[0].copy_(torch.randn(pool.state_views(0, s)[0].shape, generator=g, device="cuda") * 0.3)
+    d = {n: torch.randn((m, w), generator=g, device="cuda").to(torch.bfloat16)
+         for n, w in (("q", HQK * D), ("k", HQK * D), ("v", HV * D), ("z", HV * D), ("a", HV), ("b", HV))}
+    x = {n: torch.randn((T, w), generator=g, device="cuda").to(torch.bfloat16)
+         for n, w in (("q", HQK * D), ("k", HQK * D), ("v", HV * D), ("z", HV * D), ("a", HV), ("b", HV))}
+    ptrs = pool.slot_ptrs(0, torch.tensor(dec, dtype=torch.int32, device="cuda"))
+    cu = torch.tensor([0] + list(__import__("itertools").accumulate(lengths)), dtype=torch.int32, device="cuda")
+    ids = torch.tensor(pre, dtype=torch.int32, device="cuda")
+    dout = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
+    pout = torch.empty((T, HV * D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def mixed():
+        pool.mixed_step(0, ptrs, m, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], dout, cu, ids, len(lengths), T,
+                        x["q"], x["k"], x["v"], x["a"], x["b"], x["z"], pout, stream)
+
+    def separate():
+        pool.decode_step(0, ptrs, m, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], dout, stream)
+        pool.prefill_varlen(0, cu, ids, len(lengths), T, x["q"], x["k"], x["v"], x["a"], x["b"], x["z"], pout, stream)
+
+    def timed(fn):
+        times = []
+        for it in range(warmup + iters):
+            for s in pre:
+                pool.recycle(s, stream)
+                pool.alloc()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if it >= warmup:
+                times.append(a.elapsed_time(b))
+        return statistics.median(times)
+
+    ms_sep = timed(separate)
+    ms_mix = timed(mixed)
+    assert pool.device_status() == 0
+    pool.close()
+    return ms_mix, ms_sep, m * decode_bytes_per_slot_step() + prefill_bytes(list(lengths))
+
+
 def cpu_baseline_decode(seconds=10.0, m_sample=16):
     """fp64 oracle decode steps over a sample of slots, on all host cores, for about `seconds`."""
     import numpy as np
@@ -555,6 +612,11 @@ def run_ours(args):
         result["prefill_80k"] = {"workload": "one 80 000-token prefill, bf16 io, zero state", "ms": lms,
                                  "tok_per_s": 80000 / (lms * 1e-3),
                                  "frac_hbm": prefill_bytes([80000]) / (lms * 1e-3) / 1e9 / hbm}
+        mix, sep, mb = time_mixed(torch, binding, synth)
+        result["mixed_step"] = {"workload": "gdn_mixed_step: 32 decode slots + two 8192-token prompts into zeroed "
+                                            "slots, bf16 io (the mixed-batch iteration)",
+                                "ms": mix, "ms_separate_calls": sep, "bytes": mb,
+                                "gbs": mb / (mix * 1e-3) / 1e9, "frac_hbm": mb / (mix * 1e-3) / 1e9 / hbm}
         l30 = time_decode_layers(torch, binding, synth)
         result["decode_30_layers"] = {"workload": "one token step of 30 stacked GDN layers at m = 256 "
                                                   "(30 x 256 slots, 16.1 GB of state), CUDA-graph replay",

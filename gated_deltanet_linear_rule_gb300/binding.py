@@ -29,7 +29,7 @@ EXPORTS = [
     "gdn_pool_create", "gdn_pool_destroy", "gdn_pool_reset", "gdn_slot_alloc", "gdn_slot_recycle",
     "gdn_slot_addr", "gdn_slot_ptrs", "gdn_layer_params", "gdn_decode_step", "gdn_prefill_varlen",
     "gdn_last_device_status", "gdn_pool_get_info", "gdn_status_string", "gdn_version",
-    "gdn_prefill_varlen_noalloc", "gdn_slot_snapshot", "gdn_slot_restore",
+    "gdn_prefill_varlen_noalloc", "gdn_slot_snapshot", "gdn_slot_restore", "gdn_mixed_step",
 ]
 
 
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_layer_params.argtypes = [vp, i, vp, vp, vp, vp]
         L.gdn_decode_step.argtypes = [vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gdn_prefill_varlen.argtypes = [vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_mixed_step.argtypes = [vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, vp, vp,
+                                     vp, vp]
         L.gdn_last_device_status.argtypes = [vp, vp]
         L.gdn_pool_get_info.argtypes = [vp, ctypes.POINTER(GdnPoolInfo)]
         L.gdn_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(GdnShape), vp, vp, vp, vp, vp, i, vp, vp, i, i,
@@ -254,6 +256,14 @@ class Pool:
         _check(lib().gdn_prefill_varlen(self._h, int(layer), _p(cu_seqlens), _p(slot_ids), int(n_seqs),
                                         int(total_tokens), _p(q), _p(k), _p(v), _p(a), _p(b), _p(z), _p(out),
                                         _stream(stream)), "gdn_prefill_varlen")
+
+    def mixed_step(self, layer: int, slot_ptrs, m: int, dq, dk, dv, da, db, dz, dout, cu_seqlens, slot_ids,
+                   n_seqs: int, total_tokens: int, pq, pk, pv, pa, pb, pz, pout, stream=None):
+        """gdn_mixed_step: m decode rows and n_seqs prefill sequences of `layer` in one call."""
+        _check(lib().gdn_mixed_step(self._h, int(layer), _p(slot_ptrs), int(m), _p(dq), _p(dk), _p(dv), _p(da),
+                                    _p(db), _p(dz), _p(dout), _p(cu_seqlens), _p(slot_ids), int(n_seqs),
+                                    int(total_tokens), _p(pq), _p(pk), _p(pv), _p(pa), _p(pb), _p(pz), _p(pout),
+                                    _stream(stream)), "gdn_mixed_step")
 
     def device_status(self, stream=None) -> int:
         return _check(lib().gdn_last_device_status(self._h, _stream(stream)), "gdn_last_device_status")

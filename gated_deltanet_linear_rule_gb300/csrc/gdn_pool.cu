@@ -8,7 +8,9 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <unordered_map>
 
 #include "gdn_internal.cuh"
 
@@ -155,10 +157,15 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     return GDN_OK;
 }
 
+namespace {
+void release_mixed_streams(const gdn_pool* P);  // the internal stream of gdn_mixed_step, below
+}
+
 int gdn_pool_destroy(gdn_pool* P)
 {
     if (!P) return GDN_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
+    release_mixed_streams(P);
     cudaFree(P->base);
     cudaFree(P->live_dev);
     cudaFree(P->status_dev);
@@ -258,21 +265,23 @@ int gdn_layer_params(gdn_pool* P, int layer, const float* conv_w, const float* A
     return GDN_OK;
 }
 
-int gdn_decode_step(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m, const void* q, const void* k,
-                    const void* v, const void* a, const void* b, const void* z, void* out, void* stream)
+namespace {
+
+// the argument checks of gdn_decode_step (GDN_OK: enqueue; m == 0 passes and enqueues nothing)
+int check_decode(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m, const void* q, const void* k,
+                 const void* v, const void* a, const void* b, const void* z, void* out)
 {
     if (!P || layer < 0 || layer >= P->num_layers || m < 0) return GDN_ERR_INVALID_ARG;
     if (m == 0) return GDN_OK;
     if (!slot_ptrs_dev || !q || !k || !v || !a || !b || !z || !out) return GDN_ERR_INVALID_ARG;
     if (!P->params[(size_t)layer].set()) return GDN_ERR_NO_PARAMS;
-    cudaError_t e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, q, k, v, a, b, z, out,
-                                       reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
-int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
-                       int total_tokens, const void* q, const void* k, const void* v, const void* a, const void* b,
-                       const void* z, void* out, void* stream)
+// the argument checks of gdn_prefill_varlen (n_seqs == 0 with no tokens passes and enqueues nothing)
+int check_prefill(gdn_pool* P, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
+                  int total_tokens, const void* q, const void* k, const void* v, const void* a, const void* b,
+                  const void* z, void* out)
 {
     if (!P || layer < 0 || layer >= P->num_layers || n_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
     if (n_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
@@ -284,9 +293,106 @@ int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const 
     if (n_seqs > gdn::prefill_max_seqs(P->shape.max_prefill_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (gdn::prefill_chunked(P->shape) && gdn::prefill_call_chunks(total_tokens, n_seqs) > P->ws.chunk_cap)
         return GDN_ERR_UNSUPPORTED_SHAPE;
+    return GDN_OK;
+}
+
+// per pool: the internal stream a mixed step runs its decode on, and the fork / join events
+struct MixedStreams {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_mixed_mu;
+std::unordered_map<const gdn_pool*, MixedStreams> g_mixed;
+
+cudaError_t mixed_streams(const gdn_pool* P, MixedStreams* out)
+{
+    std::lock_guard<std::mutex> lk(g_mixed_mu);
+    auto it = g_mixed.find(P);
+    if (it != g_mixed.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    MixedStreams m;
+    cudaError_t e = cudaStreamCreateWithFlags(&m.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (m.join) cudaEventDestroy(m.join);
+        if (m.fork) cudaEventDestroy(m.fork);
+        if (m.side) cudaStreamDestroy(m.side);
+        return e;
+    }
+    g_mixed[P] = m;
+    *out = m;
+    return cudaSuccess;
+}
+
+void release_mixed_streams(const gdn_pool* P)
+{
+    std::lock_guard<std::mutex> lk(g_mixed_mu);
+    auto it = g_mixed.find(P);
+    if (it == g_mixed.end()) return;
+    cudaEventDestroy(it->second.join);
+    cudaEventDestroy(it->second.fork);
+    cudaStreamDestroy(it->second.side);
+    g_mixed.erase(it);
+}
+
+}  // namespace
+
+int gdn_decode_step(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m, const void* q, const void* k,
+                    const void* v, const void* a, const void* b, const void* z, void* out, void* stream)
+{
+    const int rc = check_decode(P, layer, slot_ptrs_dev, m, q, k, v, a, b, z, out);
+    if (rc != GDN_OK || m == 0) return rc;
+    cudaError_t e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, q, k, v, a, b, z, out,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_prefill_varlen(gdn_pool* P, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
+                       int total_tokens, const void* q, const void* k, const void* v, const void* a, const void* b,
+                       const void* z, void* out, void* stream)
+{
+    const int rc = check_prefill(P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, q, k, v, a, b, z, out);
+    if (rc != GDN_OK || n_seqs == 0) return rc;
     cudaError_t e = gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, q, k, v, a,
                                         b, z, out, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_mixed_step(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m, const void* dq, const void* dk,
+                   const void* dv, const void* da, const void* db, const void* dz, void* dout,
+                   const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs, int total_tokens, const void* pq,
+                   const void* pk, const void* pv, const void* pa, const void* pb, const void* pz, void* pout,
+                   void* stream)
+{
+    int rc = check_decode(P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout);
+    if (rc != GDN_OK) return rc;
+    rc = check_prefill(P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, pq, pk, pv, pa, pb, pz, pout);
+    if (rc != GDN_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (m == 0 || n_seqs == 0) {  // one part only: nothing to overlap
+        cudaError_t e = cudaSuccess;
+        if (m > 0) e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, st);
+        if (n_seqs > 0)
+            e = gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, pq, pk, pv, pa, pb,
+                                    pz, pout, st);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    MixedStreams ms;
+    if (mixed_streams(P, &ms) != cudaSuccess) return GDN_ERR_CUDA;
+    // fork: the decode on the side stream after everything enqueued on `stream` so far
+    cudaError_t e = cudaEventRecord(ms.fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ms.side, ms.fork, 0);
+    if (e == cudaSuccess) e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, ms.side);
+    // the prefill on `stream` meanwhile; then `stream` waits for the decode (join)
+    const cudaError_t ep = e == cudaSuccess ? gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs,
+                                                                  total_tokens, pq, pk, pv, pa, pb, pz, pout, st)
+                                            : e;
+    cudaError_t ej = cudaEventRecord(ms.join, ms.side);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, ms.join, 0);
+    return (e == cudaSuccess && ep == cudaSuccess && ej == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
 
 int gdn_last_device_status(gdn_pool* P, void* stream)

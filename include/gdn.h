@@ -189,6 +189,25 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);
 
+/* One continuous-batching step of `layer` over a mixed batch (issue #5279's serving loop, the
+ * survey's NEXT-3): m decode rows exactly as gdn_decode_step (d* arguments) and n_seqs prefill
+ * sequences exactly as gdn_prefill_varlen (p* arguments), in one call.  The result equals
+ * gdn_decode_step(...) followed by gdn_prefill_varlen(...) on `stream`, bit for bit.  The
+ * decode kernel runs on an internal stream of the pool, forked from `stream` by an event and
+ * joined back before the call's work ends, so that it overlaps the prefill's pre-pass; the
+ * work of the call is ordered after earlier work on `stream`, and later work on `stream` is
+ * ordered after all of it.  The fork and join are stream-capture safe; the first call creates
+ * the internal stream and events on the current device, so make one call before capturing.
+ * The decode rows' slots and the prefill sequences' slots must be different slots (each
+ * call's own rules apply within its part); m = 0 or n_seqs = 0 leaves that part out.  Calls
+ * on one pool from several host threads at once are not supported.
+ * Errors: those of the two calls; every argument is checked before anything is enqueued. */
+int gdn_mixed_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, int m, const void* dq_dev,
+                   const void* dk_dev, const void* dv_dev, const void* da_dev, const void* db_dev, const void* dz_dev,
+                   void* dout_dev, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs, int total_tokens,
+                   const void* pq_dev, const void* pk_dev, const void* pv_dev, const void* pa_dev, const void* pb_dev,
+                   const void* pz_dev, void* pout_dev, void* stream);
+
 /* Allocation-free varlen prefill.  The pages have no counterpart of this call; it
  * exists for callers that cannot call cudaMalloc -- code that runs where device memory
  * is owned and budgeted by someone else, or in a phase that must not allocate -- and so

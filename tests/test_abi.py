@@ -72,6 +72,7 @@ def test_null_arguments_are_rejected(lib):
     assert lib.gdn_layer_params(None, 0, None, None, None, None) == -1
     assert lib.gdn_decode_step(None, 0, None, 1, *([None] * 8)) == -1
     assert lib.gdn_prefill_varlen(None, 0, None, None, 1, 1, *([None] * 8)) == -1
+    assert lib.gdn_mixed_step(None, 0, None, 1, *([None] * 7), None, None, 1, 1, *([None] * 7), None) == -1
     assert lib.gdn_last_device_status(None, None) == -1
     assert lib.gdn_pool_get_info(None, None) == -1
 
