@@ -30,6 +30,7 @@ EXPORTS = [
     "gdn_slot_addr", "gdn_slot_ptrs", "gdn_layer_params", "gdn_decode_step", "gdn_prefill_varlen",
     "gdn_last_device_status", "gdn_pool_get_info", "gdn_status_string", "gdn_version",
     "gdn_prefill_varlen_noalloc", "gdn_slot_snapshot", "gdn_slot_restore", "gdn_mixed_step",
+    "gdn_in_proj", "gdn_out_proj",
 ]
 
 
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_layer_params.argtypes = [vp, i, vp, vp, vp, vp]
         L.gdn_decode_step.argtypes = [vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gdn_prefill_varlen.argtypes = [vp, i, vp, vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_in_proj.argtypes = [ctypes.POINTER(GdnShape), i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_out_proj.argtypes = [ctypes.POINTER(GdnShape), i, i, vp, vp, vp, vp, vp]
         L.gdn_mixed_step.argtypes = [vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, vp, vp, vp, vp, vp, vp,
                                      vp, vp]
         L.gdn_last_device_status.argtypes = [vp, vp]
@@ -285,6 +288,18 @@ def prefill_varlen_noalloc(shape: GdnShape, conv_w, A_log, dt_bias, norm_w, stat
                                             _p(states), int(num_slots), _p(cu_seqlens), _p(slot_ids), int(n_seqs),
                                             int(total_tokens), _p(q), _p(k), _p(v), _p(a), _p(b), _p(z), _p(out),
                                             _p(status), _stream(stream)), "gdn_prefill_varlen_noalloc")
+
+
+def in_proj(shape: GdnShape, hidden: int, T: int, x, w_in, q, k, v, z, a, b, status=None, stream=None):
+    """gdn_in_proj: x [T][hidden] times the concatenated weight rows -> q, k, v, z, a, b (bf16)."""
+    _check(lib().gdn_in_proj(ctypes.byref(shape), int(hidden), int(T), _p(x), _p(w_in), _p(q), _p(k), _p(v), _p(z),
+                             _p(a), _p(b), _p(status), _stream(stream)), "gdn_in_proj")
+
+
+def out_proj(shape: GdnShape, hidden: int, T: int, o, w_out, y, status=None, stream=None):
+    """gdn_out_proj: y [T][hidden] = o [T][Hv*dv] times w_out^T (bf16)."""
+    _check(lib().gdn_out_proj(ctypes.byref(shape), int(hidden), int(T), _p(o), _p(w_out), _p(y), _p(status),
+                              _stream(stream)), "gdn_out_proj")
 
 
 def version() -> int:

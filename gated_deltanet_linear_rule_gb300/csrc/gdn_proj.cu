@@ -1,0 +1,279 @@
+// gdn_proj.cu -- the projections around a GDN layer on tcgen05 tensor cores: the fused input
+// projection X -> [q | k | v | z | a | b] and the output projection O -> Y.
+//
+// The pages' layer tree ("qwen3_5.py: Qwen3_5ForCausalLM.forward()", the GatedDeltaNet layer)
+// opens the layer with the projections in_proj_qkv, in_proj_z, in_proj_b, in_proj_a and closes
+// it with out_proj.  Here the four input projections are one GEMM whose weight rows are the
+// concatenation [W_q; W_k; W_v; W_z; W_a; W_b] (each [out][hidden], row-major), and the epilogue
+// writes every output column straight into the buffer and layout the layer's calls read (q, k,
+// v, z, a, b, each [T][width] row-major), so no split or copy follows.  out_proj is the same
+// kernel with one output segment.
+//
+// C[M][N] = A[M][K] . B[N][K]^T, bf16 operands, fp32 accumulation in tensor memory, bf16 out.
+// One CTA per 128 x 256 output tile: warp 0 streams 64-wide K slices of A (128 rows) and B
+// (256 rows) by 2-D tensor copies with the 128-byte swizzle (which lays them out as the MMA's
+// K-major operand tiles) into a 4-stage ring; warp 1 issues the MMAs (M = 128, N = 256, K = 16
+// per instruction) into 256 TMEM columns, releasing each stage by a commit; warps 2-5 read the
+// accumulator (one TMEM lane quarter each, warp w -> lanes 32 (w % 4) ..), round to bf16 and
+// store 16 B at a time.  Rows past M and columns past N are zero-filled by the copies and
+// skipped by the stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+#include "gdn_tcgen05.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+constexpr size_t PROJ_SMEM = BAR_OFF + 256 + 1024;  // ring + barriers + alignment slack
+constexpr int PT = 192;                             // 6 warps
+
+constexpr int MAX_SEG = 6;
+struct Seg {
+    int n0, n1;  // output columns [n0, n1) of C ...
+    void* dst;   // ... go to dst[row * ld + (n - n0)] (bf16)
+    int ld;
+};
+struct ProjArgs {
+    int M, N, K;
+    Seg seg[MAX_SEG];
+    int nseg;
+    unsigned int* status;
+};
+struct ProjMaps {
+    CUtensorMap a, b;
+};
+
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ ProjArgs P,
+                                                       const __grid_constant__ ProjMaps T)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR_OFF);  // [STAGES] slice landed
+    uint64_t* empty = full + STAGES;                             // [STAGES] slice consumed by the MMAs
+    uint64_t* accf = empty + STAGES;                             // accumulator complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+    const int KT = P.K / BK;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::alloc(tmem_slot, 256);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    if (warp == 0) {
+        // producer: K slices of A and B, STAGES ahead of the MMAs
+        if (lane == 0) {
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)((kt / STAGES) & 1);
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, nullptr)) {
+                    atomicOr(P.status, GDN_DEV_TIMEOUT);
+                    break;
+                }
+                unsigned char* st = sm + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                tma_load(st, &T.a, kt * BK, m0, &full[s]);
+                tma_load(st + A_BYTES, &T.b, kt * BK, n0, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // MMA issuer: D[128][256] += A_slice . B_slice^T, four K = 16 steps per slice
+        if (lane == 0) {
+            bool ok = true;
+            for (int kt = 0; kt < KT && ok; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)((kt / STAGES) & 1);
+                ok = mbar_wait_bounded(&full[s], ph, nullptr);
+                if (!ok) {
+                    atomicOr(P.status, GDN_DEV_TIMEOUT);
+                    break;
+                }
+                tc::fence_after_sync();
+                unsigned char* st = sm + s * STAGE_BYTES;
+                tc::mma_k(tm, smem_addr(st), BM, smem_addr(st + A_BYTES), BN, BK, tc::idesc_bf16(BM, BN), kt > 0);
+                tc::commit(&empty[s]);
+            }
+            tc::commit(accf);  // also when a wait failed, so that the epilogue's wait ends
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of the tile
+        const bool got = mbar_wait_bounded(accf, 0u, nullptr);
+        if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
+        tc::fence_after_sync();
+        const int row = (warp & 3) * 32 + lane, m = m0 + row;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            float v[32];
+            tc::ld32(tc::taddr(tm, warp, c0), v);  // whole warp
+            tc::wait_ld();
+            const int n = n0 + c0;
+            if (!got || m >= P.M || n >= P.N) continue;
+            // the segment holding column n (constant indices: the segment table stays in registers)
+            Seg sg = P.seg[0];
+#pragma unroll
+            for (int i = 1; i < MAX_SEG; ++i)
+                if (i < P.nseg && n >= P.seg[i].n0) sg = P.seg[i];
+            if (n + 32 <= sg.n1 && ((n - sg.n0) & 7) == 0 && (sg.ld & 7) == 0) {
+                // the 32 columns lie in one segment, 16-B aligned: four 16-B stores
+                __nv_bfloat16* d = static_cast<__nv_bfloat16*>(sg.dst) + (size_t)m * sg.ld + (n - sg.n0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = tc::pack2<__nv_bfloat16>(v[8 * q + 0], v[8 * q + 1]);
+                    w.y = tc::pack2<__nv_bfloat16>(v[8 * q + 2], v[8 * q + 3]);
+                    w.z = tc::pack2<__nv_bfloat16>(v[8 * q + 4], v[8 * q + 5]);
+                    w.w = tc::pack2<__nv_bfloat16>(v[8 * q + 6], v[8 * q + 7]);
+                    *reinterpret_cast<uint4*>(d + 8 * q) = w;
+                }
+            } else {  // narrow segments (small shapes): one column at a time
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int ne = n + e;
+                    if (ne >= P.N) continue;
+                    Seg g = P.seg[0];
+#pragma unroll
+                    for (int i = 1; i < MAX_SEG; ++i)
+                        if (i < P.nseg && ne >= P.seg[i].n0) g = P.seg[i];
+                    static_cast<__nv_bfloat16*>(g.dst)[(size_t)m * g.ld + (ne - g.n0)] = __float2bfloat16_rn(v[e]);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::dealloc(tm, 256);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// [rows][k] bf16 row-major at base, read as 64-wide K slices of box_rows rows, 128-byte swizzle
+cudaError_t encode_kmajor(CUtensorMap* m, const void* base, int k, int rows, int box_rows)
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+__device__ unsigned int g_proj_status;  // status word of calls that pass none
+
+cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const Seg* seg, int nseg,
+                        unsigned int* status, cudaStream_t st)
+{
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    ProjArgs P;
+    memset(&P, 0, sizeof(P));
+    P.M = M;
+    P.N = N;
+    P.K = K;
+    P.nseg = nseg;
+    P.status = status;
+    if (!P.status) {
+        void* addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_proj_status);
+        if (e != cudaSuccess) return e;
+        P.status = static_cast<unsigned int*>(addr);
+    }
+    for (int i = 0; i < nseg; ++i) P.seg[i] = seg[i];
+    ProjMaps T;
+    memset(&T, 0, sizeof(T));
+    cudaError_t e = encode_kmajor(&T.a, a, K, M, BM);
+    if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, BN);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+    proj_kernel<<<grid, PT, PROJ_SMEM, st>>>(P, T);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// the shape facts both projections need; false when the shape is unusable here
+bool proj_shape_ok(const gdn_shape* s, int hidden)
+{
+    return s && s->hqk > 0 && s->hv > 0 && s->dk > 0 && s->dv > 0 && s->hv % s->hqk == 0 && s->io_dtype == 1 &&
+           hidden > 0 && hidden % BK == 0 && s->dk % 8 == 0 && s->dv % 8 == 0;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" int gdn_in_proj(const gdn_shape* shape, int hidden, int T, const void* x, const void* w_in, void* q,
+                           void* k, void* v, void* z, void* a, void* b, unsigned int* status_dev, void* stream)
+{
+    using namespace gdn;
+    if (!proj_shape_ok(shape, hidden) || T < 0) return GDN_ERR_INVALID_ARG;
+    if (T == 0) return GDN_OK;
+    if (!x || !w_in || !q || !k || !v || !z || !a || !b) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_in) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) ||
+        !aligned16(a) || !aligned16(b))
+        return GDN_ERR_INVALID_ARG;
+    const int Dq = shape->hqk * shape->dk, Dv = shape->hv * shape->dv, Hv = shape->hv;
+    const int N = 2 * Dq + 2 * Dv + 2 * Hv;
+    const Seg seg[6] = {{0, Dq, q, Dq},
+                        {Dq, 2 * Dq, k, Dq},
+                        {2 * Dq, 2 * Dq + Dv, v, Dv},
+                        {2 * Dq + Dv, 2 * Dq + 2 * Dv, z, Dv},
+                        {2 * Dq + 2 * Dv, 2 * Dq + 2 * Dv + Hv, a, Hv},
+                        {2 * Dq + 2 * Dv + Hv, N, b, Hv}};
+    const cudaError_t e = launch_proj(T, N, hidden, x, w_in, seg, 6, status_dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" int gdn_out_proj(const gdn_shape* shape, int hidden, int T, const void* o, const void* w_out, void* y,
+                            unsigned int* status_dev, void* stream)
+{
+    using namespace gdn;
+    if (!proj_shape_ok(shape, hidden) || T < 0) return GDN_ERR_INVALID_ARG;
+    const int Dv = shape->hv * shape->dv;
+    if (Dv % BK != 0 || shape->out_dtype != 1) return GDN_ERR_INVALID_ARG;
+    if (T == 0) return GDN_OK;
+    if (!o || !w_out || !y || !aligned16(o) || !aligned16(w_out) || !aligned16(y)) return GDN_ERR_INVALID_ARG;
+    const Seg seg[1] = {{0, hidden, y, hidden}};
+    const cudaError_t e = launch_proj(T, hidden, Dv, o, w_out, seg, 1, status_dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

@@ -238,6 +238,28 @@ int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, cons
                                const void* k_dev, const void* v_dev, const void* a_dev, const void* b_dev,
                                const void* z_dev, void* out_dev, unsigned int* status_dev, void* stream);
 
+/* The projections around the layer (the layer tree's in_proj_qkv / in_proj_z / in_proj_b /
+ * in_proj_a and out_proj; the survey's NEXT-4), bf16 on the tensor cores with fp32 accumulation.
+ *
+ * gdn_in_proj: the four input projections as one GEMM.  x_dev [T][hidden] holds the hidden
+ * states; w_in_dev [N][hidden] is the concatenation of the weight rows of q (Hqk*dk rows), k
+ * (Hqk*dk), v (Hv*dv), z (Hv*dv), a (Hv) and b (Hv), N their total, each row one output
+ * feature.  Row t of q_dev [T][Hqk*dk], k_dev, v_dev [T][Hv*dv], z_dev, a_dev [T][Hv] and b_dev
+ * receives x_t times the matching weight rows, rounded to bf16: the buffers and layouts that
+ * gdn_decode_step and gdn_prefill_varlen read.
+ * gdn_out_proj: y_dev [T][hidden] = o_dev [T][Hv*dv] times w_out_dev^T, w_out_dev [hidden][Hv*dv].
+ * shape: io_dtype (and, for gdn_out_proj, out_dtype) must be bf16; hidden a positive multiple of
+ * 64 (and Hv*dv, the out_proj reduction, too); dk, dv multiples of 8.  Every buffer is
+ * row-major, contiguous, 16-B aligned, caller-owned.  status_dev: a device word receiving
+ * GDN_DEV_TIMEOUT if a bounded wait of the kernel ran out, or NULL (a library word is used).
+ * One launch on `stream`; no allocation, no host sync.
+ * Errors: INVALID_ARG (shape, sizes, NULL or misaligned buffer); CUDA. */
+int gdn_in_proj(const gdn_shape* shape, int hidden, int T, const void* x_dev, const void* w_in_dev, void* q_dev,
+                void* k_dev, void* v_dev, void* z_dev, void* a_dev, void* b_dev, unsigned int* status_dev,
+                void* stream);
+int gdn_out_proj(const gdn_shape* shape, int hidden, int T, const void* o_dev, const void* w_out_dev, void* y_dev,
+                 unsigned int* status_dev, void* stream);
+
 /* Synchronise `stream`, then read and clear the pool's device status word.
  * Returns the GDN_DEV_* bits (>= 0), or CUDA / INVALID_ARG. */
 int gdn_last_device_status(gdn_pool* pool, void* stream);

@@ -22,6 +22,9 @@ Parity status per function (what pins it, see the tests):
   gated_rmsnorm      pinned: torch F.rms_norm * F.silu
   layer              pinned: composition of the pinned library routines above,
                      GQA head mapping, split-call and prefill/decode invariants
+  in_proj, out_proj  pinned: selector weights copy input columns, the output split
+                     order, one-hot inputs read weight columns (the projections are
+                     the plain product, numpy in float64)
 """
 from __future__ import annotations
 
@@ -187,6 +190,25 @@ class Oracle:
         if want_o:
             res["o"] = o
         return res
+
+    # The projections around the layer (the layer tree of the pages: "Projections: in_proj_qkv,
+    # in_proj_z, in_proj_b, in_proj_a" before the conv, "out_proj" after the gated RMSNorm).
+    # Each is a linear map with weight rows = output features: y = x . W^T.
+    def in_proj(self, x, w_in, hqk, hv, dk, dv):
+        """x [T][hidden], w_in [N][hidden] with rows q (hqk*dk) | k (hqk*dk) | v (hv*dv) | z (hv*dv) |
+        a (hv) | b (hv).  Returns dict(q, k, v, z, a, b), each [T][width]."""
+        y = _f64(x) @ _f64(w_in).T
+        widths = [("q", hqk * dk), ("k", hqk * dk), ("v", hv * dv), ("z", hv * dv), ("a", hv), ("b", hv)]
+        out, c = {}, 0
+        for name, w in widths:
+            out[name] = np.ascontiguousarray(y[:, c:c + w])
+            c += w
+        assert c == y.shape[1], "w_in has the wrong number of rows"
+        return out
+
+    def out_proj(self, o, w_out):
+        """o [T][hv*dv], w_out [hidden][hv*dv] -> y [T][hidden]."""
+        return _f64(o) @ _f64(w_out).T
 
     def max_threads(self) -> int:
         return int(self.lib.gdn_oracle_max_threads())

@@ -397,4 +397,58 @@ def pin_head_mask(o):
             assert np.array_equal(part["S"][:, h], c["S"][:, h]), "masked head S untouched"
 
 
+# --------------------------------------------------------- projections ----
+
+def pin_in_proj_selectors_and_split(o):
+    """Weight rows that are unit vectors copy input columns: row j of segment s selects input
+    feature f(s, j), so every output column is a known column of x; the six outputs come out in
+    the order q | k | v | z | a | b with their widths (a transposed weight or a shifted split
+    fails here)."""
+    hqk, hv, dk, dv, hidden, T = 2, 4, 8, 8, 64, 5
+    widths = [hqk * dk, hqk * dk, hv * dv, hv * dv, hv, hv]
+    N = sum(widths)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, hidden))
+    sel = (np.arange(N) * 7 + 3) % hidden  # output column n copies input feature sel[n]
+    w = np.zeros((N, hidden))
+    w[np.arange(N), sel] = 1.0
+    r = o.in_proj(x, w, hqk, hv, dk, dv)
+    c = 0
+    for name, wd in zip(("q", "k", "v", "z", "a", "b"), widths):
+        assert r[name].shape == (T, wd), name
+        assert np.array_equal(r[name], x[:, sel[c:c + wd]]), name
+        c += wd
+
+
+def pin_in_proj_is_linear_rows(o):
+    """Each output row depends on its input row only, linearly: scaling row t of x by s scales row
+    t of every output and leaves the others unchanged."""
+    hqk, hv, dk, dv, hidden, T = 1, 2, 8, 8, 64, 4
+    N = 2 * hqk * dk + 2 * hv * dv + 2 * hv
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((T, hidden))
+    w = rng.standard_normal((N, hidden))
+    r0 = o.in_proj(x, w, hqk, hv, dk, dv)
+    x2 = x.copy()
+    x2[2] *= -3.0
+    r1 = o.in_proj(x2, w, hqk, hv, dk, dv)
+    for name in r0:
+        _close(r1[name][2], -3.0 * r0[name][2], 1e-14, name)
+        assert np.array_equal(np.delete(r1[name], 2, 0), np.delete(r0[name], 2, 0)), name
+
+
+def pin_out_proj_one_hot(o):
+    """A one-hot input row e_j reads column j of the weight: y = w_out[:, j]."""
+    hidden, D = 16, 24
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((hidden, D))
+    x = np.zeros((3, D))
+    for t, j in enumerate((0, 5, 23)):
+        x[t, j] = 1.0
+    y = o.out_proj(x, w)
+    assert y.shape == (3, hidden)
+    for t, j in enumerate((0, 5, 23)):
+        assert np.array_equal(y[t], w[:, j])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
