@@ -10,16 +10,19 @@
 // kernel with one output segment.
 //
 // C[M][N] = A[M][K] . B[N][K]^T, bf16 operands, fp32 accumulation in tensor memory, bf16 out.
-// One CTA per 128 x 256 output tile: warp 0 streams 64-wide K slices of A (128 rows) and B
-// (256 rows) by 2-D tensor copies with the 128-byte swizzle (which lays them out as the MMA's
-// K-major operand tiles) into a 4-stage ring; warp 1 issues the MMAs (M = 128, N = 256, K = 16
-// per instruction) into 256 TMEM columns, releasing each stage by a commit; warps 2-5 read the
-// accumulator (one TMEM lane quarter each, warp w -> lanes 32 (w % 4) ..), round to bf16 and
-// store 16 B at a time.  Rows past M and columns past N are zero-filled by the copies and
+// 128 x 256 output tiles, persistent CTAs (one per SM, tiles t = blockIdx, + gridDim, ...): warp 0
+// streams 64-wide K slices of A (128 rows) and B (256 rows) by 2-D tensor copies with the
+// 128-byte swizzle (which lays them out as the MMA's K-major operand tiles) into a 4-stage ring
+// that runs on across tiles; warp 1 issues the MMAs (M = 128, N = 256, K = 16 per instruction)
+// into one of two 256-column TMEM accumulators, releasing each stage by a commit; warps 2-5
+// read the other accumulator meanwhile (one TMEM lane quarter each, warp w -> lanes 32 (w % 4)
+// ..), round to bf16 and store 16 B at a time, so a tile's epilogue overlaps the next tile's
+// products.  Rows past M and columns past N are zero-filled by the copies and
 // skipped by the stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -62,6 +65,40 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, int 
         : "memory");
 }
 
+// the 32 output columns n .. n + 31 of row m (in registers) to their segments' buffers
+__device__ __forceinline__ void store_cols(const ProjArgs& P, int m, int n, const float (&v)[32])
+{
+    // the segment holding column n (constant indices: the segment table stays in registers)
+    Seg sg = P.seg[0];
+#pragma unroll
+    for (int i = 1; i < MAX_SEG; ++i)
+        if (i < P.nseg && n >= P.seg[i].n0) sg = P.seg[i];
+    if (n + 32 <= sg.n1 && ((n - sg.n0) & 7) == 0 && (sg.ld & 7) == 0) {
+        // the 32 columns lie in one segment, 16-B aligned: four 16-B stores
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(sg.dst) + (size_t)m * sg.ld + (n - sg.n0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = tc::pack2<__nv_bfloat16>(v[8 * q + 0], v[8 * q + 1]);
+            w.y = tc::pack2<__nv_bfloat16>(v[8 * q + 2], v[8 * q + 3]);
+            w.z = tc::pack2<__nv_bfloat16>(v[8 * q + 4], v[8 * q + 5]);
+            w.w = tc::pack2<__nv_bfloat16>(v[8 * q + 6], v[8 * q + 7]);
+            *reinterpret_cast<uint4*>(d + 8 * q) = w;
+        }
+    } else {  // narrow segments (small shapes): one column at a time
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int ne = n + e;
+            if (ne >= P.N) continue;
+            Seg g = P.seg[0];
+#pragma unroll
+            for (int i = 1; i < MAX_SEG; ++i)
+                if (i < P.nseg && ne >= P.seg[i].n0) g = P.seg[i];
+            static_cast<__nv_bfloat16*>(g.dst)[(size_t)m * g.ld + (ne - g.n0)] = __float2bfloat16_rn(v[e]);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ ProjArgs P,
                                                        const __grid_constant__ ProjMaps T)
 {
@@ -69,108 +106,113 @@ __global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ Pro
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR_OFF);  // [STAGES] slice landed
     uint64_t* empty = full + STAGES;                             // [STAGES] slice consumed by the MMAs
-    uint64_t* accf = empty + STAGES;                             // accumulator complete
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    uint64_t* accf = empty + STAGES;                             // [2] accumulator complete
+    uint64_t* acce = accf + 2;                                   // [2] accumulator read out (4 warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
     const int KT = P.K / BK;
+    const int tiles_n = (P.N + BN - 1) / BN, tiles = tiles_n * ((P.M + BM - 1) / BM);
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accf, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);
+        }
         fence_mbar_init();
     }
-    if (warp == 1) tc::alloc(tmem_slot, 256);
+    if (warp == 1) tc::alloc(tmem_slot, 512);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *tmem_slot;
 
+    // tiles of this CTA: blockIdx.x, + gridDim.x, ...; N-tiles vary fastest (the CTAs running at
+    // once share a few A row blocks and stream B through L2)
     if (warp == 0) {
-        // producer: K slices of A and B, STAGES ahead of the MMAs
+        // producer: K slices of A and B, STAGES ahead of the MMAs, across tiles
         if (lane == 0) {
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (uint32_t)((kt / STAGES) & 1);
-                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, nullptr)) {
-                    atomicOr(P.status, GDN_DEV_TIMEOUT);
-                    break;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int n0 = (t % tiles_n) * BN, m0 = (t / tiles_n) * BM;
+                for (int kt = 0; kt < KT; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)((it / STAGES) & 1);
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u, nullptr)) {
+                        atomicOr(P.status, GDN_DEV_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* st = sm + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                    tma_load(st, &T.a, kt * BK, m0, &full[s]);
+                    tma_load(st + A_BYTES, &T.b, kt * BK, n0, &full[s]);
                 }
-                unsigned char* st = sm + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                tma_load(st, &T.a, kt * BK, m0, &full[s]);
-                tma_load(st + A_BYTES, &T.b, kt * BK, n0, &full[s]);
             }
         }
     } else if (warp == 1) {
-        // MMA issuer: D[128][256] += A_slice . B_slice^T, four K = 16 steps per slice
+        // MMA issuer: tile i accumulates into TMEM columns 256 (i % 2) ..; the commits release the
+        // slices and hand the accumulator to the epilogue.  A failed wait still commits, so that
+        // every other wait ends.
         if (lane == 0) {
+            int it = 0, i = 0;
             bool ok = true;
-            for (int kt = 0; kt < KT && ok; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (uint32_t)((kt / STAGES) & 1);
-                ok = mbar_wait_bounded(&full[s], ph, nullptr);
-                if (!ok) {
+            for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+                const int ab = i & 1;
+                if (ok && !mbar_wait_bounded(&acce[ab], (uint32_t)(((i >> 1) & 1) ^ 1), nullptr)) {
                     atomicOr(P.status, GDN_DEV_TIMEOUT);
-                    break;
+                    ok = false;
                 }
                 tc::fence_after_sync();
-                unsigned char* st = sm + s * STAGE_BYTES;
-                tc::mma_k(tm, smem_addr(st), BM, smem_addr(st + A_BYTES), BN, BK, tc::idesc_bf16(BM, BN), kt > 0);
-                tc::commit(&empty[s]);
+                for (int kt = 0; kt < KT; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)((it / STAGES) & 1);
+                    if (ok && !mbar_wait_bounded(&full[s], ph, nullptr)) {
+                        atomicOr(P.status, GDN_DEV_TIMEOUT);
+                        ok = false;
+                    }
+                    tc::fence_after_sync();
+                    unsigned char* st = sm + s * STAGE_BYTES;
+                    if (ok)
+                        tc::mma_k(tm + 256 * ab, smem_addr(st), BM, smem_addr(st + A_BYTES), BN, BK,
+                                  tc::idesc_bf16(BM, BN), kt > 0);
+                    tc::commit(&empty[s]);
+                }
+                tc::commit(&accf[ab]);
             }
-            tc::commit(accf);  // also when a wait failed, so that the epilogue's wait ends
         }
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of the tile
-        const bool got = mbar_wait_bounded(accf, 0u, nullptr);
-        if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
-        tc::fence_after_sync();
-        const int row = (warp & 3) * 32 + lane, m = m0 + row;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            float v[32];
-            tc::ld32(tc::taddr(tm, warp, c0), v);  // whole warp
-            tc::wait_ld();
-            const int n = n0 + c0;
-            if (!got || m >= P.M || n >= P.N) continue;
-            // the segment holding column n (constant indices: the segment table stays in registers)
-            Seg sg = P.seg[0];
-#pragma unroll
-            for (int i = 1; i < MAX_SEG; ++i)
-                if (i < P.nseg && n >= P.seg[i].n0) sg = P.seg[i];
-            if (n + 32 <= sg.n1 && ((n - sg.n0) & 7) == 0 && (sg.ld & 7) == 0) {
-                // the 32 columns lie in one segment, 16-B aligned: four 16-B stores
-                __nv_bfloat16* d = static_cast<__nv_bfloat16*>(sg.dst) + (size_t)m * sg.ld + (n - sg.n0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w;
-                    w.x = tc::pack2<__nv_bfloat16>(v[8 * q + 0], v[8 * q + 1]);
-                    w.y = tc::pack2<__nv_bfloat16>(v[8 * q + 2], v[8 * q + 3]);
-                    w.z = tc::pack2<__nv_bfloat16>(v[8 * q + 4], v[8 * q + 5]);
-                    w.w = tc::pack2<__nv_bfloat16>(v[8 * q + 6], v[8 * q + 7]);
-                    *reinterpret_cast<uint4*>(d + 8 * q) = w;
-                }
-            } else {  // narrow segments (small shapes): one column at a time
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int ne = n + e;
-                    if (ne >= P.N) continue;
-                    Seg g = P.seg[0];
-#pragma unroll
-                    for (int i = 1; i < MAX_SEG; ++i)
-                        if (i < P.nseg && ne >= P.seg[i].n0) g = P.seg[i];
-                    static_cast<__nv_bfloat16*>(g.dst)[(size_t)m * g.ld + (ne - g.n0)] = __float2bfloat16_rn(v[e]);
-                }
+        int i = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const int ab = i & 1;
+            const int n0 = (t % tiles_n) * BN, m0 = (t / tiles_n) * BM;
+            const bool got = mbar_wait_bounded(&accf[ab], (uint32_t)((i >> 1) & 1), nullptr);
+            if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
+            tc::fence_after_sync();
+            const int row = (warp & 3) * 32 + lane, m = m0 + row;
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tc::ld32(tc::taddr(tm + 256 * ab, warp, c0), v);  // whole warp
+                tc::wait_ld();
+                const int n = n0 + c0;
+                if (!got || m >= P.M || n >= P.N) continue;
+                store_cols(P, m, n, v);
             }
+            // this warp has read its quarter of the accumulator: the MMAs may reuse it
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[ab]);
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) tc::dealloc(tm, 256);
+    if (warp == 1) tc::dealloc(tm, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -225,7 +267,15 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const long tiles = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+    const int grid = (int)std::min<long>(tiles, num_sms);  // persistent: one CTA per SM at most
     proj_kernel<<<grid, PT, PROJ_SMEM, st>>>(P, T);
     return cudaGetLastError();
 }
