@@ -504,6 +504,55 @@ def time_mixed(torch, binding, synth, iters=5, warmup=2, m=32, lengths=(8192, 81
     return ms_mix, ms_sep, m * decode_bytes_per_slot_step() + prefill_bytes(list(lengths))
 
 
+def time_proj(torch, binding, reps=20):
+    """The layer's projections (16/32 heads, d = 128, hidden 2048, bf16): gdn_in_proj (N = 12 352
+    output columns routed to q|k|v|z|a|b) and gdn_out_proj (4096 -> 2048) at the decode batch
+    (256 tokens) and the 8-sequence prefill batch (15 998 tokens).  Device time per call (mean over
+    `reps` back-to-back calls on the current stream), with torch.matmul (cuBLAS) on the same
+    product timed beside it for context."""
+    sh = binding.GdnShape(hqk=HQK, hv=HV, dk=D, dv=D, conv_w=W, chunk=64, io_dtype=1, out_dtype=1, l2_eps=1e-6,
+                          norm_eps=1e-6, max_prefill_tokens=0)
+    hidden = 2048
+    Dq, Dv = HQK * D, HV * D
+    N = 2 * Dq + 2 * Dv + 2 * HV
+    stream = torch.cuda.current_stream()
+
+    def mean_ms(fn):
+        for _ in range(3):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    out = []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    w_in = (torch.randn((N, hidden), generator=g, device="cuda") * hidden ** -0.5).to(torch.bfloat16)
+    w_out = (torch.randn((hidden, Dv), generator=g, device="cuda") * Dv ** -0.5).to(torch.bfloat16)
+    for T in (M_HEAD, sum(PREFILL_LENGTHS)):
+        x = torch.randn((T, hidden), generator=g, device="cuda").to(torch.bfloat16)
+        o = {n: torch.empty((T, w), dtype=torch.bfloat16, device="cuda")
+             for n, w in (("q", Dq), ("k", Dq), ("v", Dv), ("z", Dv), ("a", HV), ("b", HV))}
+        y_ref = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        ms = mean_ms(lambda: binding.in_proj(sh, hidden, T, x, w_in, o["q"], o["k"], o["v"], o["z"], o["a"],
+                                             o["b"], stream=stream))
+        ms_cb = mean_ms(lambda: torch.matmul(x, w_in.t(), out=y_ref))
+        out.append(("in_proj", T, N, hidden, ms, ms_cb))
+        ov = torch.randn((T, Dv), generator=g, device="cuda").to(torch.bfloat16)
+        y = torch.empty((T, hidden), dtype=torch.bfloat16, device="cuda")
+        ms = mean_ms(lambda: binding.out_proj(sh, hidden, T, ov, w_out, y, stream=stream))
+        ms_cb = mean_ms(lambda: torch.matmul(ov, w_out.t(), out=y))
+        out.append(("out_proj", T, hidden, Dv, ms, ms_cb))
+        del x, o, y_ref, ov, y
+    return out
+
+
 def cpu_baseline_decode(seconds=10.0, m_sample=16):
     """fp64 oracle decode steps over a sample of slots, on all host cores, for about `seconds`."""
     import numpy as np
@@ -617,6 +666,15 @@ def run_ours(args):
                                             "slots, bf16 io (the mixed-batch iteration)",
                                 "ms": mix, "ms_separate_calls": sep, "bytes": mb,
                                 "gbs": mb / (mix * 1e-3) / 1e9, "frac_hbm": mb / (mix * 1e-3) / 1e9 / hbm}
+        proj = []
+        for name, T, N, K, ms, ms_cb in time_proj(torch, binding):
+            tf = 2.0 * T * N * K / (ms * 1e-3) / 1e12
+            proj.append({"call": name, "tokens": T, "n": N, "k": K, "us": ms * 1e3, "tflops": tf,
+                         "frac_tensor": tf / bf16, "cublas_us": ms_cb * 1e3})
+        result["projections"] = {"workload": "gdn_in_proj (2048 -> 12 352 columns: q|k|v|z|a|b) and gdn_out_proj "
+                                             "(4096 -> 2048), bf16, at the decode batch and the 8-sequence "
+                                             "prefill batch; cuBLAS (torch.matmul) on the same product beside it",
+                                 "bound": "tensor", "peak_tflops": bf16, "calls": proj}
         l30 = time_decode_layers(torch, binding, synth)
         result["decode_30_layers"] = {"workload": "one token step of 30 stacked GDN layers at m = 256 "
                                                   "(30 x 256 slots, 16.1 GB of state), CUDA-graph replay",

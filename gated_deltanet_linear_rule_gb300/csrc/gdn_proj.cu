@@ -10,15 +10,18 @@
 // kernel with one output segment.
 //
 // C[M][N] = A[M][K] . B[N][K]^T, bf16 operands, fp32 accumulation in tensor memory, bf16 out.
-// 128 x 256 output tiles, persistent CTAs (one per SM, tiles t = blockIdx, + gridDim, ...): warp 0
-// streams 64-wide K slices of A (128 rows) and B (256 rows) by 2-D tensor copies with the
-// 128-byte swizzle (which lays them out as the MMA's K-major operand tiles) into a 4-stage ring
-// that runs on across tiles; warp 1 issues the MMAs (M = 128, N = 256, K = 16 per instruction)
-// into one of two 256-column TMEM accumulators, releasing each stage by a commit; warps 2-5
-// read the other accumulator meanwhile (one TMEM lane quarter each, warp w -> lanes 32 (w % 4)
-// ..), round to bf16 and store 16 B at a time, so a tile's epilogue overlaps the next tile's
-// products.  Rows past M and columns past N are zero-filled by the copies and
-// skipped by the stores.
+// Two persistent kernels, both warp-specialised: warp 0 streams 64-wide K slices of A and B by
+// 2-D tensor copies with the 128-byte swizzle (which lays them out as the MMA's K-major operand
+// tiles) into a stage ring that runs on across tiles; warp 1 issues the MMAs (K = 16 per
+// instruction) into one of two 256-column TMEM accumulators, releasing each stage by a commit;
+// warps 2-5 read the other accumulator meanwhile (one TMEM lane quarter each, warp w -> lanes
+// 32 (w % 4) ..), round to bf16 and store 16 B at a time, so a tile's epilogue overlaps the next
+// tile's products.  Tiles t = block (or pair) index, + grid size, ..., N tiles fastest.
+//  - proj_kernel: one CTA per 128 x 256 tile (cta_group::1, 4 stages of 48 KiB).
+//  - proj_pair_kernel: clusters of two CTAs share 256 x 256 tiles (cta_group::2, M = 256): each
+//    CTA holds 128 rows of A and 128 rows of B per K slice (6 stages of 32 KiB) and receives
+//    its 128 rows of the result, so an SM streams half the operand bytes per output.
+// Rows past M and columns past N are zero-filled by the copies and skipped by the stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -215,6 +218,151 @@ __global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ Pro
     if (warp == 1) tc::dealloc(tm, 512);
 }
 
+// ---- CTA-pair kernel: 256 x 256 tiles, one MMA (M = 256) over the two CTAs of a cluster ----
+// CTA r of a pair holds rows 128 r .. of the tile's A rows and of its B rows in its own stage ring
+// (16 KiB each per 64-wide K slice, so 6 stages fit), and receives D rows 128 r .. in its own
+// TMEM.  Per output element each SM thus streams half the operand bytes of the single-CTA
+// kernel.  The even CTA's warp 1 issues the MMAs; the odd CTA's copies complete on the even
+// CTA's full barriers, and the MMA commits arrive on the stage and accumulator barriers of both.
+constexpr int STAGES2 = 6;
+constexpr uint32_t HALF_BYTES = 128 * BK * 2;      // 128 rows of a 64-wide K slice
+constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;  // this CTA's A rows + B rows
+constexpr uint32_t BAR2_OFF = STAGES2 * STAGE2_BYTES;
+constexpr size_t PROJ2_SMEM = BAR2_OFF + 256 + 1024;
+
+// 2-D tile copy whose completion may be counted on the mbarrier of the other CTA of the pair
+// (bar is a shared::cluster address)
+__device__ __forceinline__ void tma_load_pair(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+__global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant__ ProjArgs P,
+                                                            const __grid_constant__ ProjMaps T)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR2_OFF);  // [STAGES2] both CTAs' slices landed (even CTA)
+    uint64_t* empty = full + STAGES2;                             // [STAGES2] slice consumed by the MMAs
+    uint64_t* accf = empty + STAGES2;                             // [2] accumulator complete
+    uint64_t* acce = accf + 2;                                    // [2] accumulator read out, 8 warps (even CTA)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int KT = P.K / BK;
+    const int tiles_n = (P.N + 255) / 256, tiles = tiles_n * ((P.M + 255) / 256);
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 8);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::alloc_pair(tmem_slot, 512);
+    tc::fence_before_sync();
+    cluster_sync_all();  // both CTAs' barriers and TMEM exist before either side touches them
+    tc::fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    if (warp == 0) {
+        // producer: this CTA's 128 A rows and 128 B rows of each K slice
+        if (lane == 0) {
+            const uint32_t full0 = map_to_rank(smem_addr(&full[0]), 0);
+            int it = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                const int n0 = (t % tiles_n) * 256 + 128 * (int)rank, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
+                for (int kt = 0; kt < KT; ++kt, ++it) {
+                    const int s = it % STAGES2;
+                    const uint32_t ph = (uint32_t)((it / STAGES2) & 1);
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u, nullptr)) {
+                        atomicOr(P.status, GDN_DEV_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* st = sm + s * STAGE2_BYTES;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * STAGE2_BYTES);
+                    const uint32_t fb = full0 + (uint32_t)(s * 8);
+                    tma_load_pair(st, &T.a, kt * BK, m0, fb);
+                    tma_load_pair(st + HALF_BYTES, &T.b, kt * BK, n0, fb);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // MMA issuer (even CTA): tile i into TMEM columns 256 (i % 2) .. of both CTAs.  A failed wait
+        // still commits, so that every other wait ends.
+        if (lane == 0 && rank == 0) {
+            int it = 0, i = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles; t += npairs, ++i) {
+                const int ab = i & 1;
+                if (ok && !mbar_wait_cluster_bounded(&acce[ab], (uint32_t)(((i >> 1) & 1) ^ 1))) {
+                    atomicOr(P.status, GDN_DEV_TIMEOUT);
+                    ok = false;
+                }
+                tc::fence_after_sync();
+                for (int kt = 0; kt < KT; ++kt, ++it) {
+                    const int s = it % STAGES2;
+                    const uint32_t ph = (uint32_t)((it / STAGES2) & 1);
+                    if (ok && !mbar_wait_bounded(&full[s], ph, nullptr)) {
+                        atomicOr(P.status, GDN_DEV_TIMEOUT);
+                        ok = false;
+                    }
+                    tc::fence_after_sync();
+                    unsigned char* st = sm + s * STAGE2_BYTES;
+                    if (ok)
+                        tc::mma_pair_k64(tm + 256 * ab, smem_addr(st), smem_addr(st + HALF_BYTES),
+                                         tc::idesc_bf16(256, 256), kt > 0);
+                    tc::commit_pair_mc(&empty[s], 0x3);
+                }
+                tc::commit_pair_mc(&accf[ab], 0x3);
+            }
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows 128 rank + .. of the tile
+        const uint32_t acce0 = map_to_rank(smem_addr(&acce[0]), 0);
+        int i = 0;
+        for (int t = pair; t < tiles; t += npairs, ++i) {
+            const int ab = i & 1;
+            const int n0 = (t % tiles_n) * 256, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
+            const bool got = mbar_wait_cluster_bounded(&accf[ab], (uint32_t)((i >> 1) & 1));
+            if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
+            tc::fence_after_sync();
+            const int m = m0 + (warp & 3) * 32 + lane;
+            for (int c0 = 0; c0 < 256; c0 += 32) {
+                float v[32];
+                tc::ld32(tc::taddr(tm + 256 * ab, warp, c0), v);  // whole warp
+                tc::wait_ld();
+                const int n = n0 + c0;
+                if (!got || m >= P.M || n >= P.N) continue;
+                store_cols(P, m, n, v);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce0 + (uint32_t)(ab * 8));
+        }
+    }
+    tc::fence_before_sync();
+    cluster_sync_all();  // neither CTA leaves while the other may still arrive on its barriers
+    if (warp == 1) tc::dealloc_pair(tm, 512);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -260,23 +408,67 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
         P.status = static_cast<unsigned int*>(addr);
     }
     for (int i = 0; i < nseg; ++i) P.seg[i] = seg[i];
-    ProjMaps T;
-    memset(&T, 0, sizeof(T));
-    cudaError_t e = encode_kmajor(&T.a, a, K, M, BM);
-    if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, BN);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
-    if (e != cudaSuccess) return e;
-    static int num_sms = 0;
+    cudaError_t e = cudaSuccess;
+    static int num_sms = 0, num_pairs = 0;  // resident CTAs / CTA pairs of the device
     if (num_sms == 0) {
         int dev = 0;
         e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(proj_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ2_SMEM);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
+            cfg.blockDim = dim3(PT);
+            cfg.dynamicSmemBytes = PROJ2_SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&num_pairs, proj_pair_kernel, &cfg);
+        }
+        if (e != cudaSuccess) {
+            num_sms = 0;
+            return e;
+        }
     }
-    const long tiles = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
-    const int grid = (int)std::min<long>(tiles, num_sms);  // persistent: one CTA per SM at most
-    proj_kernel<<<grid, PT, PROJ_SMEM, st>>>(P, T);
+    // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
+    // CTA pairs (256 x 256 tiles, half the operand traffic per SM); the pairs are used unless they
+    // need more rounds over the tiles than single CTAs do (a few rows past a multiple of 256)
+    const long tiles1 = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+    const long tiles2 = (long)((N + 255) / 256) * ((M + 255) / 256);
+    const long rounds1 = (tiles1 + num_sms - 1) / num_sms;
+    const long rounds2 = num_pairs > 0 ? (tiles2 + num_pairs - 1) / num_pairs : rounds1 + 1;
+    const bool pairs = rounds2 <= rounds1;
+    // A is read 128 rows at a time on both paths; B 256 rows per CTA, or 128 per CTA of a pair
+    ProjMaps T;
+    memset(&T, 0, sizeof(T));
+    e = encode_kmajor(&T.a, a, K, M, 128);
+    if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, pairs ? 128 : BN);
+    if (e != cudaSuccess) return e;
+    if (pairs) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (unsigned)std::min<long>(tiles2, num_pairs));
+        cfg.blockDim = dim3(PT);
+        cfg.dynamicSmemBytes = PROJ2_SMEM;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, proj_pair_kernel, P, T);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    proj_kernel<<<(unsigned)std::min<long>(tiles1, num_sms), PT, PROJ_SMEM, st>>>(P, T);
     return cudaGetLastError();
 }
 

@@ -138,6 +138,57 @@ __device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// ---- CTA pairs (cta_group::2): one MMA spans the two CTAs of a cluster pair ----
+// A kernel uses one cta_group throughout.  With M = 256 the even CTA of the pair issues the MMA;
+// each CTA holds 128 rows of A and N/2 rows of B at the same shared-memory offsets, and its TMEM
+// receives its own 128 rows of D (lane i = row i of its half) over all N columns.
+
+// D[tmem, both CTAs] (+)= A[smem, both] * B[smem, both]^T for one K = 16 slice
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// K = 64 slice of K-major swizzled tiles (one 64-wide K tile each): four K = 16 MMAs
+__device__ __forceinline__ void mma_pair_k64(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    const uint64_t a0 = sdesc(a_saddr), b0 = sdesc(b_saddr);
+#pragma unroll
+    for (int k16 = 0; k16 < 4; ++k16)
+        mma_pair(d_tmem, a0 + (uint64_t)(k16 * 2), b0 + (uint64_t)(k16 * 2), idesc, (k16 > 0 || accumulate) ? 1u : 0u);
+}
+
+// Arrive once on the mbarrier at this shared offset in every CTA of cta_mask when every
+// tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void commit_pair_mc(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// One full warp in EACH CTA of the pair: ncols TMEM columns in both CTAs, base address in *dst.
+__device__ __forceinline__ void alloc_pair(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

@@ -59,10 +59,13 @@ def test_in_proj_small_shapes(hqk, hv, d, hidden, T):
     _in_proj_case(hqk, hv, d, hidden, T, seed=hidden + T)
 
 
-@pytest.mark.parametrize("T", [256, 300])
+@pytest.mark.parametrize("T", [256, 300, 1100, 2100])
 def test_in_proj_35b_layer_shape(T):
     """16 q/k and 32 v heads, d = 128, hidden 2048: N = 12 352 columns in 49 tiles of 256 (the last 64
-    wide: a | b), K = 32 slices; T = 256 is the decode batch, 300 adds a partial M tile."""
+    wide: a | b), K = 32 slices.  T = 256 (the decode batch) and 2100 run on CTA pairs (256-row tiles;
+    at 2100 each pair takes several tiles in turn and the last tile's second CTA holds no valid row);
+    300 and 1100 fall a few rows past a multiple of 256 and run on single CTAs (128-row tiles, at
+    1100 several per CTA)."""
     _in_proj_case(16, 32, 128, 2048, T, seed=T)
 
 
