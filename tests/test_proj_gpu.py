@@ -69,7 +69,7 @@ def test_in_proj_35b_layer_shape(T):
     _in_proj_case(16, 32, 128, 2048, T, seed=T)
 
 
-@pytest.mark.parametrize("hidden,T", [(2048, 300), (256, 77)])
+@pytest.mark.parametrize("hidden,T", [(2048, 300), (256, 77), (2048, 2100)])
 def test_out_proj(hidden, T):
     hqk, hv, d = 16, 32, 128
     Dv = hv * d
