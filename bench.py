@@ -517,17 +517,21 @@ def time_proj(torch, binding, reps=20):
     N = 2 * Dq + 2 * Dv + 2 * HV
     stream = torch.cuda.current_stream()
 
-    def mean_ms(fn):
+    def mean_ms(fn, tag=None):
         for _ in range(3):
             fn()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        if tag:
+            torch.cuda.nvtx.range_push(tag)
         a.record(stream)
         for _ in range(reps):
             fn()
         b.record(stream)
         torch.cuda.synchronize()
+        if tag:
+            torch.cuda.nvtx.range_pop()
         return a.elapsed_time(b) / reps
 
     out = []
@@ -541,12 +545,12 @@ def time_proj(torch, binding, reps=20):
              for n, w in (("q", Dq), ("k", Dq), ("v", Dv), ("z", Dv), ("a", HV), ("b", HV))}
         y_ref = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         ms = mean_ms(lambda: binding.in_proj(sh, hidden, T, x, w_in, o["q"], o["k"], o["v"], o["z"], o["a"],
-                                             o["b"], stream=stream))
+                                             o["b"], stream=stream), tag=f"proj_timed_in_{T}")
         ms_cb = mean_ms(lambda: torch.matmul(x, w_in.t(), out=y_ref))
         out.append(("in_proj", T, N, hidden, ms, ms_cb))
         ov = torch.randn((T, Dv), generator=g, device="cuda").to(torch.bfloat16)
         y = torch.empty((T, hidden), dtype=torch.bfloat16, device="cuda")
-        ms = mean_ms(lambda: binding.out_proj(sh, hidden, T, ov, w_out, y, stream=stream))
+        ms = mean_ms(lambda: binding.out_proj(sh, hidden, T, ov, w_out, y, stream=stream), tag=f"proj_timed_out_{T}")
         ms_cb = mean_ms(lambda: torch.matmul(ov, w_out.t(), out=y))
         out.append(("out_proj", T, hidden, Dv, ms, ms_cb))
         del x, o, y_ref, ov, y
@@ -666,6 +670,12 @@ def run_ours(args):
                                             "slots, bf16 io (the mixed-batch iteration)",
                                 "ms": mix, "ms_separate_calls": sep, "bytes": mb,
                                 "gbs": mb / (mix * 1e-3) / 1e9, "frac_hbm": mb / (mix * 1e-3) / 1e9 / hbm}
+        l30 = time_decode_layers(torch, binding, synth)
+        result["decode_30_layers"] = {"workload": "one token step of 30 stacked GDN layers at m = 256 "
+                                                  "(30 x 256 slots, 16.1 GB of state), CUDA-graph replay",
+                                      "ms_per_token_step": l30, "tokens_per_s": M_HEAD / (l30 * 1e-3),
+                                      "slot_steps_per_s": 30 * M_HEAD / (l30 * 1e-3)}
+    if rank == 0 and not args.no_proj:
         proj = []
         for name, T, N, K, ms, ms_cb in time_proj(torch, binding):
             tf = 2.0 * T * N * K / (ms * 1e-3) / 1e12
@@ -675,11 +685,6 @@ def run_ours(args):
                                              "(4096 -> 2048), bf16, at the decode batch and the 8-sequence "
                                              "prefill batch; cuBLAS (torch.matmul) on the same product beside it",
                                  "bound": "tensor", "peak_tflops": bf16, "calls": proj}
-        l30 = time_decode_layers(torch, binding, synth)
-        result["decode_30_layers"] = {"workload": "one token step of 30 stacked GDN layers at m = 256 "
-                                                  "(30 x 256 slots, 16.1 GB of state), CUDA-graph replay",
-                                      "ms_per_token_step": l30, "tokens_per_s": M_HEAD / (l30 * 1e-3),
-                                      "slot_steps_per_s": 30 * M_HEAD / (l30 * 1e-3)}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds)
     result["wall_s_timed_region"] = wall
@@ -743,6 +748,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-proj", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
