@@ -367,24 +367,46 @@ def time_prefill_long(torch, binding, synth, T=80000, reps=3):
 
 
 def time_decode_e2e(torch, pool, synth, m, steps, warmup):
-    """Public-API end to end: pinned host inputs copied in, decode, output copied back, every step."""
+    """Public-API end to end, pipelined the way a serving loop runs it: each step's inputs are copied
+    from pinned host memory on a copy-in stream (into one of two device buffer sets) while the
+    previous step computes; the decode runs on the compute stream once they have landed; its output
+    is copied back to pinned host memory on a copy-out stream while the next step computes.  Events
+    order the reuse of both buffer sets.  The timed region runs from before the first input copy to
+    after the last output copy, so every step's copies are inside it."""
     ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
     ptrs = pool.slot_ptrs(0, ids)
     n_sets = min(steps + warmup, 8)
     host_sets = [{k: v.cpu().pin_memory() for k, v in s.items()} for s in device_inputs(torch, m, n_sets, 7)]
-    dev = {k: torch.empty_like(v, device="cuda") for k, v in host_sets[0].items()}
-    out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    stream = torch.cuda.current_stream()
+    dev = [{k: torch.empty_like(v, device="cuda") for k, v in host_sets[0].items()} for _ in range(2)]
+    out = [torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    out_h = [torch.empty(out[0].shape, dtype=out[0].dtype).pin_memory() for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in_ready", "in_free", "out_ready", "out_free")}
+    for n in ev:  # every event starts out recorded (complete)
+        for e in ev[n]:
+            e.record(comp)
     h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
-    d2h = out.numel() * out.element_size()
+    d2h = out[0].numel() * out[0].element_size()
 
     def step(i):
+        j = i & 1
         hs = host_sets[i % n_sets]
-        for k in dev:
-            dev[k].copy_(hs[k], non_blocking=True)
-        pool.decode_step(0, ptrs, m, dev["q"], dev["k"], dev["v"], dev["a"], dev["b"], dev["z"], out, stream)
-        out_h.copy_(out, non_blocking=True)
+        cin.wait_event(ev["in_free"][j])  # the decode that read buffer set j (step i - 2) is done
+        with torch.cuda.stream(cin):
+            for k in dev[j]:
+                dev[j][k].copy_(hs[k], non_blocking=True)
+        ev["in_ready"][j].record(cin)
+        comp.wait_event(ev["in_ready"][j])
+        comp.wait_event(ev["out_free"][j])  # step i - 2's output has been copied out
+        pool.decode_step(0, ptrs, m, dev[j]["q"], dev[j]["k"], dev[j]["v"], dev[j]["a"], dev[j]["b"], dev[j]["z"],
+                         out[j], comp)
+        ev["in_free"][j].record(comp)
+        ev["out_ready"][j].record(comp)
+        cout.wait_event(ev["out_ready"][j])
+        with torch.cuda.stream(cout):
+            out_h[j].copy_(out[j], non_blocking=True)
+        ev["out_free"][j].record(cout)
 
     for i in range(warmup):
         step(i)
@@ -392,10 +414,13 @@ def time_decode_e2e(torch, pool, synth, m, steps, warmup):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("e2e_timed")
-    t0.record(stream)
+    t0.record(comp)
+    cin.wait_event(t0)
     for i in range(steps):
         step(warmup + i)
-    t1.record(stream)
+    for j in range(2):
+        comp.wait_event(ev["out_free"][j])
+    t1.record(comp)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     ms = t0.elapsed_time(t1) / steps
