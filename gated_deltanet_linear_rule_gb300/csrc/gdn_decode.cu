@@ -23,6 +23,7 @@
 // fixed reduction orders, no m-dependent choices, so batched output equals m = 1 output
 // bit for bit.
 #include <algorithm>
+#include <mutex>
 
 #include "gdn_internal.cuh"
 
@@ -286,15 +287,24 @@ cudaError_t launch_t(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 {
     auto kern = decode_kernel<D, TIn, TOut>;
     const size_t smem = decode_smem_bytes(D, A.r);
-    static int per_sm = -1;
-    static size_t per_sm_smem = 0;
-    if (per_sm < 0 || per_sm_smem != smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) per_sm = 1;
-        per_sm_smem = smem;
+    // resident CTAs per SM for this instantiation and shared-memory size (cached; calls from
+    // several host threads are serialised here)
+    static std::mutex mu;
+    static int cached_per_sm = -1;
+    static size_t cached_smem = 0;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached_per_sm < 0 || cached_smem != smem) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+            if (e != cudaSuccess) return e;
+            cached_per_sm = std::max(n, 1);
+            cached_smem = smem;
+        }
+        per_sm = cached_per_sm;
     }
     const int items = A.m * A.hqk;
     const int grid = std::max(1, std::min(items, per_sm * P.num_sms));

@@ -409,33 +409,42 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     }
     for (int i = 0; i < nseg; ++i) P.seg[i] = seg[i];
     cudaError_t e = cudaSuccess;
-    static int num_sms = 0, num_pairs = 0;  // resident CTAs / CTA pairs of the device
-    if (num_sms == 0) {
-        int dev = 0;
-        e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(proj_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ2_SMEM);
-        if (e == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2));
-            cfg.blockDim = dim3(PT);
-            cfg.dynamicSmemBytes = PROJ2_SMEM;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&num_pairs, proj_pair_kernel, &cfg);
+    // resident CTAs / CTA pairs of the device (cached; calls from several host threads are
+    // serialised here)
+    static std::mutex mu;
+    static int cached_sms = 0, cached_pairs = 0;
+    int num_sms = 0, num_pairs = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached_sms == 0) {
+            int dev = 0, sms = 0, pairs = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(proj_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PROJ2_SMEM);
+            if (e == cudaSuccess) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2 * (unsigned)(sms / 2));
+                cfg.blockDim = dim3(PT);
+                cfg.dynamicSmemBytes = PROJ2_SMEM;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                e = cudaOccupancyMaxActiveClusters(&pairs, proj_pair_kernel, &cfg);
+            }
+            if (e != cudaSuccess) return e;
+            cached_sms = sms;
+            cached_pairs = pairs;
         }
-        if (e != cudaSuccess) {
-            num_sms = 0;
-            return e;
-        }
+        num_sms = cached_sms;
+        num_pairs = cached_pairs;
     }
     // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
     // CTA pairs (256 x 256 tiles, half the operand traffic per SM); the pairs are used unless they

@@ -129,9 +129,10 @@ def test_prefill_rejects_bad_metadata_on_device():
 
 @pytest.mark.parametrize("io,out", [("bf16", "f32"), ("f32", "f32")])
 def test_prefill_chunked_d128_ragged(io, out):
-    """d = 128 runs the chunked tensor-core kernel: lengths around the 64-token chunk boundary, GQA 2,
-    then 4 decode steps from the handed-off states."""
-    lengths = [1, 5, 63, 64, 65, 130, 200, 7]
+    """d = 128 runs the chunked tensor-core kernel: lengths around the 64-token chunk boundary and an
+    empty sequence (its slot keeps its state and conv buffer), GQA 2, then 4 decode steps from the
+    handed-off states."""
+    lengths = [1, 5, 63, 0, 64, 65, 130, 200, 7]
     L = Layer(8, 1, 2, 128, io=io, out=out, num_slots=8, max_prefill_tokens=sum(lengths))
     n = len(lengths)
     slots = [L.pool.alloc() for _ in range(n)]
