@@ -133,7 +133,7 @@ def test_prefill_chunked_d128_ragged(io, out):
     empty sequence (its slot keeps its state and conv buffer), GQA 2, then 4 decode steps from the
     handed-off states."""
     lengths = [1, 5, 63, 0, 64, 65, 130, 200, 7]
-    L = Layer(8, 1, 2, 128, io=io, out=out, num_slots=8, max_prefill_tokens=sum(lengths))
+    L = Layer(8, 1, 2, 128, io=io, out=out, num_slots=len(lengths), max_prefill_tokens=sum(lengths))
     n = len(lengths)
     slots = [L.pool.alloc() for _ in range(n)]
     inp, cu = synth.varlen_inputs(8, 0, lengths, 1, 2, 128, 128, io)
