@@ -911,9 +911,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 //     MMA4  [W; Q~] x S0^T(:, half)   -> W S0^T rows 0-63, diag(e^G) Q S0^T rows 64-127
 //     MMA6  S^T(:, half) += K^T x Delta~(:, half)   (Delta~ = diag(gamma) Delta; both MN-major)
 //     MMA7  [0; P] x Delta(:, half)   -> accumulated onto MMA4's rows 64-127: the output O
-// MMA4 of chunk c writes TMEM columns [64, 128) + 64 (c % 2), so that MMA7 of chunk c, issued
-// after MMA4 of chunk c + 1, runs while Delta of chunk c + 1 is formed.  Only MMA4 -> Delta ->
-// MMA6 is serial from chunk to chunk.  The gated RMSNorm of an output row needs its sum of
+// MMA4 of chunk c writes TMEM columns [64, 128) + 64 (c % 2).  MMA7 of chunk c is issued right
+// after its MMA6, where the issuing thread has nothing else to do until the next chunk's S0^T
+// is formed, and runs while it is; the output warps read its result one chunk later.  Only
+// MMA4 -> Delta -> MMA6 is serial from chunk to chunk.  The gated RMSNorm of an output row needs its sum of
 // squares over all of d_v, so each CTA sends its half's 64 per-token sums into the other
 // CTA's shared memory and arrives on that CTA's mbarrier (distributed shared memory).  Warps
 // w with w % 4 < 2 hold rows 0-63 (Delta); the others hold rows 64-127 and read the output
@@ -931,8 +932,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     uint64_t* peer_bar = bar4 + 1;                               // [2] the other half's sums, by chunk parity
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_bar + 2);
     uint64_t* bar6 = peer_bar + 3;                               // MMA6 completion (one phase per chunk)
-    uint64_t* bar7 = peer_bar + 4;                               // MMA7 completion (one phase per chunk)
     uint64_t* full_p = peer_bar + 5;                             // [2] P slots
+    uint64_t* const bar7e = peer_bar + 4;                        // MMA7 completion, even chunks
+    uint64_t* const bar7o = peer_bar + 7;                        // MMA7 completion, odd chunks
     float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 128);  // [2][2][64] sums of O^2: chunk parity, column half
     float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
 
@@ -958,7 +960,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mbar_init(&full_p[1], 1);
         mbar_init(bar4, 1);
         mbar_init(bar6, 1);
-        mbar_init(bar7, 1);
+        mbar_init(bar7e, 1);
+        mbar_init(bar7o, 1);
         mbar_init(&peer_bar[0], 1);
         mbar_init(&peer_bar[1], 1);
         fence_mbar_init();
@@ -1000,15 +1003,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             fetch_p(1);
         }
     }
-    // MMA7 of chunk pc (thread 0): [0; P] x Delta accumulated onto chunk pc's MMA4 columns;
-    // the commit is issued even when the product is not, so that every wait has its phase
+    // MMA7 of chunk pc (thread 0, right after the chunk's MMA6, where nothing on the chain waits
+    // for this thread): [0; P] x Delta accumulated onto chunk pc's MMA4 columns; completes on the
+    // barrier of pc's parity; the commit is issued even when the product is not, so that every
+    // wait has its phase
     auto issue_mma7 = [&](int pc, bool go) {
         const bool gotp = mbar_wait_bounded(&full_p[pc & 1], (uint32_t)((pc >> 1) & 1), nullptr);
         if (!gotp) atomicOr(A.status, GDN_DEV_TIMEOUT);
         if (go && gotp)
             tc::mma_k_mixed(tm + 64 + 64 * (pc & 1), smem_addr(sm + S_PZ + (pc & 1) * 16384), 128, 0, 0,
                             smem_addr(sm + S_DL + (pc & 1) * 8192), 0, 1, 8192, CH, tc::idesc_f16(128, 64, 0, 1), 1);
-        tc::commit(bar7);
+        tc::commit((pc & 1) ? bar7o : bar7e);
         mma7_issued = pc + 1;
     };
     // the zero halves of MMA7's operands
@@ -1056,7 +1061,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     };
     // O of chunk pc (MMA4's rows 64-127 plus MMA7), its sums of squares
     auto complete_rows = [&](int pc) -> bool {
-        const bool got7 = mbar_wait_bounded(bar7, (uint32_t)(pc & 1), nullptr);
+        const bool got7 = mbar_wait_bounded((pc & 1) ? bar7o : bar7e, (uint32_t)((pc >> 1) & 1), nullptr);
         tc::fence_after_sync();
         tc::ld32(tc::taddr(tm, warp, 64 + 64 * (pc & 1) + 32 * hf), o);
         tc::wait_ld();
@@ -1122,13 +1127,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::fence_after_sync();
         if (!ok) break;
 
-        // MMA4: [W; Q~] x S0^T(:, half) -> columns [64, 128) + 64 (c % 2); then MMA7 of the
-        // chunk before
+        // MMA4: [W; Q~] x S0^T(:, half) -> columns [64, 128) + 64 (c % 2)
         if (tid == 0) {
             tc::mma_k_mixed(tm + 64 + 64 * (c & 1), smem_addr(buf + B_A), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192,
                             D, tc::idesc_f16(128, 64, 0, 1), 0);
             tc::commit(bar4);
-            if (c >= 1) issue_mma7(c - 1, true);
         }
         if (row < 64) {
             // Delta_i = U_i - (W S0^T)_i and Delta~_i = gamma_i Delta_i -> row i of this chunk's
@@ -1160,14 +1163,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             tc::wait_st();
             tc::fence_before_sync();
             named_bar_sync(1, NT);  // the output warps only arrive
-            // MMA6: S^T(:, half) += K^T x Delta~; the commit is issued even when the product is
-            // not, so that every wait has its phase
+            // MMA6: S^T(:, half) += K^T x Delta~, then this chunk's MMA7; the commits are issued
+            // even when the products are not, so that every wait has its phase
             if (tid == 0) {
                 tc::fence_after_sync();
                 if (ok)
                     tc::mma_k_mixed(tm, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
                                     tc::idesc_f16(128, 64, 1, 1), 1);
                 tc::commit(bar6);
+                issue_mma7(c, ok);
             }
         } else {
             // the decayed S of rows 64-127 is in TMEM: MMA6 may go ahead as far as these warps
@@ -1181,8 +1185,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 gotp = finish_rows(c - 2);
                 if (tid == PF && gotp) mbar_arrive_expect_tx(&peer_bar[c & 1], 256);
             }
-            // the chunk before: its output rows (MMA7 is done with its P slot, which PF refills;
-            // the next chunk's MMA4 overwrites these columns only after the next full barrier)
+            // the chunk before: its output rows (its MMA7, issued after its MMA6, is done with its
+            // P slot, which PF refills; the next chunk's MMA4 overwrites these columns only after
+            // the next full barrier)
             bool got7 = true;
             if (c >= 1) {
                 got7 = complete_rows(c - 1);
@@ -1207,8 +1212,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
     ok = __syncthreads_and(ok) != 0;
     if (ok) {
-        // MMA7 of the last chunk, then the last two chunks' output rows
-        if (tid == 0) issue_mma7(nch - 1, true);
+        // the last two chunks' output rows
         bool gotp = true, got7 = true;
         if (row >= 64) {
             if (nch >= 2) gotp = finish_rows(nch - 2);
@@ -1231,7 +1235,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
     // every fetched copy must land, and the last MMA7 be done, before the CTA's shared and
     // tensor memory go away
-    if (tid == 0 && mma7_issued > 0) mbar_wait_bounded(bar7, (uint32_t)((mma7_issued - 1) & 1), nullptr);
+    if (tid == 0 && mma7_issued > 0)
+        mbar_wait_bounded(((mma7_issued - 1) & 1) ? bar7o : bar7e, (uint32_t)(((mma7_issued - 1) >> 1) & 1), nullptr);
     if (tid == PF) {
         for (int c = (main_issued > 2 ? main_issued - 2 : 0); c < main_issued; ++c)
             mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
