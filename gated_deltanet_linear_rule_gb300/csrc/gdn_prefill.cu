@@ -10,10 +10,12 @@
 //                 slot ids allocated and distinct.  The verdict gates every later kernel.
 // d_k = d_v = 128 (the chunked tensor-core path, gdn_chunk.cu):
 //   2. chunk pre-pass  conv, norms, gates and the chunk-local products, one CTA per
-//                 (chunk, v-head); it reads the slots' old conv buffers
-//   3. conv_tail  one CTA per sequence: the slot's conv buffer becomes the last W-1 raw
-//                 inputs (after the pre-pass has read the old buffer)
-//   4. chunk state pass  one CTA per (sequence, v-head), output and final state
+//                 (chunk, q/k head) taking the q/k head's v-heads in turn; it reads the
+//                 slots' old conv buffers
+//   3. conv_tail  one CTA per (sequence, 256 channels): the slot's conv buffer becomes the
+//                 last W-1 raw inputs (after the pre-pass has read the old buffer)
+//   4. chunk state pass  one CTA per (sequence, v-head, d_v half), the two halves a
+//                 cluster: output and final state
 // d < 128 (the recurrent path):
 //   2. prep       one CTA per token: conv + SiLU over all C channels (the left context
 //                 before a sequence's first token comes from its slot's conv buffer),
