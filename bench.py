@@ -69,7 +69,7 @@ def decode_bytes_per_slot_step(io=2):
 
 # algorithmic flops per prefill token of the chunked form (64-token chunks, triangular halves):
 # K K^T 8 064 + Q K^T 8 320 + solve C^2/3 + W, U, intra-chunk O 3 x 8 320 + 3 state products 3 x 2 d^2,
-# times Hv (the figure of the survey's measurement plan)
+# times Hv
 PREFILL_FLOPS_PER_TOKEN = 4.51e6
 
 

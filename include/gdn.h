@@ -189,8 +189,8 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);
 
-/* One continuous-batching step of `layer` over a mixed batch (issue #5279's serving loop, the
- * survey's NEXT-3): m decode rows exactly as gdn_decode_step (d* arguments) and n_seqs prefill
+/* One continuous-batching step of `layer` over a mixed batch (issue #5279's serving loop):
+ * m decode rows exactly as gdn_decode_step (d* arguments) and n_seqs prefill
  * sequences exactly as gdn_prefill_varlen (p* arguments), in one call.  The result equals
  * gdn_decode_step(...) followed by gdn_prefill_varlen(...) on `stream`, bit for bit.  The
  * decode kernel runs on an internal stream of the pool, forked from `stream` by an event and
@@ -239,7 +239,7 @@ int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, cons
                                const void* z_dev, void* out_dev, unsigned int* status_dev, void* stream);
 
 /* The projections around the layer (the layer tree's in_proj_qkv / in_proj_z / in_proj_b /
- * in_proj_a and out_proj; the survey's NEXT-4), bf16 on the tensor cores with fp32 accumulation.
+ * in_proj_a and out_proj), bf16 on the tensor cores with fp32 accumulation.
  *
  * gdn_in_proj: the four input projections as one GEMM.  x_dev [T][hidden] holds the hidden
  * states; w_in_dev [N][hidden] is the concatenation of the weight rows of q (Hqk*dk rows), k

@@ -61,7 +61,7 @@ def test_decode_shapes_fp32(hqk, hv, d, W):
 
 
 @pytest.fixture(scope="module")
-def cfg2():
+def pool256_35b():
     """The 35B-A3B-shaped GDN layer: 16 q/k heads, 32 v heads, d = 128, conv 4, bf16 io, a 256-slot
     pool whose states are N(0, 0.1)."""
     L = Layer(2, 16, 32, 128, io="bf16", out="bf16", num_slots=256)
@@ -88,9 +88,9 @@ def _reset_states(L, S0, slots):
 
 
 @pytest.mark.parametrize("m", [1, 4, 16, 256])
-def test_decode_cfg2_parity(cfg2, m):
+def test_decode_35b_layer_parity(pool256_35b, m):
     """m active slots at random distinct pool indices; bf16 out vs the oracle on sampled rows."""
-    L, S0 = cfg2
+    L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, m, 256)]
     _reset_states(L, S0, slots)
     sample = sorted(set([0, m // 2, m - 1]))
@@ -99,9 +99,9 @@ def test_decode_cfg2_parity(cfg2, m):
     assert L.pool.device_status() == 0
 
 
-def test_decode_cfg2_100_steps_fp32_out(cfg2):
+def test_decode_35b_layer_100_steps_fp32_out(pool256_35b):
     """100 steps at m = 4 with the state checked at the end (bf16 in, fp32 out for the 1e-3 bound)."""
-    L0, S0 = cfg2
+    L0, S0 = pool256_35b
     L = Layer(2, 16, 32, 128, io="bf16", out="f32", num_slots=8)
     slots = [L.pool.alloc() for _ in range(4)]
     init = np.stack([S0[s] for s in range(4)]).astype(np.float64)
@@ -112,9 +112,9 @@ def test_decode_cfg2_100_steps_fp32_out(cfg2):
     L.close()
 
 
-def test_decode_batched_equals_single_bitwise(cfg2):
+def test_decode_batched_equals_single_bitwise(pool256_35b):
     """Each slot's output and state at m = 64 equal the same slot run alone (m = 1), bit for bit."""
-    L, S0 = cfg2
+    L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, 64, 256, sub=1)]
     _reset_states(L, S0, slots)
     outs_b = []
@@ -132,9 +132,9 @@ def test_decode_batched_equals_single_bitwise(cfg2):
         assert np.array_equal(Sg, states_b[j][0]) and np.array_equal(Cg, states_b[j][1])
 
 
-def test_decode_deterministic(cfg2):
+def test_decode_deterministic(pool256_35b):
     """The same step twice from the same state gives identical bits."""
-    L, S0 = cfg2
+    L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, 32, 256, sub=2)]
     res = []
     for _ in range(2):

@@ -80,7 +80,7 @@ def test_prefill_from_nonzero_state_and_split_calls():
     L.close()
 
 
-def test_prefill_cfg3_ragged_8_sequences():
+def test_prefill_8_sequences_15998_tokens_35b_layer():
     """Lengths {1,17,300,4095,1024,2048,513,8000} (15 998 tokens), 16/32 heads, d = 128, chunk 64, bf16 io,
     zero initial state; final states handed to 16 decode steps.  The oracle computes 4 sampled v-heads
     (covering both v-heads of one q/k head and the last head)."""
