@@ -12,8 +12,10 @@
 //
 // Kernel shape: persistent CTAs, 8 consumer warps + 1 producer warp.  The producer
 // streams each item's r*D*D fp32 state (contiguous, 128 KiB at D=128, r=2) from HBM
-// into a 4-stage shared-memory ring with 1-D bulk copies (TMA engine) completing on
-// mbarriers; it runs ahead across items.  Consumers fuse the item's conv + SiLU, L2
+// into a shared-memory ring of 16 KiB stages with 1-D bulk copies (TMA engine) completing
+// on mbarriers; it runs ahead across items.  Many items: 4 stages, 3 CTAs per SM.  Few
+// items at D = 128 (all of them in one round of CTAs): 6 stages at 2 CTAs per SM or 8 at
+// 1, so an item's state is in flight at once.  Consumers fuse the item's conv + SiLU, L2
 // norms and gates (while the first stages land), then per S row compute both dot
 // products (S.k, S.q) from one read, apply the rank-1 update and store the new row
 // with 128-bit global stores -- one HBM read and one write of S per step.  The row
@@ -34,7 +36,9 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kStageBytes = 16384;
-constexpr int kStages = 4;
+constexpr int kStages = 4;      // ring depth with 3 CTAs per SM (batches of many items)
+constexpr int kMidStages = 6;   // ring depth with 2 CTAs per SM
+constexpr int kDeepStages = 8;  // ring depth with 1 CTA per SM (an item per SM: the whole item in flight)
 
 struct DecodeArgs {
     const uint64_t* slot_ptrs;
@@ -50,17 +54,18 @@ struct DecodeArgs {
     int stall_producer;  // test hook: the producer fills no stage, so the consumers' waits run out
 };
 
-size_t decode_smem_bytes(int D, int r)
+size_t decode_smem_bytes(int D, int r, int stages)
 {
-    size_t bytes = (size_t)kStages * kStageBytes;     // stage ring
-    bytes += 2 * kStages * sizeof(uint64_t);            // full / empty barriers
+    size_t bytes = (size_t)stages * kStageBytes;      // stage ring
+    bytes += 2 * stages * sizeof(uint64_t);             // full / empty barriers
     bytes += (size_t)(2 * D + 2 * r * D + 3 * r + 4) * sizeof(float);  // qs, ks, vs, obuf, alpha, beta, rms, red
     bytes += 16;                                        // abort flag
     return bytes;
 }
 
-template <int D, typename TIn, typename TOut>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
+template <int D, typename TIn, typename TOut, int STAGES>
+__global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kMidStages ? 2 : 1)
+    decode_kernel(const DecodeArgs A)
 {
     constexpr int LPR = D / 16;    // lanes per S row (16 columns per lane)
     constexpr int RPW = 32 / LPR;  // rows per warp per stage
@@ -68,10 +73,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
+    uint64_t* empty = full + STAGES;
     const int r = A.r;
-    float* qs = reinterpret_cast<float*>(empty + kStages);
+    float* qs = reinterpret_cast<float*>(empty + STAGES);
     float* ks = qs + D;
     float* vs = ks + D;       // [r][D] conv + SiLU v of the item's v-heads
     float* obuf = vs + r * D;  // [r][D] delta-rule output before the norm
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
     const int stages_per_item = (int)((item_bytes + kStageBytes - 1) / kStageBytes);
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
         }
@@ -117,14 +122,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
                     bulk_g2s(ring + slot * kStageBytes, src + (size_t)s * kStageBytes, bytes, &full[slot]);
                     issued |= 1u << slot;
                     last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
-                    if (++slot == kStages) {
+                    if (++slot == STAGES) {
                         slot = 0;
                         phase ^= 1u;
                     }
                 }
             }
             // every issued copy must have landed before the CTA's shared memory goes away
-            for (int i = 0; i < kStages; ++i)
+            for (int i = 0; i < STAGES; ++i)
                 if ((issued >> i) & 1u) mbar_wait_bounded(&full[i], (last_parity >> i) & 1u, nullptr);
         }
         return;
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (++slot == kStages) {
+            if (++slot == STAGES) {
                 slot = 0;
                 phase ^= 1u;
             }
@@ -282,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeArgs A)
     }
 }
 
-template <int D, typename TIn, typename TOut>
+template <int D, typename TIn, typename TOut, int STAGES>
 cudaError_t launch_t(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 {
-    auto kern = decode_kernel<D, TIn, TOut>;
-    const size_t smem = decode_smem_bytes(D, A.r);
+    auto kern = decode_kernel<D, TIn, TOut, STAGES>;
+    const size_t smem = decode_smem_bytes(D, A.r, STAGES);
     // resident CTAs per SM for this instantiation and shared-memory size (cached; calls from
     // several host threads are serialised here)
     static std::mutex mu;
@@ -316,10 +321,18 @@ template <typename TIn, typename TOut>
 cudaError_t launch_d(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 {
     switch (P.shape.dk) {
-        case 16: return launch_t<16, TIn, TOut>(P, A, st);
-        case 32: return launch_t<32, TIn, TOut>(P, A, st);
-        case 64: return launch_t<64, TIn, TOut>(P, A, st);
-        case 128: return launch_t<128, TIn, TOut>(P, A, st);
+        case 16: return launch_t<16, TIn, TOut, kStages>(P, A, st);
+        case 32: return launch_t<32, TIn, TOut, kStages>(P, A, st);
+        case 64: return launch_t<64, TIn, TOut, kStages>(P, A, st);
+        case 128: {
+            // Few items: the deepest ring whose CTAs still take every item in one round (one CTA
+            // per SM with 8 stages, two with 6), so an item's state streams in about one round
+            // trip; otherwise 4 stages and 3 CTAs per SM.  The arithmetic is the same in all.
+            const size_t items = (size_t)A.m * P.shape.hqk;
+            if (items <= (size_t)P.num_sms) return launch_t<128, TIn, TOut, kDeepStages>(P, A, st);
+            if (items <= 2 * (size_t)P.num_sms) return launch_t<128, TIn, TOut, kMidStages>(P, A, st);
+            return launch_t<128, TIn, TOut, kStages>(P, A, st);
+        }
         default: return cudaErrorInvalidValue;
     }
 }

@@ -87,9 +87,11 @@ def _reset_states(L, S0, slots):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("m", [1, 4, 16, 256])
+@pytest.mark.parametrize("m", [1, 4, 8, 16, 256])
 def test_decode_35b_layer_parity(pool256_35b, m):
-    """m active slots at random distinct pool indices; bf16 out vs the oracle on sampled rows."""
+    """m active slots at random distinct pool indices; bf16 out vs the oracle on sampled rows (m = 1,
+    4, 8: one item per SM with an 8-stage ring; m = 16: 6 stages, 2 CTAs per SM; m = 256: 4 stages,
+    3 CTAs per SM)."""
     L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, m, 256)]
     _reset_states(L, S0, slots)
@@ -113,23 +115,29 @@ def test_decode_35b_layer_100_steps_fp32_out(pool256_35b):
 
 
 def test_decode_batched_equals_single_bitwise(pool256_35b):
-    """Each slot's output and state at m = 64 equal the same slot run alone (m = 1), bit for bit."""
+    """Each slot's output and state in a batch equal the same slot run alone (m = 1), bit for bit.
+    The launches differ in shape: m = 1 runs one item per SM with an 8-stage ring, m = 16 two CTAs
+    per SM with 6 stages, m = 64 three CTAs per SM with 4 stages taking several items each."""
     L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, 64, 256, sub=1)]
-    _reset_states(L, S0, slots)
-    outs_b = []
-    for step in range(2):
-        inp = L.decode_inputs(list(range(64)), step)
-        outs_b.append(L.gpu_decode(0, slots, inp).clone())
-    states_b = [L.get_state(0, s) for s in slots[:8]]
+    batched = {}
+    for m in (64, 16):
+        _reset_states(L, S0, slots)
+        outs = []
+        for step in range(2):
+            inp = L.decode_inputs(list(range(m)), step)
+            outs.append(L.gpu_decode(0, slots[:m], inp).clone())
+        batched[m] = (outs, [L.get_state(0, s) for s in slots[:8]])
     _reset_states(L, S0, slots)
     for j, s in enumerate(slots[:8]):
         for step in range(2):
             inp = L.decode_inputs([j], step)
             o = L.gpu_decode(0, [s], inp)
-            assert torch.equal(o[0], outs_b[step][j]), f"slot {s} step {step} output differs"
+            for m, (outs, _) in batched.items():
+                assert torch.equal(o[0], outs[step][j]), f"slot {s} step {step} output differs from the m = {m} batch"
         Sg, Cg = L.get_state(0, s)
-        assert np.array_equal(Sg, states_b[j][0]) and np.array_equal(Cg, states_b[j][1])
+        for m, (_, states) in batched.items():
+            assert np.array_equal(Sg, states[j][0]) and np.array_equal(Cg, states[j][1]), f"slot {s} state vs m = {m}"
 
 
 def test_decode_deterministic(pool256_35b):
