@@ -653,10 +653,10 @@ def run_ours(args):
     }
     algo = M_HEAD * decode_bytes_per_slot_step() + decode_param_bytes()
     ach = algo / (kern_mean * 1e-3) / 1e9
-    result["roofline"] = {"kernel": "decode_kernel<128,bf16,bf16>", "bound": "hbm", "achieved": ach, "peak": hbm,
+    result["roofline"] = {"kernel": "decode_kernel<128,bf16,bf16,4>", "bound": "hbm", "achieved": ach, "peak": hbm,
                           "unit": "GB/s", "frac": ach / hbm, "peak_kind": peak_kind,
                           "frac_of_8TBs": ach / 8000.0,
-                          "traffic": profiled_traffic("decode_kernel<128,bf16,bf16>", DECODE_SOURCES, M_HEAD),
+                          "traffic": profiled_traffic("decode_kernel<128,bf16,bf16,4>", DECODE_SOURCES, M_HEAD),
                           "bytes_per_launch": algo, "launch_ms": kern_mean}
     if ck:
         result["clocks"] = {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
