@@ -533,8 +533,8 @@ def time_proj(torch, binding, reps=20):
     """The layer's projections (16/32 heads, d = 128, hidden 2048, bf16): gdn_in_proj (N = 12 352
     output columns routed to q|k|v|z|a|b) and gdn_out_proj (4096 -> 2048) at the decode batch
     (256 tokens) and the 8-sequence prefill batch (15 998 tokens).  Device time per call (mean over
-    `reps` back-to-back calls on the current stream), with torch.matmul (cuBLAS) on the same
-    product timed beside it for context."""
+    `reps` calls replayed from a CUDA graph), with torch.matmul (cuBLAS) on the same product timed
+    the same way beside it for context."""
     sh = binding.GdnShape(hqk=HQK, hv=HV, dk=D, dv=D, conv_w=W, chunk=64, io_dtype=1, out_dtype=1, l2_eps=1e-6,
                           norm_eps=1e-6, max_prefill_tokens=0)
     hidden = 2048
@@ -543,16 +543,27 @@ def time_proj(torch, binding, reps=20):
     stream = torch.cuda.current_stream()
 
     def mean_ms(fn, tag=None):
-        for _ in range(3):
-            fn()
+        """Device time per call: `reps` calls captured in a CUDA graph and replayed, so that the
+        host's per-call marshalling (tens of µs from Python) does not pace the small calls."""
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for _ in range(3):
+                fn(cap)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(reps):
+                fn(cap)
+        graph.replay()  # warm replay
+        torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
         if tag:
             torch.cuda.nvtx.range_push(tag)
         a.record(stream)
-        for _ in range(reps):
-            fn()
+        graph.replay()
         b.record(stream)
         torch.cuda.synchronize()
         if tag:
@@ -569,14 +580,14 @@ def time_proj(torch, binding, reps=20):
         o = {n: torch.empty((T, w), dtype=torch.bfloat16, device="cuda")
              for n, w in (("q", Dq), ("k", Dq), ("v", Dv), ("z", Dv), ("a", HV), ("b", HV))}
         y_ref = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
-        ms = mean_ms(lambda: binding.in_proj(sh, hidden, T, x, w_in, o["q"], o["k"], o["v"], o["z"], o["a"],
-                                             o["b"], stream=stream), tag=f"proj_timed_in_{T}")
-        ms_cb = mean_ms(lambda: torch.matmul(x, w_in.t(), out=y_ref))
+        ms = mean_ms(lambda s: binding.in_proj(sh, hidden, T, x, w_in, o["q"], o["k"], o["v"], o["z"], o["a"],
+                                               o["b"], stream=s), tag=f"proj_timed_in_{T}")
+        ms_cb = mean_ms(lambda s: torch.matmul(x, w_in.t(), out=y_ref))
         out.append(("in_proj", T, N, hidden, ms, ms_cb))
         ov = torch.randn((T, Dv), generator=g, device="cuda").to(torch.bfloat16)
         y = torch.empty((T, hidden), dtype=torch.bfloat16, device="cuda")
-        ms = mean_ms(lambda: binding.out_proj(sh, hidden, T, ov, w_out, y, stream=stream), tag=f"proj_timed_out_{T}")
-        ms_cb = mean_ms(lambda: torch.matmul(ov, w_out.t(), out=y))
+        ms = mean_ms(lambda s: binding.out_proj(sh, hidden, T, ov, w_out, y, stream=s), tag=f"proj_timed_out_{T}")
+        ms_cb = mean_ms(lambda s: torch.matmul(ov, w_out.t(), out=y))
         out.append(("out_proj", T, hidden, Dv, ms, ms_cb))
         del x, o, y_ref, ov, y
     return out

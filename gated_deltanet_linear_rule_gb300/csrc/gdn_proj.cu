@@ -363,6 +363,148 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
     if (warp == 1) tc::dealloc_pair(tm, 512);
 }
 
+// ---- split-K kernel: few tiles (small T), each tile's K range shared by a cluster of KS CTAs ----
+// CTA r of a cluster accumulates K slices r * KT/KS .. into its own 256 TMEM columns (a
+// single-CTA 128 x 256 tile, as proj_kernel).  The partial sums are then reduce-scattered
+// through distributed shared memory: CTA g owns the output columns g * 256/KS .. of the tile,
+// every other CTA sends it that column group of its partial (st.async into the ring, free by
+// then), and CTA g adds the KS partials in rank order and stores its columns.
+template <int KS>
+__global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constant__ ProjArgs P,
+                                                              const __grid_constant__ ProjMaps T)
+{
+    constexpr int GW = BN / KS;         // columns of the group a CTA owns
+    constexpr int RS = GW + 4;          // padded row stride (floats) of a received partial
+    constexpr uint32_t SLOT = 128u * RS * 4u;
+    static_assert((KS - 1) * SLOT <= BAR_OFF, "received partials fit the stage ring");
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR_OFF);  // [STAGES]
+    uint64_t* empty = full + STAGES;                             // [STAGES]
+    uint64_t* accf = empty + STAGES;                             // accumulator complete
+    uint64_t* red = accf + 1;                                    // the other CTAs' partials landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
+    float* recv = reinterpret_cast<float*>(sm);                  // [KS - 1][128][RS] over the ring
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = (int)cluster_ctarank(), tile = (int)blockIdx.x / KS;
+    const int tiles_n = (P.N + BN - 1) / BN;
+    const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;
+    const int kper = (P.K / BK) / KS, kt0 = rank * kper;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        mbar_init(red, 1);
+        mbar_arrive_expect_tx(red, (uint32_t)(KS - 1) * 128u * GW * 4u);
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::alloc(tmem_slot, 256);
+    tc::fence_before_sync();
+    cluster_sync_all();  // every CTA's barriers exist before any partial is sent
+    tc::fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+
+    bool got = true;
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < kper; ++i) {
+                const int s = i % STAGES;
+                const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, nullptr)) {
+                    atomicOr(P.status, GDN_DEV_TIMEOUT);
+                    break;
+                }
+                unsigned char* st = sm + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                tma_load(st, &T.a, (kt0 + i) * BK, m0, &full[s]);
+                tma_load(st + A_BYTES, &T.b, (kt0 + i) * BK, n0, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < kper; ++i) {
+                const int s = i % STAGES;
+                const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+                if (ok && !mbar_wait_bounded(&full[s], ph, nullptr)) {
+                    atomicOr(P.status, GDN_DEV_TIMEOUT);
+                    ok = false;
+                }
+                tc::fence_after_sync();
+                unsigned char* st = sm + s * STAGE_BYTES;
+                if (ok)
+                    tc::mma_k(tm, smem_addr(st), BM, smem_addr(st + A_BYTES), BN, BK, tc::idesc_bf16(BM, BN), i > 0);
+                tc::commit(&empty[s]);
+            }
+            tc::commit(accf);
+        }
+    } else {
+        got = mbar_wait_bounded(accf, 0, nullptr);
+        if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
+    }
+    // every CTA's products are done (its stage ring is free for the partials of the others)
+    tc::fence_before_sync();
+    cluster_sync_all();
+    tc::fence_after_sync();
+    if (warp >= 2) {
+        const int row = (warp & 3) * 32 + lane, m = m0 + row;
+        // send: column group g of this CTA's partial to CTA g (slot r, or r - 1 past g)
+        for (int g = 0; g < KS; ++g) {
+            if (g == rank) continue;
+            const uint32_t slot = (uint32_t)(rank < g ? rank : rank - 1);
+            const uint32_t dst = map_to_rank(smem_addr(recv) + slot * SLOT + (uint32_t)row * RS * 4u, (uint32_t)g);
+            const uint32_t bar = map_to_rank(smem_addr(red), (uint32_t)g);
+#pragma unroll
+            for (int c0 = 0; c0 < GW; c0 += 32) {
+                float v[32];
+                tc::ld32(tc::taddr(tm, warp, g * GW + c0), v);  // whole warp
+                tc::wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_async_cluster_v4(dst + (uint32_t)(c0 + 4 * q) * 4u,
+                                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]), bar);
+            }
+        }
+        // receive the others' partials of this CTA's group, add all KS in rank order, store
+        const bool gotr = mbar_wait_cluster_bounded(red, 0);
+        if (!gotr && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
+#pragma unroll
+        for (int c0 = 0; c0 < GW; c0 += 32) {
+            float own[32], v[32];
+            tc::ld32(tc::taddr(tm, warp, rank * GW + c0), own);  // whole warp
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+            for (int k = 0; k < KS; ++k) {
+                if (k == rank) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] += own[e];
+                } else {
+                    const float* src = recv + (size_t)(k < rank ? k : k - 1) * (128 * RS) + (size_t)row * RS + c0;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 t = *reinterpret_cast<const float4*>(src + 4 * q);
+                        v[4 * q] += t.x;
+                        v[4 * q + 1] += t.y;
+                        v[4 * q + 2] += t.z;
+                        v[4 * q + 3] += t.w;
+                    }
+                }
+            }
+            const int n = n0 + rank * GW + c0;
+            if (got && gotr && m < P.M && n < P.N) store_cols(P, m, n, v);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::dealloc(tm, 256);
+    cluster_sync_all();  // no CTA leaves while its partials may still be in flight to the others
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -390,6 +532,39 @@ cudaError_t encode_kmajor(CUtensorMap* m, const void* base, int k, int rows, int
 
 __device__ unsigned int g_proj_status;  // status word of calls that pass none
 
+// clusters of c split-K CTAs resident at once (c = 2, 4, 8; cached; 0 when the query fails)
+int split_clusters(int c)
+{
+    static std::mutex mu;
+    static int cached[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[c] < 0) {
+        auto kern = c == 8 ? proj_splitk_kernel<8> : c == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
+        int n = 0;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)(c * 16));
+            cfg.blockDim = dim3(PT);
+            cfg.dynamicSmemBytes = PROJ_SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        }
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        cached[c] = n;
+    }
+    return cached[c];
+}
+
 cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const Seg* seg, int nseg,
                         unsigned int* status, cudaStream_t st)
 {
@@ -401,11 +576,21 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     P.K = K;
     P.nseg = nseg;
     P.status = status;
-    if (!P.status) {
-        void* addr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&addr, g_proj_status);
+    if (!P.status) {  // the library's own word on this device (address looked up once per device)
+        static std::mutex mu;
+        static unsigned int* addr[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        P.status = static_cast<unsigned int*>(addr);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!addr[dev]) {
+            void* a_ = nullptr;
+            e = cudaGetSymbolAddress(&a_, g_proj_status);
+            if (e != cudaSuccess) return e;
+            addr[dev] = static_cast<unsigned int*>(a_);
+        }
+        P.status = addr[dev];
     }
     for (int i = 0; i < nseg; ++i) P.seg[i] = seg[i];
     cudaError_t e = cudaSuccess;
@@ -445,6 +630,43 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
         }
         num_sms = cached_sms;
         num_pairs = cached_pairs;
+    }
+    // Few tiles (small T): split each tile's K range over a cluster of KS CTAs when at least
+    // two CTAs per tile fit on the GPU at once (KS dividing the K slices, every cluster resident).
+    {
+        const long tiles1 = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+        const int KT = K / BK;
+        int ks = 0;
+        for (int c : {8, 4, 2}) {
+            if (tiles1 * c > num_sms || KT % c != 0) continue;
+            if (split_clusters(c) < tiles1) continue;
+            ks = c;
+            break;
+        }
+        if (ks) {
+            ProjMaps T;
+            memset(&T, 0, sizeof(T));
+            e = encode_kmajor(&T.a, a, K, M, BM);
+            if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, BN);
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)ks;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)(tiles1 * ks));
+            cfg.blockDim = dim3(PT);
+            cfg.dynamicSmemBytes = PROJ_SMEM;
+            cfg.stream = st;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = ks == 8 ? cudaLaunchKernelEx(&cfg, proj_splitk_kernel<8>, P, T)
+                : ks == 4 ? cudaLaunchKernelEx(&cfg, proj_splitk_kernel<4>, P, T)
+                          : cudaLaunchKernelEx(&cfg, proj_splitk_kernel<2>, P, T);
+            if (e != cudaSuccess) return e;
+            return cudaGetLastError();
+        }
     }
     // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
     // CTA pairs (256 x 256 tiles, half the operand traffic per SM); the pairs are used unless they
