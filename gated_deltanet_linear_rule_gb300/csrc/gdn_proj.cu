@@ -224,11 +224,16 @@ __global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ Pro
 // TMEM.  Per output element each SM thus streams half the operand bytes of the single-CTA
 // kernel.  The even CTA's warp 1 issues the MMAs; the odd CTA's copies complete on the even
 // CTA's full barriers, and the MMA commits arrive on the stage and accumulator barriers of both.
+// The tile width BNP is 256, or 192 where that puts more SMs to work (each CTA then holds 128
+// or 96 rows of B).
 constexpr int STAGES2 = 6;
-constexpr uint32_t HALF_BYTES = 128 * BK * 2;      // 128 rows of a 64-wide K slice
-constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;  // this CTA's A rows + B rows
-constexpr uint32_t BAR2_OFF = STAGES2 * STAGE2_BYTES;
-constexpr size_t PROJ2_SMEM = BAR2_OFF + 256 + 1024;
+constexpr uint32_t A2_BYTES = 128 * BK * 2;  // this CTA's 128 A rows of a 64-wide K slice
+template <int BNP> struct PairCfg {
+    static constexpr uint32_t B_BYTES = (BNP / 2) * BK * 2;  // this CTA's B rows
+    static constexpr uint32_t STAGE = A2_BYTES + B_BYTES;     // a multiple of 1024
+    static constexpr uint32_t BAR_OFF = STAGES2 * STAGE;
+    static constexpr size_t SMEM = BAR_OFF + 256 + 1024;
+};
 
 // 2-D tile copy whose completion may be counted on the mbarrier of the other CTA of the pair
 // (bar is a shared::cluster address)
@@ -246,12 +251,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
+template <int BNP>
 __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant__ ProjArgs P,
                                                             const __grid_constant__ ProjMaps T)
 {
+    using C = PairCfg<BNP>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR2_OFF);  // [STAGES2] both CTAs' slices landed (even CTA)
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::BAR_OFF);  // [STAGES2] both CTAs' slices landed (even CTA)
     uint64_t* empty = full + STAGES2;                             // [STAGES2] slice consumed by the MMAs
     uint64_t* accf = empty + STAGES2;                             // [2] accumulator complete
     uint64_t* acce = accf + 2;                                    // [2] accumulator read out, 8 warps (even CTA)
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
     const uint32_t rank = cluster_ctarank();
     const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
     const int KT = P.K / BK;
-    const int tiles_n = (P.N + 255) / 256, tiles = tiles_n * ((P.M + 255) / 256);
+    const int tiles_n = (P.N + BNP - 1) / BNP, tiles = tiles_n * ((P.M + 255) / 256);
 
     if (tid == 0) {
         for (int s = 0; s < STAGES2; ++s) {
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
             int it = 0;
             bool ok = true;
             for (int t = pair; t < tiles && ok; t += npairs) {
-                const int n0 = (t % tiles_n) * 256 + 128 * (int)rank, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
+                const int n0 = (t % tiles_n) * BNP + (BNP / 2) * (int)rank, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
                 for (int kt = 0; kt < KT; ++kt, ++it) {
                     const int s = it % STAGES2;
                     const uint32_t ph = (uint32_t)((it / STAGES2) & 1);
@@ -296,11 +303,11 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
                         ok = false;
                         break;
                     }
-                    unsigned char* st = sm + s * STAGE2_BYTES;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * STAGE2_BYTES);
+                    unsigned char* st = sm + s * C::STAGE;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
                     const uint32_t fb = full0 + (uint32_t)(s * 8);
                     tma_load_pair(st, &T.a, kt * BK, m0, fb);
-                    tma_load_pair(st + HALF_BYTES, &T.b, kt * BK, n0, fb);
+                    tma_load_pair(st + A2_BYTES, &T.b, kt * BK, n0, fb);
                 }
             }
         }
@@ -325,10 +332,10 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
                         ok = false;
                     }
                     tc::fence_after_sync();
-                    unsigned char* st = sm + s * STAGE2_BYTES;
+                    unsigned char* st = sm + s * C::STAGE;
                     if (ok)
-                        tc::mma_pair_k64(tm + 256 * ab, smem_addr(st), smem_addr(st + HALF_BYTES),
-                                         tc::idesc_bf16(256, 256), kt > 0);
+                        tc::mma_pair_k64(tm + 256 * ab, smem_addr(st), smem_addr(st + A2_BYTES),
+                                         tc::idesc_bf16(256, BNP), kt > 0);
                     tc::commit_pair_mc(&empty[s], 0x3);
                 }
                 tc::commit_pair_mc(&accf[ab], 0x3);
@@ -340,12 +347,12 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
         int i = 0;
         for (int t = pair; t < tiles; t += npairs, ++i) {
             const int ab = i & 1;
-            const int n0 = (t % tiles_n) * 256, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
+            const int n0 = (t % tiles_n) * BNP, m0 = (t / tiles_n) * 256 + 128 * (int)rank;
             const bool got = mbar_wait_cluster_bounded(&accf[ab], (uint32_t)((i >> 1) & 1));
             if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
             tc::fence_after_sync();
             const int m = m0 + (warp & 3) * 32 + lane;
-            for (int c0 = 0; c0 < 256; c0 += 32) {
+            for (int c0 = 0; c0 < BNP; c0 += 32) {
                 float v[32];
                 tc::ld32(tc::taddr(tm + 256 * ab, warp, c0), v);  // whole warp
                 tc::wait_ld();
@@ -608,8 +615,11 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(proj_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)PROJ2_SMEM);
+                e = cudaFuncSetAttribute(proj_pair_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PairCfg<256>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(proj_pair_kernel<192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PairCfg<192>::SMEM);
             if (e == cudaSuccess) {
                 cudaLaunchConfig_t cfg = {};
                 cudaLaunchAttribute attr[1];
@@ -619,10 +629,10 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
                 attr[0].val.clusterDim.z = 1;
                 cfg.gridDim = dim3(2 * (unsigned)(sms / 2));
                 cfg.blockDim = dim3(PT);
-                cfg.dynamicSmemBytes = PROJ2_SMEM;
+                cfg.dynamicSmemBytes = PairCfg<256>::SMEM;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                e = cudaOccupancyMaxActiveClusters(&pairs, proj_pair_kernel, &cfg);
+                e = cudaOccupancyMaxActiveClusters(&pairs, proj_pair_kernel<256>, &cfg);
             }
             if (e != cudaSuccess) return e;
             cached_sms = sms;
@@ -670,32 +680,36 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     }
     // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
     // CTA pairs (256 x 256 tiles, half the operand traffic per SM); the pairs are used unless they
-    // need more rounds over the tiles than single CTAs do (a few rows past a multiple of 256)
+    // need more rounds over the tiles than single CTAs do (a few rows past a multiple of 256).
+    // When the pairs' tiles take a single round, 256 x 192 tiles put more SMs to work, each on
+    // three quarters of the products, if they still take a single round.
     const long tiles1 = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
     const long tiles2 = (long)((N + 255) / 256) * ((M + 255) / 256);
+    const long tiles3 = (long)((N + 191) / 192) * ((M + 255) / 256);
     const long rounds1 = (tiles1 + num_sms - 1) / num_sms;
     const long rounds2 = num_pairs > 0 ? (tiles2 + num_pairs - 1) / num_pairs : rounds1 + 1;
-    const bool pairs = rounds2 <= rounds1;
-    // A is read 128 rows at a time on both paths; B 256 rows per CTA, or 128 per CTA of a pair
+    const int bnp = rounds2 > rounds1 ? 0 : (rounds2 == 1 && tiles3 <= num_pairs && tiles3 > tiles2) ? 192 : 256;
+    // A is read 128 rows at a time on every path; B 256 rows per CTA, or bnp / 2 per CTA of a pair
     ProjMaps T;
     memset(&T, 0, sizeof(T));
     e = encode_kmajor(&T.a, a, K, M, 128);
-    if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, pairs ? 128 : BN);
+    if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, bnp ? bnp / 2 : BN);
     if (e != cudaSuccess) return e;
-    if (pairs) {
+    if (bnp) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (unsigned)std::min<long>(tiles2, num_pairs));
+        cfg.gridDim = dim3(2 * (unsigned)std::min<long>(bnp == 256 ? tiles2 : tiles3, num_pairs));
         cfg.blockDim = dim3(PT);
-        cfg.dynamicSmemBytes = PROJ2_SMEM;
+        cfg.dynamicSmemBytes = bnp == 256 ? PairCfg<256>::SMEM : PairCfg<192>::SMEM;
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, proj_pair_kernel, P, T);
+        e = bnp == 256 ? cudaLaunchKernelEx(&cfg, proj_pair_kernel<256>, P, T)
+                       : cudaLaunchKernelEx(&cfg, proj_pair_kernel<192>, P, T);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -61,11 +61,11 @@ def test_in_proj_small_shapes(hqk, hv, d, hidden, T):
 
 @pytest.mark.parametrize("T", [256, 300, 1100, 2100])
 def test_in_proj_35b_layer_shape(T):
-    """16 q/k and 32 v heads, d = 128, hidden 2048: N = 12 352 columns in 49 tiles of 256 (the last 64
-    wide: a | b), K = 32 slices.  T = 256 (the decode batch) and 2100 run on CTA pairs (256-row tiles;
-    at 2100 each pair takes several tiles in turn and the last tile's second CTA holds no valid row);
-    300 and 1100 fall a few rows past a multiple of 256 and run on single CTAs (128-row tiles, at
-    1100 several per CTA)."""
+    """16 q/k and 32 v heads, d = 128, hidden 2048: N = 12 352 columns, K = 32 slices.  T = 256 (the
+    decode batch) runs on CTA pairs with 256 x 192 tiles (one round), 2100 on pairs with 256 x 256
+    tiles (each pair takes several in turn, and the last tile's second CTA holds no valid row); 300
+    and 1100 fall a few rows past a multiple of 256 and run on single CTAs (128-row tiles, at 1100
+    several per CTA).  The small shapes above take split-K clusters or 192-wide pairs."""
     _in_proj_case(16, 32, 128, 2048, T, seed=T)
 
 
