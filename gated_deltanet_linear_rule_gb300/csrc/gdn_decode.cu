@@ -13,9 +13,9 @@
 // Kernel shape: persistent CTAs, 8 consumer warps + 1 producer warp.  The producer
 // streams each item's r*D*D fp32 state (contiguous, 128 KiB at D=128, r=2) from HBM
 // into a shared-memory ring of 16 KiB stages with 1-D bulk copies (TMA engine) completing
-// on mbarriers; it runs ahead across items.  Many items: 4 stages, 3 CTAs per SM.  Few
-// items at D = 128 (all of them in one round of CTAs): 6 stages at 2 CTAs per SM or 8 at
-// 1, so an item's state is in flight at once.  Consumers fuse the item's conv + SiLU, L2
+// on mbarriers; it runs ahead across items.  Many items: 4 stages, 3 CTAs per SM.  Fewer
+// items at D = 128: 6 stages at 2 CTAs per SM, or 8 at 1 when each item has an SM of its
+// own, so that more of an item's state is in flight at once.  Consumers fuse the item's conv + SiLU, L2
 // norms and gates (while the first stages land), then per S row compute both dot
 // products (S.k, S.q) from one read, apply the rank-1 update and store the new row
 // with 128-bit global stores -- one HBM read and one write of S per step.  The row
@@ -325,12 +325,13 @@ cudaError_t launch_d(const Pool& P, const DecodeArgs& A, cudaStream_t st)
         case 32: return launch_t<32, TIn, TOut, kStages>(P, A, st);
         case 64: return launch_t<64, TIn, TOut, kStages>(P, A, st);
         case 128: {
-            // Few items: the deepest ring whose CTAs still take every item in one round (one CTA
-            // per SM with 8 stages, two with 6), so an item's state streams in about one round
-            // trip; otherwise 4 stages and 3 CTAs per SM.  The arithmetic is the same in all.
+            // Ring depth by batch size (measured at 16 q/k heads): an item per SM -> 8 stages at
+            // 1 CTA per SM, so an item's state streams in about one round trip; up to 8 items per
+            // SM -> 6 stages at 2 CTAs per SM (m = 16 / 32 / 64: 12.4 -> 10.6, 24.4 -> 20.8,
+            // 56.2 -> 53.7 us); more -> 4 stages at 3 CTAs per SM.  The arithmetic is the same.
             const size_t items = (size_t)A.m * P.shape.hqk;
             if (items <= (size_t)P.num_sms) return launch_t<128, TIn, TOut, kDeepStages>(P, A, st);
-            if (items <= 2 * (size_t)P.num_sms) return launch_t<128, TIn, TOut, kMidStages>(P, A, st);
+            if (items <= 8 * (size_t)P.num_sms) return launch_t<128, TIn, TOut, kMidStages>(P, A, st);
             return launch_t<128, TIn, TOut, kStages>(P, A, st);
         }
         default: return cudaErrorInvalidValue;

@@ -91,7 +91,7 @@ def _reset_states(L, S0, slots):
 def test_decode_35b_layer_parity(pool256_35b, m):
     """m active slots at random distinct pool indices; bf16 out vs the oracle on sampled rows (m = 1,
     4, 8: one item per SM with an 8-stage ring; m = 16: 6 stages, 2 CTAs per SM; m = 256: 4 stages,
-    3 CTAs per SM)."""
+    3 CTAs per SM taking several items each)."""
     L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, m, 256)]
     _reset_states(L, S0, slots)
@@ -116,12 +116,12 @@ def test_decode_35b_layer_100_steps_fp32_out(pool256_35b):
 
 def test_decode_batched_equals_single_bitwise(pool256_35b):
     """Each slot's output and state in a batch equal the same slot run alone (m = 1), bit for bit.
-    The launches differ in shape: m = 1 runs one item per SM with an 8-stage ring, m = 16 two CTAs
-    per SM with 6 stages, m = 64 three CTAs per SM with 4 stages taking several items each."""
+    The launches differ in shape: m = 1 runs one item per SM with an 8-stage ring, m = 64 two CTAs
+    per SM with 6 stages, m = 256 three CTAs per SM with 4 stages, each CTA taking several items."""
     L, S0 = pool256_35b
-    slots = [int(s) for s in synth.distinct_slots(2, 64, 256, sub=1)]
+    slots = [int(s) for s in synth.distinct_slots(2, 256, 256, sub=1)]
     batched = {}
-    for m in (64, 16):
+    for m in (256, 64):
         _reset_states(L, S0, slots)
         outs = []
         for step in range(2):
