@@ -373,25 +373,37 @@ __global__ void __launch_bounds__(PT, 1) proj_pair_kernel(const __grid_constant_
 // ---- split-K kernel: few tiles (small T), each tile's K range shared by a cluster of KS CTAs ----
 // CTA r of a cluster accumulates K slices r * KT/KS .. into its own 256 TMEM columns (a
 // single-CTA 128 x 256 tile, as proj_kernel).  The partial sums are then reduce-scattered
-// through distributed shared memory: CTA g owns the output columns g * 256/KS .. of the tile,
-// every other CTA sends it that column group of its partial (st.async into the ring, free by
-// then), and CTA g adds the KS partials in rank order and stores its columns.
+// through distributed shared memory: CTA g owns the output columns g * 256/KS .. of the tile.
+// Each CTA writes the other groups of its partial into its (by then free) stage ring and sends
+// each to its owner with one bulk copy; the owner adds the KS partials in rank order and
+// stores its columns.  A group is [128 rows][GW floats] with the 16-B chunks of row i at
+// chunk position c ^ (i % 8), so that both the row-wise writes and reads are conflict-free.
+// bulk copy of `bytes` from this CTA's shared memory to another CTA's (dst and its mbarrier as
+// shared::cluster addresses), completing on that mbarrier; 16-B aligned, a multiple of 16 bytes
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(smem_addr(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 template <int KS>
 __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constant__ ProjArgs P,
                                                               const __grid_constant__ ProjMaps T)
 {
-    constexpr int GW = BN / KS;         // columns of the group a CTA owns
-    constexpr int RS = GW + 4;          // padded row stride (floats) of a received partial
-    constexpr uint32_t SLOT = 128u * RS * 4u;
-    static_assert((KS - 1) * SLOT <= BAR_OFF, "received partials fit the stage ring");
+    constexpr int GW = BN / KS;                // columns of the group a CTA owns
+    constexpr uint32_t GROUP = 128u * GW * 4u;  // bytes of one group of a partial
+    static_assert(2 * (KS - 1) * GROUP <= BAR_OFF, "sent and received groups fit the stage ring");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + BAR_OFF);  // [STAGES]
     uint64_t* empty = full + STAGES;                             // [STAGES]
     uint64_t* accf = empty + STAGES;                             // accumulator complete
-    uint64_t* red = accf + 1;                                    // the other CTAs' partials landed
+    uint64_t* red = accf + 1;                                    // the other CTAs' groups landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
-    float* recv = reinterpret_cast<float*>(sm);                  // [KS - 1][128][RS] over the ring
+    unsigned char* recv = sm;                                    // [KS - 1] groups received, by sender
+    unsigned char* sendb = sm + (KS - 1) * GROUP;                // [KS - 1] groups to send, by owner
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)cluster_ctarank(), tile = (int)blockIdx.x / KS;
@@ -406,12 +418,12 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
         }
         mbar_init(accf, 1);
         mbar_init(red, 1);
-        mbar_arrive_expect_tx(red, (uint32_t)(KS - 1) * 128u * GW * 4u);
+        mbar_arrive_expect_tx(red, (uint32_t)(KS - 1) * GROUP);
         fence_mbar_init();
     }
     if (warp == 1) tc::alloc(tmem_slot, 256);
     tc::fence_before_sync();
-    cluster_sync_all();  // every CTA's barriers exist before any partial is sent
+    cluster_sync_all();  // every CTA's barriers exist before any group is sent
     tc::fence_after_sync();
     const uint32_t tm = *tmem_slot;
 
@@ -453,30 +465,39 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
         got = mbar_wait_bounded(accf, 0, nullptr);
         if (!got && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
     }
-    // every CTA's products are done (its stage ring is free for the partials of the others)
+    // every CTA's products are done (its stage ring is free for the groups)
     tc::fence_before_sync();
     cluster_sync_all();
     tc::fence_after_sync();
     if (warp >= 2) {
         const int row = (warp & 3) * 32 + lane, m = m0 + row;
-        // send: column group g of this CTA's partial to CTA g (slot r, or r - 1 past g)
+        // this CTA's partial of every other group -> the send area, swizzled rows
         for (int g = 0; g < KS; ++g) {
             if (g == rank) continue;
-            const uint32_t slot = (uint32_t)(rank < g ? rank : rank - 1);
-            const uint32_t dst = map_to_rank(smem_addr(recv) + slot * SLOT + (uint32_t)row * RS * 4u, (uint32_t)g);
-            const uint32_t bar = map_to_rank(smem_addr(red), (uint32_t)g);
+            unsigned char* dst = sendb + (g < rank ? g : g - 1) * GROUP + (size_t)row * GW * 4;
 #pragma unroll
             for (int c0 = 0; c0 < GW; c0 += 32) {
                 float v[32];
                 tc::ld32(tc::taddr(tm, warp, g * GW + c0), v);  // whole warp
                 tc::wait_ld();
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_async_cluster_v4(dst + (uint32_t)(c0 + 4 * q) * 4u,
-                                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]), bar);
+                for (int q = 0; q < 8; ++q) {
+                    const int c = c0 / 4 + q;  // 16-B chunk of the row
+                    *reinterpret_cast<float4*>(dst + ((c ^ (row & 7)) << 4)) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
             }
         }
-        // receive the others' partials of this CTA's group, add all KS in rank order, store
+        tc::fence_proxy_async();  // the rows are read by the bulk copies
+        named_bar_sync(1, 128);   // the four epilogue warps
+        if (tid == 64)
+            for (int g = 0; g < KS; ++g) {
+                if (g == rank) continue;
+                const uint32_t slot = (uint32_t)(rank < g ? rank : rank - 1);
+                bulk_s2cluster(map_to_rank(smem_addr(recv) + slot * GROUP, (uint32_t)g),
+                               sendb + (g < rank ? g : g - 1) * GROUP, GROUP, map_to_rank(smem_addr(red), (uint32_t)g));
+            }
+        // the others' partials of this CTA's group: add all KS in rank order, store
         const bool gotr = mbar_wait_cluster_bounded(red, 0);
         if (!gotr && lane == 0) atomicOr(P.status, GDN_DEV_TIMEOUT);
 #pragma unroll
@@ -491,10 +512,11 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] += own[e];
                 } else {
-                    const float* src = recv + (size_t)(k < rank ? k : k - 1) * (128 * RS) + (size_t)row * RS + c0;
+                    const unsigned char* src = recv + (k < rank ? k : k - 1) * GROUP + (size_t)row * GW * 4;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const float4 t = *reinterpret_cast<const float4*>(src + 4 * q);
+                        const int c = c0 / 4 + q;
+                        const float4 t = *reinterpret_cast<const float4*>(src + ((c ^ (row & 7)) << 4));
                         v[4 * q] += t.x;
                         v[4 * q + 1] += t.y;
                         v[4 * q + 2] += t.z;
@@ -509,7 +531,7 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) tc::dealloc(tm, 256);
-    cluster_sync_all();  // no CTA leaves while its partials may still be in flight to the others
+    cluster_sync_all();  // no CTA leaves while its groups may still be read by the copies to the others
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -539,35 +561,61 @@ cudaError_t encode_kmajor(CUtensorMap* m, const void* base, int k, int rows, int
 
 __device__ unsigned int g_proj_status;  // status word of calls that pass none
 
-// clusters of c split-K CTAs resident at once (c = 2, 4, 8; cached; 0 when the query fails)
+using ProjKernel = void (*)(ProjArgs, ProjMaps);
+
+// launch configuration: `grid` CTAs of PT threads in clusters of `cluster` along x (grid a
+// multiple of it), `smem` bytes of dynamic shared memory each
+cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, unsigned grid, unsigned cluster, size_t smem,
+                                  cudaStream_t st)
+{
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(PT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// clusters of `cluster` CTAs of `kern` that can be resident at once (0 when the query fails)
+int resident_clusters(ProjKernel kern, unsigned cluster, size_t smem)
+{
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_config(attr, cluster * 16, cluster, smem, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+cudaError_t launch_clusters(ProjKernel kern, unsigned grid, unsigned cluster, size_t smem, cudaStream_t st,
+                            const ProjArgs& P, const ProjMaps& T)
+{
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_config(attr, grid, cluster, smem, st);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, P, T);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// clusters of c split-K CTAs resident at once (c = 2 or 4; cached; 0 when the query fails)
 int split_clusters(int c)
 {
     static std::mutex mu;
     static int cached[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
     std::lock_guard<std::mutex> lock(mu);
     if (cached[c] < 0) {
-        auto kern = c == 8 ? proj_splitk_kernel<8> : c == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
-        int n = 0;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
-        if (e == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)c;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3((unsigned)(c * 16));
-            cfg.blockDim = dim3(PT);
-            cfg.dynamicSmemBytes = PROJ_SMEM;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        }
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            n = 0;
-        }
-        cached[c] = n;
+        const ProjKernel kern = c == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
+        cached[c] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM) == cudaSuccess
+                        ? resident_clusters(kern, (unsigned)c, PROJ_SMEM)
+                        : 0;
+        (void)cudaGetLastError();
     }
     return cached[c];
 }
@@ -620,20 +668,7 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(proj_pair_kernel<192>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PairCfg<192>::SMEM);
-            if (e == cudaSuccess) {
-                cudaLaunchConfig_t cfg = {};
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.gridDim = dim3(2 * (unsigned)(sms / 2));
-                cfg.blockDim = dim3(PT);
-                cfg.dynamicSmemBytes = PairCfg<256>::SMEM;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                e = cudaOccupancyMaxActiveClusters(&pairs, proj_pair_kernel<256>, &cfg);
-            }
+            if (e == cudaSuccess) pairs = resident_clusters(proj_pair_kernel<256>, 2, PairCfg<256>::SMEM);
             if (e != cudaSuccess) return e;
             cached_sms = sms;
             cached_pairs = pairs;
@@ -647,7 +682,7 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
         const long tiles1 = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
         const int KT = K / BK;
         int ks = 0;
-        for (int c : {8, 4, 2}) {
+        for (int c : {4, 2}) {
             if (tiles1 * c > num_sms || KT % c != 0) continue;
             if (split_clusters(c) < tiles1) continue;
             ks = c;
@@ -659,23 +694,8 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
             e = encode_kmajor(&T.a, a, K, M, BM);
             if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, BN);
             if (e != cudaSuccess) return e;
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)ks;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3((unsigned)(tiles1 * ks));
-            cfg.blockDim = dim3(PT);
-            cfg.dynamicSmemBytes = PROJ_SMEM;
-            cfg.stream = st;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            e = ks == 8 ? cudaLaunchKernelEx(&cfg, proj_splitk_kernel<8>, P, T)
-                : ks == 4 ? cudaLaunchKernelEx(&cfg, proj_splitk_kernel<4>, P, T)
-                          : cudaLaunchKernelEx(&cfg, proj_splitk_kernel<2>, P, T);
-            if (e != cudaSuccess) return e;
-            return cudaGetLastError();
+            const ProjKernel kern = ks == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
+            return launch_clusters(kern, (unsigned)(tiles1 * ks), (unsigned)ks, PROJ_SMEM, st, P, T);
         }
     }
     // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
@@ -696,22 +716,9 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, bnp ? bnp / 2 : BN);
     if (e != cudaSuccess) return e;
     if (bnp) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (unsigned)std::min<long>(bnp == 256 ? tiles2 : tiles3, num_pairs));
-        cfg.blockDim = dim3(PT);
-        cfg.dynamicSmemBytes = bnp == 256 ? PairCfg<256>::SMEM : PairCfg<192>::SMEM;
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = bnp == 256 ? cudaLaunchKernelEx(&cfg, proj_pair_kernel<256>, P, T)
-                       : cudaLaunchKernelEx(&cfg, proj_pair_kernel<192>, P, T);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        const unsigned pairs = (unsigned)std::min<long>(bnp == 256 ? tiles2 : tiles3, num_pairs);
+        return bnp == 256 ? launch_clusters(proj_pair_kernel<256>, 2 * pairs, 2, PairCfg<256>::SMEM, st, P, T)
+                          : launch_clusters(proj_pair_kernel<192>, 2 * pairs, 2, PairCfg<192>::SMEM, st, P, T);
     }
     proj_kernel<<<(unsigned)std::min<long>(tiles1, num_sms), PT, PROJ_SMEM, st>>>(P, T);
     return cudaGetLastError();
