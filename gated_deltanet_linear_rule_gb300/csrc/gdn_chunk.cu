@@ -1098,7 +1098,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         if (nch > 1) mbar_arrive_expect_tx(&peer_bar[1], 256);
     }
     sync_all();
-    // MMA4, MMA6 and MMA7 complete on barriers of their own, one phase per chunk, and no
+    // MMA4 and MMA6 complete on barriers of their own, one phase per chunk; MMA7 on one barrier
+    // per chunk parity (its result is read a chunk later), one phase per two chunks.  No
     // waiter can fall two phases behind one of them.  Per-thread verdicts of the bounded
     // waits become uniform at the barrier opening the next chunk, the only full barrier of
     // the loop (so the loop runs on c alone).
