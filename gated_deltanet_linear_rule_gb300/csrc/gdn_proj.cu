@@ -10,17 +10,20 @@
 // kernel with one output segment.
 //
 // C[M][N] = A[M][K] . B[N][K]^T, bf16 operands, fp32 accumulation in tensor memory, bf16 out.
-// Two persistent kernels, both warp-specialised: warp 0 streams 64-wide K slices of A and B by
-// 2-D tensor copies with the 128-byte swizzle (which lays them out as the MMA's K-major operand
-// tiles) into a stage ring that runs on across tiles; warp 1 issues the MMAs (K = 16 per
-// instruction) into one of two 256-column TMEM accumulators, releasing each stage by a commit;
-// warps 2-5 read the other accumulator meanwhile (one TMEM lane quarter each, warp w -> lanes
-// 32 (w % 4) ..), round to bf16 and store 16 B at a time, so a tile's epilogue overlaps the next
-// tile's products.  Tiles t = block (or pair) index, + grid size, ..., N tiles fastest.
+// All kernels are warp-specialised: warp 0 streams 64-wide K slices of A and B by 2-D tensor
+// copies with the 128-byte swizzle (which lays them out as the MMA's K-major operand tiles) into
+// a stage ring; warp 1 issues the MMAs (K = 16 per instruction) into TMEM, releasing each stage
+// by a commit; warps 2-5 read the accumulator (one TMEM lane quarter each, warp w -> lanes
+// 32 (w % 4) ..), round to bf16 and store 16 B at a time.  The persistent kernels take tiles
+// t = block (or pair) index, + grid size, ..., N tiles fastest, with two 256-column
+// accumulators so that a tile's epilogue overlaps the next tile's products:
 //  - proj_kernel: one CTA per 128 x 256 tile (cta_group::1, 4 stages of 48 KiB).
-//  - proj_pair_kernel: clusters of two CTAs share 256 x 256 tiles (cta_group::2, M = 256): each
-//    CTA holds 128 rows of A and 128 rows of B per K slice (6 stages of 32 KiB) and receives
-//    its 128 rows of the result, so an SM streams half the operand bytes per output.
+//  - proj_pair_kernel<BNP>: clusters of two CTAs share 256 x BNP tiles (cta_group::2, M = 256;
+//    BNP = 256, or 192 when that puts more SMs to work in a single round): each CTA holds 128
+//    rows of A and BNP / 2 rows of B per K slice (6 stages) and receives its 128 rows of the
+//    result, so an SM streams about half the operand bytes per output.
+//  - proj_splitk_kernel<KS> (few tiles): a cluster of KS CTAs splits one 128 x 256 tile's K
+//    range and reduce-scatters the partial accumulators through distributed shared memory.
 // Rows past M and columns past N are zero-filled by the copies and skipped by the stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -218,14 +221,14 @@ __global__ void __launch_bounds__(PT, 1) proj_kernel(const __grid_constant__ Pro
     if (warp == 1) tc::dealloc(tm, 512);
 }
 
-// ---- CTA-pair kernel: 256 x 256 tiles, one MMA (M = 256) over the two CTAs of a cluster ----
-// CTA r of a pair holds rows 128 r .. of the tile's A rows and of its B rows in its own stage ring
-// (16 KiB each per 64-wide K slice, so 6 stages fit), and receives D rows 128 r .. in its own
-// TMEM.  Per output element each SM thus streams half the operand bytes of the single-CTA
-// kernel.  The even CTA's warp 1 issues the MMAs; the odd CTA's copies complete on the even
-// CTA's full barriers, and the MMA commits arrive on the stage and accumulator barriers of both.
-// The tile width BNP is 256, or 192 where that puts more SMs to work (each CTA then holds 128
-// or 96 rows of B).
+// ---- CTA-pair kernel: 256 x BNP tiles, one MMA (M = 256) over the two CTAs of a cluster ----
+// CTA r of a pair holds rows 128 r .. of the tile's A rows and B rows BNP/2 r .. in its own stage
+// ring (16 KiB of A and BNP/2 rows of B per 64-wide K slice; 6 stages), and receives D rows
+// 128 r .. over all BNP columns in its own TMEM.  Per output element each SM thus streams about
+// half the operand bytes of the single-CTA kernel.  The even CTA's warp 1 issues the MMAs; the
+// odd CTA's copies complete on the even CTA's full barriers, and the MMA commits arrive on the
+// stage and accumulator barriers of both.  The tile width BNP is 256, or 192 where that puts
+// more SMs to work (each CTA then holds 128 or 96 rows of B).
 constexpr int STAGES2 = 6;
 constexpr uint32_t A2_BYTES = 128 * BK * 2;  // this CTA's 128 A rows of a 64-wide K slice
 template <int BNP> struct PairCfg {
