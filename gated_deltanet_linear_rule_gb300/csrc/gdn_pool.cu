@@ -146,6 +146,9 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
         cudaFree(P->status_dev);
         cudaFree(P->ws.base);
         delete P;
+        // a failed allocation is not a sticky error: clear it, so that later launches, which
+        // read the runtime's last error, do not report it as their own
+        (void)cudaGetLastError();
         return rc;
     }
     P->live.assign((size_t)num_slots, 0);
