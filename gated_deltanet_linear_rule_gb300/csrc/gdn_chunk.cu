@@ -1003,6 +1003,42 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             fetch_p(1);
         }
     }
+    // While the first records arrive: the slot's conv buffer becomes the sequence's last W-1
+    // raw inputs (older buffer rows where the sequence is shorter).  The pre-pass, which read
+    // the old rows, is complete, and this pass never reads them.  This CTA's channels: its d_v
+    // half of the v-head's channels, and when h is the q/k head's first v-head its half of the
+    // q/k head's q and k channels -- disjoint across the CTAs of the call.
+    {
+        TIn* cbuf = reinterpret_cast<TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes +
+                                           A.state_bytes);
+        const int Dq = A.hqk * D, W = A.W, C = A.C;
+        if (tid < (h % A.r == 0 ? 192 : 64)) {
+            const int ch = tid < 64    ? 2 * Dq + h * D + half * 64 + tid           // v
+                           : tid < 128 ? hk * D + half * 64 + (tid - 64)            // q
+                                       : Dq + hk * D + half * 64 + (tid - 128);     // k
+            TIn old[7];
+#pragma unroll
+            for (int j = 0; j < 7; ++j)
+                if (j < W - 1) old[j] = static_cast<const TIn*>(static_cast<const void*>(cbuf))[(size_t)j * C + ch];
+#pragma unroll
+            for (int i = 0; i < 7; ++i) {
+                if (i >= W - 1) break;
+                const int pp = L - (W - 1) + i;
+                TIn x = old[0];
+                if (pp >= 0) {
+                    const size_t t = (size_t)(t0 + pp);
+                    x = ch < Dq       ? static_cast<const TIn*>(A.q)[t * Dq + ch]
+                        : ch < 2 * Dq ? static_cast<const TIn*>(A.k)[t * Dq + (ch - Dq)]
+                                      : static_cast<const TIn*>(A.v)[t * (size_t)(A.hv * D) + (ch - 2 * Dq)];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 7; ++j)
+                        if (j == W - 1 + pp) x = old[j];
+                }
+                cbuf[(size_t)i * C + ch] = x;
+            }
+        }
+    }
     // MMA7 of chunk pc (thread 0, right after the chunk's MMA6, where nothing on the chain waits
     // for this thread): [0; P] x Delta accumulated onto chunk pc's MMA4 columns; completes on the
     // barrier of pc's parity; the commit is issued even when the product is not, so that every

@@ -12,10 +12,9 @@
 //   2. chunk pre-pass  conv, norms, gates and the chunk-local products, one CTA per
 //                 (chunk, q/k head) taking the q/k head's v-heads in turn; it reads the
 //                 slots' old conv buffers
-//   3. conv_tail  one CTA per (sequence, 256 channels): the slot's conv buffer becomes the
-//                 last W-1 raw inputs (after the pre-pass has read the old buffer)
-//   4. chunk state pass  one CTA per (sequence, v-head, d_v half), the two halves a
-//                 cluster: output and final state
+//   3. chunk state pass  one CTA per (sequence, v-head, d_v half), the two halves a
+//                 cluster: output, final state, and the slot's conv buffer advanced to the
+//                 last W-1 raw inputs (the pre-pass has read the old rows by then)
 // d < 128 (the recurrent path):
 //   2. prep       one CTA per token: conv + SiLU over all C channels (the left context
 //                 before a sequence's first token comes from its slot's conv buffer),
@@ -254,10 +253,7 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
     if (A.T > 0 && A.D == 128) {
         cudaError_t e = launch_chunk_prep<TIn>(A, st);  // reads the conv buffers ...
         if (e != cudaSuccess) return e;
-        conv_tail_kernel<TIn><<<dim3(A.n, (A.C + 255) / 256), 256, 0, st>>>(A);  // ... then they advance
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_chunk_state<TIn, TOut>(A, st);
+        return launch_chunk_state<TIn, TOut>(A, st);     // ... which the state pass then advances
     }
     if (A.T > 0) {
         const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);
