@@ -89,6 +89,10 @@ def prefill_bytes(lengths, io=2):
 
 DECODE_SOURCES = ["gated_deltanet_linear_rule_gb300/csrc/gdn_decode.cu",
                   "gated_deltanet_linear_rule_gb300/csrc/gdn_internal.cuh"]
+PREFILL_SOURCES = ["gated_deltanet_linear_rule_gb300/csrc/gdn_chunk.cu",
+                   "gated_deltanet_linear_rule_gb300/csrc/gdn_prefill.cu",
+                   "gated_deltanet_linear_rule_gb300/csrc/gdn_internal.cuh",
+                   "gated_deltanet_linear_rule_gb300/csrc/gdn_tcgen05.cuh"]
 
 
 def sources_sha256(paths):
@@ -696,12 +700,16 @@ def run_ours(args):
         pms, T = time_prefill(torch, binding, synth, max(3, min(args.steps, 10)), 2)
         pb = prefill_bytes(PREFILL_LENGTHS)
         flops = PREFILL_FLOPS_PER_TOKEN * T
+        traffic = profiled_traffic("chunked_prefill_varlen8", PREFILL_SOURCES, 1)
         result["prefill"] = {"workload": "8 sequences {1,17,300,4095,1024,2048,513,8000}, bf16 io, zero state",
                              "tokens": T, "ms": pms, "tok_per_s": T / (pms * 1e-3),
                              "gbs": pb / (pms * 1e-3) / 1e9, "frac_hbm": pb / (pms * 1e-3) / 1e9 / hbm,
                              "bytes": pb, "tflops": flops / (pms * 1e-3) / 1e12,
                              "frac_tensor": flops / (pms * 1e-3) / 1e12 / bf16,
-                             "bound": "hbm (137 flop/B < ridge 279)"}
+                             "bound": "hbm (137 flop/B < ridge 279)",
+                             # DRAM bytes the two passes move (ncu, this source): the records between them
+                             "traffic": traffic,
+                             "traffic_gbs": traffic / (pms * 1e-3) / 1e9 if traffic else None}
         lms = time_prefill_long(torch, binding, synth)
         result["prefill_80k"] = {"workload": "one 80 000-token prefill, bf16 io, zero state", "ms": lms,
                                  "tok_per_s": 80000 / (lms * 1e-3),
