@@ -790,14 +790,16 @@ def run_reference(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-proj", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1, help="ranks (one per GPU, launched by torchrun for N > 1)")
+    ap.add_argument("--steps", type=int, default=5000, help="timed decode steps at m = 256")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (at least 3 are run)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"],
+                    help="ours: the CUDA library; reference: the fp64 oracle on the host cores")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the m-sweep and graph-replay timings")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill, 80k prefill, mixed-step and 30-layer timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle baseline sample")
+    ap.add_argument("--no-proj", action="store_true", help="skip the in_proj / out_proj timings")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
