@@ -800,7 +800,7 @@ def main():
                     help="skip the prefill, 80k prefill, mixed-step and 30-layer timings")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle baseline sample")
     ap.add_argument("--no-proj", action="store_true", help="skip the in_proj / out_proj timings")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the oracle baseline sample")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
     if args.impl == "reference":
