@@ -22,7 +22,7 @@ STATUS = {
     -5: "device wait timed out", -6: "unsupported shape", -7: "layer parameters not registered",
     -8: "device reported skipped work",
 }
-DEV_BAD_SLOT_PTR, DEV_BAD_SLOT_ID, DEV_BAD_SEQLENS, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_SLOT_PTR, DEV_BAD_SLOT_ID, DEV_BAD_SEQLENS, DEV_TIMEOUT, DEV_SLOT_OVERLAP = 0x1, 0x2, 0x4, 0x8, 0x10
 
 # every extern "C" symbol include/gdn.h declares
 EXPORTS = [

@@ -26,17 +26,24 @@
 //     blocked triangular inverse of I + A on the CUDA cores (16-wide diagonal blocks, then
 //     16 -> 32 -> 64 by  T_21 = -T_22 A_21 T_11)
 //     MMA3  [T2; 0] x V + [0; T1] x K   -> U (rows 0-63), W (rows 64-127)       128 x 128 x 128
-//   and writes per (chunk, v-head) a record: the W, U and P images, the decay factors and the
-//   output gates silu(z) * w_n; per (chunk, q/k head) the K and Q images.
+//   and writes per (chunk, v-head) a record: the W, U and P images and the chunk's scalars
+//   (decay factors, scale exponents); per (chunk, q/k head) the [K; Q] tile.
 // State pass (chunk_state_kernel, double-buffered bulk copies of the records):
-//     MMA4  [W; Q] x S0^T    -> W S0^T (rows 0-63), Q S0^T (rows 64-127)          128 x 128 x 128
+//     MMA4  [W; Q] x S0^T    -> W S0^T (rows 0-63), Q S0^T (rows 64-127)          128 x 64 x 128
 //     Delta
-//     MMA6  S += Delta~^T x K   (S pre-scaled by e^{G_last} in TMEM)              128 x 128 x 64
-//     MMA7  [.; P] x Delta  -> P Delta (rows 64-127), off the chain              128 x 128 x 64
-//     O = diag(e^G) Q S0^T + P Delta with the gated RMSNorm fused, output written
+//     MMA6  X = K^T x Delta~   (Delta~ = diag(gamma) Delta)                         128 x 64 x 64
+//     MMA7  [0; P] x Delta  -> P Delta (rows 64-127), off the chain                128 x 64 x 64
+//     S <- e^{G_last} S + X in fp32;  O = diag(e^G) (Q S0^T) + P Delta with the gated RMSNorm
 // Operands are fp16 (11-bit significand; bf16's 8 bits put the chunked result at ~5e-3 of
-// the recurrent definition) with fp32 accumulation.  Transposed operands (K, V, W, U as
-// the N side; Delta~ as the M side) are read MN-major straight from row-wise tiles.
+// the recurrent definition) with fp32 accumulation.  fp16 spans 2^-24 .. 65504, far less
+// than the layer's inputs may: every fp16 operand whose size follows the data carries a
+// power-of-two scale of its own, chosen per chunk from measured maxima (V, U, W from the
+// pre-pass's reductions; S0^T and Delta from the state's measured maximum and bounds on
+// its growth), and the products are taken back to true units in fp32.  Power-of-two scales
+// are exact, so they change no rounding but that of values that would otherwise overflow
+// or fall below fp16's normal range.  The decay factors e^{G_i} multiply the output rows in
+// fp32, after MMA4, for the same reason.  Transposed operands (K, V, W, U as the N side;
+// Delta~ as the M side) are read MN-major straight from row-wise tiles.
 // Every tcgen05.ld / st is executed by whole warps (they are warp-collective); per-token
 // conditions only guard stores.
 #include <cuda.h>
@@ -56,46 +63,66 @@ constexpr int D = 128, CH = 64, NT = 256;
 using Op = __half;
 
 // record of one (chunk, v-head), written by the pre-pass, read by the state pass
-constexpr uint32_t REC_W = 0;        // W image [token][dk]: two 64-wide halves 8 KiB apart
-constexpr uint32_t REC_U = 16384;    // U image [token][dv], same layout
-constexpr uint32_t REC_GZ = 32768;   // output gates silu(z) * w_n, fp16 [token][dv], same layout
-constexpr uint32_t REC_SC = 49152;   // gamma[64] = e^{G_last - G_j} (0 past the end), then e^{G_last}
-constexpr uint32_t REC_P = 49664;    // P image [i][j], 64 x 64
-constexpr uint32_t REC_Q = 57856;    // Q~ = diag(e^G) Q image [token][dk], halves 8 KiB apart
-constexpr uint32_t REC_BYTES = 74240;
-constexpr uint32_t KIMG_BYTES = 16384;  // per (chunk, q/k head): K image [token][dk], halves 8 KiB apart
+constexpr uint32_t REC_W = 0;        // W' image [token][dk]: two 64-wide halves 8 KiB apart (W = W' 2^ew)
+constexpr uint32_t REC_U = 16384;    // U' image [token][dv], same layout (U = U' 2^eu)
+constexpr uint32_t REC_P = 32768;    // P image [i][j], 64 x 64
+constexpr uint32_t REC_SC = 40960;   // the chunk's scalars, SC_* below
+constexpr uint32_t REC_BYTES = 41984;
+// per (chunk, q/k head): the [K; Q] tile, two 64-wide d_k halves of 128 rows (64 K rows, then
+// 64 Q rows), 16 KiB apart
+constexpr uint32_t QK_BYTES = 32768;
+// scalars of a record, in 4-byte words
+constexpr int SC_GAM = 0;    // [64] gamma_j = e^{G_last - G_j} (0 past the end)
+constexpr int SC_EG = 64;    // [64] e^{G_i}
+constexpr int SC_EGL = 128;  // e^{G_last}
+constexpr int SC_EU = 129;   // eu (int): U = U' 2^eu
+constexpr int SC_EW = 130;   // ew (int): W = W' 2^ew
+constexpr int SC_MU = 131;   // max |U'|
+constexpr int SC_MW = 132;   // max |W'|
+constexpr uint32_t SC_BYTES = 544;
 
 // pre-pass shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1 and MMA3; the K and Q images of the record)
+constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1 and MMA3; leaves as the (chunk, q/k head) [K; Q] tile)
 // Five 8 KiB blocks T2 | Z | P | Z | T1 (64 rows of 64 fp16, swizzled; Z zero) hold the
 // 128-row left operands of the block-diagonal products: [T2; Z] at P_T2, [Z; P] at P_Z0,
 // [P; Z] at P_P and [Z; T1] at P_Z1.
-constexpr uint32_t P_T2 = 32768;      // T diag(beta)
+constexpr uint32_t P_T2 = 32768;      // T diag(beta) 2^-eb
 constexpr uint32_t P_Z0 = 40960;
 constexpr uint32_t P_P = 49152;       // P
 constexpr uint32_t P_Z1 = 57344;
-constexpr uint32_t P_T1 = 65536;      // inverse scratch, then T diag(beta e^G)
-constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V image, then the U image
-constexpr uint32_t P_R5 = 91136;      // gates, then T (fp32, stride 68), then the W image
+constexpr uint32_t P_T1 = 65536;      // inverse scratch, then T diag(beta e^G) 2^-eg
+constexpr uint32_t P_R4 = 73728;      // A (fp32, stride 68), then the V' image, then the U' image
+constexpr uint32_t P_R5 = 91136;      // T (fp32, stride 68), then the W' image
 constexpr uint32_t P_RAW = P_T2;      // first: raw bf16 k, q, v rows of the chunk (3 x (64 + WM - 1) x 256 B)
 constexpr uint32_t P_SMALL = 108544;
-constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.7 KB) + alignment slack
+constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.8 KB) + alignment slack
 constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
 // state-pass shared memory (one CTA per (sequence, v-head, d_v half))
-// One record buffer: the [W; Q] operand (2 K-tiles of 128 rows) | K image | U half | gates
-// half | scalars.  P goes to a slot of its own (two of them, by chunk parity), each after an
-// 8 KiB zero block: MMA7 reads [0; P] as its 128-row operand.
-constexpr uint32_t B_A = 0, B_K = 32768, B_U = 49152, B_GZ = 57344, B_SC = 65536;
-constexpr uint32_t SC_BYTES = 512;   // the scalars fetched: gamma[64], e^{G_last}
-constexpr uint32_t S_TX = 32768 + 16384 + 8192 + 8192 + SC_BYTES;  // bytes fetched into one record buffer
-constexpr uint32_t S_BUF = 66560;
-constexpr uint32_t S_S0 = 2 * S_BUF;     // S0^T(:, half) in fp16, MN-major: 128 rows (d_k) of 64 d_v
-constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) [token][64 d_v]
-constexpr uint32_t S_DL = S_A6 + 8192;   // [2] Delta(:, half) [token][64 d_v], by chunk parity
+// One record buffer: the [W'; Q] operand (2 K-tiles of 128 rows) | K image | U' half |
+// scalars.  P goes to a slot of its own (two of them, by chunk parity), each after an 8 KiB
+// zero block: MMA7 reads [0; P] as its 128-row operand.
+constexpr uint32_t B_A = 0, B_K = 32768, B_U = 49152, B_SC = 57344;
+constexpr uint32_t S_TX = 32768 + 16384 + 8192 + SC_BYTES;  // bytes fetched into one record buffer
+constexpr uint32_t S_BUF = 58368;
+constexpr uint32_t S_S0 = 2 * S_BUF;     // S0^T(:, half) 2^-Es in fp16, MN-major: 128 rows (d_k) of 64 d_v
+constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) 2^-Ed [token][64 d_v]
+constexpr uint32_t S_DL = S_A6 + 8192;   // [2] Delta(:, half) 2^-Ed [token][64 d_v], by chunk parity
 constexpr uint32_t S_PZ = S_DL + 16384;  // [2] zero block | P [i][j], by chunk parity
 constexpr uint32_t S_SMALL = S_PZ + 32768;
-constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, sums) + slack
+constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, sums, maxima) + slack
+
+// state-pass tensor memory (512 columns): S^T(:, half) in true units, X = K^T Delta~ of the
+// last chunk, MMA4's and MMA7's results by chunk parity
+constexpr uint32_t TS = 0, TX = 64, TM4 = 128, TM7 = 256;
+
+// 2^k for an integer k (0 below 2^-126, 2^127 above)
+__device__ __forceinline__ float pow2f(int k) { return k < -126 ? 0.f : __int_as_float((min(k, 127) + 127) << 23); }
+// floor(log2 m) of a finite m > 0 in fp32's normal range
+__device__ __forceinline__ int ilog2f(float m) { return ((__float_as_int(m) >> 23) & 255) - 127; }
+// the power-of-two scale exponent e that brings magnitudes up to m below 2^(b+1): m 2^-e < 2^(b+1)
+// (0 for m = 0; clamped to [-100, 100], far outside any finite input the layer takes in fp32)
+__device__ __forceinline__ int scale_exp(float m, int b) { return m > 0.f ? max(-100, min(100, ilog2f(m) - b)) : 0; }
 
 __device__ __forceinline__ void sync_all()
 {
@@ -239,12 +266,18 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = align1024(smem_raw);
     // two sets (by head parity) of per-token gate arrays, 5 x 64 floats each: beta e^G, G,
-    // beta, e^G, gamma = e^{G_last - G}; then e^{G_last} per set
+    // beta, e^G, gamma = e^{G_last - G}; then per set e^{G_last} and the two scanning warps'
+    // maxima of beta and of beta e^G (bit patterns of non-negative floats)
     float* sSet = reinterpret_cast<float*>(sm + P_SMALL);
     float* sMisc2 = sSet + 640;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sSet + 656);
     uint64_t* sbar = bar + 1;  // raw rows staged (one phase per batch of tensor copies)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
+    // per v-head of the CTA (at most 8): max |V| over the chunk (true units), max |U'|, max |W'|,
+    // as bit patterns of non-negative floats, combined by atomicMax
+    unsigned int* s_vmax = reinterpret_cast<unsigned int*>(sSet + 664);
+    unsigned int* s_umax = s_vmax + 8;
+    unsigned int* s_wmax = s_vmax + 16;
     float* FA = reinterpret_cast<float*>(sm + P_R4);
     float* FT = reinterpret_cast<float*>(sm + P_R5);
     float* X = reinterpret_cast<float*>(sm + P_T1);
@@ -264,7 +297,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2;
     const int h0 = hk * A.r, Dq = A.hqk * D, Dv = A.hv * D;
-    unsigned char* kimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * KIMG_BYTES;
+    unsigned char* qkimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * QK_BYTES;
     const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
                                                                 A.slot_bytes + A.state_bytes);
 
@@ -276,12 +309,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg;
 
     // Per-head inputs nothing waits for yet are loaded one head ahead: the gate inputs a, b of
-    // token tid and the head's A_log, dt_bias (warps 0 and 1), the chunk's z rows, and (bf16)
-    // the head's v conv taps.
+    // token tid and the head's A_log, dt_bias (warps 0 and 1) and (bf16) the head's v conv taps.
     TIn ga = TIn(0.f), gb = TIn(0.f);
     float a_log = 0.f, dt_b = 0.f;
-    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
-    uint4 zpark[4][ZW];
     constexpr int KV = D * WM / NT;  // v taps per thread
     float tvv[KV];
     // gate inputs of head h for the threads of warp pair `pair` (token tid % 64)
@@ -297,15 +327,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
     };
     auto prefetch_head = [&](int h) {
-        const TIn* zin = static_cast<const TIn*>(A.z);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
-#pragma unroll
-            for (int wd = 0; wd < ZW; ++wd)
-                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-        }
         if constexpr (sizeof(TIn) == 2) {
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
@@ -342,9 +363,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h0 * D, y0, sbar);
         }
     }
+    if (tid < 24) s_vmax[tid] = 0u;
     if (warp == 0) tc::alloc(tmem_slot, 256);
     sync_all();
-    const uint32_t tm = *tmem_slot;  // columns [0, 128): MMA3 / MMA5 of a head; [128, 192): MMA1
+    const uint32_t tm = *tmem_slot;  // columns [0, 128): MMA3 of a head; [128, 192): MMA1
     uint32_t phase = 0;
     bool ok = true;
     auto mma_done = [&]() {
@@ -360,8 +382,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     // warp pair `pair` (which hold the head's gate inputs): a shuffle scan per warp, then the
     // second warp adds the first's total.  Heads 0 and 1 are scanned at the start by pairs 0
     // and 1; a head after that by pair 0 when its turn comes.
+    // A log decay below kMinLogDecay is taken as kMinLogDecay: alpha = e^-40 = 4e-18 is already
+    // zero against fp32's 6e-8 relative rounding of everything it is added to, and the bound
+    // keeps |G| <= 64 * 40 within a chunk, so that G_i - G_j (a difference of two prefix sums)
+    // keeps an absolute error near 2^-12.
     auto scan_set = [&](int k, int pair) {
         if ((tid >> 6) == pair) {
+            constexpr float kMinLogDecay = -40.f;
             const int t = tid & 63;
             float* G = sSet + k * 320 + 64;
             float* B = G + 64;
@@ -369,7 +396,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             float* GAM = EG + 64;
             float* BEG = G - 64;
             const bool in = t < n;
-            float x = in ? log_decay(a_log, to_f(ga), dt_b) : 0.f;
+            float x = in ? fmaxf(log_decay(a_log, to_f(ga), dt_b), kMinLogDecay) : 0.f;
             B[t] = in ? sigmoid_f(to_f(gb)) : 0.f;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -385,6 +412,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             BEG[t] = B[t] * EG[t];
             GAM[t] = t < n ? expf(gl - G[t]) : 0.f;
             if (t == 0) sMisc2[k * 8] = expf(gl);
+            // the column scales of T diag(beta) and T diag(beta e^G): their maxima (zero past the end)
+            const unsigned ub = __reduce_max_sync(0xffffffffu, __float_as_uint(B[t]));
+            const unsigned ug = __reduce_max_sync(0xffffffffu, __float_as_uint(BEG[t]));
+            if (lane == 0) {
+                sMisc2[k * 8 + 2 + (t >> 5)] = __uint_as_float(ub);
+                sMisc2[k * 8 + 4 + (t >> 5)] = __uint_as_float(ug);
+            }
         }
     };
 
@@ -446,16 +480,24 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
         }
     };
-    auto v_row = [&](int o, const float (&y)[8]) {
+    // v row r0 + o times the power of two sc, rounded to fp16 (zero past the chunk's end)
+    auto v_row = [&](int o, const float (&y)[8], float sc) {
         const bool in = r0 + o < n;
+        const float2 s2 = make_float2(sc, sc);
         uint4 pk;
-        pk.x = in ? pack_half2(y[0], y[1]) : 0u;
-        pk.y = in ? pack_half2(y[2], y[3]) : 0u;
-        pk.z = in ? pack_half2(y[4], y[5]) : 0u;
-        pk.w = in ? pack_half2(y[6], y[7]) : 0u;
+        float2 p2 = mul2(make_float2(y[0], y[1]), s2);
+        pk.x = in ? pack_half2(p2.x, p2.y) : 0u;
+        p2 = mul2(make_float2(y[2], y[3]), s2);
+        pk.y = in ? pack_half2(p2.x, p2.y) : 0u;
+        p2 = mul2(make_float2(y[4], y[5]), s2);
+        pk.z = in ? pack_half2(p2.x, p2.y) : 0u;
+        p2 = mul2(make_float2(y[6], y[7]), s2);
+        pk.w = in ? pack_half2(p2.x, p2.y) : 0u;
         return pk;
     };
-    uint4 vpark[4];  // v rows r0 .. r0 + 3, channels 8 cg .. 8 cg + 7, fp16
+    uint4 vpark[4];  // v rows r0 .. r0 + 3, channels 8 cg .. 8 cg + 7, times 2^-vexp, fp16
+    int vexp = 0;    // the scale exponent of this thread's parked rows
+    int vhead = 0;   // the CTA's v-head (0 .. r-1) whose rows are being parked
     // bf16: taps of channel pairs (8 cg + 2 p, 8 cg + 2 p + 1) from a [tap][channel] table
     float2 w2[4][WM];
     auto load_taps = [&](const float* table) {
@@ -496,9 +538,21 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             }
         emit(y);
     };
+    // park v rows r0 .. r0 + 3 under this thread's own scale (2^-vexp brings its largest value
+    // below 64), and bring the rows' maximum to the head's chunk maximum; the rows are brought
+    // to the chunk's common scale when the V' image is written
     auto v_emit = [&](const float (&y)[4][8]) {
+        float m = 0.f;
 #pragma unroll
-        for (int o = 0; o < 4; ++o) vpark[o] = v_row(o, y[o]);
+        for (int o = 0; o < 4; ++o)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m = r0 + o < n ? fmaxf(m, fabsf(y[o][e])) : m;
+        vexp = scale_exp(m, 5);
+        const float sc = pow2f(-vexp);
+#pragma unroll
+        for (int o = 0; o < 4; ++o) vpark[o] = v_row(o, y[o], sc);
+        const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+        if (lane == 0) atomicMax(s_vmax + vhead, mb);
     };
     // a sequence's first chunk: rows r < 0 of a staged tile from the slot's conv buffer (zero
     // before it); channel base ch0 of the conv's C channels
@@ -568,58 +622,32 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             ConvRows<TIn, WM> x;
             x.load(vin, Dv, h * D + 8 * cg, cbuf, A.C, 2 * Dq + h * D + 8 * cg, A.W, tc0, p0, r0, n);
             ConvRows<TIn, WM>::taps(w, A.conv_w, 2 * Dq + h * D + 8 * cg, A.W);
+            float y[4][8];
 #pragma unroll
-            for (int o = 0; o < 4; ++o) {
-                float y[8];
-                x.row(w, o, y);
-                vpark[o] = v_row(o, y);
-            }
+            for (int o = 0; o < 4; ++o) x.row(w, o, y[o]);
+            v_emit(y);
         }
     };
     conv_v_f32(h0);
     tc::fence_proxy_async();
     sync_all();
-    if (tid == 0) {  // the K rows of both K-tiles are the (chunk, q/k head) K image
-        bulk_s2g(kimg, sm + P_A1, 8192);
-        bulk_s2g(kimg + 8192, sm + P_A1 + 16384, 8192);
+    if (tid == 0) {  // the [K; Q] tile is the (chunk, q/k head) part of the record
+        bulk_s2g(qkimg, sm + P_A1, QK_BYTES);
         bulk_commit();
     }
 
-    // the output gates silu(z) * w_n of the head into the W area, from where one bulk copy
-    // takes them to the record.  Every record part is assembled in shared memory and leaves
-    // by bulk copies.
-    auto gates = [&]() {
-        float2 nw[4];  // the norm weights of this thread's 8 channels (the same for every q)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) nw[e] = make_float2(__ldg(A.norm_w + 8 * cg + 2 * e), __ldg(A.norm_w + 8 * cg + 2 * e + 1));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
-            const TIn* zv = reinterpret_cast<const TIn*>(zpark[q]);
-            float2 g2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))), nw[e]);
-            uint4 wv;
-            wv.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
-            wv.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
-            wv.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
-            wv.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
-            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = wv;
-        }
-        tc::fence_proxy_async();
-    };
     auto zero_block = [&](uint32_t off) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) *reinterpret_cast<uint4*>(sm + off + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
     };
 
-    // (b) MMA1: [K; Q] x K^T into columns [128, 192); meanwhile the first head's gates are formed
-    //     and the two zero blocks are cleared (the staging area they lie in is dead)
+    // (b) MMA1: [K; Q] x K^T into columns [128, 192); meanwhile the two zero blocks are cleared
+    //     (the staging area they lie in is dead)
     if (tid == 0)
         tc::mma_k(tm + 128, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
     zero_block(P_Z0);
     zero_block(P_Z1);
-    gates();
+    tc::fence_proxy_async();
     mma_done();
 
     for (int jh = 0; jh < A.r && ok; ++jh) {
@@ -633,10 +661,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         float* sGam = sEG + 64;
         const float* sMisc = sMisc2 + cs * 8;
         if (jh > 0) {
-            // the head's v rows were staged at P_T2 by a copy issued once the previous head's MMA5
+            // the head's v rows were staged at P_T2 by a copy issued once the previous head's MMA3
             // was done (bf16); its taps follow the tile.  The staging overlaps the Z0 block, which
             // is cleared again once the rows are consumed.
             if (jh > 1) scan_set(cs, 0);
+            vhead = jh;
             if constexpr (sizeof(TIn) == 2) {
                 float* vt = reinterpret_cast<float*>(sm + P_T2 + NRT * 256);
                 store_vtaps(vt);
@@ -652,12 +681,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 conv_v_f32(h);
             }
             if constexpr (sizeof(TIn) == 2) zero_block(P_Z0);  // it held these v rows
-            gates();
+            tc::fence_proxy_async();
             sync_all();
-        }
-        if (tid == 0) {
-            bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
-            bulk_commit();
         }
         if (jh + 1 < A.r) {
             prefetch_head(h + 1);
@@ -701,7 +726,6 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             }
         }
         tc::fence_proxy_async();  // P leaves for the record by a bulk copy
-        if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the W area
         __syncthreads();
         if (tid == 0) {
             bulk_s2g(rec + REC_P, sm + P_P, 8192);
@@ -817,47 +841,52 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             for (int q = 0; q < 4; ++q) FT[(32 + i0 + 8 * q) * FS + j] = -a[q];
         }
         __syncthreads();
-        //     T2 = T diag(beta), T1 = T diag(beta e^G), one 8-column chunk per item; a warp
-        //     takes 32 consecutive rows of one chunk column (conflict-free row reads)
+        //     T2 = T diag(beta) 2^-eb, T1 = T diag(beta e^G) 2^-eg, with the powers of two that
+        //     bring the largest beta and beta e^G of the chunk into [1, 2) (a chunk of tiny write
+        //     strengths or strong decay keeps its relative precision), one 8-column chunk per
+        //     item; a warp takes 32 consecutive rows of one chunk column (conflict-free row reads)
+        const int eb = scale_exp(fmaxf(sMisc[2], sMisc[3]), 0), eg = scale_exp(fmaxf(sMisc[4], sMisc[5]), 0);
+        const float fb = pow2f(-eb), fg = pow2f(-eg);
         for (int idx = tid; idx < 128 * 8; idx += NT) {
             const int r = idx & 127, c8 = idx >> 7, i = r & 63;
             const float* sc = (r < 64 ? sB : sBEG) + c8 * 8;
+            const float f = r < 64 ? fb : fg;
             const float4 t0 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8);
             const float4 t1 = *reinterpret_cast<const float4*>(FT + i * FS + c8 * 8 + 4);
             const float4 s0 = *reinterpret_cast<const float4*>(sc), s1 = *reinterpret_cast<const float4*>(sc + 4);
-            float v[8] = {t0.x * s0.x, t0.y * s0.y, t0.z * s0.z, t0.w * s0.w,
-                          t1.x * s1.x, t1.y * s1.y, t1.z * s1.z, t1.w * s1.w};
+            float v[8] = {t0.x * (s0.x * f), t0.y * (s0.y * f), t0.z * (s0.z * f), t0.w * (s0.w * f),
+                          t1.x * (s1.x * f), t1.y * (s1.y * f), t1.z * (s1.z * f), t1.w * (s1.w * f)};
             tc::st_chunk<Op>(sm + (r < 64 ? P_T2 : P_T1), i, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
-        // (d') V image [token][dv] for MMA3's second product, from the rows parked in registers
+        // (d') V' image [token][dv] = V 2^-ev for MMA3's second product, from the rows parked in
+        //     registers, where each thread's rows sit at a scale of their own
+        const int ev = scale_exp(__uint_as_float(s_vmax[jh]), 5);
+        if (ev != vexp) {
+            const float2 f2 = make_float2(pow2f(vexp - ev), pow2f(vexp - ev));
+#pragma unroll
+            for (int o = 0; o < 4; ++o) {
+                uint32_t* wv = reinterpret_cast<uint32_t*>(&vpark[o]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 x = mul2(__half22float2(*reinterpret_cast<const __half2*>(&wv[q])), f2);
+                    wv[q] = pack_half2(x.x, x.y);
+                }
+            }
+        }
 #pragma unroll
         for (int o = 0; o < 4; ++o)
             *reinterpret_cast<uint4*>(sm + P_R4 + (cg >> 3) * 8192 + tc::sw128_chunk(r0 + o, cg & 7)) = vpark[o];
         tc::fence_proxy_async();
         sync_all();
 
-        // (e) MMA3, block diagonal: [T2; Z] x V + [Z; T1] x K (V and K read MN-major; K from
-        //     the [K; Q] tile) -> U in rows 0-63, W in rows 64-127.  Meanwhile Q~ = diag(e^G) Q
-        //     goes to the record, 16 B per store.
+        // (e) MMA3, block diagonal: [T2; Z] x V' + [Z; T1] x K (V' and K read MN-major; K from
+        //     the [K; Q] tile) -> U' = U 2^-(eb+ev) in rows 0-63, W' = W 2^-eg in rows 64-127
         if (tid == 0) {
             tc::mma_k_mixed(tm, smem_addr(sm + P_T2), 128, 0, 0, smem_addr(sm + P_R4), 0, 1, 8192, CH,
                             tc::idesc_f16(128, 128, 0, 1), 0);
             tc::mma_k_mixed(tm, smem_addr(sm + P_Z1), 128, 0, 0, smem_addr(sm + P_A1), 0, 1, 16384, CH,
                             tc::idesc_f16(128, 128, 0, 1), 1);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int idx = tid + NT * k, kt = idx >> 9, i = (idx >> 3) & 63, j = idx & 7;
-            float qv[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + P_A1 + kt * 16384 + tc::sw128_chunk(64 + i, j)), qv);
-            const float eg = sEG[i];
-            uint4 w;
-            w.x = pack_half2(eg * qv[0], eg * qv[1]);
-            w.y = pack_half2(eg * qv[2], eg * qv[3]);
-            w.z = pack_half2(eg * qv[4], eg * qv[5]);
-            w.w = pack_half2(eg * qv[6], eg * qv[7]);
-            *reinterpret_cast<uint4*>(rec + REC_Q + kt * 8192 + tc::sw128_chunk(i, j)) = w;
         }
         mma_done();
         if (!ok) break;
@@ -871,20 +900,25 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             }
         }
 
-        // (f) U (rows 0-63) -> the U image (over the dead V image); W (rows 64-127) -> the
-        //     W image; both go to the record with the decay factors
+        // (f) U' (rows 0-63) -> the U' image (over the dead V' image); W' (rows 64-127) -> the
+        //     W' image, with their maxima; both go to the record with the chunk's scalars
         {
             const int row = qd * 32 + lane, i = row & 63;
+            float mx = 0.f;
             for (int c0 = 64 * hf; c0 < 64 * hf + 64; c0 += 32) {
                 float v[32];
                 tc::ld32(tc::taddr(tm, warp, c0), v);
                 tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
                     tc::st_chunk<Op>(sm + (row >= 64 ? P_R5 : P_R4) + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                 }
             }
+            const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+            if (lane == 0) atomicMax((row >= 64 ? s_wmax : s_umax) + jh, mb);
         }
         tc::fence_proxy_async();
         sync_all();
@@ -894,8 +928,17 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             bulk_commit();
         }
         float* scr = reinterpret_cast<float*>(rec + REC_SC);
-        if (tid < 64) scr[tid] = sGam[tid];
-        if (tid == 0) scr[64] = sMisc[0];
+        if (tid < 64) {
+            scr[SC_GAM + tid] = sGam[tid];
+            scr[SC_EG + tid] = sEG[tid];
+        }
+        if (tid == 0) {
+            scr[SC_EGL] = sMisc[0];
+            reinterpret_cast<int*>(scr)[SC_EU] = eb + ev;
+            reinterpret_cast<int*>(scr)[SC_EW] = eg;
+            scr[SC_MU] = __uint_as_float(s_umax[jh]);
+            scr[SC_MW] = __uint_as_float(s_wmax[jh]);
+        }
         if (tid == 0) bulk_wait_read_all();  // the next head reuses every area
         sync_all();
     }
@@ -906,21 +949,31 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 
 // ================================================================== state pass ====
 // One CTA per (sequence, v-head, d_v half); the two halves of a (sequence, v-head) form a
-// cluster of two.  A CTA keeps S^T restricted to its half, [d_k][64 d_v], in TMEM columns
-// [0, 64) (lane = d_k), so the products have M = 128 and N = 64:
-//     MMA4  [W; Q~] x S0^T(:, half)   -> W S0^T rows 0-63, diag(e^G) Q S0^T rows 64-127
-//     MMA6  S^T(:, half) += K^T x Delta~(:, half)   (Delta~ = diag(gamma) Delta; both MN-major)
-//     MMA7  [0; P] x Delta(:, half)   -> accumulated onto MMA4's rows 64-127: the output O
-// MMA4 of chunk c writes TMEM columns [64, 128) + 64 (c % 2).  MMA7 of chunk c is issued right
-// after its MMA6, where the issuing thread has nothing else to do until the next chunk's S0^T
-// is formed, and runs while it is; the output warps read its result one chunk later.  Only
-// MMA4 -> Delta -> MMA6 is serial from chunk to chunk.  The gated RMSNorm of an output row needs its sum of
-// squares over all of d_v, so each CTA sends its half's 64 per-token sums into the other
-// CTA's shared memory and arrives on that CTA's mbarrier (distributed shared memory).  Warps
-// w with w % 4 < 2 hold rows 0-63 (Delta); the others hold rows 64-127 and read the output
-// one chunk behind the chain, finishing its rows one more behind (once the other CTA's sums
-// are in); thread PF of warp 2 fetches the records, thread 0 issues the products.  8 warps:
-// warp w reads TMEM lane quarter w % 4 and works on columns 32 (w / 4) .. + 31.
+// cluster of two.  A CTA keeps S^T restricted to its half, [d_k][64 d_v], in fp32 TMEM
+// columns TS .. TS + 63 (lane = d_k) in true units, so the products have M = 128 and N = 64:
+//     MMA4  [W'; Q] x S0^T(:, half) 2^-Es  -> rows 0-63: W' S0^T, rows 64-127: Q S0^T
+//     MMA6  X = K^T x Delta~(:, half) 2^-Ed   (Delta~ = diag(gamma) Delta; both MN-major)
+//     MMA7  [0; P] x Delta(:, half) 2^-Ed  -> rows 64-127: P Delta
+// and the next chunk starts from S <- e^{G_last} S + 2^Ed X, formed in fp32 while that
+// chunk's S0^T is rounded.  MMA4 of chunk c writes TMEM columns TM4 + 64 (c % 2), MMA7
+// TM7 + 64 (c % 2).  MMA7 of chunk c is issued right after its MMA6 and runs while the next
+// S0^T is formed; the output warps read both results one chunk later:
+//     O_i = e^{G_i} 2^Es (Q S0^T)_i + 2^Ed (P Delta)_i.
+// Only S0^T -> MMA4 -> Delta -> MMA6 is serial from chunk to chunk.
+// The scales: 2^-Es brings a bound on max |S0| below 2^13 -- the measured maximum for the
+// first chunk; after that e^{G_last} times the last chunk's measured maximum plus 64 times
+// the last chunk's Delta bound (|K^T Delta~| <= 64 max |Delta~| for unit keys) -- and 2^-Ed
+// brings the bound max |U| + 128 max |W| max |S0| on |Delta| below 2^13.  The measured
+// maximum of S0 comes from per-warp maxima of the values being rounded, read after the
+// barrier that opens the chunk (no barrier of their own).
+// The gated RMSNorm of an output row needs its sum of squares over all of d_v, so each CTA
+// sends its half's 64 per-token sums into the other CTA's shared memory and arrives on that
+// CTA's mbarrier (distributed shared memory).  Warps w with w % 4 < 2 hold rows 0-63 (Delta);
+// the others hold rows 64-127 and read the output one chunk behind the chain, finishing its
+// rows one more behind (once the other CTA's sums are in), with the output gate silu(z) w_n
+// formed from z in fp32; thread PF of warp 2 fetches the records, thread 0 issues the
+// products.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
+// 32 (w / 4) .. + 31.
 
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
@@ -937,6 +990,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     uint64_t* const bar7o = peer_bar + 7;                        // MMA7 completion, odd chunks
     float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 128);  // [2][2][64] sums of O^2: chunk parity, column half
     float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
+    float* s_nw = peer_ss + 128;                                 // [64] norm weights of this CTA's d_v half
+    // [2][8] per-warp max |S0| by chunk parity, then [16] the incoming state's maximum (bit
+    // patterns of non-negative floats)
+    unsigned int* s_smax = reinterpret_cast<unsigned int*>(s_nw + 64);
 
     // both CTAs of a cluster take these exits together (they depend on the sequence only)
     if (!*A.ws.valid) return;
@@ -965,8 +1022,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         mbar_init(&peer_bar[0], 1);
         mbar_init(&peer_bar[1], 1);
         fence_mbar_init();
+        s_smax[16] = 0u;
     }
-    if (warp == 0) tc::alloc(tmem_slot, 256);
+    if (tid < 64) s_nw[tid] = __ldg(A.norm_w + half * 64 + tid);
+    if (warp == 0) tc::alloc(tmem_slot, 512);
     sync_all();
     cluster_sync_all();  // the other CTA's barriers exist before anything arrives on them
     const uint32_t tm = *tmem_slot;
@@ -975,19 +1034,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     int main_issued = 0, p_issued = 0;  // fetches so far (thread PF)
     int mma7_issued = 0;                // MMA7s so far (thread 0)
     auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
-    auto fetch_main = [&](int c) {  // the record's [W; Q~] operand, K image, U, gates and scalars
+    // the record's [W'; Q] operand (the W' image and the Q rows of the [K; Q] tile, per 64-wide
+    // d_k half), the K rows of the tile, the U' half and the scalars
+    auto fetch_main = [&](int c) {
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = record(c);
-        const unsigned char* kimg = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * KIMG_BYTES;
-        mbar_arrive_expect_tx(&full[c & 1], S_TX);
-        bulk_g2s(dst + B_A, rec + REC_W, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_A + 16384, rec + REC_W + 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_A + 8192, rec + REC_Q, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_A + 16384 + 8192, rec + REC_Q + 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_K, kimg, 16384, &full[c & 1]);
-        bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, &full[c & 1]);
-        bulk_g2s(dst + B_SC, rec + REC_SC, SC_BYTES, &full[c & 1]);
+        const unsigned char* qk = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * QK_BYTES;
+        uint64_t* fb = &full[c & 1];
+        mbar_arrive_expect_tx(fb, S_TX);
+        bulk_g2s(dst + B_A, rec + REC_W, 8192, fb);
+        bulk_g2s(dst + B_A + 16384, rec + REC_W + 8192, 8192, fb);
+        bulk_g2s(dst + B_A + 8192, qk + 8192, 8192, fb);
+        bulk_g2s(dst + B_A + 16384 + 8192, qk + 16384 + 8192, 8192, fb);
+        bulk_g2s(dst + B_K, qk, 8192, fb);
+        bulk_g2s(dst + B_K + 8192, qk + 16384, 8192, fb);
+        bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, fb);
+        bulk_g2s(dst + B_SC, rec + REC_SC, SC_BYTES, fb);
         main_issued = c + 1;
     };
     auto fetch_p = [&](int c) {
@@ -1040,15 +1102,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         }
     }
     // MMA7 of chunk pc (thread 0, right after the chunk's MMA6, where nothing on the chain waits
-    // for this thread): [0; P] x Delta accumulated onto chunk pc's MMA4 columns; completes on the
-    // barrier of pc's parity; the commit is issued even when the product is not, so that every
-    // wait has its phase
+    // for this thread): [0; P] x Delta into chunk pc's MMA7 columns; completes on the barrier of
+    // pc's parity; the commit is issued even when the product is not, so that every wait has
+    // its phase
     auto issue_mma7 = [&](int pc, bool go) {
         const bool gotp = mbar_wait_bounded(&full_p[pc & 1], (uint32_t)((pc >> 1) & 1), nullptr);
         if (!gotp) atomicOr(A.status, GDN_DEV_TIMEOUT);
         if (go && gotp)
-            tc::mma_k_mixed(tm + 64 + 64 * (pc & 1), smem_addr(sm + S_PZ + (pc & 1) * 16384), 128, 0, 0,
-                            smem_addr(sm + S_DL + (pc & 1) * 8192), 0, 1, 8192, CH, tc::idesc_f16(128, 64, 0, 1), 1);
+            tc::mma_k_mixed(tm + TM7 + 64 * (pc & 1), smem_addr(sm + S_PZ + (pc & 1) * 16384), 128, 0, 0,
+                            smem_addr(sm + S_DL + (pc & 1) * 8192), 0, 1, 8192, CH, tc::idesc_f16(128, 64, 0, 1), 0);
         tc::commit((pc & 1) ? bar7o : bar7e);
         mma7_issued = pc + 1;
     };
@@ -1060,22 +1122,30 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
     tc::fence_proxy_async();
 
-    // incoming state: S^T(:, half) into TMEM columns [0, 64); lane = d_k, column j = d_v 64 half + j
+    // incoming state: S^T(:, half) into TMEM columns TS .. TS + 63 (lane = d_k, column j = d_v
+    // 64 half + j), true units; its maximum sets the first chunk's scale
     {
         float v[32];
+        float m = 0.f;
         const int dv0 = half * 64 + 32 * hf;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = Sg[(size_t)(dv0 + e) * D + row];
-        tc::st32(tc::taddr(tm, warp, 32 * hf), v);
+        for (int e = 0; e < 32; ++e) {
+            v[e] = Sg[(size_t)(dv0 + e) * D + row];
+            m = fmaxf(m, fabsf(v[e]));
+        }
+        tc::st32(tc::taddr(tm, warp, TS + 32 * hf), v);
         tc::wait_st();
+        const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+        if (lane == 0) atomicMax(s_smax + 16, mb);
     }
 
-    // output rows (rows >= 64 only, this thread's 32 columns): gzn holds the gates of the chunk
-    // just computed; o / gzr the O_i and gates of the chunk before, waiting for the other CTA's
-    // sums
+    // output rows (rows >= 64 only, this thread's 32 columns): o holds O_i of the chunk waiting
+    // for the other CTA's sums, zr its z values; eg_n is e^{G_i} of the chunk just computed
     float o[32];
-    uint4 gzn[4], gzr[4];
-    const int orow = row - 64;
+    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 z values
+    uint4 zr[4 * ZW];
+    float eg_n = 0.f;
+    const int orow = row - 64, col0 = half * 64 + 32 * hf;
     auto finish_rows = [&](int pc) -> bool {  // false when the sums never came
         const bool gotp = mbar_wait_cluster_bounded(&peer_bar[pc & 1], (uint32_t)((pc >> 1) & 1));
         const int pn = min(CH, L - pc * CH);
@@ -1083,30 +1153,48 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             const float rs =
                 rms_scale(s_ss[(pc & 1) * 128 + orow] + s_ss[(pc & 1) * 128 + 64 + orow] + peer_ss[(pc & 1) * 64 + orow],
                           A.norm_eps, D);
-            TOut* dst = out + (size_t)(t0 + pc * CH + orow) * Dv + (size_t)h * D + half * 64 + 32 * hf;
+            TOut* dst = out + (size_t)(t0 + pc * CH + orow) * Dv + (size_t)h * D + col0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float gz[8], y[8];
-                unpack8(gzr[q], gz);
+                const TIn* zq = reinterpret_cast<const TIn*>(zr + q * ZW);
+                const float4 w0 = *reinterpret_cast<const float4*>(s_nw + 32 * hf + 8 * q);
+                const float4 w1 = *reinterpret_cast<const float4*>(s_nw + 32 * hf + 8 * q + 4);
+                const float nw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = o[8 * q + e] * rs * gz[e];
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 g = mul2(silu2(make_float2(to_f(zq[e]), to_f(zq[e + 1]))), make_float2(nw[e], nw[e + 1]));
+                    y[e] = o[8 * q + e] * rs * g.x;
+                    y[e + 1] = o[8 * q + e + 1] * rs * g.y;
+                }
                 store8<TOut>(dst + 8 * q, y);
             }
         }
         return gotp;
     };
-    // O of chunk pc (MMA4's rows 64-127 plus MMA7), its sums of squares
-    auto complete_rows = [&](int pc) -> bool {
+    // O of chunk pc from MMA4's rows 64-127 (scale 2^es) and MMA7 (scale 2^ed), its sums of
+    // squares, and the z values of its rows for finish_rows
+    auto complete_rows = [&](int pc, int es_c, int ed_c) -> bool {
         const bool got7 = mbar_wait_bounded((pc & 1) ? bar7o : bar7e, (uint32_t)((pc >> 1) & 1), nullptr);
         tc::fence_after_sync();
-        tc::ld32(tc::taddr(tm, warp, 64 + 64 * (pc & 1) + 32 * hf), o);
+        float zz[32];
+        tc::ld32(tc::taddr(tm, warp, TM4 + 64 * (pc & 1) + 32 * hf), o);
+        tc::ld32(tc::taddr(tm, warp, TM7 + 64 * (pc & 1) + 32 * hf), zz);
         tc::wait_ld();
+        const float fy = eg_n * pow2f(es_c), fz = pow2f(ed_c);
         float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) gzr[q] = gzn[q];
+        for (int e = 0; e < 32; ++e) {
+            o[e] = fmaf(fz, zz[e], fy * o[e]);
+            ss = fmaf(o[e], o[e], ss);
+        }
         s_ss[(pc & 1) * 128 + hf * 64 + orow] = ss;
+        const int pn = min(CH, L - pc * CH);
+        const uint4* zs = reinterpret_cast<const uint4*>(static_cast<const TIn*>(A.z) +
+                                                         (size_t)(t0 + pc * CH + min(orow, pn - 1)) * Dv +
+                                                         (size_t)h * D + col0);
+#pragma unroll
+        for (int w = 0; w < 4 * ZW; ++w) zr[w] = __ldg(zs + w);
         return got7;
     };
     // this half's per-token sums of squares of chunk pc -> the other CTA, by asynchronous
@@ -1134,6 +1222,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         if (nch > 1) mbar_arrive_expect_tx(&peer_bar[1], 256);
     }
     sync_all();
+    // Scale state carried from chunk to chunk, the same in every thread: the last chunk's
+    // e^{G_last}, measured max |S0|, Delta bound and the exponents of its S0^T and Delta.
+    float egl_p = 1.f, smax_p = __uint_as_float(s_smax[16]), dbound_p = 0.f;
+    int es_p = 0, ed_p = 0;
     // MMA4 and MMA6 complete on barriers of their own, one phase per chunk; MMA7 on one barrier
     // per chunk parity (its result is read a chunk later), one phase per two chunks.  No
     // waiter can fall two phases behind one of them.  Per-thread verdicts of the bounded
@@ -1143,20 +1235,42 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         unsigned char* buf = sm + (c & 1) * S_BUF;
         const bool got = mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         if (!got && tid == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
+        // the chunk's scalars (read before this buffer is refetched)
         const float* sc = reinterpret_cast<const float*>(buf + B_SC);
+        const float egl = sc[SC_EGL], mu = sc[SC_MU], mw = sc[SC_MW];
+        const int eu = __float_as_int(sc[SC_EU]), ew = __float_as_int(sc[SC_EW]);
 
-        // S0^T (fp16, MN-major: row = d_k) for MMA4; S^T <- e^{G_last} S^T for MMA6 (columns
-        // [0, 64), which MMA4 does not touch; the store completes before MMA6 is issued)
+        // S0 of this chunk (from the last chunk: e^{G_last} S + 2^Ed X, back to TMEM) and S0^T
+        // 2^-Es in fp16 (MN-major: row = d_k) for MMA4, with this thread's share of max |S0|
+        const int es = scale_exp(c == 0 ? smax_p : fmaf(egl_p, smax_p, 64.f * dbound_p), 12);
         {
             float v[32];
-            tc::ld32(tc::taddr(tm, warp, 32 * hf), v);
-            tc::wait_ld();
+            tc::ld32(tc::taddr(tm, warp, TS + 32 * hf), v);
+            if (c > 0) {
+                float x[32];
+                tc::ld32(tc::taddr(tm, warp, TX + 32 * hf), x);
+                tc::wait_ld();
+                const float fx = pow2f(ed_p);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + S_S0, row, 4 * hf + q, v + 8 * q);
-            const float egl = sc[64];
+                for (int e = 0; e < 32; ++e) v[e] = fmaf(fx, x[e], egl_p * v[e]);
+                tc::st32(tc::taddr(tm, warp, TS + 32 * hf), v);
+            } else {
+                tc::wait_ld();
+            }
+            float m = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= egl;
-            tc::st32(tc::taddr(tm, warp, 32 * hf), v);
+            for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(v[e]));
+            const float f = pow2f(-es);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float t8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t8[e] = v[8 * q + e] * f;
+                tc::st_chunk<Op>(sm + S_S0, row, 4 * hf + q, t8);
+            }
+            const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+            if (lane == 0) s_smax[(c & 1) * 8 + warp] = mb;
+            tc::wait_st();
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -1164,56 +1278,62 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::fence_after_sync();
         if (!ok) break;
 
-        // MMA4: [W; Q~] x S0^T(:, half) -> columns [64, 128) + 64 (c % 2)
+        // MMA4: [W'; Q] x S0^T(:, half) 2^-Es -> columns TM4 + 64 (c % 2)
         if (tid == 0) {
-            tc::mma_k_mixed(tm + 64 + 64 * (c & 1), smem_addr(buf + B_A), 128, 0, 0, smem_addr(sm + S_S0), 0, 1, 8192,
-                            D, tc::idesc_f16(128, 64, 0, 1), 0);
+            tc::mma_k_mixed(tm + TM4 + 64 * (c & 1), smem_addr(buf + B_A), 128, 0, 0, smem_addr(sm + S_S0), 0, 1,
+                            8192, D, tc::idesc_f16(128, 64, 0, 1), 0);
             tc::commit(bar4);
         }
+        // this chunk's measured max |S0|, the bound on |Delta| and its scale
+        float smax;
+        {
+            const uint4 a = *reinterpret_cast<const uint4*>(s_smax + (c & 1) * 8);
+            const uint4 b = *reinterpret_cast<const uint4*>(s_smax + (c & 1) * 8 + 4);
+            smax = __uint_as_float(max(max(max(a.x, a.y), max(a.z, a.w)), max(max(b.x, b.y), max(b.z, b.w))));
+        }
+        const float dbound = fmaf(128.f * mw * pow2f(ew), smax, mu * pow2f(eu));
+        const int ed = scale_exp(dbound, 12);
         if (row < 64) {
-            // Delta_i = U_i - (W S0^T)_i and Delta~_i = gamma_i Delta_i -> row i of this chunk's
-            // Delta image and of the Delta~ image, then MMA6
+            // Delta_i 2^-Ed = U'_i 2^(eu-Ed) - (W' S0^T 2^-Es)_i 2^(ew+Es-Ed) and Delta~_i = gamma_i
+            // Delta_i -> row i of this chunk's Delta image and of the Delta~ image, then MMA6
             float u[32];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 unpack8(*reinterpret_cast<const uint4*>(buf + B_U + tc::sw128_chunk(row, 4 * hf + q)), u + 8 * q);
-            const float gm = sc[row];
+            const float gm = sc[SC_GAM + row];
+            const float fu = pow2f(eu - ed), fd = pow2f(ew + es - ed);
             const bool got4 = mbar_wait_bounded(bar4, (uint32_t)(c & 1), nullptr);
             if (!got4 && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
             ok = got4;
             tc::fence_after_sync();
             float d[32];
-            tc::ld32(tc::taddr(tm, warp, 64 + 64 * (c & 1) + 32 * hf), d);
+            tc::ld32(tc::taddr(tm, warp, TM4 + 64 * (c & 1) + 32 * hf), d);
             tc::wait_ld();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float dl[8], dg[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    dl[e] = u[8 * q + e] - d[8 * q + e];
+                    dl[e] = fmaf(u[8 * q + e], fu, -(d[8 * q + e] * fd));
                     dg[e] = gm * dl[e];
                 }
                 tc::st_chunk<Op>(sm + S_A6, row, 4 * hf + q, dg);
                 tc::st_chunk<Op>(sm + S_DL + (c & 1) * 8192, row, 4 * hf + q, dl);
             }
             tc::fence_proxy_async();
-            tc::wait_st();
             tc::fence_before_sync();
             named_bar_sync(1, NT);  // the output warps only arrive
-            // MMA6: S^T(:, half) += K^T x Delta~, then this chunk's MMA7; the commits are issued
-            // even when the products are not, so that every wait has its phase
+            // MMA6: X = K^T x Delta~ 2^-Ed, then this chunk's MMA7; the commits are issued even
+            // when the products are not, so that every wait has its phase
             if (tid == 0) {
                 tc::fence_after_sync();
                 if (ok)
-                    tc::mma_k_mixed(tm, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
-                                    tc::idesc_f16(128, 64, 1, 1), 1);
+                    tc::mma_k_mixed(tm + TX, smem_addr(buf + B_K), 0, 1, 8192, smem_addr(sm + S_A6), 0, 1, 8192, CH,
+                                    tc::idesc_f16(128, 64, 1, 1), 0);
                 tc::commit(bar6);
                 issue_mma7(c, ok);
             }
         } else {
-            // the decayed S of rows 64-127 is in TMEM: MMA6 may go ahead as far as these warps
-            // are concerned
-            tc::wait_st();
             tc::fence_before_sync();
             named_bar_arrive(1, NT);
             // the chunk before last: finished rows out; the next sums barrier phase armed
@@ -1223,19 +1343,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 if (tid == PF && gotp) mbar_arrive_expect_tx(&peer_bar[c & 1], 256);
             }
             // the chunk before: its output rows (its MMA7, issued after its MMA6, is done with its
-            // P slot, which PF refills; the next chunk's MMA4 overwrites these columns only after
-            // the next full barrier)
+            // P slot, which PF refills; the next chunk's MMA4 and MMA7 overwrite these columns
+            // only after the next full barrier)
             bool got7 = true;
             if (c >= 1) {
-                got7 = complete_rows(c - 1);
+                got7 = complete_rows(c - 1, es_p, ed_p);
                 if (tid == PF && got7 && c + 1 < nch) fetch_p(c + 1);
             }
             if ((!gotp || !got7) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
             ok = gotp && got7;
-            // this chunk's gates, read before this buffer is refetched
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                gzn[q] = *reinterpret_cast<const uint4*>(buf + B_GZ + tc::sw128_chunk(orow, 4 * hf + q));
+            // this chunk's e^{G_i} of the thread's row, read before this buffer is refetched
+            eg_n = sc[SC_EG + orow];
             named_bar_sync(2, NT / 2);  // the four output warps: sums of chunk c - 1 written, buffer read
             if (c >= 1) send_sums(c - 1);
         }
@@ -1246,6 +1364,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         // this buffer is free (MMA4 and MMA6 are done, its rows were read before barriers 1
         // and 2): fetch the record two chunks ahead into it
         if (tid == PF && ok && c + 2 < nch) fetch_main(c + 2);
+        egl_p = egl;
+        smax_p = smax;
+        dbound_p = dbound;
+        es_p = es;
+        ed_p = ed;
     }
     ok = __syncthreads_and(ok) != 0;
     if (ok) {
@@ -1253,7 +1376,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         bool gotp = true, got7 = true;
         if (row >= 64) {
             if (nch >= 2) gotp = finish_rows(nch - 2);
-            got7 = complete_rows(nch - 1);
+            got7 = complete_rows(nch - 1, es_p, ed_p);
             named_bar_sync(2, NT / 2);
             send_sums(nch - 1);
             gotp = finish_rows(nch - 1) && gotp;
@@ -1263,12 +1386,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
 
     if (ok) {
-        float v[32];
-        tc::ld32(tc::taddr(tm, warp, 32 * hf), v);
+        // the final state S <- e^{G_last} S + 2^Ed X of the last chunk, in true units
+        float v[32], x[32];
+        tc::ld32(tc::taddr(tm, warp, TS + 32 * hf), v);
+        tc::ld32(tc::taddr(tm, warp, TX + 32 * hf), x);
         tc::wait_ld();
+        const float fx = pow2f(ed_p);
         const int dv0 = half * 64 + 32 * hf;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = v[e];
+        for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = fmaf(fx, x[e], egl_p * v[e]);
     }
     // every fetched copy must land, and the last MMA7 be done, before the CTA's shared and
     // tensor memory go away
@@ -1281,7 +1407,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             mbar_wait_bounded(&full_p[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
     }
     sync_all();
-    if (warp == 0) tc::dealloc(tm, 256);
+    if (warp == 0) tc::dealloc(tm, 512);
     // Neither CTA leaves while the other may still write into its shared memory.  Both reach
     // this barrier: every wait above is bounded and a failed wait ends the loop in both CTAs.
     cluster_sync_all();
@@ -1289,7 +1415,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 
 }  // namespace
 
-size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (size_t)hqk * KIMG_BYTES; }
+size_t chunk_record_bytes(int hv, int hqk) { return (size_t)hv * REC_BYTES + (size_t)hqk * QK_BYTES; }
 
 namespace {
 

@@ -52,6 +52,7 @@ struct DecodeArgs {
     uint32_t state_bytes;
     float l2_eps, norm_eps;
     int stall_producer;  // test hook: the producer fills no stage, so the consumers' waits run out
+    const int* gate;     // when non-null and *gate != 0 the launch does nothing (mixed-step overlap check)
 };
 
 size_t decode_smem_bytes(int D, int r, int stages)
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
     const int items = A.m * A.hqk;
     const uint32_t item_bytes = (uint32_t)r * D * D * 4;
     const int stages_per_item = (int)((item_bytes + kStageBytes - 1) / kStageBytes);
+    if (A.gate && *A.gate) return;  // a mixed step whose parts name a common slot: nothing runs
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -292,24 +294,27 @@ cudaError_t launch_t(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 {
     auto kern = decode_kernel<D, TIn, TOut, STAGES>;
     const size_t smem = decode_smem_bytes(D, A.r, STAGES);
-    // resident CTAs per SM for this instantiation and shared-memory size (cached; calls from
-    // several host threads are serialised here)
+    // resident CTAs per SM for this instantiation and shared-memory size, per device (the
+    // attribute is a per-device setting; cached; calls from several host threads are serialised here)
+    constexpr int kMaxDevices = 64;
     static std::mutex mu;
-    static int cached_per_sm = -1;
-    static size_t cached_smem = 0;
+    static int cached_per_sm[kMaxDevices] = {};
+    static size_t cached_smem[kMaxDevices] = {};
+    const int dev = P.device;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (cached_per_sm < 0 || cached_smem != smem) {
+        if (cached_per_sm[dev] <= 0 || cached_smem[dev] != smem) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             int n = 0;
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
             if (e != cudaSuccess) return e;
-            cached_per_sm = std::max(n, 1);
-            cached_smem = smem;
+            cached_per_sm[dev] = std::max(n, 1);
+            cached_smem[dev] = smem;
         }
-        per_sm = cached_per_sm;
+        per_sm = cached_per_sm[dev];
     }
     const int items = A.m * A.hqk;
     const int grid = std::max(1, std::min(items, per_sm * P.num_sms));
@@ -341,7 +346,8 @@ cudaError_t launch_d(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 }  // namespace
 
 cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, int m, const void* q, const void* k,
-                          const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st)
+                          const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st,
+                          const int* gate)
 {
     const LayerParams& L = P.params[(size_t)layer];
     DecodeArgs A;
@@ -369,6 +375,7 @@ cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, i
     A.l2_eps = P.shape.l2_eps;
     A.norm_eps = P.shape.norm_eps;
     A.stall_producer = P.debug_flags & 1;
+    A.gate = gate;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return launch_d<__nv_bfloat16, __nv_bfloat16>(P, A, st);
     if (in_bf16) return launch_d<__nv_bfloat16, float>(P, A, st);

@@ -52,6 +52,7 @@ struct Pool {
     char* base = nullptr;
     unsigned char* live_dev = nullptr;   // [num_slots] 1 = allocated (read by device-side checks)
     unsigned int* status_dev = nullptr;  // device status word (GDN_DEV_* bits)
+    int* gate_dev = nullptr;             // [1] set when a mixed step's two parts name a common slot
     std::vector<int> free_list;          // free slot ids, popped from the back (lowest id first)
     std::vector<unsigned char> live;     // host mirror of live_dev
     std::vector<LayerParams> params;
@@ -78,6 +79,7 @@ struct PrefillArgs {
     float l2_eps, norm_eps;
     PrefillWorkspace ws;
     float* kq;  // [T][Hqk] k_hat . q_hat (workspace)
+    const int* gate;  // when non-null and *gate != 0 the call does nothing (a mixed step's overlap check)
 };
 
 // Facts every kernel needs to check a slot pointer before touching memory.
@@ -409,12 +411,14 @@ __device__ __forceinline__ int row_col(int j, int cl) { return (j >> 2) * 4 * LP
 // --------------------------------------------------------- launchers ----
 
 // Each returns cudaSuccess or the launch error.
+// `gate` (device, may be null): when *gate != 0 at run time the launch does nothing
 cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, int m, const void* q, const void* k,
-                          const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st);
+                          const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st,
+                          const int* gate = nullptr);
 
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
-                           const void* b, const void* z, void* out, cudaStream_t st);
+                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate = nullptr);
 
 // the row tensors of a prefill call are read and written in 16-B pieces (and by tensor copies)
 inline bool rows_aligned16(const void* q, const void* k, const void* v, const void* z, const void* out)

@@ -47,6 +47,31 @@ __global__ void slot_ptrs_kernel(const int* ids, int m, uint64_t base, uint64_t 
     out[i] = base + ((uint64_t)id * num_layers + layer) * slot_bytes;
 }
 
+// A mixed step's overlap check (one CTA): does a decode row's slot pointer equal the address of
+// (a prefill sequence's slot, layer)?  Writes the verdict to *gate (read by both parts' kernels,
+// which then do nothing) and sets GDN_DEV_SLOT_OVERLAP.  Ids the prefill's own validation will
+// reject are skipped here (they name no slot).
+__global__ void mixed_overlap_kernel(const uint64_t* ptrs, int m, const int* ids, int n, uint64_t base,
+                                     uint64_t slot_bytes, int num_layers, int num_slots, int layer, int* gate,
+                                     unsigned int* status)
+{
+    __shared__ int hit;
+    if (threadIdx.x == 0) hit = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        const uint64_t p = ptrs[i];
+        for (int j = 0; j < n; ++j) {
+            const int id = ids[j];
+            if (id >= 0 && id < num_slots && p == base + ((uint64_t)id * num_layers + layer) * slot_bytes) hit = 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        *gate = hit;
+        if (hit) atomicOr(status, GDN_DEV_SLOT_OVERLAP);
+    }
+}
+
 cudaError_t enqueue_zero(void* p, size_t bytes, cudaStream_t st, int num_sms)
 {
     // every region zeroed here is 256-B aligned and a multiple of 256 B long
@@ -127,7 +152,9 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     }
     if (rc == GDN_OK && cudaMalloc(&P->base, P->total_bytes) != cudaSuccess) rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && cudaMalloc(&P->live_dev, (size_t)num_slots) != cudaSuccess) rc = GDN_ERR_CUDA;
-    if (rc == GDN_OK && cudaMalloc(&P->status_dev, sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
+    // the status word and, beside it, the mixed step's overlap gate
+    if (rc == GDN_OK && cudaMalloc(&P->status_dev, 2 * sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
+    if (rc == GDN_OK) P->gate_dev = reinterpret_cast<int*>(P->status_dev + 1);
     if (rc == GDN_OK && P->shape.max_prefill_tokens > 0) {
         const int cap = gdn::prefill_pool_chunk_cap(P->shape, P->shape.max_prefill_tokens);
         P->ws.bytes = gdn::prefill_workspace_bytes(P->shape, P->shape.max_prefill_tokens, cap);
@@ -137,7 +164,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     if (rc == GDN_OK) {
         if (enqueue_zero(P->base, P->total_bytes, 0, P->num_sms) != cudaSuccess) rc = GDN_ERR_CUDA;
         if (cudaMemset(P->live_dev, 0, (size_t)num_slots) != cudaSuccess) rc = GDN_ERR_CUDA;
-        if (cudaMemset(P->status_dev, 0, sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
+        if (cudaMemset(P->status_dev, 0, 2 * sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
         if (cudaDeviceSynchronize() != cudaSuccess) rc = GDN_ERR_CUDA;
     }
     if (rc != GDN_OK) {
@@ -181,7 +208,8 @@ int gdn_pool_reset(gdn_pool* P, void* stream)
 {
     if (!P) return GDN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemset(P->live_dev, 0, (size_t)P->num_slots) != cudaSuccess) return GDN_ERR_CUDA;
+    // on the stream, after the work already queued there that still reads the live flags
+    if (cudaMemsetAsync(P->live_dev, 0, (size_t)P->num_slots, st) != cudaSuccess) return GDN_ERR_CUDA;
     if (enqueue_zero(P->base, P->total_bytes, st, P->num_sms) != cudaSuccess) return GDN_ERR_CUDA;
     std::fill(P->live.begin(), P->live.end(), 0);
     P->free_list.resize((size_t)P->num_slots);
@@ -207,8 +235,9 @@ int gdn_slot_recycle(gdn_pool* P, int slot_id, void* stream)
     if (!P) return GDN_ERR_INVALID_ARG;
     if (slot_id < 0 || slot_id >= P->num_slots || !P->live[(size_t)slot_id]) return GDN_ERR_BAD_SLOT;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    unsigned char zero = 0;
-    if (cudaMemcpy(P->live_dev + slot_id, &zero, 1, cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+    // the device live flag is cleared on the stream, so that a prefill or slot_ptrs call queued
+    // there earlier still sees the slot allocated
+    if (cudaMemsetAsync(P->live_dev + slot_id, 0, 1, st) != cudaSuccess) return GDN_ERR_CUDA;
     // the slot's layers are contiguous: one region of num_layers * slot_bytes
     char* p = P->base + (size_t)slot_id * P->num_layers * P->slot_bytes;
     if (enqueue_zero(p, P->slot_bytes * P->num_layers, st, P->num_sms) != cudaSuccess) return GDN_ERR_CUDA;
@@ -385,13 +414,20 @@ int gdn_mixed_step(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m,
     }
     MixedStreams ms;
     if (mixed_streams(P, &ms) != cudaSuccess) return GDN_ERR_CUDA;
+    // the two parts must name different slots: checked on the device first, both parts gated on it
+    mixed_overlap_kernel<<<1, 256, 0, st>>>(slot_ptrs_dev, m, slot_ids_dev, n_seqs, reinterpret_cast<uint64_t>(P->base),
+                                            P->slot_bytes, P->num_layers, P->num_slots, layer, P->gate_dev,
+                                            P->status_dev);
+    cudaError_t e = cudaGetLastError();
     // fork: the decode on the side stream after everything enqueued on `stream` so far
-    cudaError_t e = cudaEventRecord(ms.fork, st);
+    if (e == cudaSuccess) e = cudaEventRecord(ms.fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ms.side, ms.fork, 0);
-    if (e == cudaSuccess) e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, ms.side);
+    if (e == cudaSuccess)
+        e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, ms.side, P->gate_dev);
     // the prefill on `stream` meanwhile; then `stream` waits for the decode (join)
     const cudaError_t ep = e == cudaSuccess ? gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs,
-                                                                  total_tokens, pq, pk, pv, pa, pb, pz, pout, st)
+                                                                  total_tokens, pq, pk, pv, pa, pb, pz, pout, st,
+                                                                  P->gate_dev)
                                             : e;
     cudaError_t ej = cudaEventRecord(ms.join, ms.side);
     if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, ms.join, 0);

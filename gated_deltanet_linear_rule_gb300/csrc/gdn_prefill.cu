@@ -36,6 +36,10 @@ namespace {
 __global__ void validate_kernel(PrefillArgs A)
 {
     __shared__ int bad;
+    if (A.gate && *A.gate) {  // a mixed step whose parts overlap: nothing runs
+        if (threadIdx.x == 0) *A.ws.valid = 0;
+        return;
+    }
     if (threadIdx.x == 0) bad = 0;
     __syncthreads();
     if (threadIdx.x == 0 && (A.cu[0] != 0 || A.cu[A.n] != A.T)) atomicOr(&bad, 1);
@@ -331,7 +335,7 @@ bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
 
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
-                           const void* b, const void* z, void* out, cudaStream_t st)
+                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate)
 {
     const LayerParams& L = P.params[(size_t)layer];
     PrefillArgs A;
@@ -368,6 +372,7 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.norm_eps = P.shape.norm_eps;
     A.ws = P.ws;
     A.kq = P.ws.kq;
+    A.gate = gate;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st);
     if (in_bf16) return run<__nv_bfloat16, float>(A, st);
@@ -504,6 +509,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     A.norm_eps = s.norm_eps;
     A.ws = ws;
     A.kq = ws.kq;
+    A.gate = nullptr;
     cudaError_t e;
     const bool in_bf16 = s.io_dtype == 1, out_bf16 = s.out_dtype == 1;
     if (in_bf16 && out_bf16) e = run<__nv_bfloat16, __nv_bfloat16>(A, st);

@@ -607,20 +607,29 @@ cudaError_t launch_clusters(ProjKernel kern, unsigned grid, unsigned cluster, si
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// clusters of c split-K CTAs resident at once (c = 2 or 4; cached; 0 when the query fails)
-int split_clusters(int c)
+constexpr int kMaxDevices = 64;  // per-device caches below (kernel attributes are per device)
+
+// clusters of c split-K CTAs resident at once on device dev (c = 2 or 4; cached; 0 when the
+// query fails)
+int split_clusters(int dev, int c)
 {
     static std::mutex mu;
-    static int cached[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    static int cached[kMaxDevices][5];
+    static bool init[kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
-    if (cached[c] < 0) {
+    if (!init[dev]) {
+        for (int& x : cached[dev]) x = -1;
+        init[dev] = true;
+    }
+    if (cached[dev][c] < 0) {
         const ProjKernel kern = c == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
-        cached[c] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM) == cudaSuccess
-                        ? resident_clusters(kern, (unsigned)c, PROJ_SMEM)
-                        : 0;
+        cached[dev][c] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM) ==
+                                 cudaSuccess
+                             ? resident_clusters(kern, (unsigned)c, PROJ_SMEM)
+                             : 0;
         (void)cudaGetLastError();
     }
-    return cached[c];
+    return cached[dev][c];
 }
 
 cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const Seg* seg, int nseg,
@@ -634,13 +643,16 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     P.K = K;
     P.nseg = nseg;
     P.status = status;
-    if (!P.status) {  // the library's own word on this device (address looked up once per device)
-        static std::mutex mu;
-        static unsigned int* addr[64] = {};
-        int dev = 0;
+    int dev = 0;
+    {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    }
+    if (!P.status) {  // the library's own word on this device (address looked up once per device)
+        static std::mutex mu;
+        static unsigned int* addr[kMaxDevices] = {};
+        cudaError_t e = cudaSuccess;
         std::lock_guard<std::mutex> lock(mu);
         if (!addr[dev]) {
             void* a_ = nullptr;
@@ -652,17 +664,16 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
     }
     for (int i = 0; i < nseg; ++i) P.seg[i] = seg[i];
     cudaError_t e = cudaSuccess;
-    // resident CTAs / CTA pairs of the device (cached; calls from several host threads are
-    // serialised here)
+    // resident CTAs / CTA pairs of the device (cached per device; calls from several host threads
+    // are serialised here)
     static std::mutex mu;
-    static int cached_sms = 0, cached_pairs = 0;
+    static int cached_sms[kMaxDevices] = {}, cached_pairs[kMaxDevices] = {};
     int num_sms = 0, num_pairs = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (cached_sms == 0) {
-            int dev = 0, sms = 0, pairs = 0;
-            e = cudaGetDevice(&dev);
-            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cached_sms[dev] == 0) {
+            int sms = 0, pairs = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM);
             if (e == cudaSuccess)
@@ -673,11 +684,11 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
                                          (int)PairCfg<192>::SMEM);
             if (e == cudaSuccess) pairs = resident_clusters(proj_pair_kernel<256>, 2, PairCfg<256>::SMEM);
             if (e != cudaSuccess) return e;
-            cached_sms = sms;
-            cached_pairs = pairs;
+            cached_sms[dev] = sms;
+            cached_pairs[dev] = pairs;
         }
-        num_sms = cached_sms;
-        num_pairs = cached_pairs;
+        num_sms = cached_sms[dev];
+        num_pairs = cached_pairs[dev];
     }
     // Few tiles (small T): split each tile's K range over a cluster of KS CTAs when at least
     // two CTAs per tile fit on the GPU at once (KS dividing the K slices, every cluster resident).
@@ -687,7 +698,7 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
         int ks = 0;
         for (int c : {4, 2}) {
             if (tiles1 * c > num_sms || KT % c != 0) continue;
-            if (split_clusters(c) < tiles1) continue;
+            if (split_clusters(dev, c) < tiles1) continue;
             ks = c;
             break;
         }

@@ -43,6 +43,10 @@
  *     in the pool's device status word, read by gdn_last_device_status.
  *   - Work on one slot is ordered by the stream; calls on different streams
  *     that touch the same slot must be ordered by the caller.
+ *   - Input range: any finite inputs whose conv outputs, states and per-row sums of
+ *     squares of the outputs stay within fp32 range (|v|, |z| and |S| up to about 1e18).
+ *     The chunked prefill's 16-bit tensor-core operands carry per-chunk power-of-two
+ *     scales, so its range is fp32's, not fp16's.
  *   - Not thread-safe: one host thread per pool at a time.
  *   - Test hook: if the environment variable GDN_DEBUG_FLAGS holds 1 when a pool is
  *     created, that pool's decode kernel fills none of its pipeline stages, so every
@@ -75,6 +79,8 @@ typedef enum {
 #define GDN_DEV_BAD_SLOT_ID 0x2u   /* gdn_slot_ptrs / prefill got a freed, repeated or out-of-range id */
 #define GDN_DEV_BAD_SEQLENS 0x4u   /* prefill cu_seqlens not 0-based, non-decreasing, ending at total */
 #define GDN_DEV_TIMEOUT 0x8u       /* a pipeline wait gave up (the kernel returned early) */
+#define GDN_DEV_SLOT_OVERLAP 0x10u /* gdn_mixed_step: a decode row and a prefill sequence named the same
+                                      slot; the whole step was skipped */
 
 typedef struct {
     int hqk;        /* q/k heads */
@@ -113,7 +119,9 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
 /* Free the pool and everything it owns ("cleanup").  Waits for the device. */
 int gdn_pool_destroy(gdn_pool* pool);
 
-/* Mark every slot free and enqueue zeroing of all state memory on `stream` ("reset"). */
+/* Mark every slot free and enqueue, on `stream`, the clearing of the device-side allocation
+ * flags and the zeroing of all state memory ("reset"): work queued on `stream` before the call
+ * still sees its slots allocated. */
 int gdn_pool_reset(gdn_pool* pool, void* stream);
 
 /* Take a free slot ("add slot").  The slot is zero (S and conv buffer of every
@@ -122,9 +130,11 @@ int gdn_pool_reset(gdn_pool* pool, void* stream);
 int gdn_slot_alloc(gdn_pool* pool, int* slot_id);
 
 /* Return a slot to the free list ("recycle slot") after enqueuing, on
- * `stream`, the zeroing of its S and conv buffer in every layer, so that a
- * later owner starts from a clean state (the slot-reuse contamination checks
- * of the qLLM README, "Results").  Errors: INVALID_ARG, BAD_SLOT (free or out of range). */
+ * `stream`, the clearing of its device-side allocation flag and the zeroing of
+ * its S and conv buffer in every layer, so that a later owner starts from a
+ * clean state (the slot-reuse contamination checks of the qLLM README,
+ * "Results").  Work queued on `stream` before the call still sees the slot
+ * allocated.  Errors: INVALID_ARG, BAD_SLOT (free or out of range). */
 int gdn_slot_recycle(gdn_pool* pool, int slot_id, void* stream);
 
 /* Device address of (slot, layer) (host computation, no GPU work). */
@@ -179,12 +189,17 @@ int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, in
  * gdn_decode_step reads them (the System Design page, "GDN Kernel Dispatch
  * Detail": prefill, then "Update temporal_state").  total_tokens must equal
  * cu_seqlens_dev[n_seqs] and not exceed the pool's max_prefill_tokens; slot
- * ids must be allocated and distinct.  q, k, v, z and out are row-major
+ * ids must be allocated and distinct.  At d = 128 the call also needs
+ * ceil(total_tokens / 64) + n_seqs <= 2 ceil(max_prefill_tokens / 64) + 64 (the pool's
+ * chunk records, one per 64-token chunk of each sequence): a call with many short
+ * prompts may carry about ceil(max_prefill_tokens / 64) + 64 of them; split larger
+ * batches into several calls.  q, k, v, z and out are row-major
  * [total_tokens][width] device buffers whose base addresses are 16-B aligned
  * (they are moved in 16-B pieces and, at d = 128 in bf16, by tensor copies).
  * Uses the pool's workspace: calls on one pool must not overlap on the GPU.
  * Errors: INVALID_ARG (incl. a misaligned row buffer), NO_PARAMS,
- * UNSUPPORTED_SHAPE (too many tokens), CUDA. */
+ * UNSUPPORTED_SHAPE (too many tokens, or too many sequences for the chunk
+ * records), CUDA. */
 int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);
@@ -199,7 +214,9 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
  * ordered after all of it.  The fork and join are stream-capture safe; the first call creates
  * the internal stream and events on the current device, so make one call before capturing.
  * The decode rows' slots and the prefill sequences' slots must be different slots (each
- * call's own rules apply within its part); m = 0 or n_seqs = 0 leaves that part out.  Calls
+ * call's own rules apply within its part): a kernel on `stream` compares them first, and if
+ * any slot is named by both parts it sets GDN_DEV_SLOT_OVERLAP and neither part runs (no
+ * output, state or conv buffer is written).  m = 0 or n_seqs = 0 leaves that part out.  Calls
  * on one pool from several host threads at once are not supported.
  * Errors: those of the two calls; every argument is checked before anything is enqueued. */
 int gdn_mixed_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, int m, const void* dq_dev,

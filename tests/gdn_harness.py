@@ -127,31 +127,42 @@ class Layer:
                                  head_mask=head_mask, threads=threads)
 
 
-def oracle_heads(L: "Layer", layer, cu, inp, S0, conv0, heads, threads=0):
+def oracle_heads(L: "Layer", layer, cu, inp, S0, conv0, heads, threads=0, workers=None):
     """The oracle for selected v-heads only, each on a head-sliced problem (1 q/k head, 1 v head):
     heads are independent apart from the q/k head they read, so the slice is the same computation.
+    The heads run concurrently on host threads (the oracle's C call releases the interpreter lock).
     inp: host arrays (or device tensors) as for Layer.oracle_run; S0 [n][Hv][d][d]; conv0 [n][W-1][C].
     Returns {h: (out [T][d], S [n][d][d])}."""
+    import concurrent.futures as cf
+    import os
+
     d, r, W = L.d, L.hv // L.hqk, L.W
     Cq = L.hqk * d
     p = L.params[layer]
     shape = dict(L.oshape, hqk=1, hv=1)
-    res = {}
-    for h in heads:
+
+    def slice_head(h):
         hk = h // r
         qs, ks, vs = slice(hk * d, (hk + 1) * d), slice(hk * d, (hk + 1) * d), slice(h * d, (h + 1) * d)
-        ch = np.concatenate([np.arange(hk * d, (hk + 1) * d), Cq + np.arange(hk * d, (hk + 1) * d),
-                             2 * Cq + np.arange(h * d, (h + 1) * d)])
         sub = {"q": inp["q"][:, qs], "k": inp["k"][:, ks], "v": inp["v"][:, vs], "z": inp["z"][:, vs],
                "a": inp["a"][:, h:h + 1], "b": inp["b"][:, h:h + 1]}
         # device tensors are sliced on the device and only the head's columns come to the host
-        sub = {k: (host(v) if isinstance(v, torch.Tensor) else np.asarray(v)) for k, v in sub.items()}
+        return {k: (host(v) if isinstance(v, torch.Tensor) else np.asarray(v)) for k, v in sub.items()}
+
+    def run(h, sub):
+        hk = h // r
+        ch = np.concatenate([np.arange(hk * d, (hk + 1) * d), Cq + np.arange(hk * d, (hk + 1) * d),
+                             2 * Cq + np.arange(h * d, (h + 1) * d)])
         o = L.oracle.layer(shape, np.asarray(cu, dtype=np.int64), sub["q"], sub["k"], sub["v"], sub["a"], sub["b"],
                            sub["z"], p["conv_w"][ch], p["A_log"][h:h + 1], p["dt_bias"][h:h + 1], p["norm_w"],
                            np.ascontiguousarray(S0[:, h:h + 1]), np.ascontiguousarray(conv0[:, :, ch]),
                            threads=threads)
-        res[h] = (o["out"], o["S"][:, 0])
-    return res
+        return h, (o["out"], o["S"][:, 0])
+
+    subs = {h: slice_head(h) for h in heads}
+    n = workers or min(len(heads), os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        return dict(ex.map(lambda h: run(h, subs[h]), heads))
 
 
 def random_states(workload, layer, slots, hv, d, var=0.1):

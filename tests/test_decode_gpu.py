@@ -115,11 +115,14 @@ def test_decode_35b_layer_100_steps_fp32_out(pool256_35b):
 
 
 def test_decode_batched_equals_single_bitwise(pool256_35b):
-    """Each slot's output and state in a batch equal the same slot run alone (m = 1), bit for bit.
+    """Each slot's output and state in a batch equal the same slot run alone (m = 1), bit for bit, for
+    64 slots.
     The launches differ in shape: m = 1 runs one item per SM with an 8-stage ring, m = 64 two CTAs
     per SM with 6 stages, m = 256 three CTAs per SM with 4 stages, each CTA taking several items."""
     L, S0 = pool256_35b
     slots = [int(s) for s in synth.distinct_slots(2, 256, 256, sub=1)]
+    N = 64  # slots run alone: every row of the m = 64 batch and the first 64 rows of the m = 256 one
+    blk = L.pool.state_block(0)
     batched = {}
     for m in (256, 64):
         _reset_states(L, S0, slots)
@@ -127,17 +130,30 @@ def test_decode_batched_equals_single_bitwise(pool256_35b):
         for step in range(2):
             inp = L.decode_inputs(list(range(m)), step)
             outs.append(L.gpu_decode(0, slots[:m], inp).clone())
-        batched[m] = (outs, [L.get_state(0, s) for s in slots[:8]])
+        batched[m] = (outs, blk[slots[:N]].clone(), [L.pool.state_views(0, s)[1].clone() for s in slots[:N]])
     _reset_states(L, S0, slots)
-    for j, s in enumerate(slots[:8]):
+    for j, s in enumerate(slots[:N]):
         for step in range(2):
             inp = L.decode_inputs([j], step)
             o = L.gpu_decode(0, [s], inp)
-            for m, (outs, _) in batched.items():
+            for m, (outs, _, _) in batched.items():
                 assert torch.equal(o[0], outs[step][j]), f"slot {s} step {step} output differs from the m = {m} batch"
-        Sg, Cg = L.get_state(0, s)
-        for m, (_, states) in batched.items():
-            assert np.array_equal(Sg, states[j][0]) and np.array_equal(Cg, states[j][1]), f"slot {s} state vs m = {m}"
+    torch.cuda.synchronize()
+    alone = blk[slots[:N]]
+    for m, (_, states, convs) in batched.items():
+        assert torch.equal(alone, states), f"states of the slots run alone vs the m = {m} batch"
+        for j, s in enumerate(slots[:N]):
+            assert torch.equal(L.pool.state_views(0, s)[1], convs[j]), f"slot {s} conv buffer vs m = {m}"
+
+
+def test_decode_m256_every_row_against_oracle(pool256_35b):
+    """One step of the headline batch (m = 256 slots at random pool indices): every row's output and
+    every slot's final state and conv buffer against the oracle."""
+    L, S0 = pool256_35b
+    slots = [int(s) for s in synth.distinct_slots(2, 256, 256)]
+    _reset_states(L, S0, slots)
+    _decode_run(L, 0, slots, 1, S0[slots].astype(np.float64), np.zeros((256, 3, L.C)))
+    assert L.pool.device_status() == 0
 
 
 def test_decode_deterministic(pool256_35b):

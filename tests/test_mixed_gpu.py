@@ -161,3 +161,39 @@ def test_mixed_step_with_one_part_empty():
     check_out(host(out_p), ref["out"], "bf16", PREFILL_TOL, "mixed step prefill-only out")
     assert L.pool.device_status() == 0
     L.close()
+
+
+def test_mixed_step_with_overlapping_slots_does_nothing():
+    """A slot named by a decode row and by a prefill sequence: the device check sets
+    GDN_DEV_SLOT_OVERLAP and neither part runs -- no output, state or conv buffer changes; the next
+    call with disjoint slots runs normally."""
+    L, dec_slots, pre_slots, dec_in, pre_in, cu = _setup(44)
+    T = int(cu[-1])
+    all_slots = dec_slots + pre_slots
+    init = _states(L, all_slots)
+    clash = list(pre_slots)
+    clash[1] = dec_slots[5]  # the second prefill sequence names the sixth decode row's slot
+    ptrs = L.pool.slot_ptrs(0, torch.tensor(dec_slots, dtype=torch.int32, device="cuda"))
+    cu_d = torch.tensor(cu, device="cuda")
+    p = L.to_dev(pre_in)
+    d = dec_in
+    out_d = torch.full((M_DEC, HV * D), 7.0, dtype=torch.bfloat16, device="cuda")
+    out_p = torch.full((T, HV * D), 7.0, dtype=torch.bfloat16, device="cuda")
+    L.pool.mixed_step(0, ptrs, M_DEC, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], out_d, cu_d,
+                      torch.tensor(clash, dtype=torch.int32, device="cuda"), len(clash), T, p["q"], p["k"], p["v"],
+                      p["a"], p["b"], p["z"], out_p)
+    torch.cuda.synchronize()
+    assert L.pool.device_status() & 0x10
+    assert torch.all(out_d == 7.0) and torch.all(out_p == 7.0)
+    for (S0, C0), (S1, C1) in zip(init, _states(L, all_slots)):
+        assert torch.equal(S0, S1) and torch.equal(C0, C1)
+    # disjoint slots: the step runs (and clears the gate for the calls after it)
+    L.pool.mixed_step(0, ptrs, M_DEC, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], out_d, cu_d,
+                      torch.tensor(pre_slots, dtype=torch.int32, device="cuda"), len(pre_slots), T, p["q"], p["k"],
+                      p["v"], p["a"], p["b"], p["z"], out_p)
+    torch.cuda.synchronize()
+    assert L.pool.device_status() == 0
+    n = len(PRE_LENGTHS)
+    ref = L.oracle_run(0, cu, pre_in, np.zeros((n, HV, D, D)), np.zeros((n, L.W - 1, L.C)))
+    check_out(host(out_p), ref["out"], "bf16", PREFILL_TOL, "mixed step prefill out after an overlap")
+    L.close()

@@ -111,3 +111,53 @@ def test_contamination_reused_slots_equal_isolated_runs():
         for a, b in zip(got, rows):
             assert np.array_equal(a, b), f"sequence {sid} differs from its isolated run"
         I.close()
+
+
+def test_recycle_and_reset_are_ordered_after_work_queued_on_their_stream():
+    """gdn_slot_recycle and gdn_pool_reset clear the device allocation flags on the stream they are
+    given: a prefill queued earlier on that (non-blocking) stream still finds its slot allocated and
+    runs, and the zeroing follows it."""
+    L = Layer(3, 2, 2, 16, io="f32", num_slots=2, max_prefill_tokens=64)
+    inp, cu = synth.varlen_inputs(3, 0, [20], 2, 2, 16, 16, "f32")
+    d = L.to_dev(inp)
+    cu_d = torch.tensor(cu, device="cuda")
+    st = torch.cuda.Stream()
+    for how in ("recycle", "reset"):
+        s = L.pool.alloc()
+        ids = torch.tensor([s], dtype=torch.int32, device="cuda")
+        out = torch.full((20, 32), 7.0, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            torch.cuda._sleep(20_000_000)  # keeps the prefill queued while the host goes on
+            L.pool.prefill_varlen(0, cu_d, ids, 1, 20, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], out, stream=st)
+            if how == "recycle":
+                L.pool.recycle(s, stream=st)
+            else:
+                L.pool.reset(stream=st)
+        st.synchronize()
+        assert L.pool.device_status(stream=st) == 0, how
+        assert not torch.any(out == 7.0), f"{how}: the queued prefill did not run"
+        Sg, Cg = L.get_state(0, s)
+        assert not Sg.any() and not Cg.any(), f"{how}: the slot was not zeroed after the prefill"
+    L.close()
+
+
+def test_chunked_prefill_sequence_bound():
+    """At d = 128 a call needs ceil(T / 64) + n_seqs chunk records at most, and the pool holds
+    2 ceil(max_prefill_tokens / 64) + 64: 80 short prompts in 1 024 tokens fill a 1 024-token pool's
+    96 records exactly and run (against the oracle); 81 are refused with UNSUPPORTED_SHAPE."""
+    L = Layer(33, 1, 2, 128, io="bf16", out="f32", num_slots=81, max_prefill_tokens=1024)
+    slots = [L.pool.alloc() for _ in range(81)]
+    lengths = [12] * 79 + [76]
+    inp, cu = synth.varlen_inputs(33, 0, lengths, 1, 2, 128, 128, "bf16")
+    o = host(L.gpu_prefill(0, slots[:80], inp, cu))
+    n = len(lengths)
+    ref = L.oracle_run(0, cu, inp, np.zeros((n, 2, 128, 128)), np.zeros((n, 3, L.C)))
+    assert np.abs(o - ref["out"]).max() <= 5e-3 * np.abs(ref["out"]).max()
+    assert L.pool.device_status() == 0
+    lengths = [12] * 80 + [64]
+    inp, cu = synth.varlen_inputs(33, 0, lengths, 1, 2, 128, 128, "bf16")
+    with pytest.raises(binding.GdnError) as e:
+        L.gpu_prefill(0, slots, inp, cu)
+    assert e.value.code == -6
+    L.close()

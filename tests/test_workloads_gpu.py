@@ -4,12 +4,12 @@ Mixed continuous batch with slot reuse: a 512-slot pool of the 35B-A3B-shaped la
 iteration finishes 2 random sequences (their slots are recycled), admits 2 new 8192-token
 prompts into the recycled slots and decodes 32 random active sequences one step; 50
 iterations.  No contamination: every sequence's outputs equal an isolated run of the same
-sequence (same kernels, alone in a fresh pool) bit for bit, and sampled heads of one sequence
-match the fp64 oracle.
+sequence (same kernels, alone in a fresh pool) bit for bit, and eight of the 32 heads of one
+sequence match the fp64 oracle.
 
 Long context: one 80 000-token prefill (1 250 chunks), then decode at m = 256 on each of 30
-stacked layer pools (30 x 256 slots, 16.1 GB of fp32 state); sampled heads and slots against
-the oracle.  Inputs are drawn on the device by the seeded generator (too large for the host
+stacked layer pools (30 x 256 slots, 16.1 GB of fp32 state); eight of the 32 heads and sampled
+slots against the oracle.  Inputs are drawn on the device by the seeded generator (too large for the host
 generator); the oracle runs per sampled head on the head's slice of the inputs.
 """
 import numpy as np
@@ -80,10 +80,10 @@ def test_mixed_continuous_batch_with_slot_reuse():
             od = I.gpu_decode(0, [s], dinp)
             assert torch.equal(od[0], row), f"sequence {sid}: decode step {step} differs from its isolated run"
         I.pool.recycle(s)
-    # the oracle on two heads of the sequence that decoded the most steps
+    # the oracle on eight heads of the sequence that decoded the most steps
     sid = max(rec_dec, key=lambda k: len(rec_dec[k]))
     inp = synth.device_token_inputs(4, 0, sid, PL, HQK, HV, D, D, "bf16")
-    heads = [3, 30]
+    heads = [0, 1, 3, 12, 17, 22, 30, 31]
     C = I.C
     ref = oracle_heads(I, 0, [0, PL], inp, np.zeros((1, HV, D, D)), np.zeros((1, W - 1, C)), heads)
     got = host(rec_pre[sid])
@@ -105,7 +105,7 @@ def test_long_prefill_80k_then_30_layer_decode():
 
     inp = synth.device_token_inputs(5, 0, 0, T, HQK, HV, D, D, "bf16")
     out = L.gpu_prefill(0, [slots[0]], inp, [0, T])
-    heads = [0, 31]
+    heads = [0, 1, 9, 14, 17, 22, 30, 31]
     ref = oracle_heads(L, 0, [0, T], inp, np.zeros((1, HV, D, D)), np.zeros((1, W - 1, L.C)), heads)
     got = host(out)
     S0, C0 = L.get_state(0, slots[0])
