@@ -26,8 +26,8 @@
 //     blocked triangular inverse of I + A on the CUDA cores (16-wide diagonal blocks, then
 //     16 -> 32 -> 64 by  T_21 = -T_22 A_21 T_11)
 //     MMA3  [T2; 0] x V + [0; T1] x K   -> U (rows 0-63), W (rows 64-127)       128 x 128 x 128
-//   and writes per (chunk, v-head) a record: the W, U and P images and the chunk's scalars
-//   (decay factors, scale exponents); per (chunk, q/k head) the [K; Q] tile.
+//   and writes per (chunk, v-head) a record: the W, U, P and output-gate images and the
+//   chunk's scalars (decay factors, scale exponents); per (chunk, q/k head) the [K; Q] tile.
 // State pass (chunk_state_kernel, double-buffered bulk copies of the records):
 //     MMA4  [W; Q] x S0^T    -> W S0^T (rows 0-63), Q S0^T (rows 64-127)          128 x 64 x 128
 //     Delta
@@ -42,7 +42,8 @@
 // its growth), and the products are taken back to true units in fp32.  Power-of-two scales
 // are exact, so they change no rounding but that of values that would otherwise overflow
 // or fall below fp16's normal range.  The decay factors e^{G_i} multiply the output rows in
-// fp32, after MMA4, for the same reason.  Transposed operands (K, V, W, U as the N side;
+// fp32, after MMA4, for the same reason; the output gates silu(z) w_n are stored in fp16
+// with a power-of-two scale per token.  Transposed operands (K, V, W, U as the N side;
 // Delta~ as the M side) are read MN-major straight from row-wise tiles.
 // Every tcgen05.ld / st is executed by whole warps (they are warp-collective); per-token
 // conditions only guard stores.
@@ -66,8 +67,9 @@ using Op = __half;
 constexpr uint32_t REC_W = 0;        // W' image [token][dk]: two 64-wide halves 8 KiB apart (W = W' 2^ew)
 constexpr uint32_t REC_U = 16384;    // U' image [token][dv], same layout (U = U' 2^eu)
 constexpr uint32_t REC_P = 32768;    // P image [i][j], 64 x 64
-constexpr uint32_t REC_SC = 40960;   // the chunk's scalars, SC_* below
-constexpr uint32_t REC_BYTES = 41984;
+constexpr uint32_t REC_GZ = 40960;   // output gates silu(z) w_n 2^-ez(token), fp16 [token][dv], W' layout
+constexpr uint32_t REC_SC = 57344;   // the chunk's scalars, SC_* below
+constexpr uint32_t REC_BYTES = 58368;
 // per (chunk, q/k head): the [K; Q] tile, two 64-wide d_k halves of 128 rows (64 K rows, then
 // 64 Q rows), 16 KiB apart
 constexpr uint32_t QK_BYTES = 32768;
@@ -79,7 +81,8 @@ constexpr int SC_EU = 129;   // eu (int): U = U' 2^eu
 constexpr int SC_EW = 130;   // ew (int): W = W' 2^ew
 constexpr int SC_MU = 131;   // max |U'|
 constexpr int SC_MW = 132;   // max |W'|
-constexpr uint32_t SC_BYTES = 544;
+constexpr int SC_EZ = 136;   // [64] ez (int): token i's gates are stored times 2^-ez
+constexpr uint32_t SC_BYTES = 800;
 
 // pre-pass shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t P_A1 = 0;          // [K; Q] (MMA1 and MMA3; leaves as the (chunk, q/k head) [K; Q] tile)
@@ -99,12 +102,12 @@ constexpr size_t P_SMEM = P_SMALL + 3072 + 1024;  // small area (2.8 KB) + align
 constexpr int FS = 68;                // fp32 matrix row stride: 16-B aligned rows, 4-wide row loads and stores
 
 // state-pass shared memory (one CTA per (sequence, v-head, d_v half))
-// One record buffer: the [W'; Q] operand (2 K-tiles of 128 rows) | K image | U' half |
-// scalars.  P goes to a slot of its own (two of them, by chunk parity), each after an 8 KiB
-// zero block: MMA7 reads [0; P] as its 128-row operand.
-constexpr uint32_t B_A = 0, B_K = 32768, B_U = 49152, B_SC = 57344;
-constexpr uint32_t S_TX = 32768 + 16384 + 8192 + SC_BYTES;  // bytes fetched into one record buffer
-constexpr uint32_t S_BUF = 58368;
+// One record buffer: the [W'; Q] operand (2 K-tiles of 128 rows) | K image | U' half | gates
+// half | scalars.  P goes to a slot of its own (two of them, by chunk parity), each after an
+// 8 KiB zero block: MMA7 reads [0; P] as its 128-row operand.
+constexpr uint32_t B_A = 0, B_K = 32768, B_U = 49152, B_GZ = 57344, B_SC = 65536;
+constexpr uint32_t S_TX = 32768 + 16384 + 8192 + 8192 + SC_BYTES;  // bytes fetched into one record buffer
+constexpr uint32_t S_BUF = 66560;
 constexpr uint32_t S_S0 = 2 * S_BUF;     // S0^T(:, half) 2^-Es in fp16, MN-major: 128 rows (d_k) of 64 d_v
 constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) 2^-Ed [token][64 d_v]
 constexpr uint32_t S_DL = S_A6 + 8192;   // [2] Delta(:, half) 2^-Ed [token][64 d_v], by chunk parity
@@ -278,6 +281,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     unsigned int* s_vmax = reinterpret_cast<unsigned int*>(sSet + 664);
     unsigned int* s_umax = s_vmax + 8;
     unsigned int* s_wmax = s_vmax + 16;
+    int* sEZ = reinterpret_cast<int*>(sSet + 688);  // [64] the current head's gate scale exponents per token
     float* FA = reinterpret_cast<float*>(sm + P_R4);
     float* FT = reinterpret_cast<float*>(sm + P_R5);
     float* X = reinterpret_cast<float*>(sm + P_T1);
@@ -309,9 +313,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg;
 
     // Per-head inputs nothing waits for yet are loaded one head ahead: the gate inputs a, b of
-    // token tid and the head's A_log, dt_bias (warps 0 and 1) and (bf16) the head's v conv taps.
+    // token tid and the head's A_log, dt_bias (warps 0 and 1), the chunk's z rows, and (bf16)
+    // the head's v conv taps.
     TIn ga = TIn(0.f), gb = TIn(0.f);
     float a_log = 0.f, dt_b = 0.f;
+    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 values
+    uint4 zpark[4][ZW];
     constexpr int KV = D * WM / NT;  // v taps per thread
     float tvv[KV];
     // gate inputs of head h for the threads of warp pair `pair` (token tid % 64)
@@ -327,6 +334,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
     };
     auto prefetch_head = [&](int h) {
+        const TIn* zin = static_cast<const TIn*>(A.z);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
+#pragma unroll
+            for (int wd = 0; wd < ZW; ++wd)
+                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        }
         if constexpr (sizeof(TIn) == 2) {
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
@@ -636,6 +652,39 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         bulk_commit();
     }
 
+    // the output gates silu(z) w_n of the head into the W area, from where one bulk copy takes
+    // them to the record.  A token's gates are stored times 2^-ez, ez chosen from the token's
+    // largest gate by the 16 threads that hold its 128 channels (a half-warp), so that any z
+    // keeps fp16's relative precision; ez goes to the record with the chunk's scalars.
+    auto gates = [&]() {
+        float2 nw[4];  // the norm weights of this thread's 8 channels (the same for every q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) nw[e] = make_float2(__ldg(A.norm_w + 8 * cg + 2 * e), __ldg(A.norm_w + 8 * cg + 2 * e + 1));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
+            const TIn* zv = reinterpret_cast<const TIn*>(zpark[q]);
+            float2 g2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g2[e] = mul2(silu2(make_float2(to_f(zv[2 * e]), to_f(zv[2 * e + 1]))), nw[e]);
+            float m = fmaxf(fmaxf(fmaxf(fabsf(g2[0].x), fabsf(g2[0].y)), fmaxf(fabsf(g2[1].x), fabsf(g2[1].y))),
+                            fmaxf(fmaxf(fabsf(g2[2].x), fabsf(g2[2].y)), fmaxf(fabsf(g2[3].x), fabsf(g2[3].y))));
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            const int ez = scale_exp(m, 14);
+            const float2 f2 = make_float2(pow2f(-ez), pow2f(-ez));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g2[e] = mul2(g2[e], f2);
+            uint4 wv;
+            wv.x = i < n ? pack_half2(g2[0].x, g2[0].y) : 0u;
+            wv.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
+            wv.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
+            wv.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
+            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = wv;
+            if ((idx & 15) == 0) sEZ[i] = ez;
+        }
+        tc::fence_proxy_async();
+    };
     auto zero_block = [&](uint32_t off) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) *reinterpret_cast<uint4*>(sm + off + (tid + q * NT) * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -647,7 +696,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         tc::mma_k(tm + 128, smem_addr(sm + P_A1), 128, smem_addr(sm + P_A1), 128, D, tc::idesc_f16(128, 64), 0);
     zero_block(P_Z0);
     zero_block(P_Z1);
-    tc::fence_proxy_async();
+    gates();
     mma_done();
 
     for (int jh = 0; jh < A.r && ok; ++jh) {
@@ -681,8 +730,12 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                 conv_v_f32(h);
             }
             if constexpr (sizeof(TIn) == 2) zero_block(P_Z0);  // it held these v rows
-            tc::fence_proxy_async();
+            gates();
             sync_all();
+        }
+        if (tid == 0) {
+            bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
+            bulk_commit();
         }
         if (jh + 1 < A.r) {
             prefetch_head(h + 1);
@@ -726,6 +779,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             }
         }
         tc::fence_proxy_async();  // P leaves for the record by a bulk copy
+        if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the W area
         __syncthreads();
         if (tid == 0) {
             bulk_s2g(rec + REC_P, sm + P_P, 8192);
@@ -931,6 +985,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         if (tid < 64) {
             scr[SC_GAM + tid] = sGam[tid];
             scr[SC_EG + tid] = sEG[tid];
+            reinterpret_cast<int*>(scr)[SC_EZ + tid] = sEZ[tid];
         }
         if (tid == 0) {
             scr[SC_EGL] = sMisc[0];
@@ -970,9 +1025,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 // sends its half's 64 per-token sums into the other CTA's shared memory and arrives on that
 // CTA's mbarrier (distributed shared memory).  Warps w with w % 4 < 2 hold rows 0-63 (Delta);
 // the others hold rows 64-127 and read the output one chunk behind the chain, finishing its
-// rows one more behind (once the other CTA's sums are in), with the output gate silu(z) w_n
-// formed from z in fp32; thread PF of warp 2 fetches the records, thread 0 issues the
-// products.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
+// rows one more behind (once the other CTA's sums are in); thread PF of warp 2 fetches the
+// records, thread 0 issues the products.  8 warps: warp w reads TMEM lane quarter w % 4 and works on columns
 // 32 (w / 4) .. + 31.
 
 template <typename TIn, typename TOut>
@@ -990,10 +1044,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     uint64_t* const bar7o = peer_bar + 7;                        // MMA7 completion, odd chunks
     float* s_ss = reinterpret_cast<float*>(sm + S_SMALL + 128);  // [2][2][64] sums of O^2: chunk parity, column half
     float* peer_ss = s_ss + 256;                                 // [2][64] the other CTA's sums, by chunk parity
-    float* s_nw = peer_ss + 128;                                 // [64] norm weights of this CTA's d_v half
     // [2][8] per-warp max |S0| by chunk parity, then [16] the incoming state's maximum (bit
     // patterns of non-negative floats)
-    unsigned int* s_smax = reinterpret_cast<unsigned int*>(s_nw + 64);
+    unsigned int* s_smax = reinterpret_cast<unsigned int*>(peer_ss + 128);
 
     // both CTAs of a cluster take these exits together (they depend on the sequence only)
     if (!*A.ws.valid) return;
@@ -1024,7 +1077,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         fence_mbar_init();
         s_smax[16] = 0u;
     }
-    if (tid < 64) s_nw[tid] = __ldg(A.norm_w + half * 64 + tid);
     if (warp == 0) tc::alloc(tmem_slot, 512);
     sync_all();
     cluster_sync_all();  // the other CTA's barriers exist before anything arrives on them
@@ -1035,7 +1087,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     int mma7_issued = 0;                // MMA7s so far (thread 0)
     auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
     // the record's [W'; Q] operand (the W' image and the Q rows of the [K; Q] tile, per 64-wide
-    // d_k half), the K rows of the tile, the U' half and the scalars
+    // d_k half), the K rows of the tile, the U' half, the gates half and the scalars
     auto fetch_main = [&](int c) {
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = record(c);
@@ -1049,6 +1101,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         bulk_g2s(dst + B_K, qk, 8192, fb);
         bulk_g2s(dst + B_K + 8192, qk + 16384, 8192, fb);
         bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, fb);
+        bulk_g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, fb);
         bulk_g2s(dst + B_SC, rec + REC_SC, SC_BYTES, fb);
         main_issued = c + 1;
     };
@@ -1140,10 +1193,11 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     }
 
     // output rows (rows >= 64 only, this thread's 32 columns): o holds O_i of the chunk waiting
-    // for the other CTA's sums, zr its z values; eg_n is e^{G_i} of the chunk just computed
+    // for the other CTA's sums, gzr / ezr its gates and their scale exponent; gzn / ezn and eg_n
+    // the gates, exponent and e^{G_i} of the chunk just computed
     float o[32];
-    constexpr int ZW = sizeof(TIn) / 2;  // 16-B words per 8 z values
-    uint4 zr[4 * ZW];
+    uint4 gzn[4], gzr[4];
+    int ezn = 0, ezr = 0;
     float eg_n = 0.f;
     const int orow = row - 64, col0 = half * 64 + 32 * hf;
     auto finish_rows = [&](int pc) -> bool {  // false when the sums never came
@@ -1152,28 +1206,21 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         if (gotp && orow < pn) {
             const float rs =
                 rms_scale(s_ss[(pc & 1) * 128 + orow] + s_ss[(pc & 1) * 128 + 64 + orow] + peer_ss[(pc & 1) * 64 + orow],
-                          A.norm_eps, D);
+                          A.norm_eps, D) *
+                pow2f(ezr);
             TOut* dst = out + (size_t)(t0 + pc * CH + orow) * Dv + (size_t)h * D + col0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const TIn* zq = reinterpret_cast<const TIn*>(zr + q * ZW);
-                const float4 w0 = *reinterpret_cast<const float4*>(s_nw + 32 * hf + 8 * q);
-                const float4 w1 = *reinterpret_cast<const float4*>(s_nw + 32 * hf + 8 * q + 4);
-                const float nw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                float y[8];
+                float gz[8], y[8];
+                unpack8(gzr[q], gz);
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float2 g = mul2(silu2(make_float2(to_f(zq[e]), to_f(zq[e + 1]))), make_float2(nw[e], nw[e + 1]));
-                    y[e] = o[8 * q + e] * rs * g.x;
-                    y[e + 1] = o[8 * q + e + 1] * rs * g.y;
-                }
+                for (int e = 0; e < 8; ++e) y[e] = o[8 * q + e] * rs * gz[e];
                 store8<TOut>(dst + 8 * q, y);
             }
         }
         return gotp;
     };
-    // O of chunk pc from MMA4's rows 64-127 (scale 2^es) and MMA7 (scale 2^ed), its sums of
-    // squares, and the z values of its rows for finish_rows
+    // O of chunk pc from MMA4's rows 64-127 (scale 2^es) and MMA7 (scale 2^ed), its sums of squares
     auto complete_rows = [&](int pc, int es_c, int ed_c) -> bool {
         const bool got7 = mbar_wait_bounded((pc & 1) ? bar7o : bar7e, (uint32_t)((pc >> 1) & 1), nullptr);
         tc::fence_after_sync();
@@ -1188,13 +1235,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             o[e] = fmaf(fz, zz[e], fy * o[e]);
             ss = fmaf(o[e], o[e], ss);
         }
-        s_ss[(pc & 1) * 128 + hf * 64 + orow] = ss;
-        const int pn = min(CH, L - pc * CH);
-        const uint4* zs = reinterpret_cast<const uint4*>(static_cast<const TIn*>(A.z) +
-                                                         (size_t)(t0 + pc * CH + min(orow, pn - 1)) * Dv +
-                                                         (size_t)h * D + col0);
 #pragma unroll
-        for (int w = 0; w < 4 * ZW; ++w) zr[w] = __ldg(zs + w);
+        for (int q = 0; q < 4; ++q) gzr[q] = gzn[q];
+        ezr = ezn;
+        s_ss[(pc & 1) * 128 + hf * 64 + orow] = ss;
         return got7;
     };
     // this half's per-token sums of squares of chunk pc -> the other CTA, by asynchronous
@@ -1245,6 +1289,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         const int es = scale_exp(c == 0 ? smax_p : fmaf(egl_p, smax_p, 64.f * dbound_p), 12);
         {
             float v[32];
+            tc::wait_st();  // the last chunk's store of S (long complete by now)
             tc::ld32(tc::taddr(tm, warp, TS + 32 * hf), v);
             if (c > 0) {
                 float x[32];
@@ -1257,9 +1302,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             } else {
                 tc::wait_ld();
             }
-            float m = 0.f;
+            float mx[8];  // max |v| as a tree (independent partial maxima)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(v[e]));
+            for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fmaxf(fabsf(v[e]), fabsf(v[e + 8])), fmaxf(fabsf(v[e + 16]), fabsf(v[e + 24])));
+            const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float f = pow2f(-es);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -1270,7 +1316,6 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             }
             const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
             if (lane == 0) s_smax[(c & 1) * 8 + warp] = mb;
-            tc::wait_st();
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
@@ -1352,7 +1397,12 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             }
             if ((!gotp || !got7) && lane == 0) atomicOr(A.status, GDN_DEV_TIMEOUT);
             ok = gotp && got7;
-            // this chunk's e^{G_i} of the thread's row, read before this buffer is refetched
+            // this chunk's gates, their exponent and e^{G_i} of the thread's row, read before this
+            // buffer is refetched
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                gzn[q] = *reinterpret_cast<const uint4*>(buf + B_GZ + tc::sw128_chunk(orow, 4 * hf + q));
+            ezn = __float_as_int(sc[SC_EZ + orow]);
             eg_n = sc[SC_EG + orow];
             named_bar_sync(2, NT / 2);  // the four output warps: sums of chunk c - 1 written, buffer read
             if (c >= 1) send_sums(c - 1);
@@ -1388,6 +1438,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     if (ok) {
         // the final state S <- e^{G_last} S + 2^Ed X of the last chunk, in true units
         float v[32], x[32];
+        tc::wait_st();
         tc::ld32(tc::taddr(tm, warp, TS + 32 * hf), v);
         tc::ld32(tc::taddr(tm, warp, TX + 32 * hf), x);
         tc::wait_ld();
@@ -1406,6 +1457,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         for (int c = (p_issued > 2 ? p_issued - 2 : 0); c < p_issued; ++c)
             mbar_wait_bounded(&full_p[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
     }
+    tc::wait_st();
     sync_all();
     if (warp == 0) tc::dealloc(tm, 512);
     // Neither CTA leaves while the other may still write into its shared memory.  Both reach
