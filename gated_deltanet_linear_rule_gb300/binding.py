@@ -137,7 +137,7 @@ class Pool:
     """One slot pool (gdn_pool_create) and the calls that act on it."""
 
     def __init__(self, hqk: int, hv: int, dk: int, dv: int, num_slots: int, num_layers: int = 1, conv_w: int = 4,
-                 io_dtype: str = "bf16", out_dtype: str | None = None, chunk: int = 64, max_prefill_tokens: int = 0,
+                 io_dtype: str = "bf16", out_dtype: str | None = None, chunk: int = 0, max_prefill_tokens: int = 0,
                  l2_eps: float = 1e-6, norm_eps: float = 1e-6):
         self.io_dtype, self.out_dtype = io_dtype, out_dtype or io_dtype
         self.torch_io = _DTYPES[self.io_dtype][1]

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
-SOURCES = ["gdn_pool.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_chunk.cu", "gdn_proj.cu"]
+SOURCES = ["gdn_pool.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_chunk.cu", "gdn_chunk_small.cu", "gdn_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -80,6 +80,7 @@ struct PrefillArgs {
     PrefillWorkspace ws;
     float* kq;  // [T][Hqk] k_hat . q_hat (workspace)
     const int* gate;  // when non-null and *gate != 0 the call does nothing (a mixed step's overlap check)
+    int chunk;        // chunk length of the d < 128 chunked kernel (8, 16, 32 or 64)
 };
 
 // Facts every kernel needs to check a slot pointer before touching memory.
@@ -447,6 +448,9 @@ size_t chunk_record_bytes(int hv, int hqk);
 // chunked tensor-core prefill of the delta rule + gated RMSNorm (d_k = d_v = 128), in two
 // launches: the parallel pre-pass (conv, norms, gates and the chunk-local products; it reads
 // the slots' conv buffers, so it runs before they are updated) and the state pass
+// chunked prefill of the delta rule at d < 128 in fp32 on the CUDA cores (pre-norm output into
+// ws.o and the final states), from the prep kernel's per-token rows
+cudaError_t launch_chunk_small(const PrefillArgs& A, int chunk, cudaStream_t st);
 template <typename TIn>
 cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st);
 template <typename TIn, typename TOut>

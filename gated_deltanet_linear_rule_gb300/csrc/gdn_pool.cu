@@ -134,7 +134,6 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     gdn_pool* P = new (std::nothrow) gdn_pool();
     if (!P) return GDN_ERR_INVALID_ARG;
     P->shape = *shape;
-    if (P->shape.chunk == 0) P->shape.chunk = 64;
     P->num_slots = num_slots;
     P->num_layers = num_layers;
     P->C = 2 * shape->hqk * shape->dk + shape->hv * shape->dv;

@@ -15,16 +15,19 @@
 //   3. chunk state pass  one CTA per (sequence, v-head, d_v half), the two halves a
 //                 cluster: output, final state, and the slot's conv buffer advanced to the
 //                 last W-1 raw inputs (the pre-pass has read the old rows by then)
-// d < 128 (the recurrent path):
+// d < 128:
 //   2. prep       one CTA per token: conv + SiLU over all C channels (the left context
 //                 before a sequence's first token comes from its slot's conv buffer),
 //                 L2 scales of q and k, k.q per q/k head, gates per v-head.
 //   3. conv_tail  as above
-//   4. recurrent  one CTA per (sequence, v-head, row tile of S): the tile of S stays in
-//                 registers across the whole sequence, token after token.
+//   4. with a chunk length set in the shape (8, 16, 32 or 64): chunk_small_kernel
+//                 (gdn_chunk_small.cu), the chunked form in fp32, one CTA per (sequence,
+//                 v-head); with chunk = 0: recurrent, one CTA per (sequence, v-head, row
+//                 tile of S), the tile of S in registers across the whole sequence, token
+//                 after token (measured faster at these head sizes).
 //   5. epilogue   gated RMSNorm per (token, v-head).
-// On the recurrent path kernels 2, 4 and 5 use the decode kernel's arithmetic in the same
-// order, so a prefill of L tokens equals L decode steps bit for bit.
+// The recurrent kernel and kernels 2 and 5 use the decode kernel's arithmetic in the same
+// order, so with chunk = 0 a prefill of L tokens equals L decode steps bit for bit.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -270,13 +273,18 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
     }
     conv_tail_kernel<TIn><<<dim3(A.n, (A.C + 255) / 256), 256, 0, st>>>(A);
     if (A.T > 0) {
-        const int rows = std::min(A.D, 8 * (32 / (A.D / 16)));
-        dim3 grid(A.n, A.hv, A.D / rows);
-        switch (A.D) {
-            case 16: recurrent_kernel<16><<<grid, 256, 0, st>>>(A); break;
-            case 32: recurrent_kernel<32><<<grid, 256, 0, st>>>(A); break;
-            case 64: recurrent_kernel<64><<<grid, 256, 0, st>>>(A); break;
-            default: return cudaErrorInvalidValue;
+        if (A.chunk > 0) {  // the chunked form, with the chunk length the caller asked for
+            cudaError_t e = launch_chunk_small(A, A.chunk, st);
+            if (e != cudaSuccess) return e;
+        } else {  // the token-recurrent kernel (faster at these head sizes)
+            const int rows = std::min(A.D, 8 * (32 / (A.D / 16)));
+            dim3 grid(A.n, A.hv, A.D / rows);
+            switch (A.D) {
+                case 16: recurrent_kernel<16><<<grid, 256, 0, st>>>(A); break;
+                case 32: recurrent_kernel<32><<<grid, 256, 0, st>>>(A); break;
+                case 64: recurrent_kernel<64><<<grid, 256, 0, st>>>(A); break;
+                default: return cudaErrorInvalidValue;
+            }
         }
         const int pairs = A.T * A.hv;
         epilogue_kernel<TIn, TOut><<<(pairs + 7) / 8, 256, 0, st>>>(A);
@@ -373,6 +381,7 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.ws = P.ws;
     A.kq = P.ws.kq;
     A.gate = gate;
+    A.chunk = P.shape.chunk;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st);
     if (in_bf16) return run<__nv_bfloat16, float>(A, st);
@@ -510,6 +519,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     A.ws = ws;
     A.kq = ws.kq;
     A.gate = nullptr;
+    A.chunk = s.chunk;
     cudaError_t e;
     const bool in_bf16 = s.io_dtype == 1, out_bf16 = s.out_dtype == 1;
     if (in_bf16 && out_bf16) e = run<__nv_bfloat16, __nv_bfloat16>(A, st);

@@ -87,7 +87,10 @@ typedef struct {
     int hv;         /* v heads; a multiple of hqk (GQA ratio r = hv / hqk) */
     int dk, dv;     /* head dims; this build supports dk == dv in {16, 32, 64, 128} */
     int conv_w;     /* causal conv taps W, 1..8 */
-    int chunk;      /* prefill chunk length (0 = 64); a performance parameter only */
+    int chunk;      /* prefill chunk length: 0 = the library's choice, or 8, 16, 32, 64.  At d = 128
+                       the tensor-core path always takes chunks of 64.  At d < 128, 0 runs the
+                       token-recurrent kernel and 8..64 the chunked form with that chunk length
+                       (both fp32; the result depends on it only through rounding). */
     int io_dtype;   /* q, k, v, z, a, b and the conv buffer: 0 = fp32, 1 = bf16 */
     int out_dtype;  /* out: 0 = fp32, 1 = bf16 */
     float l2_eps;   /* q, k L2 norm: x * rsqrt(sum x^2 + l2_eps) */

@@ -57,7 +57,7 @@ class Layer:
     """One GDN layer shape with seeded parameters, a pool, and the matching oracle shape."""
 
     def __init__(self, workload: int, hqk: int, hv: int, d: int, conv_w: int = 4, io: str = "bf16",
-                 out: str | None = None, num_slots: int = 8, num_layers: int = 1, chunk: int = 64,
+                 out: str | None = None, num_slots: int = 8, num_layers: int = 1, chunk: int = 0,
                  max_prefill_tokens: int = 0, layer_ids=(0,)):
         self.workload, self.hqk, self.hv, self.d, self.W = workload, hqk, hv, d, conv_w
         self.io, self.out = io, out or io

@@ -232,3 +232,37 @@ def test_prefill_chunked_d128_gqa_ratios(hqk, hv):
         assert np.array_equal(L.get_state(0, s)[1], ref["convbuf"][j])
     assert L.pool.device_status() == 0
     L.close()
+
+
+@pytest.mark.parametrize("d,chunk,io", [(16, 8, "f32"), (32, 16, "f32"), (32, 32, "bf16"), (64, 64, "f32"),
+                                        (64, 16, "bf16")])
+def test_prefill_chunked_small_d(d, chunk, io):
+    """d < 128 runs the chunked (WY) form in fp32 on the CUDA cores with the pool's chunk length: lengths
+    around the chunk boundary, an empty sequence, GQA 2, from random states and conv buffers, against the
+    oracle; then 3 decode steps from the handed-off states."""
+    lengths = [1, chunk - 1, chunk, chunk + 1, 0, 3 * chunk + 5, 2]
+    n = len(lengths)
+    L = Layer(16, 2, 4, d, io=io, out="f32", num_slots=n, chunk=chunk, max_prefill_tokens=sum(lengths))
+    slots = [L.pool.alloc() for _ in range(n)]
+    S0 = np.stack([synth.initial_state(16, 0, j, 4, d, d) for j in range(n)]).astype(np.float64)
+    conv0 = np.stack([synth.initial_convbuf(16, 0, j, 4, L.C, io) for j in range(n)]).astype(np.float64)
+    for j, s in enumerate(slots):
+        L.set_state(0, s, S0[j], conv0[j])
+    inp, cu = synth.varlen_inputs(16, 0, lengths, 2, 4, d, d, io)
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    ref = L.oracle_run(0, cu, inp, S0, conv0)
+    r_out = relerr(o, ref["out"])
+    r_S = max(relerr(L.get_state(0, s)[0], ref["S"][j]) for j, s in enumerate(slots))
+    print(f"chunked d={d} chunk={chunk} io={io}: out {r_out:.2e}, S {r_S:.2e}")
+    assert r_out <= 2e-5 and r_S <= 2e-5
+    for j, s in enumerate(slots):
+        assert np.array_equal(L.get_state(0, s)[1], ref["convbuf"][j])
+    S, conv = ref["S"], ref["convbuf"]
+    for step in range(3):
+        dinp = L.decode_inputs(list(range(n)), step)
+        og = host(L.gpu_decode(0, slots, dinp))
+        r = L.oracle_run(0, np.arange(n + 1), dinp, S, conv)
+        S, conv = r["S"], r["convbuf"]
+        assert relerr(og, r["out"]) <= 2e-5
+    assert L.pool.device_status() == 0
+    L.close()
