@@ -237,17 +237,28 @@ def device_inputs(torch, m, n_sets, seed):
     return [{n: full[n][i] for n in widths} for i in range(n_sets)]
 
 
+def slot_groups(torch, pool, synth, m):
+    """Slot-pointer arrays of the 256 // m disjoint groups of m slots of the pool (random order).  A
+    timed loop at m slots takes the groups in turn, one per step, so that at small m the states a
+    step reads were last touched 256 // m - 1 steps earlier, with (256 - m) x 2.1 MB of other states
+    in between -- more than the 129 MB L2 -- and come from HBM, as the whole 256-slot pool does."""
+    perm = synth.distinct_slots(WORKLOAD_DECODE, NUM_SLOTS, NUM_SLOTS, sub=m)
+    groups = [perm[i * m:(i + 1) * m] for i in range(NUM_SLOTS // m)]
+    return [pool.slot_ptrs(0, torch.tensor(g, dtype=torch.int32, device="cuda")) for g in groups]
+
+
 def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
     """Device time of `steps` back-to-back decode launches at m slots (events on the launching
-    stream around the whole region): (ms per step, ms per launch, ms per launch)."""
-    ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
-    ptrs = pool.slot_ptrs(0, ids)
+    stream around the whole region), each step on the next of the pool's disjoint m-slot groups:
+    (ms per step, ms per launch, ms per launch)."""
+    groups = slot_groups(torch, pool, synth, m)
     n_sets = min(steps + warmup, 200)
     sets = device_inputs(torch, m, n_sets, seed)
     out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     for i in range(warmup):
         s = sets[i % n_sets]
+        ptrs = groups[i % len(groups)]
         pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, stream)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -256,6 +267,7 @@ def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
     t0.record(stream)
     for i in range(steps):
         s = sets[(warmup + i) % n_sets]
+        ptrs = groups[(warmup + i) % len(groups)]
         pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -269,19 +281,20 @@ def time_decode(torch, pool, synth, m, steps, warmup, seed=1):
 
 def time_decode_graph(torch, pool, synth, m, steps, seed=11):
     """Device time per decode step when `steps` steps are replayed from one CUDA graph (no per-call
-    host overhead): the kernel-level number for small m, where launches dominate eager timing."""
-    ids = torch.tensor(synth.distinct_slots(WORKLOAD_DECODE, m, NUM_SLOTS), dtype=torch.int32, device="cuda")
-    ptrs = pool.slot_ptrs(0, ids)
+    host overhead): the kernel-level number for small m, where launches dominate eager timing.
+    Each step takes the next of the pool's disjoint m-slot groups, as in time_decode."""
+    groups = slot_groups(torch, pool, synth, m)
     sets = device_inputs(torch, m, steps, seed)
     out = torch.empty((m, HV * D), dtype=torch.bfloat16, device="cuda")
     cap = torch.cuda.Stream()
     s0 = sets[0]
-    pool.decode_step(0, ptrs, m, s0["q"], s0["k"], s0["v"], s0["a"], s0["b"], s0["z"], out)  # attributes set
+    pool.decode_step(0, groups[0], m, s0["q"], s0["k"], s0["v"], s0["a"], s0["b"], s0["z"], out)  # attributes set
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
-            for s in sets:
+            for i, s in enumerate(sets):
+                ptrs = groups[i % len(groups)]
                 pool.decode_step(0, ptrs, m, s["q"], s["k"], s["v"], s["a"], s["b"], s["z"], out, cap)
     graph.replay()  # warm-up
     torch.cuda.synchronize()
@@ -597,36 +610,56 @@ def time_proj(torch, binding, reps=20):
     return out
 
 
-def cpu_baseline_decode(seconds=10.0, m_sample=16):
-    """fp64 oracle decode steps over a sample of slots, on all host cores, for about `seconds`."""
+def cpu_baseline(seconds=5.0):
+    """The fp64 oracle, as it stands, on the host cores, single-thread and on all cores:
+    decode at m = 256 (a sample of the 256 slots, all 32 heads; the oracle's cost is linear in the
+    slots, so slot-steps/s of the sample is that of the full batch) and prefill tok/s (a prefix of
+    the 80 000-token prompt's shape, all 32 heads; linear in tokens)."""
     import numpy as np
 
     import oracle
     from gated_deltanet_linear_rule_gb300 import synth
 
     o = oracle.load()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
     p = synth.layer_params(WORKLOAD_DECODE, 0, HQK, HV, D, D, W)
     shape = {"hqk": HQK, "hv": HV, "dk": D, "dv": D, "conv_w": W, "l2_eps": 1e-6, "norm_eps": 1e-6}
-    slots = synth.distinct_slots(WORKLOAD_DECODE, M_HEAD, NUM_SLOTS)[:m_sample]
-    S = np.stack([synth.initial_state(WORKLOAD_DECODE, 0, int(s), HV, D, D) for s in slots]).astype(np.float64)
-    conv = np.zeros((m_sample, W - 1, C))
-    done, t0 = 0, time.perf_counter()
-    step = 0
-    while True:
-        inp = synth.batch_inputs(WORKLOAD_DECODE, 0, list(range(m_sample)), 1, HQK, HV, D, D, "bf16", tag="decode",
-                                 sub=step)
-        ts = time.perf_counter()
-        r = o.layer(shape, np.arange(m_sample + 1), inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"],
-                    p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], S, conv)
-        done += m_sample
-        S, conv = r["S"], r["convbuf"]
-        step += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-        del ts
-    el = time.perf_counter() - t0
-    return {"value": done / el, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
-            "sample": f"{step} decode steps of {m_sample} of the 256 slots (all 32 heads), {el:.1f} s"}
+
+    def decode(threads, m_sample):
+        slots = synth.distinct_slots(WORKLOAD_DECODE, M_HEAD, NUM_SLOTS)[:m_sample]
+        S = np.stack([synth.initial_state(WORKLOAD_DECODE, 0, int(s), HV, D, D) for s in slots]).astype(np.float64)
+        conv = np.zeros((m_sample, W - 1, C))
+        done, step, el = 0, 0, 0.0
+        while el < seconds:
+            inp = synth.batch_inputs(WORKLOAD_DECODE, 0, list(range(m_sample)), 1, HQK, HV, D, D, "bf16",
+                                     tag="decode", sub=step)
+            t0 = time.perf_counter()
+            r = o.layer(shape, np.arange(m_sample + 1), inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"],
+                        p["conv_w"], p["A_log"], p["dt_bias"], p["norm_w"], S, conv, threads=threads)
+            el += time.perf_counter() - t0
+            S, conv = r["S"], r["convbuf"]
+            done += m_sample
+            step += 1
+        return done / el, f"{step} decode steps of {m_sample} of the 256 slots, all 32 heads, {el:.1f} s"
+
+    def prefill(threads, T):
+        inp = synth.token_inputs(5, 0, 0, T, HQK, HV, D, D, "bf16")
+        t0 = time.perf_counter()
+        o.layer(shape, np.array([0, T]), inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["z"], p["conv_w"],
+                p["A_log"], p["dt_bias"], p["norm_w"], np.zeros((1, HV, D, D)), np.zeros((1, W - 1, C)),
+                threads=threads)
+        el = time.perf_counter() - t0
+        return T / el, f"the first {T} tokens of an 80 000-token prompt (one sequence, all 32 heads), {el:.1f} s"
+
+    dec_all, dec_all_s = decode(cores, 16)
+    dec_one, dec_one_s = decode(1, 2)
+    pre_all, pre_all_s = prefill(cores, 8192)
+    pre_one, pre_one_s = prefill(1, 2048)
+    return {"value": dec_all, "unit": UNIT, "cores": cores, "threads": cores, "kind": "oracle",
+            "sample": dec_all_s,
+            "decode_single_thread": {"value": dec_one, "unit": UNIT, "threads": 1, "sample": dec_one_s},
+            "prefill": {"value": pre_all, "unit": "tok/s", "threads": cores, "sample": pre_all_s},
+            "prefill_single_thread": {"value": pre_one, "unit": "tok/s", "threads": 1, "sample": pre_one_s}}
 
 
 def run_ours(args):
@@ -683,11 +716,16 @@ def run_ours(args):
             sm, km, _ = time_decode(torch, pool, synth, m, max(10, min(args.steps, 500)), 3, seed=100 + m)
             gm = time_decode_graph(torch, pool, synth, m, 100, seed=200 + m)
             b = m * decode_bytes_per_slot_step() + decode_param_bytes()
-            sweep.append({"m": m, "slot_steps_per_s": m / (sm * 1e-3), "us_per_step": sm * 1e3,
+            sweep.append({"m": m, "bytes_per_step": b, "slot_steps_per_s": m / (sm * 1e-3), "us_per_step": sm * 1e3,
                           "gbs": b / (km * 1e-3) / 1e9, "frac": b / (km * 1e-3) / 1e9 / hbm,
                           "graph_us_per_step": gm * 1e3, "graph_slot_steps_per_s": m / (gm * 1e-3),
                           "graph_frac": b / (gm * 1e-3) / 1e9 / hbm})
-        result["decode_sweep"] = sweep
+        result["decode_sweep"] = {
+            "method": "each step on the next of the 256-slot pool's disjoint m-slot groups (so a step's states "
+                      "were last touched 256/m - 1 steps earlier, with more than the 129 MB L2 of other states in "
+                      "between: HBM, not L2); eager: back-to-back launches; graph: 100 steps replayed from one "
+                      "CUDA graph",
+            "points": sweep}
     if rank == 0:
         e2e, h2d, d2h = time_decode_e2e(torch, pool, synth, M_HEAD, min(args.steps, 2000), args.warmup)
         result["e2e"] = {"value": e2e * world, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -735,7 +773,7 @@ def run_ours(args):
                                              "prefill batch; cuBLAS (torch.matmul) on the same product beside it",
                                  "bound": "tensor", "peak_tflops": bf16, "calls": proj}
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     result["wall_s_timed_region"] = wall
     if rank == 0:
         print(json.dumps(result))
@@ -800,7 +838,8 @@ def main():
                     help="skip the prefill, 80k prefill, mixed-step and 30-layer timings")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle baseline sample")
     ap.add_argument("--no-proj", action="store_true", help="skip the in_proj / out_proj timings")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the oracle baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=5.0,
+                    help="length of each decode sample of the oracle baseline (single-thread and all cores)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
     if args.impl == "reference":
