@@ -22,7 +22,7 @@ STATUS = {
     -5: "device wait timed out", -6: "unsupported shape", -7: "layer parameters not registered",
     -8: "device reported skipped work",
 }
-DEV_BAD_SLOT_PTR, DEV_BAD_SLOT_ID, DEV_BAD_SEQLENS, DEV_TIMEOUT, DEV_SLOT_OVERLAP = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_BAD_SLOT_PTR, DEV_BAD_SLOT_ID, DEV_BAD_SEQLENS, DEV_TIMEOUT, DEV_SLOT_OVERLAP, DEV_BOUNDS = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 
 # every extern "C" symbol include/gdn.h declares
 EXPORTS = [
@@ -57,7 +57,9 @@ class GdnPoolInfo(ctypes.Structure):
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """libgdn.so, or the checked debug build (libgdn_checked.so) when the environment variable
+    GDN_LIBRARY_VARIANT is "checked"."""
+    return _build.LIB_CHECKED if os.environ.get("GDN_LIBRARY_VARIANT") == "checked" else _build.LIB
 
 
 def lib() -> ctypes.CDLL:

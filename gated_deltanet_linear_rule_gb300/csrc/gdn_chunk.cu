@@ -307,10 +307,21 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 
     constexpr int NRT = CH + WM - 1;  // raw rows of a tensor: r = -(WM-1) .. 63 (row slot r + WM - 1)
     const int rb = tid >> 4, cg = tid & 15, r0 = 4 * rb, p0 = c * CH;
+    // the regions a checked build tests this kernel's computed accesses against
+    const size_t sm_bytes = (size_t)(smem_raw + P_SMEM - sm);
+    const size_t rec_region = (size_t)A.ws.chunk_cap * A.hv * REC_BYTES;
+    const size_t qk_region = (size_t)A.ws.chunk_cap * A.hqk * QK_BYTES;
+    const size_t slots_region = (size_t)A.num_slots * A.num_layers * A.slot_bytes;
+    const size_t rowsq = (size_t)A.T * A.hqk * D * sizeof(TIn), rowsv = (size_t)A.T * A.hv * D * sizeof(TIn);
+    auto sm_ok = [&](const void* p, size_t b) { return chk(within(p, b, sm, sm_bytes), A.status); };
+    auto tile_ok = [&](const void* p, size_t b, uint32_t off, uint32_t region) {
+        return chk(within(p, b, sm + off, region), A.status);
+    };
+    auto rec_ok = [&](const void* p, size_t b) { return chk(within(p, b, A.ws.rec, rec_region), A.status); };
     const TIn* qin = static_cast<const TIn*>(A.q);
     const TIn* kin = static_cast<const TIn*>(A.k);
     const TIn* vin = static_cast<const TIn*>(A.v);
-    const int chq = hk * D + 8 * cg, chk = Dq + hk * D + 8 * cg;
+    const int ch_q = hk * D + 8 * cg, ch_k = Dq + hk * D + 8 * cg;
 
     // Per-head inputs nothing waits for yet are loaded one head ahead: the gate inputs a, b of
     // token tid and the head's A_log, dt_bias (warps 0 and 1), the chunk's z rows, and (bf16)
@@ -327,9 +338,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             const int t = tid & 63;
             a_log = __ldg(A.A_log + h);
             dt_b = __ldg(A.dt_bias + h);
-            if (t < n) {
-                ga = static_cast<const TIn*>(A.a)[(size_t)(tc0 + t) * A.hv + h];
-                gb = static_cast<const TIn*>(A.b)[(size_t)(tc0 + t) * A.hv + h];
+            const size_t gi = (size_t)(tc0 + t) * A.hv + h;
+            if (t < n && chk(within(static_cast<const TIn*>(A.a) + gi, sizeof(TIn), A.a, (size_t)A.T * A.hv * sizeof(TIn)),
+                             A.status)) {
+                ga = static_cast<const TIn*>(A.a)[gi];
+                gb = static_cast<const TIn*>(A.b)[gi];
             }
         }
     };
@@ -339,9 +352,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         for (int q = 0; q < 4; ++q) {
             const int idx = tid + q * NT, i = idx >> 4, c8 = (idx & 15) * 8;
 #pragma unroll
-            for (int wd = 0; wd < ZW; ++wd)
-                zpark[q][wd] = i < n ? __ldg(reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+            for (int wd = 0; wd < ZW; ++wd) {
+                const uint4* zp = reinterpret_cast<const uint4*>(zin + (size_t)(tc0 + i) * Dv + (size_t)h * D + c8) + wd;
+                zpark[q][wd] = i < n && chk(within(zp, 16, A.z, rowsv), A.status) ? __ldg(zp) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         if constexpr (sizeof(TIn) == 2) {
 #pragma unroll
@@ -374,9 +388,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             // raw bf16 k, q and the first head's v rows of the chunk by three tensor copies; rows
             // past the tensor are zero, rows of a neighbouring sequence are replaced or never used
             mbar_arrive_expect_tx(sbar, 3 * NRT * 256);
-            tma_load_2d(sm + P_RAW, &M.k, hk * D, y0, sbar);
-            tma_load_2d(sm + P_RAW + NRT * 256, &M.q, hk * D, y0, sbar);
-            tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h0 * D, y0, sbar);
+            if (sm_ok(sm + P_RAW, 3 * NRT * 256)) {
+                tma_load_2d(sm + P_RAW, &M.k, hk * D, y0, sbar);
+                tma_load_2d(sm + P_RAW + NRT * 256, &M.q, hk * D, y0, sbar);
+                tma_load_2d(sm + P_RAW + 2 * NRT * 256, &M.v, h0 * D, y0, sbar);
+            }
         }
     }
     if (tid < 24) s_vmax[tid] = 0u;
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             pk.w = pack_half2(z2[3].x, z2[3].y);
             const int i = r0 + r;
             const uint32_t off = (cg >> 3) * 16384 + tc::sw128_chunk(is_q ? 64 + i : i, cg & 7);
-            *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
+            if (tile_ok(sm + P_A1 + off, 16, P_A1, 32768)) *reinterpret_cast<uint4*>(sm + P_A1 + off) = pk;
         }
     };
     // v row r0 + o times the power of two sc, rounded to fp16 (zero past the chunk's end)
@@ -575,8 +591,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     auto halo = [&](unsigned char* tile_base, int ch0, int idx) {
         const int j = idx >> 4, c16 = idx & 15, p = j - (WM - 1);
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (p >= -(A.W - 1)) x = *reinterpret_cast<const uint4*>(cbuf + (size_t)(A.W - 1 + p) * A.C + ch0 + 8 * c16);
-        *reinterpret_cast<uint4*>(tile_base + (uint32_t)j * 256 + c16 * 16) = x;
+        const TIn* src = cbuf + (size_t)(A.W - 1 + p) * A.C + ch0 + 8 * c16;
+        if (p >= -(A.W - 1) && chk(within(src, 16, A.base, slots_region), A.status))
+            x = *reinterpret_cast<const uint4*>(src);
+        unsigned char* dst = tile_base + (uint32_t)j * 256 + c16 * 16;
+        if (sm_ok(dst, 16)) *reinterpret_cast<uint4*>(dst) = x;
     };
     // bf16: the v taps of a head (prefetched) into a [tap][channel] table
     auto store_vtaps = [&](float* table) {
@@ -615,16 +634,16 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     } else {
         // fp32: the rows through registers, one tensor at a time
         ConvRows<TIn, WM> x;
-        x.load(kin, Dq, hk * D + 8 * cg, cbuf, A.C, chk, A.W, tc0, p0, r0, n);
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chk, A.W);
+        x.load(kin, Dq, hk * D + 8 * cg, cbuf, A.C, ch_k, A.W, tc0, p0, r0, n);
+        ConvRows<TIn, WM>::taps(w, A.conv_w, ch_k, A.W);
         {
             float y[4][8];
 #pragma unroll
             for (int o = 0; o < 4; ++o) x.row(w, o, y[o]);
             qk_rows4(y, false);
         }
-        x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, chq, A.W, tc0, p0, r0, n);
-        ConvRows<TIn, WM>::taps(w, A.conv_w, chq, A.W);
+        x.load(qin, Dq, hk * D + 8 * cg, cbuf, A.C, ch_q, A.W, tc0, p0, r0, n);
+        ConvRows<TIn, WM>::taps(w, A.conv_w, ch_q, A.W);
         {
             float y[4][8];
 #pragma unroll
@@ -647,7 +666,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     conv_v_f32(h0);
     tc::fence_proxy_async();
     sync_all();
-    if (tid == 0) {  // the [K; Q] tile is the (chunk, q/k head) part of the record
+    if (tid == 0 && chk(within(qkimg, QK_BYTES, A.ws.kimg, qk_region), A.status)) {
+        // the [K; Q] tile is the (chunk, q/k head) part of the record
         bulk_s2g(qkimg, sm + P_A1, QK_BYTES);
         bulk_commit();
     }
@@ -680,8 +700,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             wv.y = i < n ? pack_half2(g2[1].x, g2[1].y) : 0u;
             wv.z = i < n ? pack_half2(g2[2].x, g2[2].y) : 0u;
             wv.w = i < n ? pack_half2(g2[3].x, g2[3].y) : 0u;
-            *reinterpret_cast<uint4*>(sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3)) = wv;
-            if ((idx & 15) == 0) sEZ[i] = ez;
+            unsigned char* dst = sm + P_R5 + (c8 >> 6) * 8192 + tc::sw128_chunk(i, (c8 & 63) >> 3);
+            if (tile_ok(dst, 16, P_R5, 16384)) *reinterpret_cast<uint4*>(dst) = wv;
+            if ((idx & 15) == 0 && chk(i < 64, A.status)) sEZ[i] = ez;
         }
         tc::fence_proxy_async();
     };
@@ -733,7 +754,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             gates();
             sync_all();
         }
-        if (tid == 0) {
+        if (tid == 0 && rec_ok(rec + REC_GZ, 16384)) {
             bulk_s2g(rec + REC_GZ, sm + P_R5, 16384);
             bulk_commit();
         }
@@ -762,7 +783,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                     a.y = bi * __expf(Gi - g.y) * v[e4 + 1];
                     a.z = bi * __expf(Gi - g.z) * v[e4 + 2];
                     a.w = bi * __expf(Gi - g.w) * v[e4 + 3];
-                    *reinterpret_cast<float4*>(FA + i * FS + c0 + e4) = a;
+                    if (tile_ok(FA + i * FS + c0 + e4, 16, P_R4, 64 * FS * 4))
+                        *reinterpret_cast<float4*>(FA + i * FS + c0 + e4) = a;
                 }
             } else {
                 float p[32];
@@ -775,13 +797,15 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
                         p[e4 + e] = (c0 + e4 + e <= i) ? __expf(Gi - gg[e]) * v[e4 + e] : 0.f;
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
+                for (int q = 0; q < 4; ++q)
+                    if (tile_ok(sm + P_P + tc::sw128_chunk(i, c0 / 8 + q), 16, P_P, 8192))
+                        tc::st_chunk<Op>(sm + P_P, i, c0 / 8 + q, p + 8 * q);
             }
         }
         tc::fence_proxy_async();  // P leaves for the record by a bulk copy
         if (tid == 0) bulk_wait_read_all();  // the gates' copy has read the W area
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && rec_ok(rec + REC_P, 8192)) {
             bulk_s2g(rec + REC_P, sm + P_P, 8192);
             bulk_commit();
         }
@@ -910,7 +934,8 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             const float4 s0 = *reinterpret_cast<const float4*>(sc), s1 = *reinterpret_cast<const float4*>(sc + 4);
             float v[8] = {t0.x * (s0.x * f), t0.y * (s0.y * f), t0.z * (s0.z * f), t0.w * (s0.w * f),
                           t1.x * (s1.x * f), t1.y * (s1.y * f), t1.z * (s1.z * f), t1.w * (s1.w * f)};
-            tc::st_chunk<Op>(sm + (r < 64 ? P_T2 : P_T1), i, c8, v);
+            const uint32_t toff = r < 64 ? P_T2 : P_T1;
+            if (tile_ok(sm + toff + tc::sw128_chunk(i, c8), 16, toff, 8192)) tc::st_chunk<Op>(sm + toff, i, c8, v);
         }
         __syncthreads();  // A (fp32) is dead from here: its space takes the V image
         // (d') V' image [token][dv] = V 2^-ev for MMA3's second product, from the rows parked in
@@ -929,8 +954,10 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             }
         }
 #pragma unroll
-        for (int o = 0; o < 4; ++o)
-            *reinterpret_cast<uint4*>(sm + P_R4 + (cg >> 3) * 8192 + tc::sw128_chunk(r0 + o, cg & 7)) = vpark[o];
+        for (int o = 0; o < 4; ++o) {
+            unsigned char* dst = sm + P_R4 + (cg >> 3) * 8192 + tc::sw128_chunk(r0 + o, cg & 7);
+            if (tile_ok(dst, 16, P_R4, 16384)) *reinterpret_cast<uint4*>(dst) = vpark[o];
+        }
         tc::fence_proxy_async();
         sync_all();
 
@@ -950,7 +977,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
             if (tid == 0 && jh + 1 < A.r) {
                 bulk_wait_read_all();
                 mbar_arrive_expect_tx(sbar, NRT * 256);
-                tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
+                if (sm_ok(sm + P_T2, NRT * 256)) tma_load_2d(sm + P_T2, &M.v, (h + 1) * D, y0, sbar);
             }
         }
 
@@ -968,7 +995,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 & 63) / 8 + q;
-                    tc::st_chunk<Op>(sm + (row >= 64 ? P_R5 : P_R4) + (c0 >> 6) * 8192, i, ch, v + 8 * q);
+                    const uint32_t toff = row >= 64 ? P_R5 : P_R4;
+                    if (tile_ok(sm + toff + (c0 >> 6) * 8192 + tc::sw128_chunk(i, ch), 16, toff, 16384))
+                        tc::st_chunk<Op>(sm + toff + (c0 >> 6) * 8192, i, ch, v + 8 * q);
                 }
             }
             const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
@@ -976,12 +1005,13 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
         }
         tc::fence_proxy_async();
         sync_all();
-        if (tid == 0) {
+        if (tid == 0 && rec_ok(rec + REC_W, 16384) && rec_ok(rec + REC_U, 16384)) {
             bulk_s2g(rec + REC_W, sm + P_R5, 16384);
             bulk_s2g(rec + REC_U, sm + P_R4, 16384);
             bulk_commit();
         }
         float* scr = reinterpret_cast<float*>(rec + REC_SC);
+        if (!rec_ok(scr, SC_BYTES)) break;
         if (tid < 64) {
             scr[SC_GAM + tid] = sGam[tid];
             scr[SC_EG + tid] = sEG[tid];
@@ -1062,6 +1092,16 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
     TOut* out = static_cast<TOut*>(A.out);
+    // the regions a checked build tests this kernel's computed accesses against
+    const size_t sm_bytes = (size_t)(smem_raw + S_SMEM - sm);
+    const size_t rec_region = (size_t)A.ws.chunk_cap * A.hv * REC_BYTES;
+    const size_t qk_region = (size_t)A.ws.chunk_cap * A.hqk * QK_BYTES;
+    const size_t slots_region = (size_t)A.num_slots * A.num_layers * A.slot_bytes;
+    auto sm_ok = [&](const void* p, size_t b) { return chk(within(p, b, sm, sm_bytes), A.status); };
+    auto slot_ok = [&](const void* p, size_t b) { return chk(within(p, b, A.base, slots_region), A.status); };
+    auto g2s = [&](void* dst, const void* src, uint32_t b, uint64_t* bar, const void* lo, size_t region) {
+        if (sm_ok(dst, b) && chk(within(src, b, lo, region), A.status)) bulk_g2s(dst, src, b, bar);
+    };
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
@@ -1084,30 +1124,32 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     bool ok = true;
     constexpr int PF = 64;  // the thread that fetches the records (warp 2 works on output rows)
     int main_issued = 0, p_issued = 0;  // fetches so far (thread PF)
-    int mma7_issued = 0;                // MMA7s so far (thread 0)
+    int mma7_issued = 0;    // MMA7s so far (thread 0)
     auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
     // the record's [W'; Q] operand (the W' image and the Q rows of the [K; Q] tile, per 64-wide
-    // d_k half), the K rows of the tile, the U' half, the gates half and the scalars
+    // d_k half), the K rows of the tile, the U' half, the gates half and the scalars.  (Issuing a
+    // bulk copy costs its thread tens of nanoseconds; spreading these over three Delta-warp
+    // threads measured slower: every warp of the chunk is on its critical path.)
     auto fetch_main = [&](int c) {
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = record(c);
         const unsigned char* qk = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * QK_BYTES;
         uint64_t* fb = &full[c & 1];
         mbar_arrive_expect_tx(fb, S_TX);
-        bulk_g2s(dst + B_A, rec + REC_W, 8192, fb);
-        bulk_g2s(dst + B_A + 16384, rec + REC_W + 8192, 8192, fb);
-        bulk_g2s(dst + B_A + 8192, qk + 8192, 8192, fb);
-        bulk_g2s(dst + B_A + 16384 + 8192, qk + 16384 + 8192, 8192, fb);
-        bulk_g2s(dst + B_K, qk, 8192, fb);
-        bulk_g2s(dst + B_K + 8192, qk + 16384, 8192, fb);
-        bulk_g2s(dst + B_U, rec + REC_U + half * 8192, 8192, fb);
-        bulk_g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, fb);
-        bulk_g2s(dst + B_SC, rec + REC_SC, SC_BYTES, fb);
+        g2s(dst + B_A, rec + REC_W, 8192, fb, A.ws.rec, rec_region);
+        g2s(dst + B_A + 16384, rec + REC_W + 8192, 8192, fb, A.ws.rec, rec_region);
+        g2s(dst + B_A + 8192, qk + 8192, 8192, fb, A.ws.kimg, qk_region);
+        g2s(dst + B_A + 16384 + 8192, qk + 16384 + 8192, 8192, fb, A.ws.kimg, qk_region);
+        g2s(dst + B_K, qk, 8192, fb, A.ws.kimg, qk_region);
+        g2s(dst + B_K + 8192, qk + 16384, 8192, fb, A.ws.kimg, qk_region);
+        g2s(dst + B_U, rec + REC_U + half * 8192, 8192, fb, A.ws.rec, rec_region);
+        g2s(dst + B_GZ, rec + REC_GZ + half * 8192, 8192, fb, A.ws.rec, rec_region);
+        g2s(dst + B_SC, rec + REC_SC, SC_BYTES, fb, A.ws.rec, rec_region);
         main_issued = c + 1;
     };
     auto fetch_p = [&](int c) {
         mbar_arrive_expect_tx(&full_p[c & 1], 8192);
-        bulk_g2s(sm + S_PZ + (c & 1) * 16384 + 8192, record(c) + REC_P, 8192, &full_p[c & 1]);
+        g2s(sm + S_PZ + (c & 1) * 16384 + 8192, record(c) + REC_P, 8192, &full_p[c & 1], A.ws.rec, rec_region);
         p_issued = c + 1;
     };
     if (tid == PF) {
@@ -1134,7 +1176,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             TIn old[7];
 #pragma unroll
             for (int j = 0; j < 7; ++j)
-                if (j < W - 1) old[j] = static_cast<const TIn*>(static_cast<const void*>(cbuf))[(size_t)j * C + ch];
+                if (j < W - 1 && slot_ok(cbuf + (size_t)j * C + ch, sizeof(TIn)))
+                    old[j] = static_cast<const TIn*>(static_cast<const void*>(cbuf))[(size_t)j * C + ch];
 #pragma unroll
             for (int i = 0; i < 7; ++i) {
                 if (i >= W - 1) break;
@@ -1142,7 +1185,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                 TIn x = old[0];
                 if (pp >= 0) {
                     const size_t t = (size_t)(t0 + pp);
-                    x = ch < Dq       ? static_cast<const TIn*>(A.q)[t * Dq + ch]
+                    const bool in = chk(t < (size_t)A.T, A.status);
+                    x = !in           ? x
+                        : ch < Dq     ? static_cast<const TIn*>(A.q)[t * Dq + ch]
                         : ch < 2 * Dq ? static_cast<const TIn*>(A.k)[t * Dq + (ch - Dq)]
                                       : static_cast<const TIn*>(A.v)[t * (size_t)(A.hv * D) + (ch - 2 * Dq)];
                 } else {
@@ -1150,14 +1195,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                     for (int j = 0; j < 7; ++j)
                         if (j == W - 1 + pp) x = old[j];
                 }
-                cbuf[(size_t)i * C + ch] = x;
+                if (slot_ok(cbuf + (size_t)i * C + ch, sizeof(TIn))) cbuf[(size_t)i * C + ch] = x;
             }
         }
     }
-    // MMA7 of chunk pc (thread 0, right after the chunk's MMA6, where nothing on the chain waits
-    // for this thread): [0; P] x Delta into chunk pc's MMA7 columns; completes on the barrier of
-    // pc's parity; the commit is issued even when the product is not, so that every wait has
-    // its phase
+    // MMA7 of chunk pc (thread 0, right after the chunk's MMA6; issued from a second thread it
+    // measured slower: the two threads' products do not issue in parallel, and that thread's warp
+    // then reaches the next chunk's barrier late): [0; P] x Delta into chunk pc's MMA7 columns;
+    // completes on the barrier of pc's parity; the commit is issued even when the product is not,
+    // so that every wait has its phase
     auto issue_mma7 = [&](int pc, bool go) {
         const bool gotp = mbar_wait_bounded(&full_p[pc & 1], (uint32_t)((pc >> 1) & 1), nullptr);
         if (!gotp) atomicOr(A.status, GDN_DEV_TIMEOUT);
@@ -1181,9 +1227,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         float v[32];
         float m = 0.f;
         const int dv0 = half * 64 + 32 * hf;
+        const bool sok = slot_ok(Sg + (size_t)dv0 * D, (size_t)32 * D * sizeof(float));
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            v[e] = Sg[(size_t)(dv0 + e) * D + row];
+            v[e] = sok ? Sg[(size_t)(dv0 + e) * D + row] : 0.f;
             m = fmaxf(m, fabsf(v[e]));
         }
         tc::st32(tc::taddr(tm, warp, TS + 32 * hf), v);
@@ -1209,13 +1256,14 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
                           A.norm_eps, D) *
                 pow2f(ezr);
             TOut* dst = out + (size_t)(t0 + pc * CH + orow) * Dv + (size_t)h * D + col0;
+            const bool ook = chk(within(dst, 32 * sizeof(TOut), out, (size_t)A.T * Dv * sizeof(TOut)), A.status);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float gz[8], y[8];
                 unpack8(gzr[q], gz);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = o[8 * q + e] * rs * gz[e];
-                store8<TOut>(dst + 8 * q, y);
+                if (ook) store8<TOut>(dst + 8 * q, y);
             }
         }
         return gotp;
@@ -1444,8 +1492,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         tc::wait_ld();
         const float fx = pow2f(ed_p);
         const int dv0 = half * 64 + 32 * hf;
+        if (slot_ok(Sg + (size_t)dv0 * D, (size_t)32 * D * sizeof(float))) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = fmaf(fx, x[e], egl_p * v[e]);
+            for (int e = 0; e < 32; ++e) Sg[(size_t)(dv0 + e) * D + row] = fmaf(fx, x[e], egl_p * v[e]);
+        }
     }
     // every fetched copy must land, and the last MMA7 be done, before the CTA's shared and
     // tensor memory go away

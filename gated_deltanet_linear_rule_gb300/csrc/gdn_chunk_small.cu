@@ -107,6 +107,11 @@ __global__ void __launch_bounds__(SNT) chunk_small_kernel(PrefillArgs A)
     const int tid = threadIdx.x, hk = h / A.r, Dq = A.hqk * D, Dv = A.hv * D;
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
+    // a checked build tests the computed global ranges before the accesses
+    const bool sok = chk(within(Sg, (size_t)D * D * sizeof(float), A.base,
+                                (size_t)A.num_slots * A.num_layers * A.slot_bytes) && t0 >= 0 && t0 + L <= A.T,
+                         A.status);
+    if (!sok) return;
     for (int idx = tid; idx < D * D; idx += SNT) sS[(idx / D) * PD + idx % D] = Sg[idx];
 
     for (int c0 = 0; c0 < L; c0 += C) {

@@ -83,6 +83,37 @@ struct PrefillArgs {
     int chunk;        // chunk length of the d < 128 chunked kernel (8, 16, 32 or 64)
 };
 
+// ------------------------------------------------------- checked builds ----
+// A checked build (compiled with GDN_CHECKED into libgdn_checked.so) has the chunked prefill and
+// projection kernels test every computed global and shared-memory range against the region it
+// belongs to before the access: a failed test sets GDN_DEV_BOUNDS in the call's status word and the
+// access is skipped.  It stands in for a device memory checker.  In normal builds kChecked is false
+// and the tests compile away.
+#ifdef GDN_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// [p, p + bytes) inside [lo, lo + region)
+__device__ __forceinline__ bool within(const void* p, size_t bytes, const void* lo, size_t region)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(lo);
+    return a >= b && a - b <= region && bytes <= region - (a - b);
+}
+
+// true when the access may go ahead: always in normal builds; in checked builds when ok, else the
+// status bit is set
+__device__ __forceinline__ bool chk(bool ok, unsigned int* status)
+{
+    if constexpr (kChecked) {
+        if (!ok) atomicOr(status, GDN_DEV_BOUNDS);
+        return ok;
+    } else {
+        return true;
+    }
+}
+
 // Facts every kernel needs to check a slot pointer before touching memory.
 struct SlotCheck {
     uint64_t base, total_bytes, slot_bytes;

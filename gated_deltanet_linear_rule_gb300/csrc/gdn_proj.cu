@@ -74,6 +74,7 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, int 
 // the 32 output columns n .. n + 31 of row m (in registers) to their segments' buffers
 __device__ __forceinline__ void store_cols(const ProjArgs& P, int m, int n, const float (&v)[32])
 {
+    if (!chk(m >= 0 && m < P.M && n >= 0 && n < P.N, P.status)) return;
     // the segment holding column n (constant indices: the segment table stays in registers)
     Seg sg = P.seg[0];
 #pragma unroll

@@ -81,6 +81,8 @@ typedef enum {
 #define GDN_DEV_TIMEOUT 0x8u       /* a pipeline wait gave up (the kernel returned early) */
 #define GDN_DEV_SLOT_OVERLAP 0x10u /* gdn_mixed_step: a decode row and a prefill sequence named the same
                                       slot; the whole step was skipped */
+#define GDN_DEV_BOUNDS 0x20u       /* checked builds only (libgdn_checked.so): a kernel computed an address
+                                      outside the region it belongs to; that access was skipped */
 
 typedef struct {
     int hqk;        /* q/k heads */
