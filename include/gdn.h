@@ -249,10 +249,12 @@ int gdn_mixed_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, int
  * kernels read from it is written earlier in the same call, so nothing needs clearing, but
  * calls that overlap on the GPU (on different streams, or from different host threads)
  * race on it.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; make that first call
+ * before any stream capture, and do not call this entry point again after a
+ * cudaDeviceReset in the same process (the kept address does not survive it).
  * Errors: INVALID_ARG; UNSUPPORTED_SHAPE when the shape is not built or the call needs more
- * than the 64 MiB of scratch (at Hqk 16, Hv 32, d 128 about 41 KB per token plus 2.6 MB per
- * sequence, i.e. up to 1 536 tokens of one sequence per call: split longer prompts into
+ * than the 64 MiB of scratch (at Hqk 16, Hv 32, d 128 about 37 KB per token plus 2.4 MB per
+ * sequence, i.e. up to 1 728 tokens of one sequence per call: split longer prompts into
  * several calls, which continue from the slots' state); CUDA. */
 int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* conv_w, const float* A_log, const float* dt_bias,
                                const float* norm_w, void* states_dev, int num_slots, const int* cu_seqlens_dev,
