@@ -826,6 +826,26 @@ def run_reference(args):
     }))
 
 
+def run_profile_case(args):
+    """One small case only, for an ncu capture of its kernels: `decode256` (the m = 256 decode on the
+    256-slot pool, 0.54 GB of state) or `prefill8` (the 8-sequence, 15 998-token prefill, under 2 GB
+    with its workspace): W warm-up launches (calls), then K.  Prints one line naming the case and its
+    time; it is not a bench line."""
+    import torch
+
+    from gated_deltanet_linear_rule_gb300 import binding, synth
+
+    torch.cuda.set_device(0)
+    if args.profile_case == "decode256":
+        pool = make_decode_pool(torch, binding, synth)
+        ms, _, _ = time_decode(torch, pool, synth, M_HEAD, args.steps, args.warmup)
+        pool.close()
+    else:
+        ms, _ = time_prefill(torch, binding, synth, args.steps, args.warmup)
+    print(json.dumps({"profile_case": args.profile_case, "warmup": args.warmup, "steps": args.steps,
+                      "ms_per_call": ms}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1, help="ranks (one per GPU, launched by torchrun for N > 1)")
@@ -840,9 +860,13 @@ def main():
     ap.add_argument("--no-proj", action="store_true", help="skip the in_proj / out_proj timings")
     ap.add_argument("--cpu-seconds", type=float, default=5.0,
                     help="length of each decode sample of the oracle baseline (single-thread and all cores)")
+    ap.add_argument("--profile-case", choices=["decode256", "prefill8"], default=None,
+                    help="run only this small case (for an ncu capture of its kernels) and print its time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps, whatever was asked
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
