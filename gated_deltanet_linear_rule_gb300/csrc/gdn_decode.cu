@@ -91,8 +91,6 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
     const int items = A.m * A.hqk;
     const uint32_t item_bytes = (uint32_t)r * D * D * 4;
     const int stages_per_item = (int)((item_bytes + kStageBytes - 1) / kStageBytes);
-    if (A.gate && *A.gate) return;  // a mixed step whose parts name a common slot: nothing runs
-
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
@@ -101,6 +99,13 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // The launch is programmatic (see launch_t): the setup above touches only this CTA's shared
+    // memory and may overlap the end of the previous kernel on the stream; every global access
+    // (slot pointers, states, inputs, the gate) comes after the wait.  The next decode launch may
+    // then start its own setup as soon as this grid's CTAs are all running.
+    grid_dependency_wait();
+    grid_dependents_launch();
+    if (A.gate && *A.gate) return;  // a mixed step whose parts name a common slot: nothing runs
     __syncthreads();
 
     // ------------------------------------------------------------ producer ----
@@ -318,8 +323,20 @@ cudaError_t launch_t(const Pool& P, const DecodeArgs& A, cudaStream_t st)
     }
     const int items = A.m * A.hqk;
     const int grid = std::max(1, std::min(items, per_sm * P.num_sms));
-    kern<<<grid, kThreads, smem, st>>>(A);
-    return cudaGetLastError();
+    // Programmatic stream serialization: the CTAs may be scheduled while the previous kernel on the
+    // stream finishes (at small m the launch and setup are a large part of a step); the kernel
+    // waits for that kernel's completion before its first global access.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, A);
 }
 
 template <typename TIn, typename TOut>

@@ -186,6 +186,22 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch (a kernel launched with the programmatic stream serialization
+// attribute may start before the previous kernel on its stream has finished): block until every
+// prerequisite grid has completed and its memory operations are visible.  Code before this call
+// must touch no global memory that a previous kernel writes or reads.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream, if launched with that attribute, to start its CTAs (they
+// still wait in grid_dependency_wait for this grid to complete).
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))

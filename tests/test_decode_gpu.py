@@ -114,6 +114,43 @@ def test_decode_35b_layer_100_steps_fp32_out(pool256_35b):
     L.close()
 
 
+def test_decode_steps_back_to_back_without_sync():
+    """12 decode steps at m = 8 queued on one stream with no host synchronisation between them (inputs
+    uploaded first, one output buffer per step, the slot-pointer array formed by a kernel right before
+    the first step).  A decode launch may be scheduled while the previous kernel on the stream ends
+    (programmatic launch), so this checks that every step still sees the state and conv buffer that
+    the step before it wrote: all outputs and the final states against the oracle."""
+    L = Layer(2, 16, 32, 128, io="bf16", out="f32", num_slots=16)
+    slots = [L.pool.alloc() for _ in range(8)]
+    init = random_states(2, 0, slots, 32, 128)
+    conv0 = np.stack([synth.initial_convbuf(2, 0, s, 4, L.C, "bf16") for s in slots]).astype(np.float64)
+    for s, Si, ci in zip(slots, init, conv0):
+        L.set_state(0, s, Si, ci)
+    steps = 12
+    idents = list(range(len(slots)))
+    inputs = [L.decode_inputs(idents, step) for step in range(steps)]
+    dev_inputs = [L.to_dev(inp) for inp in inputs]
+    outs = [torch.empty((len(slots), 32 * 128), dtype=torch.float32, device="cuda") for _ in range(steps)]
+    torch.cuda.synchronize()
+    ids = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    ptrs = L.pool.slot_ptrs(0, ids)
+    for step in range(steps):
+        d = dev_inputs[step]
+        L.pool.decode_step(0, ptrs, len(slots), d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], outs[step])
+    torch.cuda.synchronize()
+    S, conv = init.copy(), conv0.copy()
+    for step in range(steps):
+        ref = L.oracle_run(0, np.arange(len(slots) + 1), inputs[step], S, conv)
+        S, conv = ref["S"], ref["convbuf"]
+        check_out(host(outs[step]), ref["out"], "f32", DECODE_TOL, f"decode out step {step}")
+    for j, s in enumerate(slots):
+        Sg, Cg = L.get_state(0, s)
+        assert relerr(Sg, S[j]) <= DECODE_TOL, f"final S of slot {s}"
+        assert np.array_equal(Cg, conv[j]), f"conv buffer of slot {s}"
+    assert L.pool.device_status() == 0
+    L.close()
+
+
 def test_decode_batched_equals_single_bitwise(pool256_35b):
     """Each slot's output and state in a batch equal the same slot run alone (m = 1), bit for bit, for
     64 slots.
