@@ -287,8 +287,9 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     float* X = reinterpret_cast<float*>(sm + P_T1);
 
     if (!*A.ws.valid) return;
-    const int gc = blockIdx.x / A.hqk, hk = blockIdx.x % A.hqk;
-    if (gc >= A.ws.chunk_start[A.n]) return;
+    const int gc = A.seg_lo + (int)(blockIdx.x / A.hqk), hk = blockIdx.x % A.hqk;
+    if (gc >= A.seg_hi || gc >= A.ws.chunk_start[A.n]) return;
+    const int slot_rec = gc - A.seg_lo;  // the record's position in this segment's workspace
     int lo = 0, hi = A.n;  // the sequence of chunk gc: largest s with chunk_start[s] <= gc
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2;
     const int h0 = hk * A.r, Dq = A.hqk * D, Dv = A.hv * D;
-    unsigned char* qkimg = A.ws.kimg + ((size_t)gc * A.hqk + hk) * QK_BYTES;
+    unsigned char* qkimg = A.ws.kimg + ((size_t)slot_rec * A.hqk + hk) * QK_BYTES;
     const TIn* cbuf = reinterpret_cast<const TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) *
                                                                 A.slot_bytes + A.state_bytes);
 
@@ -722,7 +723,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
 
     for (int jh = 0; jh < A.r && ok; ++jh) {
         const int h = h0 + jh;
-        unsigned char* rec = A.ws.rec + ((size_t)gc * A.hv + h) * REC_BYTES;
+        unsigned char* rec = A.ws.rec + ((size_t)slot_rec * A.hv + h) * REC_BYTES;
         const int cs = jh & 1;  // this head's gate arrays
         float* sBEG = sSet + cs * 320;
         float* sG = sBEG + 64;
@@ -1082,12 +1083,20 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     if (!*A.ws.valid) return;
     const int half = blockIdx.x & 1, pair = blockIdx.x >> 1;
     const int s = A.ws.order[pair / A.hv], h = pair % A.hv;
-    const int t0 = A.cu[s], L = A.cu[s + 1] - t0;
-    if (L <= 0) return;
+    const int t0s = A.cu[s], Ls = A.cu[s + 1] - t0s;  // the whole sequence
+    if (Ls <= 0) return;
+    // This launch takes the sequence's chunks whose records lie in the segment [seg_lo, seg_hi):
+    // chunks cb .. ce-1, starting from the state the slot holds (the sequence's initial state, or
+    // the state the previous segment's launch left there).
+    const int nchs = (Ls + CH - 1) / CH, gcs = A.ws.chunk_start[s];
+    const int cb = max(0, A.seg_lo - gcs), ce = min(nchs, A.seg_hi - gcs);
+    if (cb >= ce) return;
+    const bool seq_end = ce == nchs;  // the sequence's last chunk is in this segment
+    const int t0 = t0s + cb * CH, L = min(Ls - cb * CH, (ce - cb) * CH);  // this segment's tokens
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2, row = qd * 32 + lane;
     const int hk = h / A.r, Dv = A.hv * D;
-    const int nch = (L + CH - 1) / CH, gc0 = A.ws.chunk_start[s];
+    const int nch = ce - cb, gc0 = gcs + cb - A.seg_lo;  // chunks here; workspace position of the first
     const uint32_t peer = cluster_ctarank() ^ 1u;
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
@@ -1160,12 +1169,13 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
             fetch_p(1);
         }
     }
-    // While the first records arrive: the slot's conv buffer becomes the sequence's last W-1
-    // raw inputs (older buffer rows where the sequence is shorter).  The pre-pass, which read
-    // the old rows, is complete, and this pass never reads them.  This CTA's channels: its d_v
-    // half of the v-head's channels, and when h is the q/k head's first v-head its half of the
-    // q/k head's q and k channels -- disjoint across the CTAs of the call.
-    {
+    // While the first records arrive (in the segment that holds the sequence's last chunk): the
+    // slot's conv buffer becomes the sequence's last W-1 raw inputs (older buffer rows where the
+    // sequence is shorter).  The pre-pass, which read the old rows, is complete, and this pass
+    // never reads them.  This CTA's channels: its d_v half of the v-head's channels, and when h is
+    // the q/k head's first v-head its half of the q/k head's q and k channels -- disjoint across
+    // the CTAs of the call.
+    if (seq_end) {
         TIn* cbuf = reinterpret_cast<TIn*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes +
                                            A.state_bytes);
         const int Dq = A.hqk * D, W = A.W, C = A.C;
@@ -1181,10 +1191,10 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 #pragma unroll
             for (int i = 0; i < 7; ++i) {
                 if (i >= W - 1) break;
-                const int pp = L - (W - 1) + i;
+                const int pp = Ls - (W - 1) + i;
                 TIn x = old[0];
                 if (pp >= 0) {
-                    const size_t t = (size_t)(t0 + pp);
+                    const size_t t = (size_t)(t0s + pp);
                     const bool in = chk(t < (size_t)A.T, A.status);
                     x = !in           ? x
                         : ch < Dq     ? static_cast<const TIn*>(A.q)[t * Dq + ch]
@@ -1563,8 +1573,10 @@ cudaError_t launch_chunk_prep(const PrefillArgs& A, cudaStream_t st)
         if ((e = encode_rows_map(&maps.k, A.k, Dq, A.T, CH + WM - 1)) != cudaSuccess) return e;
         if ((e = encode_rows_map(&maps.v, A.v, Dv, A.T, CH + WM - 1)) != cudaSuccess) return e;
     }
-    const int max_chunks = (A.T + CH - 1) / CH + A.n;  // bound on the chunks of this call
-    prep<<<max_chunks * A.hqk, NT, P_SMEM, st>>>(A, maps);
+    // the segment's records that this call can have (a bound: the exact count is on the device)
+    const int recs = std::min(A.seg_hi, prefill_call_chunks(A.T, A.n)) - A.seg_lo;
+    if (recs <= 0) return cudaSuccess;
+    prep<<<recs * A.hqk, NT, P_SMEM, st>>>(A, maps);
     return cudaGetLastError();
 }
 

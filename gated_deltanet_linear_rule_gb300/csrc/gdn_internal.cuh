@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -81,6 +82,10 @@ struct PrefillArgs {
     float* kq;  // [T][Hqk] k_hat . q_hat (workspace)
     const int* gate;  // when non-null and *gate != 0 the call does nothing (a mixed step's overlap check)
     int chunk;        // chunk length of the d < 128 chunked kernel (8, 16, 32 or 64)
+    // chunked path (d = 128): the window of global chunk records [seg_lo, seg_hi) that this
+    // pre-pass / state-pass launch pair handles; record gc is stored at workspace position
+    // gc - seg_lo (seg_hi - seg_lo <= ws.chunk_cap)
+    int seg_lo = 0, seg_hi = 0;
 };
 
 // ------------------------------------------------------- checked builds ----
@@ -484,11 +489,19 @@ inline int prefill_max_seqs(int max_tokens) { return max_tokens + 64; }
 // chunk records a pool reserves for calls of up to max_tokens tokens (chunked path, d = 128):
 // a call needs ceil(T / 64) + n_seqs of them at most
 inline bool prefill_chunked(const gdn_shape& s) { return s.dk == 128 && s.dv == 128; }
+// A call whose records exceed the workspace runs in segments of chunk_cap records (prefill_segments),
+// so a pool holds at most kPrefillMaxRecords of them, whatever max_tokens is.
+constexpr int kPrefillMaxRecords = 512;
 inline int prefill_pool_chunk_cap(const gdn_shape& s, int max_tokens)
 {
-    return prefill_chunked(s) ? 2 * ((max_tokens + 63) / 64) + 64 : 0;
+    return prefill_chunked(s) ? std::min(2 * ((max_tokens + 63) / 64) + 64, kPrefillMaxRecords) : 0;
 }
 inline int prefill_call_chunks(int total_tokens, int n_seqs) { return (total_tokens + 63) / 64 + n_seqs; }
+// segments (launch pairs) a call of that size takes with chunk_cap records per segment
+inline int prefill_segments(int total_tokens, int n_seqs, int chunk_cap)
+{
+    return chunk_cap > 0 ? (prefill_call_chunks(total_tokens, n_seqs) + chunk_cap - 1) / chunk_cap : 0;
+}
 // bytes of one chunk record set (all v-heads and q/k heads of one chunk)
 size_t chunk_record_bytes(int hv, int hqk);
 

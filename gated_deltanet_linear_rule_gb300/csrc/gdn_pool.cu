@@ -322,8 +322,6 @@ int check_prefill(gdn_pool* P, int layer, const int* cu_seqlens_dev, const int* 
     if (!P->params[(size_t)layer].set()) return GDN_ERR_NO_PARAMS;
     if (total_tokens > P->shape.max_prefill_tokens) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (n_seqs > gdn::prefill_max_seqs(P->shape.max_prefill_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
-    if (gdn::prefill_chunked(P->shape) && gdn::prefill_call_chunks(total_tokens, n_seqs) > P->ws.chunk_cap)
-        return GDN_ERR_UNSUPPORTED_SHAPE;
     return GDN_OK;
 }
 

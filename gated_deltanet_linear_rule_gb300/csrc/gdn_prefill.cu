@@ -258,9 +258,20 @@ cudaError_t run(const PrefillArgs& A, cudaStream_t st)
 {
     validate_kernel<<<1, 256, 0, st>>>(A);
     if (A.T > 0 && A.D == 128) {
-        cudaError_t e = launch_chunk_prep<TIn>(A, st);  // reads the conv buffers ...
-        if (e != cudaSuccess) return e;
-        return launch_chunk_state<TIn, TOut>(A, st);     // ... which the state pass then advances
+        // one pre-pass / state-pass pair per segment of chunk_cap records (one pair unless the
+        // call has more chunks than the workspace holds); a segment's state pass continues from
+        // the states the previous one left in the slots
+        const int nseg = prefill_segments(A.T, A.n, A.ws.chunk_cap);
+        PrefillArgs S = A;
+        for (int g = 0; g < nseg; ++g) {
+            S.seg_lo = g * A.ws.chunk_cap;
+            S.seg_hi = S.seg_lo + A.ws.chunk_cap;
+            cudaError_t e = launch_chunk_prep<TIn>(S, st);  // reads the conv buffers ...
+            if (e != cudaSuccess) return e;
+            e = launch_chunk_state<TIn, TOut>(S, st);       // ... which the state pass then advances
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     }
     if (A.T > 0) {
         const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);

@@ -97,7 +97,10 @@ typedef struct {
     int out_dtype;  /* out: 0 = fp32, 1 = bf16 */
     float l2_eps;   /* q, k L2 norm: x * rsqrt(sum x^2 + l2_eps) */
     float norm_eps; /* gated RMSNorm: o * rsqrt(mean o^2 + norm_eps) */
-    int max_prefill_tokens; /* capacity of the pool's prefill workspace, in tokens (0 = no prefill) */
+    int max_prefill_tokens; /* the most tokens one prefill call may carry (0 = no prefill).  At
+                               d = 128 the workspace holds the chunk records of at most 512 chunks of
+                               64 tokens (2.4 MB each at Hqk 16, Hv 32); a call with more chunks runs
+                               in segments of that many, one after the other. */
 } gdn_shape;
 
 typedef struct gdn_pool gdn_pool;
@@ -194,17 +197,15 @@ int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, in
  * gdn_decode_step reads them (the System Design page, "GDN Kernel Dispatch
  * Detail": prefill, then "Update temporal_state").  total_tokens must equal
  * cu_seqlens_dev[n_seqs] and not exceed the pool's max_prefill_tokens; slot
- * ids must be allocated and distinct.  At d = 128 the call also needs
- * ceil(total_tokens / 64) + n_seqs <= 2 ceil(max_prefill_tokens / 64) + 64 (the pool's
- * chunk records, one per 64-token chunk of each sequence): a call with many short
- * prompts may carry about ceil(max_prefill_tokens / 64) + 64 of them; split larger
- * batches into several calls.  q, k, v, z and out are row-major
+ * ids must be allocated and distinct; n_seqs may be up to max_prefill_tokens + 64.
+ * At d = 128 a call whose 64-token chunks (counted per sequence) exceed the pool's chunk
+ * records runs as several pre-pass / state-pass segments on the stream, each continuing
+ * from the states the one before left in the slots.  q, k, v, z and out are row-major
  * [total_tokens][width] device buffers whose base addresses are 16-B aligned
  * (they are moved in 16-B pieces and, at d = 128 in bf16, by tensor copies).
  * Uses the pool's workspace: calls on one pool must not overlap on the GPU.
  * Errors: INVALID_ARG (incl. a misaligned row buffer), NO_PARAMS,
- * UNSUPPORTED_SHAPE (too many tokens, or too many sequences for the chunk
- * records), CUDA. */
+ * UNSUPPORTED_SHAPE (too many tokens or sequences), CUDA. */
 int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, const int* slot_ids_dev, int n_seqs,
                        int total_tokens, const void* q_dev, const void* k_dev, const void* v_dev, const void* a_dev,
                        const void* b_dev, const void* z_dev, void* out_dev, void* stream);

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from gated_deltanet_linear_rule_gb300 import binding, synth
-from gdn_harness import Layer, host
+from gdn_harness import PREFILL_TOL, Layer, check_out, host, relerr
 
 pytestmark = pytest.mark.gpu
 
@@ -142,22 +142,41 @@ def test_recycle_and_reset_are_ordered_after_work_queued_on_their_stream():
     L.close()
 
 
-def test_chunked_prefill_sequence_bound():
-    """At d = 128 a call needs ceil(T / 64) + n_seqs chunk records at most, and the pool holds
-    2 ceil(max_prefill_tokens / 64) + 64: 80 short prompts in 1 024 tokens fill a 1 024-token pool's
-    96 records exactly and run (against the oracle); 81 are refused with UNSUPPORTED_SHAPE."""
-    L = Layer(33, 1, 2, 128, io="bf16", out="f32", num_slots=81, max_prefill_tokens=1024)
-    slots = [L.pool.alloc() for _ in range(81)]
-    lengths = [12] * 79 + [76]
-    inp, cu = synth.varlen_inputs(33, 0, lengths, 1, 2, 128, 128, "bf16")
-    o = host(L.gpu_prefill(0, slots[:80], inp, cu))
+def test_chunked_prefill_in_segments():
+    """At d = 128 a pool for 1 024-token calls holds 96 chunk records; a call with more chunks runs in
+    segments, each continuing from the states the one before left in the slots.  95 one-token prompts
+    then a 900-token prompt make 110 chunks: the long prompt's first chunk is in the first segment and
+    its other 14 in the second.  Outputs, final states and conv buffers against the oracle, then two
+    decode steps from those states."""
+    L = Layer(33, 1, 2, 128, io="bf16", out="f32", num_slots=96, max_prefill_tokens=1024)
+    assert L.pool.info().workspace_bytes < 16 * 2 ** 20  # 96 records of 2 x 57 KB + 32 KB, and small tables
+    slots = [L.pool.alloc() for _ in range(96)]
+    lengths = [1] * 95 + [900]
     n = len(lengths)
-    ref = L.oracle_run(0, cu, inp, np.zeros((n, 2, 128, 128)), np.zeros((n, 3, L.C)))
-    assert np.abs(o - ref["out"]).max() <= 5e-3 * np.abs(ref["out"]).max()
-    assert L.pool.device_status() == 0
-    lengths = [12] * 80 + [64]
     inp, cu = synth.varlen_inputs(33, 0, lengths, 1, 2, 128, 128, "bf16")
-    with pytest.raises(binding.GdnError) as e:
-        L.gpu_prefill(0, slots, inp, cu)
-    assert e.value.code == -6
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    ref = L.oracle_run(0, cu, inp, np.zeros((n, 2, 128, 128)), np.zeros((n, 3, L.C)))
+    check_out(o, ref["out"], "f32", PREFILL_TOL, "segmented prefill out")
+    assert L.pool.device_status() == 0
+    S, conv = ref["S"], ref["convbuf"]
+    for j in range(n):
+        Sg, Cg = L.get_state(0, slots[j])
+        assert relerr(Sg, S[j]) <= PREFILL_TOL, f"final S of sequence {j}"
+        assert np.array_equal(Cg, conv[j]), f"conv buffer of sequence {j}"
+    pick = [0, 94, 95]
+    S, conv = S[pick].copy(), conv[pick].copy()
+    for step in range(2):
+        dinp = L.decode_inputs(pick, step)
+        out = host(L.gpu_decode(0, [slots[j] for j in pick], dinp))
+        ref = L.oracle_run(0, np.arange(len(pick) + 1), dinp, S, conv)
+        S, conv = ref["S"], ref["convbuf"]
+        check_out(out, ref["out"], "f32", PREFILL_TOL, f"decode step {step} after the segmented prefill")
+    L.close()
+
+
+def test_chunked_prefill_workspace_is_bounded():
+    """A pool for 80 000-token prefills holds 512 chunk records (1.2 GB at 16/32 heads), not one per
+    chunk of the longest call."""
+    L = Layer(34, 16, 32, 128, io="bf16", num_slots=1, max_prefill_tokens=80000)
+    assert L.pool.info().workspace_bytes < 1.3e9
     L.close()
