@@ -51,6 +51,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -113,7 +114,8 @@ constexpr uint32_t S_A6 = S_S0 + 16384;  // Delta~(:, half) 2^-Ed [token][64 d_v
 constexpr uint32_t S_DL = S_A6 + 8192;   // [2] Delta(:, half) 2^-Ed [token][64 d_v], by chunk parity
 constexpr uint32_t S_PZ = S_DL + 16384;  // [2] zero block | P [i][j], by chunk parity
 constexpr uint32_t S_SMALL = S_PZ + 32768;
-constexpr size_t S_SMEM = S_SMALL + 2048 + 1024;  // small area (barriers, sums, maxima) + slack
+constexpr uint32_t S_POS = S_SMALL + 2048;  // [kPrefillMaxRecords] workspace positions of the segment's chunks
+constexpr size_t S_SMEM = S_POS + 4 * kPrefillMaxRecords + 1024;  // small area (barriers, sums, maxima) + slack
 
 // state-pass tensor memory (512 columns): S^T(:, half) in true units, X = K^T Delta~ of the
 // last chunk, MMA4's and MMA7's results by chunk parity
@@ -287,16 +289,11 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     float* X = reinterpret_cast<float*>(sm + P_T1);
 
     if (!*A.ws.valid) return;
-    const int gc = A.seg_lo + (int)(blockIdx.x / A.hqk), hk = blockIdx.x % A.hqk;
-    if (gc >= A.seg_hi || gc >= A.ws.chunk_start[A.n]) return;
+    const int gc = A.seg_lo + (int)(blockIdx.x / A.hqk), hk = blockIdx.x % A.hqk;  // record, q/k head
+    if (gc >= A.seg_hi || gc >= A.ws.coff[A.ws.valid[1]]) return;
     const int slot_rec = gc - A.seg_lo;  // the record's position in this segment's workspace
-    int lo = 0, hi = A.n;  // the sequence of chunk gc: largest s with chunk_start[s] <= gc
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (A.ws.chunk_start[mid] <= gc) lo = mid;
-        else hi = mid;
-    }
-    const int s = lo, c = gc - A.ws.chunk_start[s];
+    const int2 cp = A.ws.rec_cp[gc];     // chunk index, rank of the sequence
+    const int s = A.ws.order[cp.y], c = cp.x;
     const int tc0 = A.cu[s] + c * CH;
     const int n = min(CH, A.cu[s + 1] - tc0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1085,18 +1082,45 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     const int s = A.ws.order[pair / A.hv], h = pair % A.hv;
     const int t0s = A.cu[s], Ls = A.cu[s + 1] - t0s;  // the whole sequence
     if (Ls <= 0) return;
-    // This launch takes the sequence's chunks whose records lie in the segment [seg_lo, seg_hi):
-    // chunks cb .. ce-1, starting from the state the slot holds (the sequence's initial state, or
-    // the state the previous segment's launch left there).
-    const int nchs = (Ls + CH - 1) / CH, gcs = A.ws.chunk_start[s];
-    const int cb = max(0, A.seg_lo - gcs), ce = min(nchs, A.seg_hi - gcs);
+    // This launch takes the sequence's chunks whose records (chunk c: coff[c] + rank) lie in the
+    // segment [seg_lo, seg_hi): chunks cb .. ce-1, a contiguous run as the record numbers grow
+    // with c, starting from the state the slot holds (the sequence's initial state, or the state
+    // the previous segment's launch left there).
+    const int rank = pair / A.hv, nchs = (Ls + CH - 1) / CH;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int cb = 0, ce = nchs;
+    if (A.seg_hi != INT_MAX) {
+        // cb, ce = the numbers of chunks c whose record coff[c] + rank lies below seg_lo, seg_hi
+        // (it grows with c): counted by all threads at once, one load per thread and step
+        int nlo = 0, nhi = 0;
+        for (int c = tid; c < nchs; c += NT) {
+            const int r = A.ws.coff[c] + rank;
+            nlo += r < A.seg_lo;
+            nhi += r < A.seg_hi;
+        }
+        int* cnt = reinterpret_cast<int*>(sm + S_POS);
+        if (tid == 0) cnt[0] = cnt[1] = 0;
+        __syncthreads();
+        if (nlo) atomicAdd(&cnt[0], nlo);
+        if (nhi) atomicAdd(&cnt[1], nhi);
+        __syncthreads();
+        cb = cnt[0];
+        ce = cnt[1];
+        __syncthreads();
+    }
     if (cb >= ce) return;
     const bool seq_end = ce == nchs;  // the sequence's last chunk is in this segment
     const int t0 = t0s + cb * CH, L = min(Ls - cb * CH, (ce - cb) * CH);  // this segment's tokens
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, hf = warp >> 2, row = qd * 32 + lane;
     const int hk = h / A.r, Dv = A.hv * D;
-    const int nch = ce - cb, gc0 = gcs + cb - A.seg_lo;  // chunks here; workspace position of the first
+    const int nch = ce - cb;  // chunks here (at most kPrefillMaxRecords: one record each)
+    if (nch > kPrefillMaxRecords) {  // cannot happen (segments hold at most that many records); both CTAs leave
+        if (threadIdx.x == 0) atomicOr(A.status, GDN_DEV_BOUNDS);
+        return;
+    }
+    // workspace positions of this segment's chunks
+    int* s_pos = reinterpret_cast<int*>(sm + S_POS);
+    for (int i = tid; i < nch; i += NT) s_pos[i] = A.ws.coff[cb + i] + rank - A.seg_lo;
     const uint32_t peer = cluster_ctarank() ^ 1u;
     float* Sg = reinterpret_cast<float*>(A.base + ((uint64_t)A.ids[s] * A.num_layers + A.layer) * A.slot_bytes) +
                 (size_t)h * D * D;
@@ -1134,7 +1158,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     constexpr int PF = 64;  // the thread that fetches the records (warp 2 works on output rows)
     int main_issued = 0, p_issued = 0;  // fetches so far (thread PF)
     int mma7_issued = 0;    // MMA7s so far (thread 0)
-    auto record = [&](int c) { return A.ws.rec + ((size_t)(gc0 + c) * A.hv + h) * REC_BYTES; };
+    auto record = [&](int c) { return A.ws.rec + ((size_t)s_pos[c] * A.hv + h) * REC_BYTES; };
     // the record's [W'; Q] operand (the W' image and the Q rows of the [K; Q] tile, per 64-wide
     // d_k half), the K rows of the tile, the U' half, the gates half and the scalars.  (Issuing a
     // bulk copy costs its thread tens of nanoseconds; spreading these over three Delta-warp
@@ -1142,7 +1166,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     auto fetch_main = [&](int c) {
         unsigned char* dst = sm + (c & 1) * S_BUF;
         const unsigned char* rec = record(c);
-        const unsigned char* qk = A.ws.kimg + ((size_t)(gc0 + c) * A.hqk + hk) * QK_BYTES;
+        const unsigned char* qk = A.ws.kimg + ((size_t)s_pos[c] * A.hqk + hk) * QK_BYTES;
         uint64_t* fb = &full[c & 1];
         mbar_arrive_expect_tx(fb, S_TX);
         g2s(dst + B_A, rec + REC_W, 8192, fb, A.ws.rec, rec_region);

@@ -36,13 +36,28 @@ struct PrefillWorkspace {
     float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm (recurrent path)
     float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat                     (recurrent path)
     int* order = nullptr;    // [T + 64] sequences ranked by length, longest first
-    int* chunk_start = nullptr;    // [n + 1] first chunk record of each sequence (chunked path)
+    // Chunked path: the call's chunk records are numbered chunk-index-major -- every sequence's
+    // chunk 0 (in length order), then every chunk 1, ... -- so that a segment of records holds a
+    // stretch of chunks of all the sequences still running.  Chunk c of the sequence of rank p is
+    // record coff[c] + p.
+    int* coff = nullptr;     // [ceil(T / 64) + 2] records of chunk index < c; coff[nc] = all records
+    int* ctmp = nullptr;     // [ceil(T / 64) + 2] scratch of the validation kernel
+    int2* rec_cp = nullptr;  // [ceil(T / 64) + T + 64] record -> (chunk index c, rank p)
     unsigned char* rec = nullptr;  // [chunk_cap][Hv] per-(chunk, v-head) records of the chunked path
     unsigned char* kimg = nullptr; // [chunk_cap][Hqk] per-(chunk, q/k head) K images
     int chunk_cap = 0;             // chunk records the workspace holds
-    int* valid = nullptr;    // [1] 1 when the call's cu_seqlens / slot ids passed validation
+    int* valid = nullptr;    // [0] 1 when the call's cu_seqlens / slot ids passed validation;
+                             // [1] chunks of the longest sequence (nc)
     void* base = nullptr;
     size_t bytes = 0;
+};
+
+// A pool's second stream for the chunked prefill's segments: the state pass of segment g runs on
+// it (high priority) while the caller's stream runs the pre-pass of segment g + 1 into the other
+// half of the workspace; events order the two.
+struct SegStreams {
+    cudaStream_t side = nullptr;
+    cudaEvent_t prep[2] = {nullptr, nullptr}, state[2] = {nullptr, nullptr};
 };
 
 struct Pool {
@@ -60,6 +75,7 @@ struct Pool {
     PrefillWorkspace ws;
     int device = 0, num_sms = 0;
     int debug_flags = 0;  // GDN_DEBUG_FLAGS at creation; bit 0: decode producer fills no stage (timeout test)
+    SegStreams seg;       // chunked prefill (d = 128, max_prefill_tokens > 0) only
 };
 
 // Everything the prefill kernels of one call need (device pointers and sizes).
@@ -83,8 +99,8 @@ struct PrefillArgs {
     const int* gate;  // when non-null and *gate != 0 the call does nothing (a mixed step's overlap check)
     int chunk;        // chunk length of the d < 128 chunked kernel (8, 16, 32 or 64)
     // chunked path (d = 128): the window of global chunk records [seg_lo, seg_hi) that this
-    // pre-pass / state-pass launch pair handles; record gc is stored at workspace position
-    // gc - seg_lo (seg_hi - seg_lo <= ws.chunk_cap)
+    // pre-pass / state-pass launch pair handles (seg_hi = INT_MAX: all of them, the call being one
+    // segment); record gc is stored at workspace position gc - seg_lo (< ws.chunk_cap)
     int seg_lo = 0, seg_hi = 0;
 };
 
@@ -469,6 +485,10 @@ cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, i
                           const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st,
                           const int* gate = nullptr);
 
+// the pool's segment stream (highest priority) and events; destroy_seg_streams accepts a partial set
+cudaError_t create_seg_streams(SegStreams* ss);
+void destroy_seg_streams(SegStreams* ss);
+
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
                            const void* b, const void* z, void* out, cudaStream_t st, const int* gate = nullptr);
@@ -491,7 +511,7 @@ inline int prefill_max_seqs(int max_tokens) { return max_tokens + 64; }
 inline bool prefill_chunked(const gdn_shape& s) { return s.dk == 128 && s.dv == 128; }
 // A call whose records exceed the workspace runs in segments of chunk_cap records (prefill_segments),
 // so a pool holds at most kPrefillMaxRecords of them, whatever max_tokens is.
-constexpr int kPrefillMaxRecords = 512;
+constexpr int kPrefillMaxRecords = 512;  // also the most records of one segment (the state pass's table)
 inline int prefill_pool_chunk_cap(const gdn_shape& s, int max_tokens)
 {
     return prefill_chunked(s) ? std::min(2 * ((max_tokens + 63) / 64) + 64, kPrefillMaxRecords) : 0;

@@ -159,6 +159,8 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
         P->ws.bytes = gdn::prefill_workspace_bytes(P->shape, P->shape.max_prefill_tokens, cap);
         if (cudaMalloc(&P->ws.base, P->ws.bytes) != cudaSuccess) rc = GDN_ERR_CUDA;
         else if (!gdn::prefill_workspace_carve(P->ws, P->shape, P->shape.max_prefill_tokens, cap)) rc = GDN_ERR_CUDA;
+        if (rc == GDN_OK && gdn::prefill_chunked(P->shape) && gdn::create_seg_streams(&P->seg) != cudaSuccess)
+            rc = GDN_ERR_CUDA;
     }
     if (rc == GDN_OK) {
         if (enqueue_zero(P->base, P->total_bytes, 0, P->num_sms) != cudaSuccess) rc = GDN_ERR_CUDA;
@@ -167,6 +169,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
         if (cudaDeviceSynchronize() != cudaSuccess) rc = GDN_ERR_CUDA;
     }
     if (rc != GDN_OK) {
+        gdn::destroy_seg_streams(&P->seg);
         cudaFree(P->base);
         cudaFree(P->live_dev);
         cudaFree(P->status_dev);
@@ -195,6 +198,7 @@ int gdn_pool_destroy(gdn_pool* P)
     if (!P) return GDN_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
     release_mixed_streams(P);
+    gdn::destroy_seg_streams(&P->seg);
     cudaFree(P->base);
     cudaFree(P->live_dev);
     cudaFree(P->status_dev);

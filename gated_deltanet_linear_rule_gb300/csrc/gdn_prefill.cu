@@ -29,6 +29,7 @@
 // The recurrent kernel and kernels 2 and 5 use the decode kernel's arithmetic in the same
 // order, so with chunk = 0 a prefill of L tokens equals L decode steps bit for bit.
 #include <algorithm>
+#include <climits>
 
 #include "gdn_internal.cuh"
 
@@ -36,7 +37,31 @@ namespace gdn {
 
 namespace {
 
-__global__ void validate_kernel(PrefillArgs A)
+// In-place exclusive prefix sum of a[0 .. n) by one CTA of 256 threads (every thread calls it).
+__device__ void block_exclusive_scan(int* a, int n)
+{
+    __shared__ int part[256];
+    const int per = (n + 255) / 256, lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += a[i];
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {  // inclusive scan of the 256 partial sums
+        const int v = threadIdx.x >= (unsigned)off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int i = lo; i < hi; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) validate_kernel(PrefillArgs A)
 {
     __shared__ int bad;
     if (A.gate && *A.gate) {  // a mixed step whose parts overlap: nothing runs
@@ -52,19 +77,44 @@ __global__ void validate_kernel(PrefillArgs A)
         bool ok = id >= 0 && id < A.num_slots && A.live[id];
         for (int j = 0; ok && j < s; ++j) ok = A.ids[j] != id;
         if (!ok) atomicOr(&bad, 2);
-        // rank by length, longest first (ties by index): long sequences start in the first wave
-        const int len = A.cu[s + 1] - A.cu[s];
-        int rank = 0;
-        for (int j = 0; j < A.n; ++j) {
-            const int lj = A.cu[j + 1] - A.cu[j];
-            rank += (lj > len) || (lj == len && j < s);
+    }
+    __syncthreads();
+    if (bad == 0) {
+        for (int s = threadIdx.x; s < A.n; s += blockDim.x) {
+            // rank by length, longest first (ties by index): long sequences start in the first wave
+            const int len = A.cu[s + 1] - A.cu[s];
+            int rank = 0;
+            for (int j = 0; j < A.n; ++j) {
+                const int lj = A.cu[j + 1] - A.cu[j];
+                rank += (lj > len) || (lj == len && j < s);
+            }
+            A.ws.order[rank] = s;
         }
-        A.ws.order[rank] = s;
-        // first chunk record of the sequence: chunks of 64 tokens of the sequences before it
-        int cs = 0;
-        for (int j = 0; j < s; ++j) cs += (A.cu[j + 1] - A.cu[j] + 63) / 64;
-        A.ws.chunk_start[s] = cs;
-        if (s == A.n - 1) A.ws.chunk_start[A.n] = cs + (len + 63) / 64;
+        if (A.D == 128) {  // the chunked path's record numbering (chunk-index-major)
+            __syncthreads();
+            const int nc = (A.cu[A.ws.order[0] + 1] - A.cu[A.ws.order[0]] + 63) / 64;  // longest sequence
+            int* cnt = A.ws.ctmp;  // [nc + 1]: sequences with exactly v chunks, then the prefix sums
+            for (int v = threadIdx.x; v <= nc; v += blockDim.x) cnt[v] = 0;
+            __syncthreads();
+            for (int s = threadIdx.x; s < A.n; s += blockDim.x) atomicAdd(&cnt[(A.cu[s + 1] - A.cu[s] + 63) / 64], 1);
+            __syncthreads();
+            block_exclusive_scan(cnt, nc + 1);  // cnt[v] = sequences with fewer than v chunks
+            // sequences with more than c chunks, then the records of chunk index < c
+            for (int c = threadIdx.x; c <= nc; c += blockDim.x) A.ws.coff[c] = c < nc ? A.n - cnt[c + 1] : 0;
+            __syncthreads();
+            block_exclusive_scan(A.ws.coff, nc + 1);
+            const int total = A.ws.coff[nc];
+            for (int r = threadIdx.x; r < total; r += blockDim.x) {
+                int lo = 0, hi = nc;  // the largest c with coff[c] <= r
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (A.ws.coff[mid] <= r) lo = mid;
+                    else hi = mid;
+                }
+                A.ws.rec_cp[r] = make_int2(lo, r - A.ws.coff[lo]);
+            }
+            if (threadIdx.x == 0) A.ws.valid[1] = nc;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -253,26 +303,51 @@ __global__ void __launch_bounds__(256) epilogue_kernel(PrefillArgs A)
         out[base + i] = from_f<TOut>(o[i] * rs * A.norm_w[i] * silu_f(to_f(zin[base + i])));
 }
 
+// The chunked path (d = 128) as one pre-pass / state-pass pair per segment of records (one pair
+// unless the call has more chunks than the workspace holds); a segment's state pass continues from
+// the states the previous one left in the slots.  With the pool's segment stream, the workspace is
+// split in two halves: the state pass of segment g runs on that stream while the caller's stream
+// runs the pre-pass of segment g + 1 into the other half (its records are independent of every
+// state; the conv buffers it reads belong to sequences that start in it, which no earlier state
+// pass touches), so one long prompt's state chain no longer leaves the other SMs idle.
 template <typename TIn, typename TOut>
-cudaError_t run(const PrefillArgs& A, cudaStream_t st)
+cudaError_t run_chunked(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss)
+{
+    const int cap = std::min(A.ws.chunk_cap, kPrefillMaxRecords);
+    const bool two = ss && ss->side && cap >= 2 && prefill_segments(A.T, A.n, cap) > 1;
+    const int seg = two ? cap / 2 : cap;
+    const int nseg = prefill_segments(A.T, A.n, seg);
+    PrefillArgs S = A;
+    cudaError_t e = cudaSuccess;
+    for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
+        S.seg_lo = g * seg;
+        S.seg_hi = nseg == 1 ? INT_MAX : S.seg_lo + seg;  // INT_MAX: every record of the call
+        if (!two) {
+            e = launch_chunk_prep<TIn>(S, st);  // reads the conv buffers ...
+            if (e == cudaSuccess) e = launch_chunk_state<TIn, TOut>(S, st);  // ... which the state pass advances
+            continue;
+        }
+        const int half = g & 1;
+        S.ws.chunk_cap = seg;
+        S.ws.rec = A.ws.rec + (size_t)half * seg * chunk_record_bytes(A.hv, 0);
+        S.ws.kimg = A.ws.kimg + (size_t)half * seg * chunk_record_bytes(0, A.hqk);
+        if (g >= 2) e = cudaStreamWaitEvent(st, ss->state[half], 0);  // segment g - 2 has read this half
+        if (e == cudaSuccess) e = launch_chunk_prep<TIn>(S, st);
+        if (e == cudaSuccess) e = cudaEventRecord(ss->prep[half], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->side, ss->prep[half], 0);
+        if (e == cudaSuccess) e = launch_chunk_state<TIn, TOut>(S, ss->side);
+        if (e == cudaSuccess) e = cudaEventRecord(ss->state[half], ss->side);
+    }
+    // join: the caller's stream continues after the last state pass
+    if (two && e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->state[(nseg - 1) & 1], 0);
+    return e;
+}
+
+template <typename TIn, typename TOut>
+cudaError_t run(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss)
 {
     validate_kernel<<<1, 256, 0, st>>>(A);
-    if (A.T > 0 && A.D == 128) {
-        // one pre-pass / state-pass pair per segment of chunk_cap records (one pair unless the
-        // call has more chunks than the workspace holds); a segment's state pass continues from
-        // the states the previous one left in the slots
-        const int nseg = prefill_segments(A.T, A.n, A.ws.chunk_cap);
-        PrefillArgs S = A;
-        for (int g = 0; g < nseg; ++g) {
-            S.seg_lo = g * A.ws.chunk_cap;
-            S.seg_hi = S.seg_lo + A.ws.chunk_cap;
-            cudaError_t e = launch_chunk_prep<TIn>(S, st);  // reads the conv buffers ...
-            if (e != cudaSuccess) return e;
-            e = launch_chunk_state<TIn, TOut>(S, st);       // ... which the state pass then advances
-            if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
-    }
+    if (A.T > 0 && A.D == 128) return run_chunked<TIn, TOut>(A, st, ss);
     if (A.T > 0) {
         const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);
         if (smem > 48 * 1024) {
@@ -318,7 +393,10 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
         b += align256((size_t)T * s.hv * 4) * 2;      // g, beta
     }
     b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
-    b += align256((size_t)(prefill_max_seqs(T) + 1) * 4);  // chunk starts
+    if (prefill_chunked(s)) {
+        b += align256((size_t)((T + 63) / 64 + 2) * 4) * 2;  // coff, ctmp
+        b += align256((size_t)prefill_call_chunks(T, prefill_max_seqs(T)) * 8);  // rec_cp
+    }
     b += (size_t)chunk_cap * chunk_record_bytes(s.hv, s.hqk);  // chunk records (multiple of 256)
     b += 256;                                         // valid flag
     return b;
@@ -343,7 +421,11 @@ bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
         ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     }
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
-    ws.chunk_start = reinterpret_cast<int*>(take((size_t)(prefill_max_seqs(T) + 1) * 4));
+    if (prefill_chunked(s)) {
+        ws.coff = reinterpret_cast<int*>(take((size_t)((T + 63) / 64 + 2) * 4));
+        ws.ctmp = reinterpret_cast<int*>(take((size_t)((T + 63) / 64 + 2) * 4));
+        ws.rec_cp = reinterpret_cast<int2*>(take((size_t)prefill_call_chunks(T, prefill_max_seqs(T)) * 8));
+    }
     ws.rec = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * chunk_record_bytes(s.hv, 0)));
     ws.kimg = reinterpret_cast<unsigned char*>(take((size_t)chunk_cap * chunk_record_bytes(0, s.hqk)));
     ws.chunk_cap = chunk_cap;
@@ -394,10 +476,33 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.gate = gate;
     A.chunk = P.shape.chunk;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
-    if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st);
-    if (in_bf16) return run<__nv_bfloat16, float>(A, st);
-    if (out_bf16) return run<float, __nv_bfloat16>(A, st);
-    return run<float, float>(A, st);
+    if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st, &P.seg);
+    if (in_bf16) return run<__nv_bfloat16, float>(A, st, &P.seg);
+    if (out_bf16) return run<float, __nv_bfloat16>(A, st, &P.seg);
+    return run<float, float>(A, st, &P.seg);
+}
+
+cudaError_t create_seg_streams(SegStreams* ss)
+{
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&ss->side, cudaStreamNonBlocking, greatest);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&ss->prep[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss->state[i], cudaEventDisableTiming);
+    }
+    return e;
+}
+
+void destroy_seg_streams(SegStreams* ss)
+{
+    for (int i = 0; i < 2; ++i) {
+        if (ss->prep[i]) cudaEventDestroy(ss->prep[i]);
+        if (ss->state[i]) cudaEventDestroy(ss->state[i]);
+        ss->prep[i] = ss->state[i] = nullptr;
+    }
+    if (ss->side) cudaStreamDestroy(ss->side);
+    ss->side = nullptr;
 }
 
 }  // namespace gdn
@@ -533,10 +638,10 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     A.chunk = s.chunk;
     cudaError_t e;
     const bool in_bf16 = s.io_dtype == 1, out_bf16 = s.out_dtype == 1;
-    if (in_bf16 && out_bf16) e = run<__nv_bfloat16, __nv_bfloat16>(A, st);
-    else if (in_bf16) e = run<__nv_bfloat16, float>(A, st);
-    else if (out_bf16) e = run<float, __nv_bfloat16>(A, st);
-    else e = run<float, float>(A, st);
+    if (in_bf16 && out_bf16) e = run<__nv_bfloat16, __nv_bfloat16>(A, st, nullptr);
+    else if (in_bf16) e = run<__nv_bfloat16, float>(A, st, nullptr);
+    else if (out_bf16) e = run<float, __nv_bfloat16>(A, st, nullptr);
+    else e = run<float, float>(A, st, nullptr);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

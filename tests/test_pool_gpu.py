@@ -142,17 +142,19 @@ def test_recycle_and_reset_are_ordered_after_work_queued_on_their_stream():
     L.close()
 
 
-def test_chunked_prefill_in_segments():
+@pytest.mark.parametrize("lengths", [[1] * 95 + [900], [150] * 4 + [4] * 85, [4] * 40 + [150, 600] + [2] * 50],
+                         ids=["one_long", "four_of_three_chunks", "two_long_among_short"])
+def test_chunked_prefill_in_segments(lengths):
     """At d = 128 a pool for 1 024-token calls holds 96 chunk records; a call with more chunks runs in
-    segments, each continuing from the states the one before left in the slots.  95 one-token prompts
-    then a 900-token prompt make 110 chunks: the long prompt's first chunk is in the first segment and
-    its other 14 in the second.  Outputs, final states and conv buffers against the oracle, then two
-    decode steps from those states."""
+    segments of 48 (the state pass of one overlapping the pre-pass of the next), each continuing from
+    the states the one before left in the slots.  Records are numbered chunk-index-major (every
+    sequence's chunk 0, then chunk 1, ...), so with these mixes the long prompts' chunks fall into
+    two or three segments, some of which hold no chunk of a given sequence.  Outputs, final states and
+    conv buffers against the oracle, then two decode steps from those states."""
     L = Layer(33, 1, 2, 128, io="bf16", out="f32", num_slots=96, max_prefill_tokens=1024)
     assert L.pool.info().workspace_bytes < 16 * 2 ** 20  # 96 records of 2 x 57 KB + 32 KB, and small tables
-    slots = [L.pool.alloc() for _ in range(96)]
-    lengths = [1] * 95 + [900]
     n = len(lengths)
+    slots = [L.pool.alloc() for _ in range(n)]
     inp, cu = synth.varlen_inputs(33, 0, lengths, 1, 2, 128, 128, "bf16")
     o = host(L.gpu_prefill(0, slots, inp, cu))
     ref = L.oracle_run(0, cu, inp, np.zeros((n, 2, 128, 128)), np.zeros((n, 3, L.C)))
@@ -163,7 +165,7 @@ def test_chunked_prefill_in_segments():
         Sg, Cg = L.get_state(0, slots[j])
         assert relerr(Sg, S[j]) <= PREFILL_TOL, f"final S of sequence {j}"
         assert np.array_equal(Cg, conv[j]), f"conv buffer of sequence {j}"
-    pick = [0, 94, 95]
+    pick = [0, n // 2, n - 1]
     S, conv = S[pick].copy(), conv[pick].copy()
     for step in range(2):
         dinp = L.decode_inputs(pick, step)
