@@ -53,6 +53,7 @@ struct DecodeArgs {
     float l2_eps, norm_eps;
     int stall_producer;  // test hook: the producer fills no stage, so the consumers' waits run out
     const int* gate;     // when non-null and *gate != 0 the launch does nothing (mixed-step overlap check)
+    int sms;             // SMs the launch is sized for (host side: the pool's SM count, or fewer)
 };
 
 size_t decode_smem_bytes(int D, int r, int stages)
@@ -322,7 +323,7 @@ cudaError_t launch_t(const Pool& P, const DecodeArgs& A, cudaStream_t st)
         per_sm = cached_per_sm[dev];
     }
     const int items = A.m * A.hqk;
-    const int grid = std::max(1, std::min(items, per_sm * P.num_sms));
+    const int grid = std::max(1, std::min(items, per_sm * A.sms));
     // Programmatic stream serialization: the CTAs may be scheduled while the previous kernel on the
     // stream finishes (at small m the launch and setup are a large part of a step); the kernel
     // waits for that kernel's completion before its first global access.
@@ -352,8 +353,8 @@ cudaError_t launch_d(const Pool& P, const DecodeArgs& A, cudaStream_t st)
             // SM -> 6 stages at 2 CTAs per SM (m = 16 / 32 / 64: 12.4 -> 10.6, 24.4 -> 20.8,
             // 56.2 -> 53.7 us); more -> 4 stages at 3 CTAs per SM.  The arithmetic is the same.
             const size_t items = (size_t)A.m * P.shape.hqk;
-            if (items <= (size_t)P.num_sms) return launch_t<128, TIn, TOut, kDeepStages>(P, A, st);
-            if (items <= 8 * (size_t)P.num_sms) return launch_t<128, TIn, TOut, kMidStages>(P, A, st);
+            if (items <= (size_t)A.sms) return launch_t<128, TIn, TOut, kDeepStages>(P, A, st);
+            if (items <= 8 * (size_t)A.sms) return launch_t<128, TIn, TOut, kMidStages>(P, A, st);
             return launch_t<128, TIn, TOut, kStages>(P, A, st);
         }
         default: return cudaErrorInvalidValue;
@@ -364,7 +365,7 @@ cudaError_t launch_d(const Pool& P, const DecodeArgs& A, cudaStream_t st)
 
 cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, int m, const void* q, const void* k,
                           const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st,
-                          const int* gate)
+                          const int* gate, int sms)
 {
     const LayerParams& L = P.params[(size_t)layer];
     DecodeArgs A;
@@ -393,6 +394,7 @@ cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, i
     A.norm_eps = P.shape.norm_eps;
     A.stall_producer = P.debug_flags & 1;
     A.gate = gate;
+    A.sms = sms > 0 ? std::min(sms, P.num_sms) : P.num_sms;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return launch_d<__nv_bfloat16, __nv_bfloat16>(P, A, st);
     if (in_bf16) return launch_d<__nv_bfloat16, float>(P, A, st);

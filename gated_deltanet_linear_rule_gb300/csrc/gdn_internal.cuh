@@ -483,7 +483,7 @@ __device__ __forceinline__ int row_col(int j, int cl) { return (j >> 2) * 4 * LP
 // `gate` (device, may be null): when *gate != 0 at run time the launch does nothing
 cudaError_t launch_decode(const Pool& P, int layer, const uint64_t* slot_ptrs, int m, const void* q, const void* k,
                           const void* v, const void* a, const void* b, const void* z, void* out, cudaStream_t st,
-                          const int* gate = nullptr);
+                          const int* gate = nullptr, int sms = 0);  // sms > 0: size the launch for that many SMs
 
 // the pool's segment stream (highest priority) and events; destroy_seg_streams accepts a partial set
 cudaError_t create_seg_streams(SegStreams* ss);
@@ -491,7 +491,11 @@ void destroy_seg_streams(SegStreams* ss);
 
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
-                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate = nullptr);
+                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate = nullptr,
+                           cudaEvent_t prep_done = nullptr, bool* split = nullptr);
+// With prep_done (a mixed step): when the call is one chunked segment, the state pass runs on the
+// pool's segment stream (highest priority) after prep_done, recorded on st once the pre-pass is
+// enqueued, and st then waits for it; *split tells whether that happened.
 
 // the row tensors of a prefill call are read and written in 16-B pieces (and by tensor copies)
 inline bool rows_aligned16(const void* q, const void* k, const void* v, const void* z, const void* out)

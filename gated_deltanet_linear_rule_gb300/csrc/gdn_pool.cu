@@ -332,7 +332,7 @@ int check_prefill(gdn_pool* P, int layer, const int* cu_seqlens_dev, const int* 
 // per pool: the internal stream a mixed step runs its decode on, and the fork / join events
 struct MixedStreams {
     cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, prep = nullptr;
 };
 std::mutex g_mixed_mu;
 std::unordered_map<const gdn_pool*, MixedStreams> g_mixed;
@@ -349,7 +349,9 @@ cudaError_t mixed_streams(const gdn_pool* P, MixedStreams* out)
     cudaError_t e = cudaStreamCreateWithFlags(&m.side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.join, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m.prep, cudaEventDisableTiming);
     if (e != cudaSuccess) {
+        if (m.prep) cudaEventDestroy(m.prep);
         if (m.join) cudaEventDestroy(m.join);
         if (m.fork) cudaEventDestroy(m.fork);
         if (m.side) cudaStreamDestroy(m.side);
@@ -365,6 +367,7 @@ void release_mixed_streams(const gdn_pool* P)
     std::lock_guard<std::mutex> lk(g_mixed_mu);
     auto it = g_mixed.find(P);
     if (it == g_mixed.end()) return;
+    cudaEventDestroy(it->second.prep);
     cudaEventDestroy(it->second.join);
     cudaEventDestroy(it->second.fork);
     cudaStreamDestroy(it->second.side);
@@ -420,19 +423,26 @@ int gdn_mixed_step(gdn_pool* P, int layer, const uint64_t* slot_ptrs_dev, int m,
                                             P->slot_bytes, P->num_layers, P->num_slots, layer, P->gate_dev,
                                             P->status_dev);
     cudaError_t e = cudaGetLastError();
-    // fork: the decode on the side stream after everything enqueued on `stream` so far
+    // fork point: everything enqueued on `stream` so far (the overlap check among it)
     if (e == cudaSuccess) e = cudaEventRecord(ms.fork, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ms.side, ms.fork, 0);
+    // The chunked prefill's state pass takes one SM per CTA, two CTAs per (sequence, v-head); when
+    // that leaves SMs idle, the state pass runs on the pool's high-priority segment stream once the
+    // pre-pass is done and the decode, sized for the idle SMs, beside it (dispatched after it).
+    // Otherwise the decode runs beside the whole prefill from the fork point.
+    const int idle = P->num_sms - n_seqs * P->shape.hv * 2;
+    const bool beside_state = gdn::prefill_chunked(P->shape) && P->seg.side && idle >= 16;
+    bool split = false;
     if (e == cudaSuccess)
-        e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, ms.side, P->gate_dev);
-    // the prefill on `stream` meanwhile; then `stream` waits for the decode (join)
-    const cudaError_t ep = e == cudaSuccess ? gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs,
-                                                                  total_tokens, pq, pk, pv, pa, pb, pz, pout, st,
-                                                                  P->gate_dev)
-                                            : e;
-    cudaError_t ej = cudaEventRecord(ms.join, ms.side);
-    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, ms.join, 0);
-    return (e == cudaSuccess && ep == cudaSuccess && ej == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+        e = gdn::launch_prefill(*P, layer, cu_seqlens_dev, slot_ids_dev, n_seqs, total_tokens, pq, pk, pv, pa, pb, pz,
+                                pout, st, P->gate_dev, beside_state ? ms.prep : nullptr, &split);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ms.side, split ? ms.prep : ms.fork, 0);
+    if (e == cudaSuccess)
+        e = gdn::launch_decode(*P, layer, slot_ptrs_dev, m, dq, dk, dv, da, db, dz, dout, ms.side, P->gate_dev,
+                               split ? idle : 0);
+    // join: `stream` continues after the decode too
+    if (e == cudaSuccess) e = cudaEventRecord(ms.join, ms.side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ms.join, 0);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 int gdn_last_device_status(gdn_pool* P, void* stream)

@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(256) epilogue_kernel(PrefillArgs A)
 // state; the conv buffers it reads belong to sequences that start in it, which no earlier state
 // pass touches), so one long prompt's state chain no longer leaves the other SMs idle.
 template <typename TIn, typename TOut>
-cudaError_t run_chunked(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss)
+cudaError_t run_chunked(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss, cudaEvent_t prep_done,
+                        bool* split)
 {
     const int cap = std::min(A.ws.chunk_cap, kPrefillMaxRecords);
     const bool two = ss && ss->side && cap >= 2 && prefill_segments(A.T, A.n, cap) > 1;
@@ -319,6 +320,18 @@ cudaError_t run_chunked(const PrefillArgs& A, cudaStream_t st, const SegStreams*
     const int nseg = prefill_segments(A.T, A.n, seg);
     PrefillArgs S = A;
     cudaError_t e = cudaSuccess;
+    if (prep_done && ss && ss->side && nseg == 1) {  // a mixed step's prefill: the state pass on the side
+        S.seg_lo = 0;
+        S.seg_hi = INT_MAX;
+        e = launch_chunk_prep<TIn>(S, st);
+        if (e == cudaSuccess) e = cudaEventRecord(prep_done, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->side, prep_done, 0);
+        if (e == cudaSuccess) e = launch_chunk_state<TIn, TOut>(S, ss->side);
+        if (e == cudaSuccess) e = cudaEventRecord(ss->state[0], ss->side);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->state[0], 0);
+        if (split) *split = e == cudaSuccess;
+        return e;
+    }
     for (int g = 0; g < nseg && e == cudaSuccess; ++g) {
         S.seg_lo = g * seg;
         S.seg_hi = nseg == 1 ? INT_MAX : S.seg_lo + seg;  // INT_MAX: every record of the call
@@ -344,10 +357,11 @@ cudaError_t run_chunked(const PrefillArgs& A, cudaStream_t st, const SegStreams*
 }
 
 template <typename TIn, typename TOut>
-cudaError_t run(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss)
+cudaError_t run(const PrefillArgs& A, cudaStream_t st, const SegStreams* ss, cudaEvent_t prep_done = nullptr,
+                bool* split = nullptr)
 {
     validate_kernel<<<1, 256, 0, st>>>(A);
-    if (A.T > 0 && A.D == 128) return run_chunked<TIn, TOut>(A, st, ss);
+    if (A.T > 0 && A.D == 128) return run_chunked<TIn, TOut>(A, st, ss, prep_done, split);
     if (A.T > 0) {
         const size_t smem = (size_t)(A.C + 3 * A.hqk) * sizeof(float);
         if (smem > 48 * 1024) {
@@ -436,8 +450,10 @@ bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
 
 cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, const int* slot_ids, int n_seqs,
                            int total_tokens, const void* q, const void* k, const void* v, const void* a,
-                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate)
+                           const void* b, const void* z, void* out, cudaStream_t st, const int* gate,
+                           cudaEvent_t prep_done, bool* split)
 {
+    if (split) *split = false;
     const LayerParams& L = P.params[(size_t)layer];
     PrefillArgs A;
     A.cu = cu_seqlens;
@@ -476,10 +492,10 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.gate = gate;
     A.chunk = P.shape.chunk;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
-    if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st, &P.seg);
-    if (in_bf16) return run<__nv_bfloat16, float>(A, st, &P.seg);
-    if (out_bf16) return run<float, __nv_bfloat16>(A, st, &P.seg);
-    return run<float, float>(A, st, &P.seg);
+    if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st, &P.seg, prep_done, split);
+    if (in_bf16) return run<__nv_bfloat16, float>(A, st, &P.seg, prep_done, split);
+    if (out_bf16) return run<float, __nv_bfloat16>(A, st, &P.seg, prep_done, split);
+    return run<float, float>(A, st, &P.seg, prep_done, split);
 }
 
 cudaError_t create_seg_streams(SegStreams* ss)

@@ -15,14 +15,14 @@ M_DEC = 12
 PRE_LENGTHS = [300, 1, 129, 64]
 
 
-def _setup(workload: int):
-    """A pool with M_DEC decode slots holding random states and len(PRE_LENGTHS) fresh prefill slots,
+def _setup(workload: int, lengths=PRE_LENGTHS):
+    """A pool with M_DEC decode slots holding random states and len(lengths) fresh prefill slots,
     plus one step of decode inputs and one set of packed prefill inputs."""
-    T = sum(PRE_LENGTHS)
-    L = Layer(workload, HQK, HV, D, io="bf16", out="bf16", num_slots=M_DEC + len(PRE_LENGTHS) + 2,
+    T = sum(lengths)
+    L = Layer(workload, HQK, HV, D, io="bf16", out="bf16", num_slots=M_DEC + len(lengths) + 2,
               max_prefill_tokens=T)
     dec_slots = [L.pool.alloc() for _ in range(M_DEC)]
-    pre_slots = [L.pool.alloc() for _ in PRE_LENGTHS]
+    pre_slots = [L.pool.alloc() for _ in lengths]
     g = torch.Generator(device="cuda").manual_seed(workload)
     for s in dec_slots:
         Sv, Cv = L.pool.state_views(0, s)
@@ -30,7 +30,7 @@ def _setup(workload: int):
         Cv.copy_((torch.randn(Cv.shape, generator=g, device="cuda")).to(Cv.dtype))
     torch.cuda.synchronize()
     dec_in = L.to_dev(L.decode_inputs(list(range(M_DEC)), 0))
-    cu = np.concatenate([[0], np.cumsum(PRE_LENGTHS)]).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     pre_in = synth.token_inputs(workload, 0, 0, T, HQK, HV, D, D, "bf16")
     return L, dec_slots, pre_slots, dec_in, pre_in, cu
 
@@ -51,8 +51,12 @@ def _restore(L, slots, saved):
     torch.cuda.synchronize()
 
 
-def test_mixed_step_equals_decode_then_prefill_bitwise():
-    L, dec_slots, pre_slots, dec_in, pre_in, cu = _setup(41)
+@pytest.mark.parametrize("lengths", [PRE_LENGTHS, [40] * 10], ids=["decode_beside_state_pass", "decode_from_start"])
+def test_mixed_step_equals_decode_then_prefill_bitwise(lengths):
+    """With 4 prompts the state pass (2 CTAs per (sequence, v-head): 64) leaves SMs idle, and the
+    decode runs beside it once the pre-pass is done; with 10 it fills the GPU (160 CTAs), and the
+    decode runs beside the whole prefill.  Either way the results equal the two separate calls."""
+    L, dec_slots, pre_slots, dec_in, pre_in, cu = _setup(41, lengths)
     all_slots = dec_slots + pre_slots
     init = _states(L, all_slots)
     T = int(cu[-1])
@@ -86,7 +90,7 @@ def test_mixed_step_equals_decode_then_prefill_bitwise():
     assert L.pool.device_status() == 0
 
     # the prefill part against the oracle (fresh slots)
-    n = len(PRE_LENGTHS)
+    n = len(lengths)
     ref = L.oracle_run(0, cu, pre_in, np.zeros((n, HV, D, D)), np.zeros((n, L.W - 1, L.C)))
     check_out(host(out_p2), ref["out"], "bf16", PREFILL_TOL, "mixed step prefill out")
     L.close()
