@@ -176,6 +176,54 @@ def test_chunked_prefill_in_segments(lengths):
     L.close()
 
 
+def test_segmented_prefill_graph_replay_equals_eager_bitwise():
+    """A prefill that runs in pipelined segments forks work onto the pool's second stream and joins
+    it back; captured into a CUDA graph, its replay gives the eager results bit for bit (outputs,
+    states and conv buffers), twice in a row from the same starting states."""
+    L = Layer(35, 1, 2, 128, io="bf16", out="f32", num_slots=96, max_prefill_tokens=1024)
+    lengths = [4] * 40 + [150, 600] + [2] * 50
+    n = len(lengths)
+    slots = [L.pool.alloc() for _ in range(n)]
+    inp, cu = synth.varlen_inputs(35, 0, lengths, 1, 2, 128, 128, "bf16")
+    T = int(cu[-1])
+    d = L.to_dev(inp)
+    cu_d = torch.tensor(np.asarray(cu, dtype=np.int32), device="cuda")
+    ids = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, 2 * 128), dtype=torch.float32, device="cuda")
+
+    def call(stream=None):
+        L.pool.prefill_varlen(0, cu_d, ids, n, T, d["q"], d["k"], d["v"], d["a"], d["b"], d["z"], out, stream=stream)
+
+    def states():
+        return [tuple(t.clone() for t in L.pool.state_views(0, s)) for s in slots]
+
+    call()
+    torch.cuda.synchronize()
+    eager_out, eager_states = out.clone(), states()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    for s in slots:
+        L.pool.recycle(s)
+        L.pool.alloc()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            call(stream=cap)
+    for _ in range(2):
+        for s in slots:  # the same zero starting states before each replay
+            for t in L.pool.state_views(0, s):
+                t.zero_()
+        out.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager_out)
+        for (S1, C1), (S2, C2) in zip(eager_states, states()):
+            assert torch.equal(S1, S2) and torch.equal(C1, C2)
+    assert L.pool.device_status() == 0
+    L.close()
+
+
 def test_chunked_prefill_workspace_is_bounded():
     """A pool for 80 000-token prefills holds 512 chunk records (1.2 GB at 16/32 heads), not one per
     chunk of the longest call."""
