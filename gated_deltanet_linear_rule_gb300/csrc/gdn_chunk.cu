@@ -1185,8 +1185,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
         g2s(sm + S_PZ + (c & 1) * 16384 + 8192, record(c) + REC_P, 8192, &full_p[c & 1], A.ws.rec, rec_region);
         p_issued = c + 1;
     };
+    const int first_fetched = A.stall_fetch ? 1 : 0;  // the test hook leaves chunk 0's record unfetched
     if (tid == PF) {
-        fetch_main(0);
+        if (!A.stall_fetch) fetch_main(0);
         fetch_p(0);
         if (nch > 1) {
             fetch_main(1);
@@ -1536,7 +1537,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
     if (tid == 0 && mma7_issued > 0)
         mbar_wait_bounded(((mma7_issued - 1) & 1) ? bar7o : bar7e, (uint32_t)(((mma7_issued - 1) >> 1) & 1), nullptr);
     if (tid == PF) {
-        for (int c = (main_issued > 2 ? main_issued - 2 : 0); c < main_issued; ++c)
+        for (int c = max(main_issued - 2, first_fetched); c < main_issued; ++c)
             mbar_wait_bounded(&full[c & 1], (uint32_t)((c >> 1) & 1), nullptr);
         for (int c = (p_issued > 2 ? p_issued - 2 : 0); c < p_issued; ++c)
             mbar_wait_bounded(&full_p[c & 1], (uint32_t)((c >> 1) & 1), nullptr);

@@ -74,7 +74,8 @@ struct Pool {
     std::vector<LayerParams> params;
     PrefillWorkspace ws;
     int device = 0, num_sms = 0;
-    int debug_flags = 0;  // GDN_DEBUG_FLAGS at creation; bit 0: decode producer fills no stage (timeout test)
+    int debug_flags = 0;  // GDN_DEBUG_FLAGS at creation (timeout tests): bit 0: the decode producer fills
+                          // no stage; bit 1: the chunked state pass does not fetch its first record
     SegStreams seg;       // chunked prefill (d = 128, max_prefill_tokens > 0) only
 };
 
@@ -102,6 +103,7 @@ struct PrefillArgs {
     // pre-pass / state-pass launch pair handles (seg_hi = INT_MAX: all of them, the call being one
     // segment); record gc is stored at workspace position gc - seg_lo (< ws.chunk_cap)
     int seg_lo = 0, seg_hi = 0;
+    int stall_fetch = 0;  // test hook: the state pass does not fetch its first chunk's record (timeout test)
 };
 
 // ------------------------------------------------------- checked builds ----

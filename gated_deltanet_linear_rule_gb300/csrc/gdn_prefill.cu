@@ -491,6 +491,7 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.kq = P.ws.kq;
     A.gate = gate;
     A.chunk = P.shape.chunk;
+    A.stall_fetch = (P.debug_flags >> 1) & 1;
     const bool in_bf16 = P.shape.io_dtype == 1, out_bf16 = P.shape.out_dtype == 1;
     if (in_bf16 && out_bf16) return run<__nv_bfloat16, __nv_bfloat16>(A, st, &P.seg, prep_done, split);
     if (in_bf16) return run<__nv_bfloat16, float>(A, st, &P.seg, prep_done, split);

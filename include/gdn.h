@@ -48,10 +48,13 @@
  *     The chunked prefill's 16-bit tensor-core operands carry per-chunk power-of-two
  *     scales, so its range is fp32's, not fp16's.
  *   - Not thread-safe: one host thread per pool at a time.
- *   - Test hook: if the environment variable GDN_DEBUG_FLAGS holds 1 when a pool is
- *     created, that pool's decode kernel fills none of its pipeline stages, so every
- *     consumer wait runs out after its 1 s limit: the launch returns with
- *     GDN_DEV_TIMEOUT set and the outputs unwritten, and the CUDA context stays usable.
+ *   - Test hooks: GDN_DEBUG_FLAGS in the environment when a pool is created, a bit mask.
+ *     Bit 0 (value 1): that pool's decode kernel fills none of its pipeline stages, so every
+ *     consumer wait runs out after its 1 s limit: the launch returns with GDN_DEV_TIMEOUT set
+ *     and the outputs unwritten, and the CUDA context stays usable.  Bit 1 (value 2): its
+ *     chunked prefill's state pass never fetches a sequence's first chunk record, with the
+ *     same outcome for the prefill (no output row, no state written; the conv buffers are
+ *     advanced already).
  */
 #ifndef GDN_H
 #define GDN_H
