@@ -123,7 +123,9 @@ typedef struct {
  * CUDA device.  (slot, layer) lives at base + (slot * num_layers + layer) *
  * slot_bytes and holds [S: Hv x dv x dk fp32 | conv buffer: (W-1) x C io].
  * All slots start zeroed and free.  Allocates the state memory and the
- * prefill workspace (cudaMalloc); *out receives the pool.
+ * prefill workspace (cudaMalloc) and, for the chunked prefill (d = 128 with
+ * max_prefill_tokens > 0), a second stream (the device's highest priority) and four
+ * events that a prefill running in several segments uses internally; *out receives the pool.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA (allocation failed). */
 int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_pool** out);
 
@@ -202,8 +204,11 @@ int gdn_decode_step(gdn_pool* pool, int layer, const uint64_t* slot_ptrs_dev, in
  * cu_seqlens_dev[n_seqs] and not exceed the pool's max_prefill_tokens; slot
  * ids must be allocated and distinct; n_seqs may be up to max_prefill_tokens + 64.
  * At d = 128 a call whose 64-token chunks (counted per sequence) exceed the pool's chunk
- * records runs as several pre-pass / state-pass segments on the stream, each continuing
- * from the states the one before left in the slots.  q, k, v, z and out are row-major
+ * records runs as several pre-pass / state-pass segments, each continuing from the states
+ * the one before left in the slots; their state passes run on the pool's second stream,
+ * forked from `stream` and joined back by events (stream-capture safe), so that one
+ * segment's state pass overlaps the next one's pre-pass.  The call's work is ordered after
+ * earlier work on `stream` and later work on `stream` after all of it.  q, k, v, z and out are row-major
  * [total_tokens][width] device buffers whose base addresses are 16-B aligned
  * (they are moved in 16-B pieces and, at d = 128 in bf16, by tensor copies).
  * Uses the pool's workspace: calls on one pool must not overlap on the GPU.
@@ -218,9 +223,11 @@ int gdn_prefill_varlen(gdn_pool* pool, int layer, const int* cu_seqlens_dev, con
  * sequences exactly as gdn_prefill_varlen (p* arguments), in one call.  The result equals
  * gdn_decode_step(...) followed by gdn_prefill_varlen(...) on `stream`, bit for bit.  The
  * decode kernel runs on an internal stream of the pool, forked from `stream` by an event and
- * joined back before the call's work ends, so that it overlaps the prefill's pre-pass; the
- * work of the call is ordered after earlier work on `stream`, and later work on `stream` is
- * ordered after all of it.  The fork and join are stream-capture safe; the first call creates
+ * joined back before the call's work ends.  When the prefill's state pass (one SM per CTA,
+ * two CTAs per sequence and v-head) leaves at least 16 SMs idle, the state pass runs on the
+ * pool's second stream after the pre-pass and the decode, sized for the idle SMs, beside it;
+ * otherwise the decode overlaps the whole prefill.  The work of the call is ordered after
+ * earlier work on `stream`, and later work on `stream` is ordered after all of it.  The fork and join are stream-capture safe; the first call creates
  * the internal stream and events on the current device, so make one call before capturing.
  * The decode rows' slots and the prefill sequences' slots must be different slots (each
  * call's own rules apply within its part): a kernel on `stream` compares them first, and if
