@@ -165,6 +165,19 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
         }
         float* S = reinterpret_cast<float*>(p) + (size_t)hk * r * D * D;
         TIn* cbuf = reinterpret_cast<TIn*>(p + A.state_bytes);  // [W-1][C]
+        // With the deeper rings (few items; latency-bound), requested now and used at the end:
+        // this thread's z of the epilogue (one element when r * D == kConsumers) and, for the
+        // first r threads, the gate inputs of v-head hk*r + tid (at 4 stages, 3 CTAs per SM,
+        // the registers they hold cost more than the round trips they save: measured)
+        constexpr bool kEarly = STAGES != kStages;
+        TIn zpre = TIn(0.f);
+        if (kEarly && r * D <= kConsumers && tid < r * D) zpre = zin[(size_t)row * Dv + (size_t)hk * r * D + tid];
+        float g_in = 0.f, b_in = 0.f;
+        if (kEarly && tid < r) {
+            const int h = hk * r + tid;
+            g_in = log_decay(A.A_log[h], to_f(ain[(size_t)row * A.hv + h]), A.dt_bias[h]);
+            b_in = to_f(bin[(size_t)row * A.hv + h]);
+        }
 
         // conv + SiLU of the item's q, k and v channels; shift the conv buffer by one token
         const int nch = (2 + r) * D;
@@ -215,13 +228,17 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
         } else if (warp == 2) {
             const float d = warp_dot(qs, ks, D, lane);
             if (lane == 0) red[2] = d;
-        } else {
+        } else if (!kEarly) {
             for (int rr = (warp - 3) * 32 + lane; rr < r; rr += 5 * 32) {
                 const int h = hk * r + rr;
                 const float g = log_decay(A.A_log[h], to_f(ain[(size_t)row * A.hv + h]), A.dt_bias[h]);
                 gal[rr] = expf(g);
                 gbe[rr] = sigmoid_f(to_f(bin[(size_t)row * A.hv + h]));
             }
+        }
+        if (kEarly && tid < r) {
+            gal[tid] = expf(g_in);
+            gbe[tid] = sigmoid_f(b_in);
         }
         named_bar_sync(1, kConsumers);
 
@@ -288,7 +305,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == kStages ? 3 : STAGES == kM
             for (int c = tid; c < r * D; c += kConsumers) {
                 const int rr = c / D, i = c % D, h = hk * r + rr;
                 const size_t o_idx = (size_t)row * Dv + (size_t)h * D + i;
-                const float y = obuf[c] * rms[rr] * A.norm_w[i] * silu_f(to_f(zin[o_idx]));
+                const TIn zv = (kEarly && r * D <= kConsumers) ? zpre : zin[o_idx];
+                const float y = obuf[c] * rms[rr] * A.norm_w[i] * silu_f(to_f(zv));
                 out[o_idx] = from_f<TOut>(y);
             }
         }
