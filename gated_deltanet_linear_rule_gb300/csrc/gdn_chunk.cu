@@ -264,6 +264,54 @@ struct ConvRows {
 // shared by the r = Hv / Hqk v-heads of the q/k head, which the CTA then takes one after the
 // other.  8 warps: warp w reads TMEM lane quarter w % 4 and works on column half w / 4.
 
+// The sequences with chunk records in a segment [seg_lo, seg_hi) of a call run in segments, for
+// the segment's state pass: chunk c of the sequence of rank p is record coff[c] + p, and the ranks
+// with a chunk c are 0 .. K_c - 1 (K_c = coff[c+1] - coff[c], non-increasing in c), so they are
+// the ranks [0, n1) and [p_lo, p_lo + n2).  Written by one thread of the pre-pass into the slot of
+// the segment's parity (the next segment's pre-pass may run beside this segment's state pass).
+__device__ __forceinline__ int* window_slot(const PrefillArgs& A)
+{
+    return A.ws.valid + 8 + 4 * ((A.seg_lo / (A.seg_hi - A.seg_lo)) & 1);
+}
+
+__device__ void window_plan(const PrefillArgs& A)
+{
+    const int* coff = A.ws.coff;
+    const int nc = A.ws.valid[1], R = coff[nc];
+    const int lo = A.seg_lo, hi = min(A.seg_hi, R);
+    int n1 = 0, p_lo = 0, n2 = 0;
+    if (lo < hi) {
+        auto chunk_of = [&](int r) {  // the largest c < nc with coff[c] <= r
+            int a = 0, b = nc;
+            while (b - a > 1) {
+                const int m = (a + b) >> 1;
+                if (coff[m] <= r) a = m;
+                else b = m;
+            }
+            return a;
+        };
+        const int ca = chunk_of(lo), cb = chunk_of(hi - 1), ka = coff[ca + 1] - coff[ca];
+        p_lo = lo - coff[ca];
+        if (ca == cb) {
+            n2 = hi - lo;  // ranks p_lo .. of chunk ca only
+        } else {
+            // chunk ca: ranks [p_lo, ka); the later chunks: ranks [0, x)
+            const int x = cb > ca + 1 ? coff[ca + 2] - coff[ca + 1] : hi - coff[cb];
+            if (x >= p_lo) {
+                n1 = ka;
+                p_lo = 0;
+            } else {
+                n1 = x;
+                n2 = ka - p_lo;
+            }
+        }
+    }
+    int* win = window_slot(A);
+    win[0] = n1;
+    win[1] = p_lo;
+    win[2] = n2;
+}
+
 template <typename TIn, int WM>
 __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant__ PrefillArgs A,
                                                            const __grid_constant__ PrepMaps M)
@@ -289,6 +337,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     float* X = reinterpret_cast<float*>(sm + P_T1);
 
     if (!*A.ws.valid) return;
+    if (A.seg_hi != INT_MAX && blockIdx.x == 0 && threadIdx.x == 0) window_plan(A);
     const int gc = A.seg_lo + (int)(blockIdx.x / A.hqk), hk = blockIdx.x % A.hqk;  // record, q/k head
     if (gc >= A.seg_hi || gc >= A.ws.coff[A.ws.valid[1]]) return;
     const int slot_rec = gc - A.seg_lo;  // the record's position in this segment's workspace
@@ -1078,15 +1127,22 @@ __global__ void __launch_bounds__(NT, 1) chunk_state_kernel(PrefillArgs A)
 
     // both CTAs of a cluster take these exits together (they depend on the sequence only)
     if (!*A.ws.valid) return;
-    const int half = blockIdx.x & 1, pair = blockIdx.x >> 1;
-    const int s = A.ws.order[pair / A.hv], h = pair % A.hv;
+    const int half = blockIdx.x & 1, pair = blockIdx.x >> 1, h = pair % A.hv;
+    int rank = pair / A.hv;  // of the sequence in length order
+    if (A.seg_hi != INT_MAX) {  // a segment: the i-th of the sequences with records in it
+        const int* win = window_slot(A);
+        const int i = rank;
+        rank = i < win[0] ? i : i - win[0] < win[2] ? win[1] + (i - win[0]) : -1;
+        if (rank < 0) return;
+    }
+    const int s = A.ws.order[rank];
     const int t0s = A.cu[s], Ls = A.cu[s + 1] - t0s;  // the whole sequence
     if (Ls <= 0) return;
     // This launch takes the sequence's chunks whose records (chunk c: coff[c] + rank) lie in the
     // segment [seg_lo, seg_hi): chunks cb .. ce-1, a contiguous run as the record numbers grow
     // with c, starting from the state the slot holds (the sequence's initial state, or the state
     // the previous segment's launch left there).
-    const int rank = pair / A.hv, nchs = (Ls + CH - 1) / CH;
+    const int nchs = (Ls + CH - 1) / CH;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int cb = 0, ce = nchs;
     if (A.seg_hi != INT_MAX) {
@@ -1612,8 +1668,10 @@ cudaError_t launch_chunk_state(const PrefillArgs& A, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
     if (e != cudaSuccess) return e;
     // one CTA per (sequence, v-head, d_v half); the two halves form a cluster
+    // one segment of several: at most one sequence per record of the segment has records in it
+    const int seqs = A.seg_hi == INT_MAX ? A.n : std::min(A.n, A.seg_hi - A.seg_lo);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(A.n * A.hv * 2));
+    cfg.gridDim = dim3((unsigned)(seqs * A.hv * 2));
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = S_SMEM;
     cfg.stream = st;

@@ -36,6 +36,8 @@ struct PrefillWorkspace {
     float* o = nullptr;      // [T][Hv*dv]  delta-rule output before the norm (recurrent path)
     float* kq = nullptr;     // [T][Hqk]    k_hat . q_hat                     (recurrent path)
     int* order = nullptr;    // [T + 64] sequences ranked by length, longest first
+    int* lcnt = nullptr;     // [T + 2] validation scratch (length histogram; many sequences)
+    int* ltie = nullptr;     // [T + 2] validation scratch (ties of equal lengths)
     // Chunked path: the call's chunk records are numbered chunk-index-major -- every sequence's
     // chunk 0 (in length order), then every chunk 1, ... -- so that a segment of records holds a
     // stretch of chunks of all the sequences still running.  Chunk c of the sequence of rank p is
@@ -47,7 +49,8 @@ struct PrefillWorkspace {
     unsigned char* kimg = nullptr; // [chunk_cap][Hqk] per-(chunk, q/k head) K images
     int chunk_cap = 0;             // chunk records the workspace holds
     int* valid = nullptr;    // [0] 1 when the call's cu_seqlens / slot ids passed validation;
-                             // [1] chunks of the longest sequence (nc)
+                             // [1] chunks of the longest sequence (nc); [8 .. 15] the sequences
+                             // of a segment, by segment parity (chunked path, several segments)
     void* base = nullptr;
     size_t bytes = 0;
 };
@@ -67,6 +70,7 @@ struct Pool {
     size_t state_bytes = 0, conv_bytes = 0, slot_bytes = 0, total_bytes = 0;
     char* base = nullptr;
     unsigned char* live_dev = nullptr;   // [num_slots] 1 = allocated (read by device-side checks)
+    int* mark_dev = nullptr;             // [num_slots] zero between calls (prefill id check, many sequences)
     unsigned int* status_dev = nullptr;  // device status word (GDN_DEV_* bits)
     int* gate_dev = nullptr;             // [1] set when a mixed step's two parts name a common slot
     std::vector<int> free_list;          // free slot ids, popped from the back (lowest id first)
@@ -92,6 +96,7 @@ struct PrefillArgs {
     uint32_t state_bytes;
     int num_layers, layer, num_slots;
     const unsigned char* live;
+    int* mark;  // [num_slots] zero between calls: the distinct-id check of calls with many sequences
     unsigned int* status;
     int hqk, hv, r, D, W, C;
     float l2_eps, norm_eps;
@@ -512,6 +517,9 @@ inline bool rows_aligned16(const void* q, const void* k, const void* v, const vo
 size_t prefill_workspace_bytes(const gdn_shape& s, int max_tokens, int chunk_cap);
 // sequences a call may carry for a workspace of max_tokens tokens
 inline int prefill_max_seqs(int max_tokens) { return max_tokens + 64; }
+// up to this many sequences a prefill call's validation compares ids pairwise and ranks lengths by
+// counting (O(n^2), fast for few); more use per-slot marks and a length histogram
+constexpr int kPairwiseSeqs = 512;
 // chunk records a pool reserves for calls of up to max_tokens tokens (chunked path, d = 128):
 // a call needs ceil(T / 64) + n_seqs of them at most
 inline bool prefill_chunked(const gdn_shape& s) { return s.dk == 128 && s.dv == 128; }

@@ -151,6 +151,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     }
     if (rc == GDN_OK && cudaMalloc(&P->base, P->total_bytes) != cudaSuccess) rc = GDN_ERR_CUDA;
     if (rc == GDN_OK && cudaMalloc(&P->live_dev, (size_t)num_slots) != cudaSuccess) rc = GDN_ERR_CUDA;
+    if (rc == GDN_OK && cudaMalloc(&P->mark_dev, (size_t)num_slots * sizeof(int)) != cudaSuccess) rc = GDN_ERR_CUDA;
     // the status word and, beside it, the mixed step's overlap gate
     if (rc == GDN_OK && cudaMalloc(&P->status_dev, 2 * sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
     if (rc == GDN_OK) P->gate_dev = reinterpret_cast<int*>(P->status_dev + 1);
@@ -165,6 +166,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
     if (rc == GDN_OK) {
         if (enqueue_zero(P->base, P->total_bytes, 0, P->num_sms) != cudaSuccess) rc = GDN_ERR_CUDA;
         if (cudaMemset(P->live_dev, 0, (size_t)num_slots) != cudaSuccess) rc = GDN_ERR_CUDA;
+        if (cudaMemset(P->mark_dev, 0, (size_t)num_slots * sizeof(int)) != cudaSuccess) rc = GDN_ERR_CUDA;
         if (cudaMemset(P->status_dev, 0, 2 * sizeof(unsigned int)) != cudaSuccess) rc = GDN_ERR_CUDA;
         if (cudaDeviceSynchronize() != cudaSuccess) rc = GDN_ERR_CUDA;
     }
@@ -172,6 +174,7 @@ int gdn_pool_create(const gdn_shape* shape, int num_slots, int num_layers, gdn_p
         gdn::destroy_seg_streams(&P->seg);
         cudaFree(P->base);
         cudaFree(P->live_dev);
+        cudaFree(P->mark_dev);
         cudaFree(P->status_dev);
         cudaFree(P->ws.base);
         delete P;
@@ -201,6 +204,7 @@ int gdn_pool_destroy(gdn_pool* P)
     gdn::destroy_seg_streams(&P->seg);
     cudaFree(P->base);
     cudaFree(P->live_dev);
+    cudaFree(P->mark_dev);
     cudaFree(P->status_dev);
     cudaFree(P->ws.base);
     delete P;

@@ -71,24 +71,54 @@ __global__ void __launch_bounds__(256) validate_kernel(PrefillArgs A)
     if (threadIdx.x == 0) bad = 0;
     __syncthreads();
     if (threadIdx.x == 0 && (A.cu[0] != 0 || A.cu[A.n] != A.T)) atomicOr(&bad, 1);
+    // Up to kPairwiseSeqs sequences the ids are compared pairwise and ranked by counting; more take
+    // a mark per slot (mark[id], zero between calls) and a histogram of the lengths, in O(n + T).
+    const bool many = A.n > kPairwiseSeqs;
     for (int s = threadIdx.x; s < A.n; s += blockDim.x) {
         if (A.cu[s + 1] < A.cu[s]) atomicOr(&bad, 1);
         const int id = A.ids[s];
         bool ok = id >= 0 && id < A.num_slots && A.live[id];
-        for (int j = 0; ok && j < s; ++j) ok = A.ids[j] != id;
+        if (!many) {
+            for (int j = 0; ok && j < s; ++j) ok = A.ids[j] != id;
+        } else if (ok && atomicExch(A.mark + id, 1) != 0) {
+            ok = false;  // a second sequence on this slot
+        }
         if (!ok) atomicOr(&bad, 2);
     }
     __syncthreads();
-    if (bad == 0) {
+    if (many)
         for (int s = threadIdx.x; s < A.n; s += blockDim.x) {
-            // rank by length, longest first (ties by index): long sequences start in the first wave
-            const int len = A.cu[s + 1] - A.cu[s];
-            int rank = 0;
-            for (int j = 0; j < A.n; ++j) {
-                const int lj = A.cu[j + 1] - A.cu[j];
-                rank += (lj > len) || (lj == len && j < s);
+            const int id = A.ids[s];
+            if (id >= 0 && id < A.num_slots) A.mark[id] = 0;
+        }
+    if (bad == 0) {
+        // rank by length, longest first: long sequences start in the first wave
+        if (!many) {
+            for (int s = threadIdx.x; s < A.n; s += blockDim.x) {  // ties by index
+                const int len = A.cu[s + 1] - A.cu[s];
+                int rank = 0;
+                for (int j = 0; j < A.n; ++j) {
+                    const int lj = A.cu[j + 1] - A.cu[j];
+                    rank += (lj > len) || (lj == len && j < s);
+                }
+                A.ws.order[rank] = s;
             }
-            A.ws.order[rank] = s;
+        } else {
+            // ties in arrival order: which of two equal lengths comes first changes no result
+            int* cnt = A.ws.lcnt;  // [T + 2]: sequences of each length, then of shorter lengths
+            int* tie = A.ws.ltie;  // [T + 2]
+            for (int l = threadIdx.x; l < A.T + 2; l += blockDim.x) {
+                cnt[l] = 0;
+                tie[l] = 0;
+            }
+            __syncthreads();
+            for (int s = threadIdx.x; s < A.n; s += blockDim.x) atomicAdd(cnt + (A.cu[s + 1] - A.cu[s]), 1);
+            __syncthreads();
+            block_exclusive_scan(cnt, A.T + 2);
+            for (int s = threadIdx.x; s < A.n; s += blockDim.x) {
+                const int len = A.cu[s + 1] - A.cu[s];
+                A.ws.order[A.n - cnt[len + 1] + atomicAdd(tie + len, 1)] = s;  // longer ones first
+            }
         }
         if (A.D == 128) {  // the chunked path's record numbering (chunk-index-major)
             __syncthreads();
@@ -407,6 +437,7 @@ size_t prefill_workspace_bytes(const gdn_shape& s, int T, int chunk_cap)
         b += align256((size_t)T * s.hv * 4) * 2;      // g, beta
     }
     b += align256((size_t)prefill_max_seqs(T) * 4);   // length order
+    b += align256((size_t)(T + 2) * 4) * 2;             // length histogram, ties (many sequences)
     if (prefill_chunked(s)) {
         b += align256((size_t)((T + 63) / 64 + 2) * 4) * 2;  // coff, ctmp
         b += align256((size_t)prefill_call_chunks(T, prefill_max_seqs(T)) * 8);  // rec_cp
@@ -435,6 +466,8 @@ bool prefill_workspace_carve(PrefillWorkspace& ws, const gdn_shape& s, int T, in
         ws.beta = reinterpret_cast<float*>(take((size_t)T * s.hv * 4));
     }
     ws.order = reinterpret_cast<int*>(take((size_t)prefill_max_seqs(T) * 4));
+    ws.lcnt = reinterpret_cast<int*>(take((size_t)(T + 2) * 4));
+    ws.ltie = reinterpret_cast<int*>(take((size_t)(T + 2) * 4));
     if (prefill_chunked(s)) {
         ws.coff = reinterpret_cast<int*>(take((size_t)((T + 63) / 64 + 2) * 4));
         ws.ctmp = reinterpret_cast<int*>(take((size_t)((T + 63) / 64 + 2) * 4));
@@ -478,6 +511,7 @@ cudaError_t launch_prefill(const Pool& P, int layer, const int* cu_seqlens, cons
     A.layer = layer;
     A.num_slots = P.num_slots;
     A.live = P.live_dev;
+    A.mark = P.mark_dev;
     A.status = P.status_dev;
     A.hqk = P.shape.hqk;
     A.hv = P.shape.hv;
@@ -594,11 +628,13 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     if (s.dk != s.dv || (s.dk != 16 && s.dk != 32 && s.dk != 64 && s.dk != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
 
     if (n_seqs > prefill_max_seqs(total_tokens)) return GDN_ERR_UNSUPPORTED_SHAPE;
-    // everything the call needs must fit in the static scratch: workspace, live flags, status word
+    // everything the call needs must fit in the static scratch: workspace, live flags, id marks,
+    // status word
     const int chunk_cap = prefill_chunked(s) ? prefill_call_chunks(total_tokens, n_seqs) : 0;
     const size_t ws_bytes = prefill_workspace_bytes(s, total_tokens, chunk_cap);
     const size_t live_bytes = align256((size_t)num_slots);
-    if (ws_bytes + live_bytes + 256 > kStaticScratchBytes) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const size_t mark_bytes = align256((size_t)num_slots * sizeof(int));
+    if (ws_bytes + live_bytes + mark_bytes + 256 > kStaticScratchBytes) return GDN_ERR_UNSUPPORTED_SHAPE;
 
     void* scratch = nullptr;
     if (static_scratch_address(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
@@ -607,7 +643,8 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     ws.bytes = ws_bytes;
     if (!prefill_workspace_carve(ws, s, total_tokens, chunk_cap)) return GDN_ERR_CUDA;
     unsigned char* live = static_cast<unsigned char*>(scratch) + ws_bytes;
-    unsigned int* status = status_dev ? status_dev : reinterpret_cast<unsigned int*>(live + live_bytes);
+    int* mark = reinterpret_cast<int*>(live + live_bytes);
+    unsigned int* status = status_dev ? status_dev : reinterpret_cast<unsigned int*>(live + live_bytes + mark_bytes);
 
     const int C = 2 * s.hqk * s.dk + s.hv * s.dv;
     const int io_size = s.io_dtype == 1 ? 2 : 4;
@@ -616,6 +653,8 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     fill_ones_kernel<<<(num_slots + 255) / 256, 256, 0, st>>>(live, num_slots);
+    // the marks must start at zero, and this call's carve may put them where other data was
+    if (cudaMemsetAsync(mark, 0, (size_t)num_slots * sizeof(int), st) != cudaSuccess) return GDN_ERR_CUDA;
 
     PrefillArgs A;
     A.cu = cu_seqlens_dev;
@@ -640,6 +679,7 @@ extern "C" int gdn_prefill_varlen_noalloc(const gdn_shape* shape, const float* c
     A.layer = 0;
     A.num_slots = num_slots;
     A.live = live;
+    A.mark = mark;
     A.status = status;
     A.hqk = s.hqk;
     A.hv = s.hv;

@@ -176,6 +176,48 @@ def test_chunked_prefill_in_segments(lengths):
     L.close()
 
 
+@pytest.mark.parametrize("lengths", [[4] * 600, [3] * 300 + [700] + [5] * 299], ids=["600_short", "one_long_among_600"])
+def test_prefill_many_sequences(lengths):
+    """More than 512 sequences in a call: the validation checks distinct slot ids with per-slot marks
+    and ranks the lengths by a histogram instead of pairwise, and the call runs in segments whose
+    state passes take only the sequences with records in them (with one long prompt among the short
+    ones, a segment's sequences are two runs of ranks).  Outputs against the oracle, final states
+    and conv buffers of a sample; then a call naming one slot twice is refused on the device with
+    nothing written, and the marks are clear again for a valid call."""
+    n = len(lengths)
+    T = sum(lengths)
+    L = Layer(36, 1, 2, 128, io="bf16", out="f32", num_slots=n, max_prefill_tokens=T)
+    slots = [L.pool.alloc() for _ in range(n)]
+    inp, cu = synth.varlen_inputs(36, 0, lengths, 1, 2, 128, 128, "bf16")
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    assert L.pool.device_status() == 0
+    ref = L.oracle_run(0, cu, inp, np.zeros((n, 2, 128, 128)), np.zeros((n, 3, L.C)))
+    check_out(o, ref["out"], "f32", PREFILL_TOL, "many-sequence prefill out")
+    for j in sorted({0, 1, n // 2, n // 2 + 1, n - 1}):
+        Sg, Cg = L.get_state(0, slots[j])
+        assert relerr(Sg, ref["S"][j]) <= PREFILL_TOL, f"final S of sequence {j}"
+        assert np.array_equal(Cg, ref["convbuf"][j]), f"conv buffer of sequence {j}"
+    # one slot named twice: refused on the device, nothing written
+    d = L.to_dev(inp)
+    cu_d = torch.tensor(np.asarray(cu, dtype=np.int32), device="cuda")
+    dup = list(slots)
+    dup[-1] = dup[n // 3]
+    out = torch.full((T, 2 * 128), 7.0, device="cuda")
+    before = L.get_state(0, slots[n // 3])
+    L.pool.prefill_varlen(0, cu_d, torch.tensor(dup, dtype=torch.int32, device="cuda"), n, T, d["q"], d["k"], d["v"],
+                          d["a"], d["b"], d["z"], out)
+    assert L.pool.device_status() & binding.DEV_BAD_SLOT_ID
+    assert torch.all(out == 7.0)
+    after = L.get_state(0, slots[n // 3])
+    assert np.array_equal(before[0], after[0]) and np.array_equal(before[1], after[1])
+    # the marks were cleared: the same valid call runs again (from the states the first one left)
+    o2 = host(L.gpu_prefill(0, slots, inp, cu))
+    assert L.pool.device_status() == 0
+    ref2 = L.oracle_run(0, cu, inp, ref["S"], ref["convbuf"])
+    check_out(o2, ref2["out"], "f32", PREFILL_TOL, "second many-sequence prefill out")
+    L.close()
+
+
 def test_segmented_prefill_graph_replay_equals_eager_bitwise():
     """A prefill that runs in pipelined segments forks work onto the pool's second stream and joins
     it back; captured into a CUDA graph, its replay gives the eager results bit for bit (outputs,
