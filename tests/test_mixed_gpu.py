@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from gated_deltanet_linear_rule_gb300 import synth
-from gdn_harness import PREFILL_TOL, Layer, check_out, host
+from gdn_harness import PREFILL_TOL, Layer, check_out, host, random_states, relerr
 
 pytestmark = pytest.mark.gpu
 
@@ -134,6 +134,51 @@ def test_mixed_step_graph_replay_equals_eager_bitwise():
     for (S1, C1), (S2, C2) in zip(eager[2], _states(L, all_slots)):
         assert torch.equal(S1, S2) and torch.equal(C1, C2)
     assert L.pool.device_status() == 0
+    L.close()
+
+
+def test_mixed_step_with_a_segmented_prefill():
+    """A mixed step whose prefill part is one 33 000-token prompt: more chunk records than the
+    workspace's 512, so the prefill runs in pipelined segments on the pool's second stream while the
+    decode runs on the mixed step's own stream.  Results equal the two separate calls bit for bit;
+    the prefill output and final state against the oracle."""
+    hqk, hv, d, m = 1, 2, 128, 12
+    T = 33000
+    L = Layer(45, hqk, hv, d, io="bf16", out="f32", num_slots=m + 2, max_prefill_tokens=T)
+    dec_slots = [L.pool.alloc() for _ in range(m)]
+    pre_slot = L.pool.alloc()
+    S0 = random_states(45, 0, dec_slots, hv, d)
+    for s_, Si in zip(dec_slots, S0):
+        L.set_state(0, s_, Si)
+    dec = L.to_dev(L.decode_inputs(list(range(m)), 0))
+    inp, cu = synth.varlen_inputs(45, 0, [T], hqk, hv, d, d, "bf16")
+    p = L.to_dev(inp)
+    cu_d = torch.tensor(np.asarray(cu, dtype=np.int32), device="cuda")
+    ids = torch.tensor([pre_slot], dtype=torch.int32, device="cuda")
+    ptrs = L.pool.slot_ptrs(0, torch.tensor(dec_slots, dtype=torch.int32, device="cuda"))
+    all_slots = dec_slots + [pre_slot]
+    init = _states(L, all_slots)
+    out_d1 = torch.empty((m, hv * d), dtype=torch.float32, device="cuda")
+    out_p1 = torch.empty((T, hv * d), dtype=torch.float32, device="cuda")
+    L.pool.decode_step(0, ptrs, m, dec["q"], dec["k"], dec["v"], dec["a"], dec["b"], dec["z"], out_d1)
+    L.pool.prefill_varlen(0, cu_d, ids, 1, T, p["q"], p["k"], p["v"], p["a"], p["b"], p["z"], out_p1)
+    torch.cuda.synchronize()
+    sep = _states(L, all_slots)
+    _restore(L, all_slots, init)
+    out_d2 = torch.empty_like(out_d1)
+    out_p2 = torch.empty_like(out_p1)
+    L.pool.mixed_step(0, ptrs, m, dec["q"], dec["k"], dec["v"], dec["a"], dec["b"], dec["z"], out_d2, cu_d, ids, 1, T,
+                      p["q"], p["k"], p["v"], p["a"], p["b"], p["z"], out_p2)
+    torch.cuda.synchronize()
+    assert torch.equal(out_d1, out_d2)
+    assert torch.equal(out_p1, out_p2)
+    for (S1, C1), (S2, C2) in zip(sep, _states(L, all_slots)):
+        assert torch.equal(S1, S2) and torch.equal(C1, C2)
+    assert L.pool.device_status() == 0
+    ref = L.oracle_run(0, cu, inp, np.zeros((1, hv, d, d)), np.zeros((1, L.W - 1, L.C)))
+    check_out(host(out_p2), ref["out"], "f32", PREFILL_TOL, "segmented prefill in a mixed step")
+    Sg, _ = L.get_state(0, pre_slot)
+    assert relerr(Sg, ref["S"][0]) <= PREFILL_TOL
     L.close()
 
 
