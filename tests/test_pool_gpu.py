@@ -218,6 +218,31 @@ def test_prefill_many_sequences(lengths):
     L.close()
 
 
+@pytest.mark.parametrize("d,chunk", [(16, 0), (32, 8)], ids=["recurrent_d16", "chunked_d32"])
+def test_prefill_many_sequences_small_d(d, chunk):
+    """More than 512 sequences at d < 128 (fp32): the validation's per-slot marks and length
+    histogram feed the recurrent and the fp32 chunked kernels too.  Outputs and a sample of final
+    states against the oracle; a repeated slot id is refused on the device."""
+    lengths = [1, 2, 3, 5] * 150
+    n, T = len(lengths), sum(lengths)
+    L = Layer(37, 2, 4, d, io="f32", num_slots=n, chunk=chunk, max_prefill_tokens=T)
+    slots = [L.pool.alloc() for _ in range(n)]
+    inp, cu = synth.varlen_inputs(37, 0, lengths, 2, 4, d, d, "f32")
+    o = host(L.gpu_prefill(0, slots, inp, cu))
+    assert L.pool.device_status() == 0
+    ref = L.oracle_run(0, cu, inp, np.zeros((n, 4, d, d)), np.zeros((n, 3, L.C)))
+    check_out(o, ref["out"], "f32", PREFILL_TOL, "many-sequence small-d prefill out")
+    for j in (0, n // 2, n - 1):
+        Sg, Cg = L.get_state(0, slots[j])
+        assert relerr(Sg, ref["S"][j]) <= PREFILL_TOL
+        assert np.array_equal(Cg, ref["convbuf"][j])
+    dup = list(slots)
+    dup[5] = dup[400]
+    L.gpu_prefill(0, dup, inp, cu)
+    assert L.pool.device_status() & binding.DEV_BAD_SLOT_ID
+    L.close()
+
+
 def test_segmented_prefill_graph_replay_equals_eager_bitwise():
     """A prefill that runs in pipelined segments forks work onto the pool's second stream and joins
     it back; captured into a CUDA graph, its replay gives the eager results bit for bit (outputs,
