@@ -22,8 +22,9 @@
 //    BNP = 256, or 192 when that puts more SMs to work in a single round): each CTA holds 128
 //    rows of A and BNP / 2 rows of B per K slice (6 stages) and receives its 128 rows of the
 //    result, so an SM streams about half the operand bytes per output.
-//  - proj_splitk_kernel<KS> (few tiles): a cluster of KS CTAs splits one 128 x 256 tile's K
-//    range and reduce-scatters the partial accumulators through distributed shared memory.
+//  - proj_splitk_kernel<KS, BNS> (few tiles): a cluster of KS CTAs splits one 128 x BNS tile's
+//    K range and reduce-scatters the partial accumulators through distributed shared memory
+//    (BNS = 256, or 128 where that puts more CTAs to work).
 // Rows past M and columns past N are zero-filled by the copies and skipped by the stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -392,11 +393,12 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, ui
         : "memory");
 }
 
-template <int KS>
+template <int KS, int BNS>
 __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constant__ ProjArgs P,
                                                               const __grid_constant__ ProjMaps T)
 {
-    constexpr int GW = BN / KS;                // columns of the group a CTA owns
+    static_assert(BNS == 128 || BNS == 256, "tile width");
+    constexpr int GW = BNS / KS;               // columns of the group a CTA owns
     constexpr uint32_t GROUP = 128u * GW * 4u;  // bytes of one group of a partial
     static_assert(2 * (KS - 1) * GROUP <= BAR_OFF, "sent and received groups fit the stage ring");
     extern __shared__ unsigned char smem_raw[];
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)cluster_ctarank(), tile = (int)blockIdx.x / KS;
-    const int tiles_n = (P.N + BN - 1) / BN;
-    const int n0 = (tile % tiles_n) * BN, m0 = (tile / tiles_n) * BM;
+    const int tiles_n = (P.N + BNS - 1) / BNS;
+    const int n0 = (tile % tiles_n) * BNS, m0 = (tile / tiles_n) * BM;
     const int kper = (P.K / BK) / KS, kt0 = rank * kper;
 
     if (tid == 0) {
@@ -441,8 +443,8 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
                     atomicOr(P.status, GDN_DEV_TIMEOUT);
                     break;
                 }
-                unsigned char* st = sm + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                unsigned char* st = sm + s * STAGE_BYTES;  // B takes BNS of the stage's BN rows
+                mbar_arrive_expect_tx(&full[s], A_BYTES + (uint32_t)BNS * BK * 2);
                 tma_load(st, &T.a, (kt0 + i) * BK, m0, &full[s]);
                 tma_load(st + A_BYTES, &T.b, (kt0 + i) * BK, n0, &full[s]);
             }
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(PT, 1) proj_splitk_kernel(const __grid_constan
                 tc::fence_after_sync();
                 unsigned char* st = sm + s * STAGE_BYTES;
                 if (ok)
-                    tc::mma_k(tm, smem_addr(st), BM, smem_addr(st + A_BYTES), BN, BK, tc::idesc_bf16(BM, BN), i > 0);
+                    tc::mma_k(tm, smem_addr(st), BM, smem_addr(st + A_BYTES), BNS, BK, tc::idesc_bf16(BM, BNS), i > 0);
                 tc::commit(&empty[s]);
             }
             tc::commit(accf);
@@ -610,27 +612,35 @@ cudaError_t launch_clusters(ProjKernel kern, unsigned grid, unsigned cluster, si
 
 constexpr int kMaxDevices = 64;  // per-device caches below (kernel attributes are per device)
 
-// clusters of c split-K CTAs resident at once on device dev (c = 2 or 4; cached; 0 when the
+// the split-K kernel for c CTAs per tile (2 or 4) and tiles bn wide (128 or 256)
+ProjKernel splitk_kernel(int c, int bn)
+{
+    if (bn == 128) return c == 4 ? proj_splitk_kernel<4, 128> : proj_splitk_kernel<2, 128>;
+    return c == 4 ? proj_splitk_kernel<4, 256> : proj_splitk_kernel<2, 256>;
+}
+
+// clusters of c split-K CTAs (tiles bn wide) resident at once on device dev (cached; 0 when the
 // query fails)
-int split_clusters(int dev, int c)
+int split_clusters(int dev, int c, int bn)
 {
     static std::mutex mu;
-    static int cached[kMaxDevices][5];
+    static int cached[kMaxDevices][2][5];
     static bool init[kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
     if (!init[dev]) {
-        for (int& x : cached[dev]) x = -1;
+        for (auto& w : cached[dev])
+            for (int& x : w) x = -1;
         init[dev] = true;
     }
-    if (cached[dev][c] < 0) {
-        const ProjKernel kern = c == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
-        cached[dev][c] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM) ==
-                                 cudaSuccess
-                             ? resident_clusters(kern, (unsigned)c, PROJ_SMEM)
-                             : 0;
+    int& slot = cached[dev][bn == 128 ? 0 : 1][c];
+    if (slot < 0) {
+        const ProjKernel kern = splitk_kernel(c, bn);
+        slot = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROJ_SMEM) == cudaSuccess
+                   ? resident_clusters(kern, (unsigned)c, PROJ_SMEM)
+                   : 0;
         (void)cudaGetLastError();
     }
-    return cached[dev][c];
+    return slot;
 }
 
 cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const Seg* seg, int nseg,
@@ -692,25 +702,33 @@ cudaError_t launch_proj(int M, int N, int K, const void* a, const void* b, const
         num_pairs = cached_pairs[dev];
     }
     // Few tiles (small T): split each tile's K range over a cluster of KS CTAs when at least
-    // two CTAs per tile fit on the GPU at once (KS dividing the K slices, every cluster resident).
+    // two CTAs per tile fit on the GPU at once (KS dividing the K slices, every cluster resident),
+    // with 128 x 256 tiles, or 128 x 128 tiles where those put more CTAs to work (each then
+    // streams half the B rows: the weights are the bytes that bound a small batch).
     {
-        const long tiles1 = (long)((N + BN - 1) / BN) * ((M + BM - 1) / BM);
         const int KT = K / BK;
-        int ks = 0;
-        for (int c : {4, 2}) {
-            if (tiles1 * c > num_sms || KT % c != 0) continue;
-            if (split_clusters(dev, c) < tiles1) continue;
-            ks = c;
-            break;
+        int ks = 0, bns = 0;
+        long best = 0;
+        for (int bn : {256, 128}) {
+            const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM);
+            for (int c : {4, 2}) {
+                if (tiles * c > num_sms || KT % c != 0 || tiles * c <= best) continue;
+                if (split_clusters(dev, c, bn) < tiles) continue;
+                ks = c;
+                bns = bn;
+                best = tiles * c;
+                break;
+            }
         }
         if (ks) {
             ProjMaps T;
             memset(&T, 0, sizeof(T));
             e = encode_kmajor(&T.a, a, K, M, BM);
-            if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, BN);
+            if (e == cudaSuccess) e = encode_kmajor(&T.b, b, K, N, bns);
             if (e != cudaSuccess) return e;
-            const ProjKernel kern = ks == 4 ? proj_splitk_kernel<4> : proj_splitk_kernel<2>;
-            return launch_clusters(kern, (unsigned)(tiles1 * ks), (unsigned)ks, PROJ_SMEM, st, P, T);
+            const long tiles = (long)((N + bns - 1) / bns) * ((M + BM - 1) / BM);
+            return launch_clusters(splitk_kernel(ks, bns), (unsigned)(tiles * ks), (unsigned)ks, PROJ_SMEM, st, P,
+                                   T);
         }
     }
     // persistent grids: tiles are taken in turn by num_sms CTAs (128 x 256 tiles) or by num_pairs
