@@ -47,6 +47,14 @@
 // Delta~ as the M side) are read MN-major straight from row-wise tiles.
 // Every tcgen05.ld / st is executed by whole warps (they are warp-collective); per-token
 // conditions only guard stores.
+//
+// Records are numbered chunk-index-major (every sequence's chunk 0 in length order, then every
+// chunk 1, ...: chunk c of the sequence of rank p is record coff[c] + p).  A call whose records
+// exceed the workspace runs as segments, windows [seg_lo, seg_hi) of record numbers: the
+// pre-pass of a segment writes its records at positions gc - seg_lo, and the segment's state
+// pass takes, for each sequence with records in the window, the run of its chunks there,
+// starting from the state the slot holds; only the segment holding a sequence's last chunk
+// advances its conv buffer.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -359,7 +367,7 @@ __global__ void __launch_bounds__(NT, 2) chunk_prep_kernel(const __grid_constant
     const size_t rec_region = (size_t)A.ws.chunk_cap * A.hv * REC_BYTES;
     const size_t qk_region = (size_t)A.ws.chunk_cap * A.hqk * QK_BYTES;
     const size_t slots_region = (size_t)A.num_slots * A.num_layers * A.slot_bytes;
-    const size_t rowsq = (size_t)A.T * A.hqk * D * sizeof(TIn), rowsv = (size_t)A.T * A.hv * D * sizeof(TIn);
+    const size_t rowsv = (size_t)A.T * A.hv * D * sizeof(TIn);
     auto sm_ok = [&](const void* p, size_t b) { return chk(within(p, b, sm, sm_bytes), A.status); };
     auto tile_ok = [&](const void* p, size_t b, uint32_t off, uint32_t region) {
         return chk(within(p, b, sm + off, region), A.status);
